@@ -1,0 +1,202 @@
+"""CPU oracle for the group-wise quantised linear layer and the routed MoE FFN.
+
+TEST INFRASTRUCTURE ONLY: the test suite, the smoke check and the benchmark's
+CPU-baseline leg are the only callers.  The arithmetic lives in plain C
+(``qmm_oracle.c``, single thread, -O2 -ffp-contract=off, no -ffast-math); this
+module only marshals numpy arrays to it.  It shares no code with the CUDA
+library and never imports it.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+from dataclasses import dataclass
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "qmm_oracle.c")
+_HDR = os.path.join(_HERE, "qmm_oracle.h")
+_LIB_PATH = os.path.join(_HERE, "libqmm_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle into ``libqmm_oracle.so`` (gcc, single thread)."""
+    newest = max(os.path.getmtime(_SRC), os.path.getmtime(_HDR))
+    if not force and os.path.exists(_LIB_PATH) and os.path.getmtime(_LIB_PATH) >= newest:
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c99", "-fPIC", "-shared", "-ffp-contract=off",
+           "-fno-fast-math", _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+class _QW(ctypes.Structure):
+    _fields_ = [("bits", ctypes.c_int32), ("group", ctypes.c_int32),
+                ("N", ctypes.c_int64), ("K", ctypes.c_int64),
+                ("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p),
+                ("zps", ctypes.c_void_p)]
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            lib = ctypes.CDLL(_LIB_PATH)
+            i32, i64, vp, dbl = ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p, ctypes.c_double
+            pqw = ctypes.POINTER(_QW)
+            lib.orc_quantize.argtypes = [vp, i64, i64, ctypes.c_int, ctypes.c_int, vp, vp, vp]
+            lib.orc_quantize.restype = ctypes.c_int
+            lib.orc_code_at.argtypes = [pqw, i64, i64]
+            lib.orc_code_at.restype = i32
+            lib.orc_dequantize.argtypes = [pqw, vp]
+            lib.orc_dequantize.restype = None
+            for name in ("orc_linear_fused", "orc_linear_two_step", "orc_linear_bound"):
+                getattr(lib, name).argtypes = [vp, i64, pqw, vp]
+                getattr(lib, name).restype = None
+            lib.orc_router_logits.argtypes = [vp, i64, i64, vp, vp, i32, vp]
+            lib.orc_router_logits.restype = None
+            lib.orc_topk.argtypes = [vp, i64, i32, i32, vp, vp]
+            lib.orc_topk.restype = None
+            lib.orc_moe_ffn.argtypes = [vp, i64, i64, i64, vp, vp, i32, i32,
+                                        pqw, pqw, pqw, dbl, vp, vp]
+            lib.orc_moe_ffn.restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def _c(a: np.ndarray, dtype) -> np.ndarray:
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+@dataclass
+class QWeight:
+    """Quantised W[N,K] as the oracle stores it (numpy arrays)."""
+    bits: int
+    group: int
+    N: int
+    K: int
+    codes: np.ndarray   # uint8 [N*K] (int8 bit patterns) or [N*K/2] packed
+    scales: np.ndarray  # float32 [N, K/group]
+    zps: np.ndarray     # int32 [N, K/group]
+
+    def _struct(self) -> _QW:
+        return _QW(self.bits, self.group, self.N, self.K, self.codes.ctypes.data,
+                   self.scales.ctypes.data, self.zps.ctypes.data)
+
+
+def quantize(w: np.ndarray, bits: int, group: int) -> QWeight:
+    w = _c(w, np.float32)
+    N, K = w.shape
+    nbytes = N * K if bits == 8 else N * K // 2
+    codes = np.zeros(nbytes, dtype=np.uint8)
+    G = K // group if group > 0 else 0
+    scales = np.zeros((N, G), dtype=np.float32)
+    zps = np.zeros((N, G), dtype=np.int32)
+    rc = _load().orc_quantize(w.ctypes.data, N, K, bits, group, codes.ctypes.data,
+                              scales.ctypes.data, zps.ctypes.data)
+    if rc != 0:
+        raise ValueError(f"orc_quantize rejected N={N} K={K} bits={bits} group={group}")
+    return QWeight(bits, group, N, K, codes, scales, zps)
+
+
+def code_at(qw: QWeight, n: int, k: int) -> int:
+    s = qw._struct()
+    return int(_load().orc_code_at(ctypes.byref(s), n, k))
+
+
+def dequantize(qw: QWeight) -> np.ndarray:
+    out = np.empty((qw.N, qw.K), dtype=np.float32)
+    s = qw._struct()
+    _load().orc_dequantize(ctypes.byref(s), out.ctypes.data)
+    return out
+
+
+def _linear(name: str, x: np.ndarray, qw: QWeight) -> np.ndarray:
+    x = _c(x, np.float32)
+    if x.ndim == 1:
+        x = x[None, :]
+    M = x.shape[0]
+    assert x.shape[1] == qw.K
+    y = np.empty((M, qw.N), dtype=np.float64)
+    s = qw._struct()
+    getattr(_load(), name)(x.ctypes.data, M, ctypes.byref(s), y.ctypes.data)
+    return y
+
+
+def linear_fused(x, qw):
+    """y[m,n] = sum_k x[m,k] (q-zp) s, dequantised inside the k loop (double)."""
+    return _linear("orc_linear_fused", x, qw)
+
+
+def linear_two_step(x, qw):
+    """Dequantise the whole matrix, then multiply (double)."""
+    return _linear("orc_linear_two_step", x, qw)
+
+
+def linear_bound(x, qw):
+    """1e-5 * sum_k |x_k w^_k| + 1e-6 per output."""
+    return _linear("orc_linear_bound", x, qw)
+
+
+def router_logits(x: np.ndarray, wr: np.ndarray, bias: np.ndarray | None) -> np.ndarray:
+    x = _c(x, np.float32)
+    wr = _c(wr, np.float32)
+    M, H = x.shape
+    E = wr.shape[0]
+    assert wr.shape[1] == H
+    out = np.empty((M, E), dtype=np.float32)
+    bp = None
+    if bias is not None:
+        bias = _c(bias, np.float32)
+        bp = bias.ctypes.data
+    _load().orc_router_logits(x.ctypes.data, M, H, wr.ctypes.data, bp, E, out.ctypes.data)
+    return out
+
+
+def topk(logits: np.ndarray, k: int):
+    logits = _c(logits, np.float32)
+    M, E = logits.shape
+    idx = np.empty((M, k), dtype=np.int32)
+    w = np.empty((M, k), dtype=np.float32)
+    _load().orc_topk(logits.ctypes.data, M, E, k, idx.ctypes.data, w.ctypes.data)
+    return idx, w
+
+
+def _qw_array(ws, E):
+    arr = (_QW * E)()
+    for e in range(E):
+        if ws[e] is not None:
+            arr[e] = ws[e]._struct()
+    return arr
+
+
+def moe_ffn(x: np.ndarray, idx: np.ndarray, w: np.ndarray, gate, up, down,
+            dw: float = 0.0, with_bound: bool = True):
+    """Routed SwiGLU MoE output y[M,H] (double) and its per-element bound.
+
+    gate/up/down: lists of length E holding QWeight (or None for experts that
+    no token selected)."""
+    x = _c(x, np.float32)
+    idx = _c(idx, np.int32)
+    w = _c(w, np.float32)
+    M, H = x.shape
+    k = idx.shape[1]
+    E = len(gate)
+    I = next(g.N for g in gate if g is not None)
+    y = np.empty((M, H), dtype=np.float64)
+    bound = np.empty((M, H), dtype=np.float64) if with_bound else None
+    ga, ua, da = _qw_array(gate, E), _qw_array(up, E), _qw_array(down, E)
+    rc = _load().orc_moe_ffn(x.ctypes.data, M, H, I, idx.ctypes.data, w.ctypes.data, k, E,
+                             ga, ua, da, dw, y.ctypes.data,
+                             bound.ctypes.data if bound is not None else None)
+    if rc != 0:
+        raise ValueError(f"orc_moe_ffn failed ({rc})")
+    return y, bound

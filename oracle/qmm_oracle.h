@@ -1,0 +1,48 @@
+/*
+ * qmm_oracle.h -- CPU oracle (test infrastructure only; see qmm_oracle.c).
+ * Its own types: nothing here is shared with the CUDA library.
+ */
+#ifndef QMM_ORACLE_H
+#define QMM_ORACLE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A quantised weight W[N,K]: codes int8 (stored q-128) [N*K] or packed uint8
+ * [N*K/2] (low nibble = even column), scales fp32 [N, K/group], zps int32
+ * [N, K/group]. */
+typedef struct orc_qweight {
+  int32_t bits, group;
+  int64_t N, K;
+  const void *codes;
+  const float *scales;
+  const int32_t *zps;
+} orc_qweight;
+
+int orc_quantize(const float *w, int64_t N, int64_t K, int bits, int group,
+                 void *codes, float *scales, int32_t *zps);
+int32_t orc_code_at(const orc_qweight *w, int64_t n, int64_t k);
+void orc_dequantize(const orc_qweight *w, float *out);
+void orc_linear_fused(const float *x, int64_t M, const orc_qweight *w, double *y);
+void orc_linear_two_step(const float *x, int64_t M, const orc_qweight *w, double *y);
+void orc_linear_bound(const float *x, int64_t M, const orc_qweight *w, double *bound);
+void orc_router_logits(const float *x, int64_t M, int64_t H, const float *wr,
+                       const float *bias, int32_t E, float *logits);
+void orc_topk(const float *logits, int64_t M, int32_t E, int32_t k, int32_t *idx,
+              float *w);
+/* gate/up/down: arrays of E descriptors (only experts named in idx are read).
+ * dw: bound on |w_gpu - w_oracle| of the routing weights (0 when both sides
+ * use the same weights).  y and bound are [M, H] doubles. */
+int orc_moe_ffn(const float *x, int64_t M, int64_t H, int64_t I,
+                const int32_t *idx, const float *tw, int32_t k, int32_t E,
+                const orc_qweight *gate, const orc_qweight *up,
+                const orc_qweight *down, double dw, double *y, double *bound);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif
