@@ -1,0 +1,448 @@
+"""Benchmark of the group-wise quantised linear / routed MoE hot path on GB300.
+
+Default workload (the headline metric): one decode step of the INT8 group-64
+GEMV workload -- x[1, 4096] through the 4096x4096 trunk projection, then the
+result through the 129280x4096 vocab head -- with the weights resident in HBM.
+value = algorithmic weight bytes per step (codes + fp32 scale + int32 zero
+point per group) / device time per step, in GB/s.  The two MoE workloads
+(decode M=8 INT4 g64; batched prefill M=512 bf16 INT8 g128 with Zipf-biased
+routing) are measured in the same run and reported under "moe_decode" and
+"moe_prefill" (tokens/s and GB/s).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--no-moe] [--cpu-seconds S]
+
+--impl reference times the CPU oracle (single thread) on a bounded sample of
+the same workload and prints the same JSON line with "impl": "reference".
+Under torchrun every rank runs an independent replica ("replicas only": the
+path has no exchange step); the max time over ranks is reported.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from synth import recipes  # noqa: E402
+import synth  # noqa: E402
+
+PEAKS_PATH = os.path.join(ROOT, "MEASURED_PEAKS.json")
+TRAFFIC_PATH = os.path.join(ROOT, "profiles", "traffic.json")
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+def weight_bytes(N: int, K: int, bits: int, group: int) -> int:
+    """Algorithmic bytes of one quantised matrix: packed codes + 8 B/group."""
+    return N * K * bits // 8 + N * (K // group) * 8
+
+
+def load_peaks():
+    try:
+        with open(PEAKS_PATH) as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": FALLBACK_HBM_GBS, "bf16_tflops": FALLBACK_BF16_TFLOPS,
+                "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def source_hash(*names: str) -> str:
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "group_quantized_moe_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_for(kernel: str, src_files: tuple[str, ...], workload: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current source of the kernel; otherwise None."""
+    try:
+        with open(TRAFFIC_PATH) as f:
+            t = json.load(f)
+        ent = t[workload][kernel]
+        if ent.get("source_hash") != source_hash(*src_files):
+            return None
+        return float(ent["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    """Samples SM clocks and throttle reasons with nvidia-smi while running."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines: list[str] = []
+        self.thread = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            if self.thread:
+                self.thread.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": 0}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------ distributed
+
+def dist_setup(n_gpus: int):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend=backend)
+    return rank, world, local
+
+
+def dist_max(v: float, world: int) -> float:
+    if world <= 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    dev = torch.device("cuda", torch.cuda.current_device()) if dist.get_backend() == "nccl" else None
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def dist_barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ------------------------------------------------------------ GEMV workload
+
+def build_gemv(dev):
+    import torch
+    import group_quantized_moe_gb300 as q
+    mats = []
+    for r in (recipes.CFG2_TRUNK, recipes.CFG2_VOCAB):
+        w = recipes.linear_weight_rows(r)
+        wd = torch.from_numpy(w).to(dev)
+        del w
+        mats.append(q.qmm_quantize_groupwise(wd, r.bits, r.group))
+        del wd
+        torch.cuda.empty_cache()
+    x = torch.from_numpy(recipes.linear_x(recipes.CFG2_TRUNK)).to(dev)
+    return mats, x
+
+
+def run_gemv(dev, steps: int, warmup: int, world: int):
+    import torch
+    import group_quantized_moe_gb300 as q
+    (wt, wv), x = build_gemv(dev)
+    y1 = torch.empty((1, wt.N), dtype=torch.float32, device=dev)
+    y2 = torch.empty((1, wv.N), dtype=torch.float32, device=dev)
+    s = torch.cuda.current_stream()
+
+    def step(evs=None):
+        if evs:
+            evs[0].record(s)
+        q.qmm_linear(x, wt, y=y1, stream=s)
+        if evs:
+            evs[1].record(s)
+        q.qmm_linear(y1, wv, y=y2, stream=s)
+        if evs:
+            evs[2].record(s)
+
+    for _ in range(max(3, warmup)):
+        step()
+    torch.cuda.synchronize()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    dist_barrier(world)
+    torch.cuda.synchronize()
+    n0 = q.qmm_launch_count()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        start.record(s)
+        for i in range(steps):
+            step(evs[i])
+        end.record(s)
+        torch.cuda.synchronize()
+    launches = q.qmm_launch_count() - n0
+    dist_barrier(world)
+    ms = start.elapsed_time(end) / steps
+    t_trunk = np.mean([e[0].elapsed_time(e[1]) for e in evs])
+    t_vocab = np.mean([e[1].elapsed_time(e[2]) for e in evs])
+
+    # end to end through the C ABI with host buffers (pinned), copies inside
+    xh = torch.from_numpy(recipes.linear_x(recipes.CFG2_TRUNK)).pin_memory()
+    yh = torch.empty((1, wv.N), dtype=torch.float32).pin_memory()
+    for _ in range(3):
+        x.copy_(xh, non_blocking=True)
+        step()
+        yh.copy_(y2, non_blocking=True)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(s)
+    for _ in range(steps):
+        x.copy_(xh, non_blocking=True)
+        step()
+        yh.copy_(y2, non_blocking=True)
+    e1.record(s)
+    torch.cuda.synchronize()
+    ms_e2e = e0.elapsed_time(e1) / steps
+
+    b_trunk = weight_bytes(wt.N, wt.K, 8, 64)
+    b_vocab = weight_bytes(wv.N, wv.K, 8, 64)
+    return {"ms": ms, "ms_e2e": ms_e2e, "bytes": b_trunk + b_vocab, "t_trunk_ms": float(t_trunk),
+            "t_vocab_ms": float(t_vocab), "b_trunk": b_trunk, "b_vocab": b_vocab,
+            "launches": int(launches), "clocks": clk.summary(),
+            "h2d": xh.numel() * 4, "d2h": yh.numel() * 4}
+
+
+# ------------------------------------------------------------ MoE workloads
+
+def run_moe(dev, r, steps: int, warmup: int):
+    import torch
+    import group_quantized_moe_gb300 as q
+
+    def fill(which, e, out):
+        recipes.moe_expert_rows(r, which, e, out=out)
+
+    t0 = time.time()
+    ex = q.quantize_experts(r.E, r.H, r.I, r.bits, r.group, fill, device=dev)
+    setup_s = time.time() - t0
+    xf, xb = recipes.moe_x(r)
+    if r.x_bf16:
+        x = torch.from_numpy(xb.view(np.int16)).to(dev).view(torch.bfloat16)
+    else:
+        x = torch.from_numpy(xf).to(dev)
+    wr, bias = recipes.moe_router(r)
+    wr_d = torch.from_numpy(wr).to(dev)
+    bias_d = torch.from_numpy(bias).to(dev) if bias is not None else None
+    M, k = r.M, r.k
+    idx = torch.empty((M, k), dtype=torch.int32, device=dev)
+    tw = torch.empty((M, k), dtype=torch.float32, device=dev)
+    cnt = torch.empty((r.E,), dtype=torch.int32, device=dev)
+    rws = torch.empty((q.moe_route_workspace_bytes(M, r.E),), dtype=torch.uint8, device=dev)
+    fws = torch.empty((q.moe_ffn_workspace_bytes(M, k, ex),), dtype=torch.uint8, device=dev)
+    ydt = torch.bfloat16 if r.x_bf16 else torch.float32
+    y = torch.empty((M, r.H), dtype=ydt, device=dev)
+    s = torch.cuda.current_stream()
+    # L2 flush buffer (the decode layer's touched weights are ~0.7 GB, but the
+    # router matrix and small layers could stay resident between steps).
+    flush = torch.empty((256 << 20,), dtype=torch.uint8, device=dev)
+
+    def step(evs=None):
+        if evs:
+            evs[0].record(s)
+        q.moe_route_topk(x, wr_d, bias_d, k, topk_idx=idx, topk_w=tw, expert_counts=cnt,
+                         workspace=rws, stream=s)
+        if evs:
+            evs[1].record(s)
+        q.moe_ffn_forward(x, idx, tw, ex, y=y, workspace=fws, stream=s)
+        if evs:
+            evs[2].record(s)
+
+    for _ in range(max(3, warmup)):
+        step()
+    torch.cuda.synchronize()
+    times, t_route, t_ffn = [], [], []
+    n0 = q.qmm_launch_count()
+    for _ in range(steps):
+        flush.zero_()
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        step(evs)
+        torch.cuda.synchronize()
+        times.append(evs[0].elapsed_time(evs[2]))
+        t_route.append(evs[0].elapsed_time(evs[1]))
+        t_ffn.append(evs[1].elapsed_time(evs[2]))
+    launches = q.qmm_launch_count() - n0
+    counts = cnt.cpu().numpy()
+    touched = int((counts > 0).sum())
+    hot = int((counts >= 64).sum())
+    ms = float(np.mean(times))
+    per_expert = weight_bytes(r.I, r.H, r.bits, r.group) * 2 + weight_bytes(r.H, r.I, r.bits, r.group)
+    bytes_ = touched * per_expert + r.E * r.H * 4
+    flops = 2.0 * M * k * 3 * r.H * r.I + 2.0 * M * r.E * r.H
+    return {"workload": r.name, "tokens_per_s": M / (ms * 1e-3), "ms_per_step": ms,
+            "route_ms": float(np.mean(t_route)), "ffn_ms": float(np.mean(t_ffn)),
+            "weight_gbs": bytes_ / (ms * 1e-3) / 1e9, "algorithmic_bytes": bytes_,
+            "flops": flops, "tflops": flops / (ms * 1e-3) / 1e12, "distinct_experts": touched,
+            "experts_ge64_tokens": hot, "max_tokens_per_expert": int(counts.max()),
+            "gpu_launches": int(launches), "setup_s": round(setup_s, 1),
+            "l2": "256 MB written between steps"}
+
+
+# ------------------------------------------------------------ oracle (CPU)
+
+def oracle_gemv_sample(seconds: float):
+    """The oracle's fused linear on rows of the vocab head (+ trunk) until
+    `seconds` of CPU time; returns GB/s of algorithmic weight bytes."""
+    import oracle
+    r = recipes.CFG2_VOCAB
+    x = recipes.linear_x(r)
+    rows_per = 1024
+    done_bytes, spent, row0 = 0, 0.0, 0
+    while spent < seconds:
+        w = recipes.linear_weight_rows(r, row0, rows_per)
+        qw = oracle.quantize(w, r.bits, r.group)
+        t0 = time.perf_counter()
+        oracle.linear_fused(x, qw)
+        spent += time.perf_counter() - t0
+        done_bytes += weight_bytes(rows_per, r.K, r.bits, r.group)
+        row0 = (row0 + rows_per) % (r.N - rows_per)
+    return done_bytes / spent / 1e9, done_bytes, spent
+
+
+# ------------------------------------------------------------------- main
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-moe", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args()
+    peaks = load_peaks()
+    metric = "fused dequant-GEMV weight GB/s & MoE layer tokens/s, % of HBM/TC roofline"
+    workload = "decode step: x[1,4096] -> INT8 g64 W[4096,4096] -> INT8 g64 W[129280,4096]"
+
+    rank, world, local = dist_setup(args.gpus)
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        gbs, nbytes, spent = 0.0, 0, 0.0
+        t_steps = []
+        for i in range(args.warmup + args.steps):
+            g, b, sp = oracle_gemv_sample(max(0.5, args.cpu_seconds / max(1, args.steps)))
+            if i >= args.warmup:
+                nbytes += b
+                spent += sp
+                t_steps.append(sp)
+        gbs = nbytes / spent / 1e9
+        line = {"impl": "reference", "metric": metric, "value": gbs, "unit": "GB/s",
+                "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": 1e3 * spent / args.steps, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                "config": {"workload": workload + " (oracle: 1024-row samples of the vocab head)"},
+                "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                                 "sample": f"{nbytes} weight bytes of vocab-head rows, "
+                                           f"{spent:.1f} s single-thread"},
+                "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    g = run_gemv(dev, args.steps, args.warmup, world)
+    ms = dist_max(g["ms"], world)
+    ms_e2e = dist_max(g["ms_e2e"], world)
+    value = world * g["bytes"] / (ms * 1e-3) / 1e9
+    ach = g["b_vocab"] / (g["t_vocab_ms"] * 1e-3) / 1e9
+    traffic = traffic_for("gemv_kernel", ("gemv.cu", "qmm_device.cuh"),
+                          "int8_g64_k4096_n129280")
+    line = {"metric": metric, "value": value, "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic (seeded N(0,0.02) weights with 1% x20 outliers, N(0,1) activations)",
+            "config": {"workload": workload, "bits": 8, "group": 64, "M": 1,
+                       "weight_bytes_per_step": g["bytes"],
+                       "l2": "inputs larger than L2 (615 MB of weights per step vs 129 MB L2)",
+                       "parallelism": f"replicas x{world}"},
+            "roofline": {"bound": "hbm", "kernel": "gemv_kernel (vocab head launch)",
+                         "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": ach / peaks["hbm_gbs"], "traffic": traffic,
+                         "peak_source": peaks["source"],
+                         "frac_vs_8tbs": ach / 8000.0},
+            "kernels_ms": {"trunk_4096": g["t_trunk_ms"], "vocab_129280": g["t_vocab_ms"]},
+            "gpu_launches": g["launches"],
+            "clocks": g["clocks"],
+            "e2e": {"value": world * g["bytes"] / (ms_e2e * 1e-3) / 1e9, "unit": "GB/s",
+                    "h2d_bytes_per_step": g["h2d"], "d2h_bytes_per_step": g["d2h"]}}
+    if not args.no_moe:
+        extras = {}
+        for key, r in (("moe_decode", recipes.CFG4), ("moe_prefill", recipes.CFG5)):
+            try:
+                mo = run_moe(dev, r, max(10, args.steps // 5), args.warmup)
+                mo["hbm_frac"] = mo["weight_gbs"] / peaks["hbm_gbs"]
+                mo["tc_frac"] = mo["tflops"] / peaks["bf16_tflops_sustained"]
+                extras[key] = mo
+            except Exception as e:  # keep the headline line even if an extra fails
+                extras[key] = {"error": f"{type(e).__name__}: {e}"}
+            torch.cuda.empty_cache()
+        line.update(extras)
+    if rank == 0:
+        gbs, nbytes, spent = oracle_gemv_sample(args.cpu_seconds)
+        line["cpu_baseline"] = {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                                "sample": f"{nbytes} weight bytes of vocab-head rows "
+                                          f"(1024-row blocks), {spent:.1f} s single-thread"}
+        print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

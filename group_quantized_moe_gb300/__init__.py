@@ -1,0 +1,345 @@
+"""Python binding of libqmm.so: group-wise INT8/INT4 quantised linear layer and
+routed SwiGLU MoE layer on GB300 (sm_103a).
+
+Thin layer over the C ABI declared in ``include/qmm.h``: every function here
+has the name of the C entry point it calls, turns torch tensors into device
+pointers and sizes, allocates outputs with torch when the caller passes none,
+and raises ``QmmError`` on a non-zero status.  All arithmetic runs in the
+library's CUDA kernels; there is no other implementation behind these names.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from dataclasses import dataclass
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libqmm.so")
+
+QMM_OK = 0
+QMM_ERR_INVALID_ARG = 1
+QMM_ERR_SHAPE = 2
+QMM_ERR_ALIGN = 3
+QMM_ERR_WORKSPACE = 4
+QMM_ERR_CUDA = 5
+QMM_ERR_UNSUPPORTED = 6
+QMM_F32 = 0
+QMM_BF16 = 1
+QMM_DEV_WAIT_TIMEOUT = 1
+QMM_DEV_BAD_EXPERT = 2
+
+EXPORTED = ("qmm_quantize_groupwise", "qmm_linear", "moe_route_workspace_bytes", "moe_route_topk",
+            "moe_ffn_workspace_bytes", "moe_ffn_forward", "qmm_last_error", "qmm_launch_count",
+            "qmm_device_status")
+
+
+class QmmError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"[qmm status {code}] {msg}")
+        self.code = code
+
+
+class _Weight(ctypes.Structure):
+    _fields_ = [("bits", ctypes.c_int32), ("group", ctypes.c_int32),
+                ("N", ctypes.c_int64), ("K", ctypes.c_int64),
+                ("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p),
+                ("zps", ctypes.c_void_p)]
+
+
+class _ExpertWeights(ctypes.Structure):
+    _fields_ = [("bits", ctypes.c_int32), ("group", ctypes.c_int32),
+                ("rows", ctypes.c_int64), ("cols", ctypes.c_int64),
+                ("codes", ctypes.c_void_p), ("codes_stride", ctypes.c_int64),
+                ("scales", ctypes.c_void_p), ("zps", ctypes.c_void_p),
+                ("groups_stride", ctypes.c_int64)]
+
+
+class _Experts(ctypes.Structure):
+    _fields_ = [("E", ctypes.c_int32), ("H", ctypes.c_int32), ("I", ctypes.c_int32),
+                ("gate", _ExpertWeights), ("up", _ExpertWeights), ("down", _ExpertWeights)]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libqmm.so.  Raises if the library has not been built: there
+    is deliberately no fallback implementation."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                                   "`python -c 'import __graft_entry__ as g; g.build()'`")
+            L = ctypes.CDLL(LIB_PATH)
+            i32, i64, u64, vp, sz = (ctypes.c_int32, ctypes.c_int64, ctypes.c_uint64,
+                                     ctypes.c_void_p, ctypes.c_size_t)
+            L.qmm_quantize_groupwise.argtypes = [vp, i64, i64, i32, i32, vp, vp, vp, vp]
+            L.qmm_quantize_groupwise.restype = ctypes.c_int
+            L.qmm_linear.argtypes = [vp, i32, i64, ctypes.POINTER(_Weight), vp, vp]
+            L.qmm_linear.restype = ctypes.c_int
+            L.moe_route_workspace_bytes.argtypes = [i64, i32]
+            L.moe_route_workspace_bytes.restype = sz
+            L.moe_route_topk.argtypes = [vp, i32, i64, i64, vp, vp, i32, i32, vp, vp, vp, vp,
+                                         sz, vp]
+            L.moe_route_topk.restype = ctypes.c_int
+            L.moe_ffn_workspace_bytes.argtypes = [i64, i32, ctypes.POINTER(_Experts)]
+            L.moe_ffn_workspace_bytes.restype = sz
+            L.moe_ffn_forward.argtypes = [vp, i32, i64, vp, vp, i32, ctypes.POINTER(_Experts), vp,
+                                          i32, vp, sz, vp]
+            L.moe_ffn_forward.restype = ctypes.c_int
+            L.qmm_last_error.argtypes = []
+            L.qmm_last_error.restype = ctypes.c_char_p
+            L.qmm_launch_count.argtypes = []
+            L.qmm_launch_count.restype = u64
+            L.qmm_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32), i32]
+            L.qmm_device_status.restype = ctypes.c_int
+            _lib = L
+    return _lib
+
+
+def _check(rc: int) -> None:
+    if rc != QMM_OK:
+        raise QmmError(rc, lib().qmm_last_error().decode(errors="replace"))
+
+
+def _ptr(t) -> int | None:
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        return int(t)
+    return t.data_ptr() if t.numel() else None
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return QMM_F32
+    if t.dtype == torch.bfloat16:
+        return QMM_BF16
+    raise TypeError(f"unsupported dtype {t.dtype} (float32 or bfloat16)")
+
+
+def _require_cuda(*ts):
+    for t in ts:
+        if t is not None and isinstance(t, torch.Tensor) and t.numel() and not t.is_cuda:
+            raise ValueError("tensors must live on a CUDA device")
+        if t is not None and isinstance(t, torch.Tensor) and not t.is_contiguous():
+            raise ValueError("tensors must be contiguous")
+
+
+@dataclass
+class QWeight:
+    """A quantised W[N, K] on the device: codes (int8 [N, K] or uint8
+    [N, K/2]), scales fp32 [N, K/group], zps int32 [N, K/group]."""
+    bits: int
+    group: int
+    N: int
+    K: int
+    codes: torch.Tensor
+    scales: torch.Tensor
+    zps: torch.Tensor
+
+    def _c(self) -> _Weight:
+        return _Weight(self.bits, self.group, self.N, self.K, _ptr(self.codes), _ptr(self.scales),
+                       _ptr(self.zps))
+
+
+def alloc_qweight(N: int, K: int, bits: int, group: int, device="cuda") -> QWeight:
+    """Uninitialised output buffers for qmm_quantize_groupwise."""
+    G = K // group
+    if bits == 8:
+        codes = torch.empty((N, K), dtype=torch.int8, device=device)
+    else:
+        codes = torch.empty((N, K // 2), dtype=torch.uint8, device=device)
+    return QWeight(bits, group, N, K, codes,
+                   torch.empty((N, G), dtype=torch.float32, device=device),
+                   torch.empty((N, G), dtype=torch.int32, device=device))
+
+
+def qmm_quantize_groupwise(w: torch.Tensor, bits: int, group: int, out: QWeight | None = None,
+                           stream=None) -> QWeight:
+    """Group-wise quantisation of fp32 w[N, K] (see include/qmm.h)."""
+    _require_cuda(w)
+    if w.dtype != torch.float32 or w.dim() != 2:
+        raise TypeError("w must be a 2-D float32 tensor")
+    N, K = w.shape
+    if out is None:
+        out = alloc_qweight(N, K, bits, group, device=w.device)
+    _check(lib().qmm_quantize_groupwise(_ptr(w), N, K, bits, group, _ptr(out.codes),
+                                        _ptr(out.scales), _ptr(out.zps), _stream(stream)))
+    return out
+
+
+def qmm_linear(x: torch.Tensor, w: QWeight, y: torch.Tensor | None = None,
+               stream=None) -> torch.Tensor:
+    """y[M, N] = x[M, K] . deq(W)^T (fp32 output)."""
+    _require_cuda(x)
+    x2 = x.reshape(-1, w.K) if x.dim() != 2 else x
+    M = x2.shape[0]
+    if y is None:
+        y = torch.empty((M, w.N), dtype=torch.float32, device=x.device)
+    desc = w._c()
+    _check(lib().qmm_linear(_ptr(x2), _dtype_code(x2), M, ctypes.byref(desc), _ptr(y),
+                            _stream(stream)))
+    return y
+
+
+def moe_route_workspace_bytes(M: int, E: int) -> int:
+    return int(lib().moe_route_workspace_bytes(M, E))
+
+
+def moe_route_topk(x: torch.Tensor, w_router: torch.Tensor, bias: torch.Tensor | None, k: int,
+                   topk_idx=None, topk_w=None, expert_counts=None, workspace=None,
+                   with_counts: bool = True, stream=None):
+    """Router: fixed-order fp32 logits, top-k (lower index wins ties) and
+    renormalised softmax weights.  Returns (topk_idx, topk_w, expert_counts)."""
+    _require_cuda(x, w_router, bias)
+    M, H = x.shape
+    E = w_router.shape[0]
+    dev = x.device
+    if topk_idx is None:
+        topk_idx = torch.empty((M, k), dtype=torch.int32, device=dev)
+    if topk_w is None:
+        topk_w = torch.empty((M, k), dtype=torch.float32, device=dev)
+    if expert_counts is None and with_counts:
+        expert_counts = torch.empty((E,), dtype=torch.int32, device=dev)
+    nbytes = moe_route_workspace_bytes(M, E)
+    if workspace is None:
+        workspace = torch.empty((nbytes,), dtype=torch.uint8, device=dev)
+    _check(lib().moe_route_topk(_ptr(x), _dtype_code(x), M, H, _ptr(w_router), _ptr(bias), E, k,
+                                _ptr(topk_idx), _ptr(topk_w), _ptr(expert_counts),
+                                _ptr(workspace), workspace.numel(), _stream(stream)))
+    return topk_idx, topk_w, expert_counts
+
+
+@dataclass
+class MoeExperts:
+    """E routed experts stacked along dim 0: gate/up codes [E, I, H*bits/8],
+    down codes [E, H, I*bits/8]; scales / zps [E, rows, cols/group]."""
+    E: int
+    H: int
+    I: int
+    bits: int
+    group: int
+    gate_codes: torch.Tensor
+    gate_scales: torch.Tensor
+    gate_zps: torch.Tensor
+    up_codes: torch.Tensor
+    up_scales: torch.Tensor
+    up_zps: torch.Tensor
+    down_codes: torch.Tensor
+    down_scales: torch.Tensor
+    down_zps: torch.Tensor
+
+    def _mat(self, which: str) -> _ExpertWeights:
+        codes = getattr(self, f"{which}_codes")
+        scales = getattr(self, f"{which}_scales")
+        zps = getattr(self, f"{which}_zps")
+        rows, cols = (self.I, self.H) if which in ("gate", "up") else (self.H, self.I)
+        return _ExpertWeights(self.bits, self.group, rows, cols, _ptr(codes),
+                              codes.stride(0) * codes.element_size(), _ptr(scales), _ptr(zps),
+                              scales.stride(0))
+
+    def _c(self) -> _Experts:
+        return _Experts(self.E, self.H, self.I, self._mat("gate"), self._mat("up"),
+                        self._mat("down"))
+
+
+def alloc_experts(E: int, H: int, I: int, bits: int, group: int, device="cuda") -> MoeExperts:
+    """Uninitialised stacked expert buffers (filled by quantising each expert)."""
+    def mat(rows, cols):
+        cb = cols if bits == 8 else cols // 2
+        dt = torch.int8 if bits == 8 else torch.uint8
+        return (torch.empty((E, rows, cb), dtype=dt, device=device),
+                torch.empty((E, rows, cols // group), dtype=torch.float32, device=device),
+                torch.empty((E, rows, cols // group), dtype=torch.int32, device=device))
+    g, u, d = mat(I, H), mat(I, H), mat(H, I)
+    return MoeExperts(E, H, I, bits, group, *g, *u, *d)
+
+
+def moe_ffn_workspace_bytes(M: int, k: int, experts: MoeExperts) -> int:
+    desc = experts._c()
+    return int(lib().moe_ffn_workspace_bytes(M, k, ctypes.byref(desc)))
+
+
+def moe_ffn_forward(x: torch.Tensor, topk_idx: torch.Tensor, topk_w: torch.Tensor,
+                    experts: MoeExperts, y: torch.Tensor | None = None,
+                    y_dtype: torch.dtype = torch.float32, workspace: torch.Tensor | None = None,
+                    stream=None) -> torch.Tensor:
+    """Routed SwiGLU MoE layer: y[m] = sum_i w[m,i] FFN_{idx[m,i]}(x[m])."""
+    _require_cuda(x, topk_idx, topk_w)
+    M, H = x.shape
+    k = topk_idx.shape[1]
+    if y is None:
+        y = torch.empty((M, H), dtype=y_dtype, device=x.device)
+    desc = experts._c()
+    nbytes = int(lib().moe_ffn_workspace_bytes(M, k, ctypes.byref(desc)))
+    if workspace is None:
+        workspace = torch.empty((nbytes,), dtype=torch.uint8, device=x.device)
+    _check(lib().moe_ffn_forward(_ptr(x), _dtype_code(x), M, _ptr(topk_idx), _ptr(topk_w), k,
+                                 ctypes.byref(desc), _ptr(y), _dtype_code(y), _ptr(workspace),
+                                 workspace.numel(), _stream(stream)))
+    return y
+
+
+def qmm_last_error() -> str:
+    return lib().qmm_last_error().decode(errors="replace")
+
+
+def qmm_launch_count() -> int:
+    return int(lib().qmm_launch_count())
+
+
+def qmm_device_status(clear: bool = False) -> int:
+    v = ctypes.c_uint32(0)
+    _check(lib().qmm_device_status(ctypes.byref(v), 1 if clear else 0))
+    return int(v.value)
+
+
+def quantize_experts(E: int, H: int, I: int, bits: int, group: int, rows_fn, device="cuda",
+                     stream=None) -> MoeExperts:
+    """Quantises the fp32 matrices of E experts into stacked device buffers.
+
+    ``rows_fn(which, e, out)`` fills ``out`` (a float32 numpy array of shape
+    [I, H] for "gate"/"up", [H, I] for "down") with expert e's weights.  Each
+    matrix is staged through pinned host memory to the device and quantised
+    there by qmm_quantize_groupwise, so no fp32 copy of the experts stays
+    resident."""
+    ex = alloc_experts(E, H, I, bits, group, device=device)
+    n = I * H
+    pinned = [torch.empty((n,), dtype=torch.float32).pin_memory() for _ in range(2)]
+    staging = [torch.empty((n,), dtype=torch.float32, device=device) for _ in range(2)]
+    s = torch.cuda.current_stream(device) if stream is None else stream
+    events = [None, None]
+    j = 0
+    for e in range(E):
+        for which in ("gate", "up", "down"):
+            rows, cols = (I, H) if which in ("gate", "up") else (H, I)
+            b = j % 2
+            if events[b] is not None:
+                events[b].synchronize()  # the previous copy out of this pinned buffer is done
+            host = pinned[b].numpy().reshape(rows, cols)
+            rows_fn(which, e, host)
+            with torch.cuda.stream(s):
+                staging[b].copy_(pinned[b], non_blocking=True)
+                out = QWeight(bits, group, rows, cols, getattr(ex, f"{which}_codes")[e],
+                              getattr(ex, f"{which}_scales")[e], getattr(ex, f"{which}_zps")[e])
+                qmm_quantize_groupwise(staging[b].view(rows, cols), bits, group, out=out, stream=s)
+                ev = torch.cuda.Event()
+                ev.record(s)
+                events[b] = ev
+            j += 1
+    torch.cuda.synchronize(device)
+    return ex

@@ -1,0 +1,319 @@
+// qmm_abi.cu -- the library's extern "C" entry points: argument validation on
+// the host, workspace carving, kernel selection and launch on the caller's
+// stream.  Declared in include/qmm.h.
+#include <atomic>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/qmm.h"
+#include "qmm_internal.h"
+
+namespace qmm {
+namespace {
+
+thread_local char g_err[512] = "";
+std::atomic<uint64_t> g_launches{0};
+
+constexpr int kMaxDevices = 64;
+int g_sms[kMaxDevices] = {0};
+uint32_t *g_status_ptr[kMaxDevices] = {nullptr};
+std::mutex g_mu;
+
+// One status word per device (a module-scope device variable; its address on
+// each device is looked up once).
+__device__ uint32_t g_status_word;
+
+int fail(int code, const char *fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof(g_err), fmt, ap);
+  va_end(ap);
+  return code;
+}
+
+int cuda_fail(cudaError_t e, const char *where) {
+  return fail(QMM_ERR_CUDA, "%s: %s", where, cudaGetErrorString(e));
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned256(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 255u) == 0; }
+
+bool group_ok(int g) { return g == 32 || g == 64 || g == 128 || g == 256; }
+
+size_t round256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
+
+int current_device() {
+  int d = 0;
+  if (cudaGetDevice(&d) != cudaSuccess) return -1;
+  return d;
+}
+
+// Common checks of one quantised matrix (bits, group, shape).
+int check_qshape(int bits, int group, int64_t rows, int64_t cols, const char *what) {
+  if (bits != 8 && bits != 4) return fail(QMM_ERR_INVALID_ARG, "%s: bits must be 8 or 4 (got %d)", what, bits);
+  if (!group_ok(group))
+    return fail(QMM_ERR_UNSUPPORTED, "%s: group must be 32, 64, 128 or 256 (got %d)", what, group);
+  if (rows < 0) return fail(QMM_ERR_SHAPE, "%s: negative row count", what);
+  if (cols <= 0 || cols % group != 0)
+    return fail(QMM_ERR_SHAPE, "%s: K=%lld must be a positive multiple of group %d", what,
+                static_cast<long long>(cols), group);
+  return QMM_OK;
+}
+
+}  // namespace
+
+void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+int sm_count() {
+  const int d = current_device();
+  if (d < 0 || d >= kMaxDevices) return 1;
+  if (g_sms[d] == 0) {
+    int v = 1;
+    cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, d);
+    g_sms[d] = v > 0 ? v : 1;
+  }
+  return g_sms[d];
+}
+
+uint32_t *device_status() {
+  const int d = current_device();
+  if (d < 0 || d >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_status_ptr[d]) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return nullptr;
+    g_status_ptr[d] = static_cast<uint32_t *>(p);
+  }
+  return g_status_ptr[d];
+}
+
+}  // namespace qmm
+
+using namespace qmm;
+
+extern "C" {
+
+const char *qmm_last_error(void) { return g_err; }
+
+uint64_t qmm_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+int qmm_device_status(uint32_t *status, int32_t clear) {
+  if (!status) return fail(QMM_ERR_INVALID_ARG, "qmm_device_status: status is NULL");
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_fail(e, "qmm_device_status");
+  e = cudaMemcpyFromSymbol(status, g_status_word, sizeof(uint32_t));
+  if (e != cudaSuccess) return cuda_fail(e, "qmm_device_status");
+  if (clear) {
+    const uint32_t zero = 0;
+    e = cudaMemcpyToSymbol(g_status_word, &zero, sizeof(uint32_t));
+    if (e != cudaSuccess) return cuda_fail(e, "qmm_device_status");
+  }
+  return QMM_OK;
+}
+
+int qmm_quantize_groupwise(const float *w, int64_t N, int64_t K, int32_t bits, int32_t group,
+                           void *codes, float *scales, int32_t *zps, qmm_stream_t stream) {
+  g_err[0] = '\0';
+  int rc = check_qshape(bits, group, N, K, "qmm_quantize_groupwise");
+  if (rc) return rc;
+  if (N == 0) return QMM_OK;
+  if (!w || !codes || !scales || !zps)
+    return fail(QMM_ERR_INVALID_ARG, "qmm_quantize_groupwise: null pointer");
+  if (!aligned16(w) || !aligned16(codes) || !aligned16(scales) || !aligned16(zps))
+    return fail(QMM_ERR_ALIGN, "qmm_quantize_groupwise: w, codes, scales and zps must be 16-byte aligned");
+  cudaError_t e = launch_quantize(w, N, K, bits, group, codes, scales, zps,
+                                  static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "qmm_quantize_groupwise");
+  return QMM_OK;
+}
+
+int qmm_linear(const void *x, int32_t x_dtype, int64_t M, const qmm_weight *w, float *y,
+               qmm_stream_t stream) {
+  g_err[0] = '\0';
+  if (!w) return fail(QMM_ERR_INVALID_ARG, "qmm_linear: weight descriptor is NULL");
+  int rc = check_qshape(w->bits, w->group, w->N, w->K, "qmm_linear");
+  if (rc) return rc;
+  if (x_dtype != QMM_F32 && x_dtype != QMM_BF16)
+    return fail(QMM_ERR_INVALID_ARG, "qmm_linear: x_dtype must be QMM_F32 or QMM_BF16");
+  if (M < 0) return fail(QMM_ERR_SHAPE, "qmm_linear: negative M");
+  if (M == 0 || w->N == 0) return QMM_OK;
+  if (!x || !y || !w->codes || !w->scales || !w->zps)
+    return fail(QMM_ERR_INVALID_ARG, "qmm_linear: null pointer");
+  if (!aligned16(x) || !aligned16(w->codes) || !aligned16(w->scales) || !aligned16(w->zps))
+    return fail(QMM_ERR_ALIGN, "qmm_linear: x, codes, scales and zps must be 16-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(y) & 3u) != 0)
+    return fail(QMM_ERR_ALIGN, "qmm_linear: y must be 4-byte aligned");
+  const int64_t rowbytes = w->K * w->bits / 8;
+  if (rowbytes > gemv_max_rowbytes())
+    return fail(QMM_ERR_UNSUPPORTED, "qmm_linear: a weight row of %lld bytes exceeds %d",
+                static_cast<long long>(rowbytes), gemv_max_rowbytes());
+  QMat q{static_cast<const uint8_t *>(w->codes), 0, w->scales, w->zps, 0, w->N, w->K,
+         w->bits, w->group};
+  cudaError_t e = launch_gemv(x, x_dtype == QMM_BF16, M, q, y, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "qmm_linear");
+  return QMM_OK;
+}
+
+size_t moe_route_workspace_bytes(int64_t M, int32_t E) {
+  if (M <= 0 || E <= 0) return 256;
+  return round256(router_logits_bytes(M, E));
+}
+
+int moe_route_topk(const void *x, int32_t x_dtype, int64_t M, int64_t H, const float *w_router,
+                   const float *bias, int32_t E, int32_t k, int32_t *topk_idx, float *topk_w,
+                   int32_t *expert_counts, void *workspace, size_t workspace_bytes,
+                   qmm_stream_t stream) {
+  g_err[0] = '\0';
+  if (x_dtype != QMM_F32 && x_dtype != QMM_BF16)
+    return fail(QMM_ERR_INVALID_ARG, "moe_route_topk: x_dtype must be QMM_F32 or QMM_BF16");
+  if (E < 1 || E > 1024) return fail(QMM_ERR_INVALID_ARG, "moe_route_topk: E must be in [1, 1024]");
+  if (k < 1 || k > 16 || k > E)
+    return fail(QMM_ERR_INVALID_ARG, "moe_route_topk: k must be in [1, min(E, 16)]");
+  if (M < 0 || H <= 0 || H % 4 != 0)
+    return fail(QMM_ERR_SHAPE, "moe_route_topk: need M >= 0 and H a positive multiple of 4");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (M == 0) {
+    if (expert_counts) {
+      cudaError_t e = cudaMemsetAsync(expert_counts, 0, sizeof(int32_t) * E, s);
+      if (e != cudaSuccess) return cuda_fail(e, "moe_route_topk");
+    }
+    return QMM_OK;
+  }
+  if (!x || !w_router || !topk_idx || !topk_w)
+    return fail(QMM_ERR_INVALID_ARG, "moe_route_topk: null pointer");
+  if (!aligned16(x) || !aligned16(w_router))
+    return fail(QMM_ERR_ALIGN, "moe_route_topk: x and w_router must be 16-byte aligned");
+  if (!workspace || workspace_bytes < moe_route_workspace_bytes(M, E))
+    return fail(QMM_ERR_WORKSPACE, "moe_route_topk: workspace needs %zu bytes",
+                moe_route_workspace_bytes(M, E));
+  if (!aligned256(workspace))
+    return fail(QMM_ERR_ALIGN, "moe_route_topk: workspace must be 256-byte aligned");
+  cudaError_t e = launch_router(x, x_dtype == QMM_BF16, M, H, w_router, bias, E, k,
+                                static_cast<float *>(workspace), topk_idx, topk_w, expert_counts, s);
+  if (e != cudaSuccess) return cuda_fail(e, "moe_route_topk");
+  return QMM_OK;
+}
+
+}  // extern "C"
+
+namespace {
+
+int check_experts(const moe_experts *ex) {
+  if (!ex) return fail(QMM_ERR_INVALID_ARG, "moe_experts descriptor is NULL");
+  if (ex->E < 1 || ex->E > 1024) return fail(QMM_ERR_INVALID_ARG, "moe_experts: E must be in [1, 1024]");
+  if (ex->H <= 0 || ex->I <= 0) return fail(QMM_ERR_SHAPE, "moe_experts: H and I must be positive");
+  const qmm_expert_weights *m[3] = {&ex->gate, &ex->up, &ex->down};
+  const char *names[3] = {"gate", "up", "down"};
+  for (int i = 0; i < 3; ++i) {
+    const int64_t rows = i < 2 ? ex->I : ex->H;
+    const int64_t cols = i < 2 ? ex->H : ex->I;
+    if (m[i]->rows != rows || m[i]->cols != cols)
+      return fail(QMM_ERR_SHAPE, "moe_experts.%s: shape [%lld, %lld], expected [%lld, %lld]", names[i],
+                  static_cast<long long>(m[i]->rows), static_cast<long long>(m[i]->cols),
+                  static_cast<long long>(rows), static_cast<long long>(cols));
+    int rc = check_qshape(m[i]->bits, m[i]->group, rows, cols, names[i]);
+    if (rc) return rc;
+    if (m[i]->bits != ex->gate.bits || m[i]->group != ex->gate.group)
+      return fail(QMM_ERR_UNSUPPORTED, "moe_experts: gate, up and down must share bits and group");
+    if (!m[i]->codes || !m[i]->scales || !m[i]->zps)
+      return fail(QMM_ERR_INVALID_ARG, "moe_experts.%s: null pointer", names[i]);
+    if (!aligned16(m[i]->codes) || !aligned16(m[i]->scales) || !aligned16(m[i]->zps) ||
+        m[i]->codes_stride % 16 != 0 || m[i]->groups_stride % 4 != 0)
+      return fail(QMM_ERR_ALIGN, "moe_experts.%s: pointers and strides must be 16-byte aligned",
+                  names[i]);
+    if (m[i]->codes_stride < 0 || m[i]->groups_stride < 0)
+      return fail(QMM_ERR_INVALID_ARG, "moe_experts.%s: negative stride", names[i]);
+  }
+  // Gate and up rows are staged together, two per copy slot.
+  if (2 * ex->H * ex->gate.bits / 8 > gemv_max_rowbytes() ||
+      ex->I * ex->down.bits / 8 > gemv_max_rowbytes())
+    return fail(QMM_ERR_UNSUPPORTED, "moe_experts: rows too long for the expert kernels");
+  return QMM_OK;
+}
+
+struct WsLayout {
+  size_t counts, offsets, active, num_active, assign, pos, h, out, total;
+};
+
+WsLayout ws_layout(int64_t M, int k, const moe_experts *ex) {
+  WsLayout L;
+  const size_t MK = static_cast<size_t>(M) * k;
+  size_t o = 0;
+  L.counts = o;     o += round256(sizeof(int32_t) * ex->E);
+  L.offsets = o;    o += round256(sizeof(int32_t) * (ex->E + 1));
+  L.active = o;     o += round256(sizeof(int32_t) * ex->E);
+  L.num_active = o; o += 256;
+  L.assign = o;     o += round256(sizeof(int32_t) * MK);
+  L.pos = o;        o += round256(sizeof(int32_t) * MK);
+  L.h = o;          o += round256(sizeof(float) * MK * ex->I);
+  L.out = o;        o += round256(sizeof(float) * MK * ex->H);
+  L.total = o;
+  return L;
+}
+
+QMat qmat(const qmm_expert_weights &w) {
+  return QMat{static_cast<const uint8_t *>(w.codes), w.codes_stride, w.scales, w.zps,
+              w.groups_stride, w.rows, w.cols, w.bits, w.group};
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t moe_ffn_workspace_bytes(int64_t M, int32_t k, const moe_experts *ex) {
+  if (!ex || M < 0 || k < 1 || ex->E < 1) return 0;
+  return ws_layout(M, k, ex).total;
+}
+
+int moe_ffn_forward(const void *x, int32_t x_dtype, int64_t M, const int32_t *topk_idx,
+                    const float *topk_w, int32_t k, const moe_experts *ex, void *y,
+                    int32_t y_dtype, void *workspace, size_t workspace_bytes,
+                    qmm_stream_t stream) {
+  g_err[0] = '\0';
+  int rc = check_experts(ex);
+  if (rc) return rc;
+  if (x_dtype != QMM_F32 && x_dtype != QMM_BF16)
+    return fail(QMM_ERR_INVALID_ARG, "moe_ffn_forward: x_dtype must be QMM_F32 or QMM_BF16");
+  if (y_dtype != QMM_F32 && y_dtype != QMM_BF16)
+    return fail(QMM_ERR_INVALID_ARG, "moe_ffn_forward: y_dtype must be QMM_F32 or QMM_BF16");
+  if (k < 1 || k > 16 || k > ex->E)
+    return fail(QMM_ERR_INVALID_ARG, "moe_ffn_forward: k must be in [1, min(E, 16)]");
+  if (M < 0) return fail(QMM_ERR_SHAPE, "moe_ffn_forward: negative M");
+  if (M == 0) return QMM_OK;
+  if (!x || !topk_idx || !topk_w || !y)
+    return fail(QMM_ERR_INVALID_ARG, "moe_ffn_forward: null pointer");
+  if (!aligned16(x) || !aligned16(y))
+    return fail(QMM_ERR_ALIGN, "moe_ffn_forward: x and y must be 16-byte aligned");
+  const WsLayout L = ws_layout(M, k, ex);
+  if (!workspace || workspace_bytes < L.total)
+    return fail(QMM_ERR_WORKSPACE, "moe_ffn_forward: workspace needs %zu bytes", L.total);
+  if (!aligned256(workspace))
+    return fail(QMM_ERR_ALIGN, "moe_ffn_forward: workspace must be 256-byte aligned");
+
+  uint8_t *base = static_cast<uint8_t *>(workspace);
+  MoeWork ws;
+  ws.counts = reinterpret_cast<int32_t *>(base + L.counts);
+  ws.offsets = reinterpret_cast<int32_t *>(base + L.offsets);
+  ws.active = reinterpret_cast<int32_t *>(base + L.active);
+  ws.num_active = reinterpret_cast<int32_t *>(base + L.num_active);
+  ws.assign = reinterpret_cast<int32_t *>(base + L.assign);
+  ws.pos = reinterpret_cast<int32_t *>(base + L.pos);
+  ws.h = reinterpret_cast<float *>(base + L.h);
+  ws.out = reinterpret_cast<float *>(base + L.out);
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const bool xb = x_dtype == QMM_BF16;
+  cudaError_t e = launch_moe_dispatch(topk_idx, M, k, ex->E, ws, s);
+  if (e != cudaSuccess) return cuda_fail(e, "moe_ffn_forward (dispatch)");
+  e = launch_moe_gateup(x, xb, M, k, ex->E, qmat(ex->gate), qmat(ex->up), ws, s);
+  if (e != cudaSuccess) return cuda_fail(e, "moe_ffn_forward (gate/up)");
+  e = launch_moe_down(M, k, ex->E, qmat(ex->down), ws, s);
+  if (e != cudaSuccess) return cuda_fail(e, "moe_ffn_forward (down)");
+  e = launch_moe_combine(M, k, ex->H, topk_w, ws, y, y_dtype == QMM_BF16, s);
+  if (e != cudaSuccess) return cuda_fail(e, "moe_ffn_forward (combine)");
+  return QMM_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,76 @@
+// qmm_internal.h -- host-side interfaces between the C ABI layer (qmm_abi.cu)
+// and the kernel translation units.  Not part of the public ABI.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace qmm {
+
+// One quantised matrix family: E matrices [rows, cols] stacked with strides
+// (a single matrix is E = 1).
+struct QMat {
+  const uint8_t *codes;
+  int64_t codes_stride;   // bytes between experts
+  const float *scales;
+  const int32_t *zps;
+  int64_t groups_stride;  // elements between experts
+  int64_t rows, cols;
+  int32_t bits, group;
+};
+
+// Workspace of the routed MoE layer (device pointers into the caller's
+// buffer).
+struct MoeWork {
+  int32_t *counts;      // [E]
+  int32_t *offsets;     // [E + 1]
+  int32_t *active;      // [E] expert ids with at least one token, ascending
+  int32_t *num_active;  // [1]
+  int32_t *assign;      // [M*k] assignment ids a = m*k + i, grouped by expert
+  int32_t *pos;         // [M*k] position of assignment a inside `assign`
+  float *h;             // [M*k, I] SwiGLU activations (fp32)
+  float *out;           // [M*k, H] per-assignment expert outputs (fp32)
+};
+
+// Counts one kernel launch (for qmm_launch_count).
+void count_launch();
+
+// Number of SMs of the current device (cached per device).
+int sm_count();
+
+// Device status word of the current device.
+uint32_t *device_status();
+
+cudaError_t launch_quantize(const float *w, int64_t N, int64_t K, int bits, int group,
+                            void *codes, float *scales, int32_t *zps, cudaStream_t s);
+
+cudaError_t launch_gemv(const void *x, bool x_bf16, int64_t M, const QMat &w, float *y,
+                        cudaStream_t s);
+
+cudaError_t launch_router(const void *x, bool x_bf16, int64_t M, int64_t H,
+                          const float *wr, const float *bias, int E, int k,
+                          float *logits_scratch, int32_t *idx, float *w, int32_t *counts,
+                          cudaStream_t s);
+
+cudaError_t launch_moe_dispatch(const int32_t *idx, int64_t M, int k, int E,
+                                const MoeWork &ws, cudaStream_t s);
+
+cudaError_t launch_moe_gateup(const void *x, bool x_bf16, int64_t M, int k, int E,
+                              const QMat &gate, const QMat &up, const MoeWork &ws,
+                              cudaStream_t s);
+
+cudaError_t launch_moe_down(int64_t M, int k, int E, const QMat &down, const MoeWork &ws,
+                            cudaStream_t s);
+
+cudaError_t launch_moe_combine(int64_t M, int k, int64_t H, const float *topk_w,
+                               const MoeWork &ws, void *y, bool y_bf16, cudaStream_t s);
+
+}  // namespace qmm
+
+namespace qmm {
+// Longest weight row (bytes) one copy slot of the CUDA-core kernels holds.
+int gemv_max_rowbytes();
+// Bytes of router logits for M tokens and E experts.
+size_t router_logits_bytes(int64_t M, int E);
+}  // namespace qmm

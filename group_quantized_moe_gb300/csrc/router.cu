@@ -1,0 +1,425 @@
+// router.cu -- MoE router (logits, top-k, renormalised weights), token
+// grouping by expert, and the weighted combine of expert outputs.
+//
+// "Why I hand-wrote a DeepSeek inference engine in pure C", section 3.5: the
+// router is a linear layer followed by a softmax and a top-k; tokens routed to
+// the same expert are gathered so that the expert's weights are read once;
+// the selected experts' outputs are combined by a weighted sum.  Section 3.4
+// (same article): subtract the maximum before exponentiating.
+//
+// Logits use a fixed fp32 summation order so that the selected experts are
+// bit-identical to any other implementation of the same order:
+//   partial p (p = 0..127) = fma chain over h = p, p+128, p+256, ...
+//   t_l = (P[4l] + P[4l+1]) + (P[4l+2] + P[4l+3]),       l = 0..31
+//   t_l = t_l + t_{l+o} for o = 16, 8, 4, 2, 1;  logit = t_0 (+ bias)
+// GPU mapping: a block of 128 threads owns the 128 partials (thread p holds
+// partial p) for a register tile of MB tokens x EB experts, reading x and the
+// router rows as coalesced 512-byte rows per step.  The tree runs in the
+// order above: adjacent-partial sums by xor shuffles 1 and 2, the o = 16 and
+// o = 8 stages across warps through shared memory, the rest by xor shuffles
+// 16, 8, 4 inside warp 0.
+#include <cstdint>
+
+#include "qmm_device.cuh"
+#include "qmm_internal.h"
+
+namespace qmm {
+namespace {
+
+constexpr int kMaxK = 16;
+constexpr int kMaxE = 1024;
+
+template <int MB, int EB, bool XBF16>
+__global__ void __launch_bounds__(128) router_logits_kernel(const void *__restrict__ x, int64_t M,
+                                                            int64_t H,
+                                                            const float *__restrict__ wr,
+                                                            const float *__restrict__ bias, int E,
+                                                            float *__restrict__ logits) {
+  __shared__ float xch[2][32][MB * EB + 1];
+  const int p = threadIdx.x;  // partial index
+  const int warp = p >> 5, lane = p & 31;
+  const int64_t m0 = static_cast<int64_t>(blockIdx.y) * MB;
+  const int e0 = blockIdx.x * EB;
+  const int mb = static_cast<int>(min64(MB, M - m0));
+  const int eb = min(EB, E - e0);
+
+  float acc[MB][EB];
+#pragma unroll
+  for (int m = 0; m < MB; ++m)
+#pragma unroll
+    for (int e = 0; e < EB; ++e) acc[m][e] = 0.0f;
+
+  for (int64_t h = p; h < H; h += 128) {
+    float xv[MB], wv[EB];
+#pragma unroll
+    for (int m = 0; m < MB; ++m) {
+      const int64_t mm = m0 + (m < mb ? m : 0);
+      if constexpr (XBF16) {
+        const uint16_t b = static_cast<const uint16_t *>(x)[mm * H + h];
+        xv[m] = __uint_as_float(static_cast<uint32_t>(b) << 16);
+      } else {
+        xv[m] = __ldg(static_cast<const float *>(x) + mm * H + h);
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < EB; ++e) wv[e] = __ldg(wr + int64_t(e0 + (e < eb ? e : 0)) * H + h);
+#pragma unroll
+    for (int m = 0; m < MB; ++m)
+#pragma unroll
+      for (int e = 0; e < EB; ++e) acc[m][e] = __fmaf_rn(xv[m], wv[e], acc[m][e]);
+  }
+
+  // Level 1: t = (P0 + P1) + (P2 + P3) inside each group of 4 lanes.
+#pragma unroll
+  for (int m = 0; m < MB; ++m)
+#pragma unroll
+    for (int e = 0; e < EB; ++e) {
+      float v = acc[m][e];
+      v = __fadd_rn(v, __shfl_xor_sync(0xFFFFFFFFu, v, 1));
+      v = __fadd_rn(v, __shfl_xor_sync(0xFFFFFFFFu, v, 2));
+      acc[m][e] = v;  // valid at lanes with lane % 4 == 0: t_l, l = p / 4
+    }
+  // o = 16: t_l += t_{l+16}; l in 0..15 lives in warps 0-1, l+16 in warps 2-3.
+  if (warp >= 2 && (lane & 3) == 0) {
+#pragma unroll
+    for (int m = 0; m < MB; ++m)
+#pragma unroll
+      for (int e = 0; e < EB; ++e) xch[warp - 2][lane][m * EB + e] = acc[m][e];
+  }
+  __syncthreads();
+  if (warp < 2 && (lane & 3) == 0) {
+#pragma unroll
+    for (int m = 0; m < MB; ++m)
+#pragma unroll
+      for (int e = 0; e < EB; ++e) acc[m][e] = __fadd_rn(acc[m][e], xch[warp][lane][m * EB + e]);
+  }
+  __syncthreads();
+  // o = 8: t_l += t_{l+8}; l in 0..7 is warp 0, l+8 is warp 1.
+  if (warp == 1 && (lane & 3) == 0) {
+#pragma unroll
+    for (int m = 0; m < MB; ++m)
+#pragma unroll
+      for (int e = 0; e < EB; ++e) xch[0][lane][m * EB + e] = acc[m][e];
+  }
+  __syncthreads();
+  if (warp == 0) {
+#pragma unroll
+    for (int m = 0; m < MB; ++m)
+#pragma unroll
+      for (int e = 0; e < EB; ++e) {
+        float v = acc[m][e];
+        if ((lane & 3) == 0) v = __fadd_rn(v, xch[0][lane][m * EB + e]);
+        // o = 4, 2, 1 <-> lanes 4l and 4(l+o): xor 16, 8, 4.
+        v = __fadd_rn(v, __shfl_xor_sync(0xFFFFFFFFu, v, 16));
+        v = __fadd_rn(v, __shfl_xor_sync(0xFFFFFFFFu, v, 8));
+        v = __fadd_rn(v, __shfl_xor_sync(0xFFFFFFFFu, v, 4));
+        if (lane == 0 && m < mb && e < eb) {
+          if (bias) v = __fadd_rn(v, bias[e0 + e]);
+          logits[(m0 + m) * E + e0 + e] = v;
+        }
+      }
+  }
+}
+
+// a beats b: larger logit, or equal logit and lower index.
+__device__ __forceinline__ bool beats(float la, int a, float lb, int b) {
+  return la > lb || (la == lb && a < b);
+}
+
+// One warp per token: top-k by repeated warp arg-max, then the weights as a
+// softmax over the selected logits (equal to the full softmax renormalised
+// over the selection), expert histogram by atomics.
+template <int EPL>  // logits per lane = ceil(E / 32)
+__global__ void __launch_bounds__(256) router_topk_kernel(const float *__restrict__ logits,
+                                                          int64_t M, int E, int k,
+                                                          int32_t *__restrict__ idx,
+                                                          float *__restrict__ w,
+                                                          int32_t *__restrict__ counts) {
+  const int lane = threadIdx.x & 31;
+  const int64_t m = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  if (m >= M) return;
+  float v[EPL];
+#pragma unroll
+  for (int t = 0; t < EPL; ++t) {
+    const int e = lane + 32 * t;
+    v[t] = e < E ? logits[m * E + e] : 0.0f;
+  }
+  uint32_t taken = 0;  // bit t: expert lane + 32t already selected
+  float sel_l[kMaxK];
+  int sel_e[kMaxK];
+  for (int i = 0; i < k; ++i) {
+    float bl = 0.0f;
+    int be = -1;
+#pragma unroll
+    for (int t = 0; t < EPL; ++t) {
+      const int e = lane + 32 * t;
+      if (e < E && !((taken >> t) & 1u) && (be < 0 || beats(v[t], e, bl, be))) {
+        bl = v[t];
+        be = e;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) {
+      const float ol = __shfl_xor_sync(0xFFFFFFFFu, bl, o);
+      const int oe = __shfl_xor_sync(0xFFFFFFFFu, be, o);
+      if (oe >= 0 && (be < 0 || beats(ol, oe, bl, be))) {
+        bl = ol;
+        be = oe;
+      }
+    }
+    sel_l[i] = bl;
+    sel_e[i] = be;
+    if ((be & 31) == lane) taken |= 1u << (be >> 5);
+  }
+  if (lane == 0) {
+    const float mx = sel_l[0];
+    float z = 0.0f;
+    float ex[kMaxK];
+    for (int i = 0; i < k; ++i) {
+      ex[i] = expf(sel_l[i] - mx);
+      z += ex[i];
+    }
+    for (int i = 0; i < k; ++i) {
+      idx[m * k + i] = sel_e[i];
+      w[m * k + i] = ex[i] / z;
+      if (counts) atomicAdd(counts + sel_e[i], 1);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Grouping by expert (one block): counts, exclusive offsets, the ascending
+// list of experts with tokens, and the assignments a = m*k + i sorted by
+// (expert, a) -- a stable counting sort, so the layout is deterministic.
+__global__ void __launch_bounds__(1024) moe_dispatch_kernel(const int32_t *__restrict__ idx,
+                                                            int64_t MK, int E, MoeWork ws,
+                                                            uint32_t *status) {
+  extern __shared__ int32_t sm[];
+  int32_t *cnt = sm;                 // [E]
+  int32_t *cursor = sm + E;          // [E]
+  int32_t *wcnt = sm + 2 * E;        // [32][E] per-warp counts of the current chunk
+  __shared__ int32_t warp_c[32], warp_f[32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int nthreads = blockDim.x;
+  const int nwarps = nthreads >> 5;
+
+  for (int e = tid; e < E; e += nthreads) cnt[e] = 0;
+  __syncthreads();
+  for (int64_t a = tid; a < MK; a += nthreads) {
+    const int e = idx[a];
+    if (e >= 0 && e < E) {
+      atomicAdd(cnt + e, 1);
+    } else {
+      atomicOr(status, kDevBadExpert);
+    }
+  }
+  __syncthreads();
+  // Exclusive scan of counts (E <= blockDim: one element per thread) and of
+  // the "has tokens" flags for the active-expert list.
+  {
+    const int e = tid;
+    const int c = (e < E) ? cnt[e] : 0;
+    const int f = c > 0 ? 1 : 0;
+    int sc = c, sf = f;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int yc = __shfl_up_sync(0xFFFFFFFFu, sc, o);
+      const int yf = __shfl_up_sync(0xFFFFFFFFu, sf, o);
+      if (lane >= o) {
+        sc += yc;
+        sf += yf;
+      }
+    }
+    if (lane == 31) {
+      warp_c[warp] = sc;
+      warp_f[warp] = sf;
+    }
+    __syncthreads();
+    if (warp == 0) {
+      int tc = lane < nwarps ? warp_c[lane] : 0;
+      int tf = lane < nwarps ? warp_f[lane] : 0;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int yc = __shfl_up_sync(0xFFFFFFFFu, tc, o);
+        const int yf = __shfl_up_sync(0xFFFFFFFFu, tf, o);
+        if (lane >= o) {
+          tc += yc;
+          tf += yf;
+        }
+      }
+      if (lane < nwarps) {  // inclusive over warps
+        warp_c[lane] = tc;
+        warp_f[lane] = tf;
+      }
+    }
+    __syncthreads();
+    const int exc = (warp > 0 ? warp_c[warp - 1] : 0) + sc - c;
+    const int exf = (warp > 0 ? warp_f[warp - 1] : 0) + sf - f;
+    if (e < E) {
+      ws.offsets[e] = exc;
+      cursor[e] = exc;
+      if (f) ws.active[exf] = e;
+      ws.counts[e] = c;
+    }
+    if (e == E - 1) {
+      ws.offsets[E] = exc + c;
+      *ws.num_active = exf + f;
+    }
+  }
+  __syncthreads();
+  // Stable placement, chunk by chunk in assignment order.
+  for (int64_t base = 0; base < MK; base += nthreads) {
+    for (int i = tid; i < nwarps * E; i += nthreads) wcnt[i] = 0;
+    __syncthreads();
+    const int64_t a = base + tid;
+    int e = -1;
+    if (a < MK) {
+      e = idx[a];
+      if (e < 0 || e >= E) e = -1;
+    }
+    const uint32_t peers = __match_any_sync(0xFFFFFFFFu, e);
+    const int rank = __popc(peers & ((1u << lane) - 1u));
+    if (e >= 0 && rank == 0) wcnt[warp * E + e] = __popc(peers);
+    __syncthreads();
+    for (int ee = tid; ee < E; ee += nthreads) {
+      int run = 0;
+      for (int w2 = 0; w2 < nwarps; ++w2) {
+        const int t = wcnt[w2 * E + ee];
+        wcnt[w2 * E + ee] = run;
+        run += t;
+      }
+      wcnt[nwarps * E + ee] = run;  // chunk total (scratch row)
+    }
+    __syncthreads();
+    if (e >= 0) {
+      const int p = cursor[e] + wcnt[warp * E + e] + rank;
+      ws.assign[p] = static_cast<int32_t>(a);
+      ws.pos[a] = p;
+    } else if (a < MK) {
+      ws.pos[a] = -1;
+    }
+    __syncthreads();
+    for (int ee = tid; ee < E; ee += nthreads) cursor[ee] += wcnt[nwarps * E + ee];
+    __syncthreads();
+  }
+}
+
+// y[m, n] = sum_{i<k} w[m, i] * out[pos(m, i), n], slot order, fp32.
+template <bool YBF16>
+__global__ void __launch_bounds__(256) moe_combine_kernel(int64_t M, int k, int64_t H,
+                                                          const float *__restrict__ tw,
+                                                          const int32_t *__restrict__ pos,
+                                                          const float *__restrict__ out,
+                                                          void *__restrict__ y) {
+  const int64_t H4 = H / 4;
+  const int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (t >= M * H4) return;
+  const int64_t m = t / H4, n4 = t % H4;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int i = 0; i < k; ++i) {
+    const int p = pos[m * k + i];
+    if (p < 0) continue;
+    const float wi = tw[m * k + i];
+    const float4 o = ldg_f4(out + int64_t(p) * H + 4 * n4);
+    acc.x = fmaf(wi, o.x, acc.x);
+    acc.y = fmaf(wi, o.y, acc.y);
+    acc.z = fmaf(wi, o.z, acc.z);
+    acc.w = fmaf(wi, o.w, acc.w);
+  }
+  if constexpr (YBF16) {
+    __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
+    __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
+    uint2 v;
+    v.x = *reinterpret_cast<uint32_t *>(&lo);
+    v.y = *reinterpret_cast<uint32_t *>(&hi);
+    reinterpret_cast<uint2 *>(y)[m * H4 + n4] = v;
+  } else {
+    reinterpret_cast<float4 *>(y)[m * H4 + n4] = acc;
+  }
+}
+
+template <int MB, int EB, bool XBF16>
+cudaError_t run_logits(const void *x, int64_t M, int64_t H, const float *wr, const float *bias,
+                       int E, float *logits, cudaStream_t s) {
+  dim3 grid((E + EB - 1) / EB, static_cast<unsigned>((M + MB - 1) / MB));
+  router_logits_kernel<MB, EB, XBF16><<<grid, 128, 0, s>>>(x, M, H, wr, bias, E, logits);
+  count_launch();
+  return cudaGetLastError();
+}
+
+template <int EPL>
+cudaError_t run_topk(const float *logits, int64_t M, int E, int k, int32_t *idx, float *w,
+                     int32_t *counts, cudaStream_t s) {
+  const int64_t threads = M * 32;
+  router_topk_kernel<EPL><<<static_cast<unsigned>((threads + 255) / 256), 256, 0, s>>>(
+      logits, M, E, k, idx, w, counts);
+  count_launch();
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t router_logits_bytes(int64_t M, int E) { return static_cast<size_t>(M) * E * 4; }
+
+cudaError_t launch_router(const void *x, bool x_bf16, int64_t M, int64_t H, const float *wr,
+                          const float *bias, int E, int k, float *logits, int32_t *idx,
+                          float *w, int32_t *counts, cudaStream_t s) {
+  cudaError_t err;
+  // Small batches: fewer experts per block so that the 4 MB router matrix is
+  // spread over more SMs.
+  if (M <= 64) {
+    err = x_bf16 ? run_logits<8, 2, true>(x, M, H, wr, bias, E, logits, s)
+                 : run_logits<8, 2, false>(x, M, H, wr, bias, E, logits, s);
+  } else {
+    err = x_bf16 ? run_logits<8, 8, true>(x, M, H, wr, bias, E, logits, s)
+                 : run_logits<8, 8, false>(x, M, H, wr, bias, E, logits, s);
+  }
+  if (err != cudaSuccess) return err;
+  if (counts) {
+    err = cudaMemsetAsync(counts, 0, sizeof(int32_t) * E, s);
+    if (err != cudaSuccess) return err;
+  }
+  const int epl = (E + 31) / 32;
+  if (epl <= 1) return run_topk<1>(logits, M, E, k, idx, w, counts, s);
+  if (epl <= 2) return run_topk<2>(logits, M, E, k, idx, w, counts, s);
+  if (epl <= 4) return run_topk<4>(logits, M, E, k, idx, w, counts, s);
+  if (epl <= 8) return run_topk<8>(logits, M, E, k, idx, w, counts, s);
+  if (epl <= 16) return run_topk<16>(logits, M, E, k, idx, w, counts, s);
+  return run_topk<32>(logits, M, E, k, idx, w, counts, s);
+}
+
+size_t moe_dispatch_smem(int E) {
+  // cnt + cursor + (32 warps + 1 total row) x E
+  return static_cast<size_t>(2 * E + 33 * E) * sizeof(int32_t);
+}
+
+cudaError_t launch_moe_dispatch(const int32_t *idx, int64_t M, int k, int E, const MoeWork &ws,
+                                cudaStream_t s) {
+  const int64_t MK = M * k;
+  int threads = 1024;
+  if (MK < 1024) threads = static_cast<int>(((MK + 31) / 32) * 32);
+  if (threads < E) threads = ((E + 31) / 32) * 32;  // the scan needs one thread per expert
+  if (threads > 1024) return cudaErrorInvalidValue;
+  const size_t smem = static_cast<size_t>(2 * E + (threads / 32 + 1) * E) * sizeof(int32_t);
+  cudaError_t err = cudaFuncSetAttribute(moe_dispatch_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(moe_dispatch_smem(E)));
+  if (err != cudaSuccess) return err;
+  moe_dispatch_kernel<<<1, threads, smem, s>>>(idx, MK, E, ws, device_status());
+  count_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_moe_combine(int64_t M, int k, int64_t H, const float *topk_w,
+                               const MoeWork &ws, void *y, bool y_bf16, cudaStream_t s) {
+  const int64_t threads = M * (H / 4);
+  const unsigned blocks = static_cast<unsigned>((threads + 255) / 256);
+  if (y_bf16)
+    moe_combine_kernel<true><<<blocks, 256, 0, s>>>(M, k, H, topk_w, ws.pos, ws.out, y);
+  else
+    moe_combine_kernel<false><<<blocks, 256, 0, s>>>(M, k, H, topk_w, ws.pos, ws.out, y);
+  count_launch();
+  return cudaGetLastError();
+}
+
+}  // namespace qmm

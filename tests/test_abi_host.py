@@ -1,0 +1,191 @@
+"""Host-side checks of the C ABI (no GPU needed): the library loads, exports
+every entry point include/qmm.h declares, and rejects bad arguments with the
+documented status codes before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import group_quantized_moe_gb300 as q
+from group_quantized_moe_gb300 import build_lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "qmm.h")
+
+# Fake, 256-byte aligned addresses: every call below must fail validation on
+# the host, so these are never dereferenced.
+P = 0x7F0000000000
+P2 = P + 0x100000
+
+
+@pytest.fixture(scope="module")
+def L():
+    build_lib.build()
+    return q.lib()
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^[A-Za-z_][\w \*]*?\b(\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_entry_points_exported(L):
+    names = _declared_functions()
+    for n in ("qmm_quantize_groupwise", "qmm_linear", "moe_route_topk", "moe_ffn_forward"):
+        assert n in names
+    for n in names:
+        assert hasattr(L, n), f"{n} declared in qmm.h but not exported"
+    assert set(names) == set(q.EXPORTED)
+
+
+def test_launch_count_starts_readable(L):
+    assert q.qmm_launch_count() >= 0
+
+
+def _w(bits=8, group=64, N=128, K=256, codes=P, scales=P, zps=P):
+    return q._Weight(bits, group, N, K, codes, scales, zps)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(bits=5), q.QMM_ERR_INVALID_ARG),
+    (dict(group=48), q.QMM_ERR_UNSUPPORTED),
+    (dict(group=16), q.QMM_ERR_UNSUPPORTED),
+    (dict(K=200), q.QMM_ERR_SHAPE),
+    (dict(K=0), q.QMM_ERR_SHAPE),
+    (dict(N=-1), q.QMM_ERR_SHAPE),
+    (dict(codes=None), q.QMM_ERR_INVALID_ARG),
+    (dict(scales=P + 4), q.QMM_ERR_ALIGN),
+    (dict(codes=P + 8), q.QMM_ERR_ALIGN),
+    (dict(K=32768, group=256), q.QMM_ERR_UNSUPPORTED),
+])
+def test_linear_rejects(L, kw, code):
+    w = _w(**kw)
+    rc = L.qmm_linear(P2, q.QMM_F32, 1, ctypes.byref(w), P2, None)
+    assert rc == code, q.qmm_last_error()
+    assert q.qmm_last_error()
+
+
+def test_linear_rejects_bad_dtype_and_x(L):
+    w = _w()
+    assert L.qmm_linear(P2, 7, 1, ctypes.byref(w), P2, None) == q.QMM_ERR_INVALID_ARG
+    assert L.qmm_linear(P2 + 4, q.QMM_F32, 1, ctypes.byref(w), P2, None) == q.QMM_ERR_ALIGN
+    assert L.qmm_linear(None, q.QMM_F32, 1, ctypes.byref(w), P2, None) == q.QMM_ERR_INVALID_ARG
+    assert L.qmm_linear(P2, q.QMM_F32, 1, None, P2, None) == q.QMM_ERR_INVALID_ARG
+    assert L.qmm_linear(P2, q.QMM_F32, -1, ctypes.byref(w), P2, None) == q.QMM_ERR_SHAPE
+
+
+def test_linear_empty_is_noop(L):
+    w = _w()
+    assert L.qmm_linear(None, q.QMM_F32, 0, ctypes.byref(w), None, None) == q.QMM_OK
+    w0 = _w(N=0)
+    assert L.qmm_linear(None, q.QMM_F32, 3, ctypes.byref(w0), None, None) == q.QMM_OK
+
+
+def test_quantize_rejects(L):
+    f = L.qmm_quantize_groupwise
+    assert f(P, 4, 256, 3, 64, P, P, P, None) == q.QMM_ERR_INVALID_ARG
+    assert f(P, 4, 250, 8, 64, P, P, P, None) == q.QMM_ERR_SHAPE
+    assert f(P, 4, 256, 8, 96, P, P, P, None) == q.QMM_ERR_UNSUPPORTED
+    assert f(None, 4, 256, 8, 64, P, P, P, None) == q.QMM_ERR_INVALID_ARG
+    assert f(P + 4, 4, 256, 8, 64, P, P, P, None) == q.QMM_ERR_ALIGN
+    assert f(P, 4, 256, 4, 64, P, P + 8, P, None) == q.QMM_ERR_ALIGN
+    assert f(None, 0, 256, 8, 64, None, None, None, None) == q.QMM_OK  # N = 0: no-op
+
+
+def test_router_rejects(L):
+    f = L.moe_route_topk
+    ws = q.moe_route_workspace_bytes(8, 256)
+    assert ws >= 8 * 256 * 4 and ws % 256 == 0
+    ok = (P, q.QMM_F32, 8, 4096, P, None, 256, 6, P2, P2, None, P2, ws, None)
+
+    def call(**kw):
+        a = list(ok)
+        names = ["x", "dt", "M", "H", "wr", "bias", "E", "k", "idx", "w", "cnt", "ws", "wsb", "s"]
+        for k_, v in kw.items():
+            a[names.index(k_)] = v
+        return f(*a)
+
+    assert call(k=7, E=6) == q.QMM_ERR_INVALID_ARG
+    assert call(k=0) == q.QMM_ERR_INVALID_ARG
+    assert call(k=17) == q.QMM_ERR_INVALID_ARG
+    assert call(E=1025) == q.QMM_ERR_INVALID_ARG
+    assert call(H=4094) == q.QMM_ERR_SHAPE
+    assert call(dt=3) == q.QMM_ERR_INVALID_ARG
+    assert call(x=None) == q.QMM_ERR_INVALID_ARG
+    assert call(x=P + 8) == q.QMM_ERR_ALIGN
+    assert call(wsb=ws - 1) == q.QMM_ERR_WORKSPACE
+    assert call(ws=None) == q.QMM_ERR_WORKSPACE
+    assert call(ws=P2 + 16) == q.QMM_ERR_ALIGN
+    assert call(M=0, x=None, idx=None, w=None) == q.QMM_OK
+
+
+def _experts(E=8, H=256, I=128, bits=4, group=64, **over):
+    def mat(nrows, ncols, **o):
+        rows, cols = nrows, ncols
+        d = dict(bits=bits, group=group, rows=rows, cols=cols, codes=P,
+                 codes_stride=rows * cols * bits // 8, scales=P, zps=P,
+                 groups_stride=rows * cols // group)
+        d.update(o)
+        return q._ExpertWeights(d["bits"], d["group"], d["rows"], d["cols"], d["codes"],
+                                d["codes_stride"], d["scales"], d["zps"], d["groups_stride"])
+    g = mat(I, H, **over.get("gate", {}))
+    u = mat(I, H, **over.get("up", {}))
+    dn = mat(H, I, **over.get("down", {}))
+    return q._Experts(over.get("E", E), H, I, g, u, dn)
+
+
+def test_moe_workspace_bytes(L):
+    ex = _experts()
+    a = L.moe_ffn_workspace_bytes(8, 6, ctypes.byref(ex))
+    b = L.moe_ffn_workspace_bytes(16, 6, ctypes.byref(ex))
+    assert a > 0 and b > a and a % 256 == 0
+    # holds at least the per-assignment activations and outputs
+    assert a >= 8 * 6 * (128 + 256) * 4
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(E=0), q.QMM_ERR_INVALID_ARG),
+    (dict(gate=dict(rows=64)), q.QMM_ERR_SHAPE),
+    (dict(down=dict(cols=256)), q.QMM_ERR_SHAPE),
+    (dict(up=dict(bits=8)), q.QMM_ERR_UNSUPPORTED),
+    (dict(down=dict(group=128)), q.QMM_ERR_UNSUPPORTED),
+    (dict(gate=dict(codes=None)), q.QMM_ERR_INVALID_ARG),
+    (dict(gate=dict(codes_stride=8)), q.QMM_ERR_ALIGN),
+    (dict(up=dict(scales=P + 4)), q.QMM_ERR_ALIGN),
+])
+def test_moe_rejects_experts(L, over, code):
+    ex = _experts(**over)
+    ws = 1 << 30
+    rc = L.moe_ffn_forward(P, q.QMM_F32, 8, P, P, 6, ctypes.byref(ex), P2, q.QMM_F32, P2, ws, None)
+    assert rc == code, q.qmm_last_error()
+
+
+def test_moe_rejects_args(L):
+    ex = _experts()
+    need = L.moe_ffn_workspace_bytes(8, 6, ctypes.byref(ex))
+    f = L.moe_ffn_forward
+    assert f(P, q.QMM_F32, 8, P, P, 6, ctypes.byref(ex), P2, q.QMM_F32, P2, need - 1, None) == q.QMM_ERR_WORKSPACE
+    assert f(P, q.QMM_F32, 8, P, P, 6, ctypes.byref(ex), P2, q.QMM_F32, P2 + 128, need, None) == q.QMM_ERR_ALIGN
+    assert f(P, q.QMM_F32, 8, P, P, 9, ctypes.byref(ex), P2, q.QMM_F32, P2, need, None) == q.QMM_ERR_INVALID_ARG
+    assert f(P, 5, 8, P, P, 6, ctypes.byref(ex), P2, q.QMM_F32, P2, need, None) == q.QMM_ERR_INVALID_ARG
+    assert f(P, q.QMM_F32, 8, P, P, 6, ctypes.byref(ex), P2, 9, P2, need, None) == q.QMM_ERR_INVALID_ARG
+    assert f(None, q.QMM_F32, 8, P, P, 6, ctypes.byref(ex), P2, q.QMM_F32, P2, need, None) == q.QMM_ERR_INVALID_ARG
+    assert f(P + 4, q.QMM_F32, 8, P, P, 6, ctypes.byref(ex), P2, q.QMM_F32, P2, need, None) == q.QMM_ERR_ALIGN
+    assert f(None, q.QMM_F32, 0, None, None, 6, ctypes.byref(ex), None, q.QMM_F32, None, 0, None) == q.QMM_OK
+    assert f(P, q.QMM_F32, 8, P, P, 6, None, P2, q.QMM_F32, P2, need, None) == q.QMM_ERR_INVALID_ARG
+    # rows longer than one copy slot holds
+    big = _experts(H=8192, I=128, bits=8, group=128)
+    assert f(P, q.QMM_F32, 8, P, P, 6, ctypes.byref(big), P2, q.QMM_F32, P2, 1 << 40, None) == q.QMM_ERR_UNSUPPORTED
+
+
+def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
+    """No silent fallback: a missing library is an error, not a CPU path."""
+    import importlib
+    monkeypatch.setattr(q, "LIB_PATH", str(tmp_path / "libqmm.so"))
+    monkeypatch.setattr(q, "_lib", None)
+    with pytest.raises(RuntimeError, match="missing"):
+        q.lib()
+    monkeypatch.undo()
+    importlib.reload(q)

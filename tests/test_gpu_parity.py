@@ -1,0 +1,374 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle on the
+same seeded inputs.
+
+Bars: bit-exact quantised codes, scales, zero points, router logits and
+top-k indices; routing weights within 2e-6; fp32 outputs within
+|err| <= 1e-5 * sum_k |x_k w_k| + 1e-6 (propagated through SwiGLU for the MoE
+layer); bf16 outputs within a 1e-2 relative L2 error per row with the same
+arg-max.  Full-size workloads are checked on sampled rows / tokens that the
+oracle computes one by one.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from synth import recipes
+import group_quantized_moe_gb300 as q
+from group_quantized_moe_gb300 import build_lib
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dev():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    build_lib.build()
+    q.lib()
+    d = torch.device("cuda:0")
+    torch.cuda.set_device(d)
+    q.qmm_device_status(clear=True)
+    yield d
+    assert q.qmm_device_status(clear=True) == 0
+
+
+def T(a, dev):
+    return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+
+def _codes_u8(qw):
+    return qw.codes.cpu().numpy().view(np.uint8).reshape(-1)
+
+
+def assert_quant_equal(gq, oq):
+    np.testing.assert_array_equal(_codes_u8(gq), oq.codes.reshape(-1))
+    np.testing.assert_array_equal(gq.scales.cpu().numpy().view(np.uint32),
+                                  oq.scales.view(np.uint32))
+    np.testing.assert_array_equal(gq.zps.cpu().numpy(), oq.zps)
+
+
+def assert_within(y, ref, bound, what=""):
+    y = np.asarray(y, dtype=np.float64)
+    err = np.abs(y - ref)
+    bad = err > bound
+    assert not bad.any(), (f"{what}: {bad.sum()} of {bad.size} outside tolerance; worst "
+                           f"err/bound {float((err / bound).max()):.3g}")
+
+
+def _weights(N, K, seed=0, stream=2, outl=False, sigma=0.02):
+    w = synth.normal(seed, stream, N * K, sigma).reshape(N, K)
+    if outl:
+        synth.outliers(seed, stream + 100, w.reshape(-1), 0.01, 20.0)
+    return w
+
+
+# ------------------------------------------------------------- quantise (A1)
+
+QSHAPES = [(8, 64, 128, 256, False), (8, 64, 4096, 4096, True), (4, 128, 4096, 4096, False),
+           (4, 128, 2048, 4096, False), (8, 32, 37, 96, False), (4, 256, 3, 512, True),
+           (8, 256, 1, 256, False), (4, 32, 5, 32, False), (4, 64, 64, 4096, False),
+           (8, 128, 96, 2048, False)]
+
+
+@pytest.mark.parametrize("bits,group,N,K,outl", QSHAPES)
+def test_quantize_bit_exact(dev, bits, group, N, K, outl):
+    w = _weights(N, K, outl=outl)
+    g = q.qmm_quantize_groupwise(T(w, dev), bits, group)
+    assert_quant_equal(g, oracle.quantize(w, bits, group))
+
+
+@pytest.mark.parametrize("bits", [8, 4])
+def test_quantize_degenerate_groups(dev, bits):
+    """Constant groups (zero, positive, negative), a group whose range is one
+    ulp (conversions saturate), and a mix with ordinary groups."""
+    K, group = 256, 32
+    rows = [np.zeros(K), np.full(K, 0.5), np.full(K, -3.0),
+            np.where(np.arange(K) % 2 == 0, 100.0, np.nextafter(np.float32(100.0), np.float32(200))),
+            _weights(1, K)[0]]
+    mix = _weights(1, K, stream=5)[0].copy()
+    mix[:32] = 7.25
+    mix[64:96] = 0.0
+    rows.append(mix)
+    w = np.stack(rows).astype(np.float32)
+    g = q.qmm_quantize_groupwise(T(w, dev), bits, group)
+    assert_quant_equal(g, oracle.quantize(w, bits, group))
+
+
+@pytest.mark.slow
+def test_quantize_vocab_head_sampled_rows(dev):
+    """Full INT8 g64 vocab head W[129280, 4096] (with outliers) quantised on
+    the GPU; 48 rows re-quantised by the oracle from regenerated rows."""
+    r = recipes.CFG2_VOCAB
+    w = recipes.linear_weight_rows(r)
+    g = q.qmm_quantize_groupwise(T(w, dev), r.bits, r.group)
+    del w
+    rng = np.random.default_rng(1)
+    rows = np.unique(np.concatenate([[0, 1, r.N - 1], rng.integers(0, r.N, 45)]))
+    codes = g.codes.cpu().numpy().view(np.uint8)
+    scales, zps = g.scales.cpu().numpy(), g.zps.cpu().numpy()
+    for n in rows:
+        oq = oracle.quantize(recipes.linear_weight_rows(r, int(n), 1), r.bits, r.group)
+        np.testing.assert_array_equal(codes[n], oq.codes)
+        np.testing.assert_array_equal(scales[n].view(np.uint32), oq.scales[0].view(np.uint32))
+        np.testing.assert_array_equal(zps[n], oq.zps[0])
+
+
+# -------------------------------------------------------------- linear (A2)
+
+def _linear_case(dev, bits, group, N, K, M, bf16, outl=False, stream=2):
+    w = _weights(N, K, outl=outl, stream=stream)
+    x = synth.normal(3, 1, M * K).reshape(M, K)
+    if bf16:
+        xb = synth.to_bf16(x)
+        x = synth.bf16_to_f32(xb)
+        xd = torch.from_numpy(xb.view(np.int16)).to(dev).view(torch.bfloat16)
+    else:
+        xd = T(x, dev)
+    oq = oracle.quantize(w, bits, group)
+    g = q.qmm_quantize_groupwise(T(w, dev), bits, group)
+    y = q.qmm_linear(xd, g).cpu().numpy()
+    assert_within(y, oracle.linear_fused(x, oq), oracle.linear_bound(x, oq),
+                  f"linear b{bits} g{group} N{N} K{K} M{M} bf16={bf16}")
+
+
+@pytest.mark.parametrize("bits,group,N,K,outl", [(8, 64, 128, 256, False),
+                                                 (8, 64, 4096, 4096, True),
+                                                 (4, 128, 4096, 4096, False),
+                                                 (4, 128, 2048, 4096, False)])
+def test_linear_configs(dev, bits, group, N, K, outl):
+    _linear_case(dev, bits, group, N, K, 1, False, outl)
+
+
+@pytest.mark.parametrize("bits,group,N,K", [(8, 64, 37, 256), (4, 32, 5, 64), (8, 256, 1, 512),
+                                            (4, 64, 333, 1024), (8, 32, 19, 8192),
+                                            (4, 128, 7, 16384)])
+@pytest.mark.parametrize("M", [1, 2, 3, 5])
+def test_linear_ragged(dev, bits, group, N, K, M):
+    _linear_case(dev, bits, group, N, K, M, False)
+
+
+@pytest.mark.parametrize("bits,group", [(8, 64), (4, 128)])
+@pytest.mark.parametrize("M", [1, 4, 9])
+def test_linear_bf16_activations(dev, bits, group, M):
+    _linear_case(dev, bits, group, 256, 1024, M, True)
+
+
+@pytest.mark.slow
+def test_linear_vocab_head_sampled(dev):
+    """Decode step of the INT8 g64 workload at full size: x[1, 4096] against
+    the 129280-row vocab head; 64 sampled outputs computed by the oracle."""
+    r = recipes.CFG2_VOCAB
+    x = recipes.linear_x(r)
+    w = recipes.linear_weight_rows(r)
+    g = q.qmm_quantize_groupwise(T(w, dev), r.bits, r.group)
+    del w
+    y = q.qmm_linear(T(x, dev), g).cpu().numpy()[0]
+    rng = np.random.default_rng(2)
+    rows = np.unique(np.concatenate([[0, r.N - 1], rng.integers(0, r.N, 62)]))
+    for n in rows:
+        oq = oracle.quantize(recipes.linear_weight_rows(r, int(n), 1), r.bits, r.group)
+        assert_within(y[n:n + 1], oracle.linear_fused(x, oq)[0], oracle.linear_bound(x, oq)[0],
+                      f"row {n}")
+
+
+# -------------------------------------------------------------- router (A3)
+
+def _router_case(dev, M, E, H, k, bias_kind, bf16, wr=None, x=None):
+    if x is None:
+        x = synth.normal(4, 1, M * H).reshape(M, H)
+    if bf16:
+        xb = synth.to_bf16(x)
+        x = synth.bf16_to_f32(xb)
+        xd = torch.from_numpy(xb.view(np.int16)).to(dev).view(torch.bfloat16)
+    else:
+        xd = T(x, dev)
+    if wr is None:
+        wr = synth.normal(4, 10, E * H, 0.02).reshape(E, H)
+    bias = None
+    if bias_kind == "zipf":
+        bias = synth.zipf_bias(0, 20, E, 1.1)
+    ws = torch.zeros(q.moe_route_workspace_bytes(M, E), dtype=torch.uint8, device=dev)
+    idx, w, cnt = q.moe_route_topk(xd, T(wr, dev), None if bias is None else T(bias, dev), k,
+                                   workspace=ws)
+    torch.cuda.synchronize()
+    logits = oracle.router_logits(x, wr, bias)
+    glog = ws[: M * E * 4].view(torch.float32).cpu().numpy().reshape(M, E)
+    np.testing.assert_array_equal(glog.view(np.uint32), logits.view(np.uint32))
+    oidx, ow = oracle.topk(logits, k)
+    np.testing.assert_array_equal(idx.cpu().numpy(), oidx)
+    assert np.abs(w.cpu().numpy() - ow).max() <= 2e-6
+    np.testing.assert_array_equal(cnt.cpu().numpy(), np.bincount(oidx.reshape(-1), minlength=E))
+
+
+@pytest.mark.parametrize("M,E,H,k,bias,bf16", [
+    (8, 256, 4096, 6, None, False),     # MoE decode router
+    (512, 256, 4096, 6, "zipf", True),  # batched prefill router, Zipf bias
+    (1, 256, 4096, 6, None, False),
+    (3, 100, 4096, 1, "zipf", False),
+    (17, 64, 4100, 16, None, True),
+    (5, 8, 64, 3, None, False),
+    (70, 1024, 256, 8, "zipf", False),
+])
+def test_router(dev, M, E, H, k, bias, bf16):
+    _router_case(dev, M, E, H, k, bias, bf16)
+
+
+def test_router_exact_ties_lower_index_wins(dev):
+    """Duplicated router rows give bit-identical logits; the lower expert
+    index must be selected first."""
+    E, H, M = 32, 512, 6
+    wr = synth.normal(5, 10, E * H, 0.02).reshape(E, H)
+    for a, b in ((3, 17), (17, 30), (5, 6), (0, 31)):
+        wr[b] = wr[a]
+    x = synth.normal(5, 1, M * H).reshape(M, H)
+    x[:, :] = x[0]  # same token repeated
+    _router_case(dev, M, E, H, 6, None, False, wr=wr, x=x)
+    wr2 = np.tile(wr[:1], (E, 1))  # every logit equal -> experts 0..k-1
+    _router_case(dev, 2, E, H, 4, None, False, wr=wr2)
+
+
+# ----------------------------------------------------------- MoE layer (A4-A6)
+
+def _small_experts(dev, E, H, I, bits, group, seed=1):
+    def fill(which, e, out):
+        stream = {"gate": 11, "up": 12, "down": 13}[which] + 10 * e
+        out[...] = synth.normal(seed, stream, out.size, 0.05).reshape(out.shape)
+    ex = q.quantize_experts(E, H, I, bits, group, fill, device=dev)
+    og, ou, od = [], [], []
+    for e in range(E):
+        for which, lst in (("gate", og), ("up", ou), ("down", od)):
+            rows, cols = (I, H) if which != "down" else (H, I)
+            buf = np.empty((rows, cols), np.float32)
+            fill(which, e, buf)
+            lst.append(oracle.quantize(buf, bits, group))
+    return ex, og, ou, od
+
+
+def _moe_check(dev, x, xd, idx, w, ex, og, ou, od, y_dtype=torch.float32, what=""):
+    y = q.moe_ffn_forward(xd, T(idx, dev), T(w, dev), ex, y_dtype=y_dtype)
+    y = y.float().cpu().numpy().astype(np.float64)
+    yref, bound = oracle.moe_ffn(x, idx, w, og, ou, od)
+    if y_dtype == torch.float32:
+        assert_within(y, yref, bound, what)
+    else:
+        rel = np.linalg.norm(y - yref, axis=1) / np.linalg.norm(yref, axis=1)
+        assert (rel <= 1e-2).all(), (what, rel.max())
+        assert (np.argmax(y, axis=1) == np.argmax(yref, axis=1)).all()
+    return y
+
+
+@pytest.mark.parametrize("bits,group,H,I", [(4, 64, 256, 128), (8, 128, 256, 256),
+                                            (4, 32, 512, 64), (8, 64, 128, 384)])
+@pytest.mark.parametrize("bf16", [False, True])
+def test_moe_small(dev, bits, group, H, I, bf16):
+    E, k, M = 8, 2, 5
+    ex, og, ou, od = _small_experts(dev, E, H, I, bits, group)
+    x = synth.normal(6, 1, M * H).reshape(M, H)
+    if bf16:
+        xb = synth.to_bf16(x)
+        x = synth.bf16_to_f32(xb)
+        xd = torch.from_numpy(xb.view(np.int16)).to(dev).view(torch.bfloat16)
+    else:
+        xd = T(x, dev)
+    wr = synth.normal(6, 10, E * H, 0.05).reshape(E, H)
+    idx, w = oracle.topk(oracle.router_logits(x, wr, None), k)
+    _moe_check(dev, x, xd, idx, w, ex, og, ou, od, what=f"b{bits} g{group} bf16={bf16}")
+    _moe_check(dev, x, xd, idx, w, ex, og, ou, od, y_dtype=torch.bfloat16, what="bf16 out")
+
+
+def test_moe_one_hot_expert_many_tokens(dev):
+    """Every token on the same expert (a long token list, ragged last chunk),
+    plus M = 1."""
+    E, H, I = 4, 256, 128
+    ex, og, ou, od = _small_experts(dev, E, H, I, 4, 64, seed=2)
+    M = 37
+    x = synth.normal(7, 1, M * H).reshape(M, H)
+    idx = np.full((M, 1), 2, np.int32)
+    w = np.ones((M, 1), np.float32)
+    _moe_check(dev, x, T(x, dev), idx, w, ex, og, ou, od, what="one expert")
+    idx2 = np.stack([np.full(M, 2), np.arange(M) % 4], axis=1).astype(np.int32)
+    idx2[idx2[:, 1] == 2, 1] = 0
+    w2 = np.full((M, 2), 0.5, np.float32)
+    _moe_check(dev, x, T(x, dev), idx2, w2, ex, og, ou, od, what="two slots")
+    _moe_check(dev, x[:1], T(x[:1], dev), idx2[:1], w2[:1], ex, og, ou, od, what="M=1")
+
+
+def test_moe_bad_expert_index_flagged(dev):
+    """An out-of-range index sets QMM_DEV_BAD_EXPERT and contributes nothing."""
+    E, H, I = 4, 256, 128
+    ex, og, ou, od = _small_experts(dev, E, H, I, 8, 64, seed=3)
+    M = 3
+    x = synth.normal(8, 1, M * H).reshape(M, H)
+    idx = np.array([[0, 9], [1, 2], [-1, 3]], np.int32)
+    w = np.array([[0.6, 0.4], [0.5, 0.5], [0.3, 0.7]], np.float32)
+    q.qmm_device_status(clear=True)
+    y = q.moe_ffn_forward(T(x, dev), T(idx, dev), T(w, dev), ex).cpu().numpy()
+    assert q.qmm_device_status(clear=True) & q.QMM_DEV_BAD_EXPERT
+    idx_ok = np.where((idx >= 0) & (idx < E), idx, 0).astype(np.int32)
+    w_ok = np.where((idx >= 0) & (idx < E), w, 0).astype(np.float32)
+    yref, bound = oracle.moe_ffn(x, idx_ok, w_ok, og, ou, od)
+    assert_within(y, yref, bound, "bad index")
+
+
+# ----------------------------------------------- full-size MoE workloads
+
+def _full_moe(dev, r):
+    def fill(which, e, out):
+        recipes.moe_expert_rows(r, which, e, out=out)
+    ex = q.quantize_experts(r.E, r.H, r.I, r.bits, r.group, fill, device=dev)
+    return ex
+
+
+def _oracle_experts(r, needed):
+    og, ou, od = [None] * r.E, [None] * r.E, [None] * r.E
+    for e in sorted(set(int(v) for v in needed)):
+        og[e] = oracle.quantize(recipes.moe_expert_rows(r, "gate", e), r.bits, r.group)
+        ou[e] = oracle.quantize(recipes.moe_expert_rows(r, "up", e), r.bits, r.group)
+        od[e] = oracle.quantize(recipes.moe_expert_rows(r, "down", e), r.bits, r.group)
+    return og, ou, od
+
+
+@pytest.mark.slow
+def test_moe_decode_full_size(dev):
+    """MoE decode layer at full size: M=8, 256 experts INT4 g64, top-6."""
+    r = recipes.CFG4
+    x, _ = recipes.moe_x(r)
+    wr, bias = recipes.moe_router(r)
+    ex = _full_moe(dev, r)
+    idx, w, cnt = q.moe_route_topk(T(x, dev), T(wr, dev), None, r.k)
+    oidx, ow = oracle.topk(oracle.router_logits(x, wr, bias), r.k)
+    np.testing.assert_array_equal(idx.cpu().numpy(), oidx)
+    assert np.abs(w.cpu().numpy() - ow).max() <= 2e-6
+    og, ou, od = _oracle_experts(r, oidx.reshape(-1))
+    # FFN from the oracle's routing, then the whole GPU pipeline with its own
+    # routing weights (|dw| <= 2e-6 enters the bound).
+    _moe_check(dev, x, T(x, dev), oidx, ow, ex, og, ou, od, what="decode ffn")
+    y = q.moe_ffn_forward(T(x, dev), idx, w, ex).cpu().numpy()
+    yref, bound = oracle.moe_ffn(x, oidx, ow, og, ou, od, dw=2e-6)
+    assert_within(y, yref, bound, "decode pipeline")
+
+
+@pytest.mark.slow
+def test_moe_prefill_full_size_sampled(dev):
+    """Batched-prefill MoE at full size: M=512 bf16 tokens, Zipf-biased
+    routing, 256 experts INT8 g128; 4 sampled tokens through the oracle."""
+    r = recipes.CFG5
+    x, xb = recipes.moe_x(r)
+    wr, bias = recipes.moe_router(r)
+    ex = _full_moe(dev, r)
+    xd = torch.from_numpy(xb.view(np.int16)).to(dev).view(torch.bfloat16)
+    idx, w, cnt = q.moe_route_topk(xd, T(wr, dev), T(bias, dev), r.k)
+    oidx, ow = oracle.topk(oracle.router_logits(x, wr, bias), r.k)
+    np.testing.assert_array_equal(idx.cpu().numpy(), oidx)
+    assert np.abs(w.cpu().numpy() - ow).max() <= 2e-6
+    for ydt in (torch.float32, torch.bfloat16):
+        y = q.moe_ffn_forward(xd, idx, w, ex, y_dtype=ydt).float().cpu().numpy()
+        toks = np.array([0, 137, 300, 511])
+        og, ou, od = _oracle_experts(r, oidx[toks].reshape(-1))
+        yref, bound = oracle.moe_ffn(x[toks], oidx[toks], ow[toks], og, ou, od, dw=2e-6)
+        ys = y[toks].astype(np.float64)
+        rel = np.linalg.norm(ys - yref, axis=1) / np.linalg.norm(yref, axis=1)
+        assert (rel <= 1e-2).all(), rel
+        assert (np.argmax(ys, axis=1) == np.argmax(yref, axis=1)).all()
