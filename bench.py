@@ -23,6 +23,7 @@ import argparse
 import hashlib
 import json
 import os
+import shutil
 import subprocess
 import sys
 import threading
@@ -82,7 +83,10 @@ def traffic_for(kernel: str, src_files: tuple[str, ...], workload: str):
 
 
 class ClockSampler:
-    """Samples SM clocks and throttle reasons with nvidia-smi while running."""
+    """Samples SM clocks and throttle reasons with nvidia-smi (100 ms period)
+    from before the timed region until after it; summary() keeps the samples
+    taken inside the region (or the nearest one if the region is shorter than
+    the sampling period)."""
 
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -91,27 +95,31 @@ class ClockSampler:
     def __init__(self, index: int):
         self.index = index
         self.proc = None
-        self.lines: list[str] = []
+        self.samples: list[tuple[float, str]] = []
         self.thread = None
 
     def __enter__(self):
+        cmd = ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+               "--format=csv,noheader,nounits", "-lms", "100"]
+        if shutil.which("stdbuf"):
+            cmd = ["stdbuf", "-oL"] + cmd
         try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
-                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True, bufsize=1)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
+            time.sleep(0.3)  # first samples before the region starts
         except Exception:
             self.proc = None
         return self
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.samples.append((time.monotonic(), line.strip()))
 
     def __exit__(self, *a):
         if self.proc:
+            time.sleep(0.25)
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
@@ -120,25 +128,30 @@ class ClockSampler:
             if self.thread:
                 self.thread.join(timeout=2)
 
-    def summary(self):
-        sm, mx, reasons = [], None, set()
+    def summary(self, t0: float, t1: float):
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        rows = []
+        for ts, ln in self.samples:
             parts = [p.strip() for p in ln.split(",")]
             if len(parts) < 8:
                 continue
             try:
-                sm.append(float(parts[0]))
-                mx = float(parts[1])
+                rows.append((ts, float(parts[0]), float(parts[1]), parts[4:8]))
             except ValueError:
                 continue
-            for nm, v in zip(names, parts[4:8]):
+        inside = [r for r in rows if t0 - 0.05 <= r[0] <= t1 + 0.15]
+        if not inside and rows:
+            inside = [min(rows, key=lambda r: abs(r[0] - 0.5 * (t0 + t1)))]
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        reasons = set()
+        for r in inside:
+            for nm, v in zip(names, r[3]):
                 if v.lower().startswith("active"):
                     reasons.add(nm)
-        if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": 0}
-        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": mx, "reasons": sorted(reasons),
-                "samples": len(sm)}
+        return {"sm_mhz": float(np.median([r[1] for r in inside])), "sm_max_mhz": inside[-1][2],
+                "reasons": sorted(reasons), "samples": len(inside),
+                "region_s": round(t1 - t0, 3)}
 
 
 # ------------------------------------------------------------ distributed
@@ -216,11 +229,13 @@ def run_gemv(dev, steps: int, warmup: int, world: int):
     n0 = q.qmm_launch_count()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(torch.cuda.current_device()) as clk:
+        t0 = time.monotonic()
         start.record(s)
         for i in range(steps):
             step(evs[i])
         end.record(s)
         torch.cuda.synchronize()
+        t1 = time.monotonic()
     launches = q.qmm_launch_count() - n0
     dist_barrier(world)
     ms = start.elapsed_time(end) / steps
@@ -249,7 +264,7 @@ def run_gemv(dev, steps: int, warmup: int, world: int):
     b_vocab = weight_bytes(wv.N, wv.K, 8, 64)
     return {"ms": ms, "ms_e2e": ms_e2e, "bytes": b_trunk + b_vocab, "t_trunk_ms": float(t_trunk),
             "t_vocab_ms": float(t_vocab), "b_trunk": b_trunk, "b_vocab": b_vocab,
-            "launches": int(launches), "clocks": clk.summary(),
+            "launches": int(launches), "clocks": clk.summary(t0, t1),
             "h2d": xh.numel() * 4, "d2h": yh.numel() * 4}
 
 
@@ -353,11 +368,14 @@ def oracle_gemv_sample(seconds: float):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-moe", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--only", choices=["gemv", "moe_decode", "moe_prefill"], default=None,
+                    help="run one workload only (profiling)")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
     args = ap.parse_args()
     peaks = load_peaks()
     metric = "fused dequant-GEMV weight GB/s & MoE layer tokens/s, % of HBM/TC roofline"
@@ -396,6 +414,12 @@ def main():
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
 
+    if args.only in ("moe_decode", "moe_prefill"):
+        r = recipes.CFG4 if args.only == "moe_decode" else recipes.CFG5
+        mo = run_moe(dev, r, args.steps, args.warmup)
+        if rank == 0:
+            print(json.dumps({"only": args.only, **mo}))
+        return
     g = run_gemv(dev, args.steps, args.warmup, world)
     ms = dist_max(g["ms"], world)
     ms_e2e = dist_max(g["ms_e2e"], world)
@@ -421,11 +445,11 @@ def main():
             "clocks": g["clocks"],
             "e2e": {"value": world * g["bytes"] / (ms_e2e * 1e-3) / 1e9, "unit": "GB/s",
                     "h2d_bytes_per_step": g["h2d"], "d2h_bytes_per_step": g["d2h"]}}
-    if not args.no_moe:
+    if not args.no_moe and args.only is None:
         extras = {}
         for key, r in (("moe_decode", recipes.CFG4), ("moe_prefill", recipes.CFG5)):
             try:
-                mo = run_moe(dev, r, max(10, args.steps // 5), args.warmup)
+                mo = run_moe(dev, r, max(10, min(100, args.steps // 10)), args.warmup)
                 mo["hbm_frac"] = mo["weight_gbs"] / peaks["hbm_gbs"]
                 mo["tc_frac"] = mo["tflops"] / peaks["bf16_tflops_sustained"]
                 extras[key] = mo
@@ -433,11 +457,12 @@ def main():
                 extras[key] = {"error": f"{type(e).__name__}: {e}"}
             torch.cuda.empty_cache()
         line.update(extras)
-    if rank == 0:
+    if rank == 0 and not args.no_cpu:
         gbs, nbytes, spent = oracle_gemv_sample(args.cpu_seconds)
         line["cpu_baseline"] = {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
                                 "sample": f"{nbytes} weight bytes of vocab-head rows "
                                           f"(1024-row blocks), {spent:.1f} s single-thread"}
+    if rank == 0:
         print(json.dumps(line))
     if world > 1:
         import torch.distributed as dist

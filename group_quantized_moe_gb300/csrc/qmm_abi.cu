@@ -146,9 +146,9 @@ int qmm_linear(const void *x, int32_t x_dtype, int64_t M, const qmm_weight *w, f
   if ((reinterpret_cast<uintptr_t>(y) & 3u) != 0)
     return fail(QMM_ERR_ALIGN, "qmm_linear: y must be 4-byte aligned");
   const int64_t rowbytes = w->K * w->bits / 8;
-  if (rowbytes > gemv_max_rowbytes())
-    return fail(QMM_ERR_UNSUPPORTED, "qmm_linear: a weight row of %lld bytes exceeds %d",
-                static_cast<long long>(rowbytes), gemv_max_rowbytes());
+  if (gemv_rows_per_tile(rowbytes, w->K / w->group, 1) < 1)
+    return fail(QMM_ERR_UNSUPPORTED, "qmm_linear: K=%lld is longer than one weight tile holds",
+                static_cast<long long>(w->K));
   QMat q{static_cast<const uint8_t *>(w->codes), 0, w->scales, w->zps, 0, w->N, w->K,
          w->bits, w->group};
   cudaError_t e = launch_gemv(x, x_dtype == QMM_BF16, M, q, y, static_cast<cudaStream_t>(stream));
@@ -227,8 +227,8 @@ int check_experts(const moe_experts *ex) {
       return fail(QMM_ERR_INVALID_ARG, "moe_experts.%s: negative stride", names[i]);
   }
   // Gate and up rows are staged together, two per copy slot.
-  if (2 * ex->H * ex->gate.bits / 8 > gemv_max_rowbytes() ||
-      ex->I * ex->down.bits / 8 > gemv_max_rowbytes())
+  if (gemv_rows_per_tile(static_cast<int64_t>(ex->H) * ex->gate.bits / 8, ex->H / ex->gate.group, 2) < 1 ||
+      gemv_rows_per_tile(static_cast<int64_t>(ex->I) * ex->down.bits / 8, ex->I / ex->down.group, 1) < 1)
     return fail(QMM_ERR_UNSUPPORTED, "moe_experts: rows too long for the expert kernels");
   return QMM_OK;
 }

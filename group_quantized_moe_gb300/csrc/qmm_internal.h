@@ -69,8 +69,9 @@ cudaError_t launch_moe_combine(int64_t M, int k, int64_t H, const float *topk_w,
 }  // namespace qmm
 
 namespace qmm {
-// Longest weight row (bytes) one copy slot of the CUDA-core kernels holds.
-int gemv_max_rowbytes();
+// Rows of `copies` matrices (row = `rowbytes` of codes + G groups) one copy
+// slot of the CUDA-core kernels holds per tile; 0 if a row does not fit.
+int gemv_rows_per_tile(int64_t rowbytes, int64_t G, int copies);
 // Bytes of router logits for M tokens and E experts.
 size_t router_logits_bytes(int64_t M, int E);
 }  // namespace qmm
