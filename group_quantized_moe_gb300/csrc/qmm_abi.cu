@@ -219,6 +219,10 @@ int check_experts(const moe_experts *ex) {
       return fail(QMM_ERR_UNSUPPORTED, "moe_experts: gate, up and down must share bits and group");
     if (!m[i]->codes || !m[i]->scales || !m[i]->zps)
       return fail(QMM_ERR_INVALID_ARG, "moe_experts.%s: null pointer", names[i]);
+    if ((cols / m[i]->group) % 4 != 0)
+      return fail(QMM_ERR_UNSUPPORTED,
+                  "moe_experts.%s: groups per row (%lld) must be a multiple of 4", names[i],
+                  static_cast<long long>(cols / m[i]->group));
     if (!aligned16(m[i]->codes) || !aligned16(m[i]->scales) || !aligned16(m[i]->zps) ||
         m[i]->codes_stride % 16 != 0 || m[i]->groups_stride % 4 != 0)
       return fail(QMM_ERR_ALIGN, "moe_experts.%s: pointers and strides must be 16-byte aligned",

@@ -148,7 +148,8 @@ typedef struct qmm_expert_weights {
 
 /* The routed experts of one MoE layer: E experts, width H, inner width I.
  * gate and up are [I, H] per expert, down is [H, I]; all three share bits and
- * group. */
+ * group, and H / group and I / group must be multiples of 4 (each tile's
+ * scales and zero points are copied as whole 16-byte units). */
 typedef struct moe_experts {
   int32_t E;
   int32_t H, I;

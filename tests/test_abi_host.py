@@ -14,15 +14,32 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "qmm.h")
 
 # Fake, 256-byte aligned addresses: every call below must fail validation on
-# the host, so these are never dereferenced.
+# the host, so these are never dereferenced.  As a second line of defence the
+# fake-pointer tests run only where no CUDA device is visible: a case that
+# wrongly passed validation must never reach a kernel launch on a real GPU.
 P = 0x7F0000000000
 P2 = P + 0x100000
+
+
+def _gpu_visible() -> bool:
+    try:
+        import torch
+        return torch.cuda.is_available()
+    except Exception:
+        return False
 
 
 @pytest.fixture(scope="module")
 def L():
     build_lib.build()
     return q.lib()
+
+
+@pytest.fixture
+def Lfake(L):
+    if _gpu_visible():
+        pytest.skip("fake device pointers are only passed where no GPU is visible")
+    return L
 
 
 def _declared_functions():
@@ -60,14 +77,16 @@ def _w(bits=8, group=64, N=128, K=256, codes=P, scales=P, zps=P):
     (dict(codes=P + 8), q.QMM_ERR_ALIGN),
     (dict(K=32768, group=256), q.QMM_ERR_UNSUPPORTED),
 ])
-def test_linear_rejects(L, kw, code):
+def test_linear_rejects(Lfake, kw, code):
+    L = Lfake
     w = _w(**kw)
     rc = L.qmm_linear(P2, q.QMM_F32, 1, ctypes.byref(w), P2, None)
     assert rc == code, q.qmm_last_error()
     assert q.qmm_last_error()
 
 
-def test_linear_rejects_bad_dtype_and_x(L):
+def test_linear_rejects_bad_dtype_and_x(Lfake):
+    L = Lfake
     w = _w()
     assert L.qmm_linear(P2, 7, 1, ctypes.byref(w), P2, None) == q.QMM_ERR_INVALID_ARG
     assert L.qmm_linear(P2 + 4, q.QMM_F32, 1, ctypes.byref(w), P2, None) == q.QMM_ERR_ALIGN
@@ -76,14 +95,16 @@ def test_linear_rejects_bad_dtype_and_x(L):
     assert L.qmm_linear(P2, q.QMM_F32, -1, ctypes.byref(w), P2, None) == q.QMM_ERR_SHAPE
 
 
-def test_linear_empty_is_noop(L):
+def test_linear_empty_is_noop(Lfake):
+    L = Lfake
     w = _w()
     assert L.qmm_linear(None, q.QMM_F32, 0, ctypes.byref(w), None, None) == q.QMM_OK
     w0 = _w(N=0)
     assert L.qmm_linear(None, q.QMM_F32, 3, ctypes.byref(w0), None, None) == q.QMM_OK
 
 
-def test_quantize_rejects(L):
+def test_quantize_rejects(Lfake):
+    L = Lfake
     f = L.qmm_quantize_groupwise
     assert f(P, 4, 256, 3, 64, P, P, P, None) == q.QMM_ERR_INVALID_ARG
     assert f(P, 4, 250, 8, 64, P, P, P, None) == q.QMM_ERR_SHAPE
@@ -94,7 +115,8 @@ def test_quantize_rejects(L):
     assert f(None, 0, 256, 8, 64, None, None, None, None) == q.QMM_OK  # N = 0: no-op
 
 
-def test_router_rejects(L):
+def test_router_rejects(Lfake):
+    L = Lfake
     f = L.moe_route_topk
     ws = q.moe_route_workspace_bytes(8, 256)
     assert ws >= 8 * 256 * 4 and ws % 256 == 0
@@ -121,7 +143,7 @@ def test_router_rejects(L):
     assert call(M=0, x=None, idx=None, w=None) == q.QMM_OK
 
 
-def _experts(E=8, H=256, I=128, bits=4, group=64, **over):
+def _experts(E=8, H=256, I=256, bits=4, group=64, **over):
     def mat(nrows, ncols, **o):
         rows, cols = nrows, ncols
         d = dict(bits=bits, group=group, rows=rows, cols=cols, codes=P,
@@ -142,27 +164,30 @@ def test_moe_workspace_bytes(L):
     b = L.moe_ffn_workspace_bytes(16, 6, ctypes.byref(ex))
     assert a > 0 and b > a and a % 256 == 0
     # holds at least the per-assignment activations and outputs
-    assert a >= 8 * 6 * (128 + 256) * 4
+    assert a >= 8 * 6 * (256 + 256) * 4
 
 
 @pytest.mark.parametrize("over,code", [
     (dict(E=0), q.QMM_ERR_INVALID_ARG),
     (dict(gate=dict(rows=64)), q.QMM_ERR_SHAPE),
-    (dict(down=dict(cols=256)), q.QMM_ERR_SHAPE),
+    (dict(gate=dict(cols=128), up=dict(cols=128), down=dict(rows=128)), q.QMM_ERR_SHAPE),
+    (dict(down=dict(cols=512)), q.QMM_ERR_SHAPE),
     (dict(up=dict(bits=8)), q.QMM_ERR_UNSUPPORTED),
     (dict(down=dict(group=128)), q.QMM_ERR_UNSUPPORTED),
     (dict(gate=dict(codes=None)), q.QMM_ERR_INVALID_ARG),
     (dict(gate=dict(codes_stride=8)), q.QMM_ERR_ALIGN),
     (dict(up=dict(scales=P + 4)), q.QMM_ERR_ALIGN),
 ])
-def test_moe_rejects_experts(L, over, code):
+def test_moe_rejects_experts(Lfake, over, code):
+    L = Lfake
     ex = _experts(**over)
     ws = 1 << 30
     rc = L.moe_ffn_forward(P, q.QMM_F32, 8, P, P, 6, ctypes.byref(ex), P2, q.QMM_F32, P2, ws, None)
     assert rc == code, q.qmm_last_error()
 
 
-def test_moe_rejects_args(L):
+def test_moe_rejects_args(Lfake):
+    L = Lfake
     ex = _experts()
     need = L.moe_ffn_workspace_bytes(8, 6, ctypes.byref(ex))
     f = L.moe_ffn_forward
@@ -175,8 +200,11 @@ def test_moe_rejects_args(L):
     assert f(P + 4, q.QMM_F32, 8, P, P, 6, ctypes.byref(ex), P2, q.QMM_F32, P2, need, None) == q.QMM_ERR_ALIGN
     assert f(None, q.QMM_F32, 0, None, None, 6, ctypes.byref(ex), None, q.QMM_F32, None, 0, None) == q.QMM_OK
     assert f(P, q.QMM_F32, 8, P, P, 6, None, P2, q.QMM_F32, P2, need, None) == q.QMM_ERR_INVALID_ARG
+    # groups per row not a multiple of 4
+    odd = _experts(H=256, I=128, bits=4, group=64)
+    assert f(P, q.QMM_F32, 8, P, P, 6, ctypes.byref(odd), P2, q.QMM_F32, P2, 1 << 40, None) == q.QMM_ERR_UNSUPPORTED
     # rows longer than one copy slot holds
-    big = _experts(H=8192, I=128, bits=8, group=128)
+    big = _experts(H=8192, I=512, bits=8, group=128)
     assert f(P, q.QMM_F32, 8, P, P, 6, ctypes.byref(big), P2, q.QMM_F32, P2, 1 << 40, None) == q.QMM_ERR_UNSUPPORTED
 
 
