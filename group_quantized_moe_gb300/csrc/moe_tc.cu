@@ -1,0 +1,657 @@
+// moe_tc.cu -- routed experts on the 5th-generation tensor cores (tcgen05)
+// for batched prefill: grouped GEMMs over the experts' token lists with the
+// weights dequantised on the fly.
+//
+// "Why I hand-wrote a DeepSeek inference engine in pure C", section 3.5:
+// tokens routed to the same expert are gathered so that the expert's weights
+// are read once for all of them; section 3.2: dequantise (q - zp) * scale
+// inside the matmul instead of materialising the weights.  "I ran a
+// 284B-parameter LLM from 3.2GB of RAM in plain C" names batched prefill with
+// expert reuse as the missing piece.
+//
+// Formulation (per expert e with tokens T_e, features tiled by 128):
+//   D[f, t] = sum_k W_e[f, k] * X[t, k]       (swap-AB: features on the MMA M
+//                                               side, tokens on N = 16..128)
+//   gate/up: D_g, D_u in TMEM, epilogue h = silu(D_g) * D_u -> fp16 [tok, I]
+//   down:    D_d in TMEM, epilogue -> fp32 out[tok, H]
+//
+// CTA = 7 warps, one CTA per SM, persistent over work items
+// (token tile of an expert, 128-feature tile):
+//   warp 4 (one lane): TMA producer of weight codes [128 rows x 64 K] into a
+//     deep ring (64B swizzle for INT8).
+//   warp 6 (one lane): TMA producer of token rows [16 x 64 K] fp16 into the
+//     B stages (128B swizzle, the canonical K-major operand layout).
+//   warps 0-3 (128 threads, thread = weight row): dequantise the stage's codes
+//     to fp16, (q - zp) * s computed exactly up to the final fp16 rounding,
+//     and store them as the K-major 128B-swizzled A operand; after the last
+//     stage of an item they run the epilogue (tcgen05.ld from TMEM).
+//   warp 5: allocates TMEM; one lane issues tcgen05.mma (kind::f16, fp32
+//     accumulate) and tcgen05.commit.
+// Every wait is bounded; on a timeout the CTA raises QMM_DEV_WAIT_TIMEOUT,
+// stops issuing work, waits (bounded) for what is in flight, frees its TMEM
+// and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "qmm_device.cuh"
+#include "qmm_internal.h"
+
+namespace qmm {
+namespace {
+
+constexpr int kBM = 128;        // weight rows per tile (MMA M)
+constexpr int kBN = 128;        // max tokens per tile (MMA N)
+constexpr int kBK = 64;         // K per stage
+constexpr int kThreads = 224;
+constexpr int kATile = kBM * kBK * 2;   // 16 KB fp16, 128B-swizzled K-major
+constexpr int kBTile = kBN * kBK * 2;   // 16 KB fp16
+constexpr int kCTile = kBM * kBK;       // 8 KB INT8 codes (64B swizzle)
+
+template <int NT>
+struct Ring;  // NT = weight tiles sharing one token tile (2: gate+up, 1: down)
+template <>
+struct Ring<2> {
+  static constexpr int kAB = 2, kC = 6;
+};
+template <>
+struct Ring<1> {
+  static constexpr int kAB = 3, kC = 8;
+};
+
+template <int NT>
+struct Smem {
+  static constexpr int kAB = Ring<NT>::kAB, kC = Ring<NT>::kC;
+  static constexpr int a_off = 0;
+  static constexpr int b_off = a_off + kAB * NT * kATile;
+  static constexpr int c_off = b_off + kAB * kBTile;
+  static constexpr int bar_off = c_off + kC * NT * kCTile;
+  // barriers: c_full[kC], c_free[kC], b_full[kAB], a_full[kAB], ab_free[kAB],
+  // acc_full, acc_free
+  static constexpr int nbar = 2 * kC + 3 * kAB + 2;
+  static constexpr int misc_off = bar_off + nbar * 8;
+  static constexpr int meta_off = misc_off + 16;  // offsets[E+1], tile_start[E+1]
+  static constexpr int bytes_for(int E) { return meta_off + 8 * (E + 1) + 1024; }
+};
+
+struct TcArgs {
+  int E, k;
+  int64_t rows;          // weight rows per expert (I for gate/up, H for down)
+  int64_t K;             // reduction length (H for gate/up, I for down)
+  int G;                 // groups per row
+  int group_shift;
+  const float *sc[2];    // scales of the NT matrices (stacked)
+  const int32_t *zp[2];
+  int64_t gstride[2];    // elements between experts
+  const int32_t *offsets;      // [E + 1] token-list offsets (sorted order)
+  const int32_t *tile_start;   // [E + 1] prefix of 128-token tiles per expert
+  void *out;             // gate/up: fp16 h [MK, I]; down: fp32 out [MK, H]
+  int64_t out_ld;        // elements per output row
+  uint32_t *status;
+};
+
+// ------------------------------------------------------------ PTX wrappers
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, int x, int y,
+                                            int z, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+               "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// D[tmem] (+)= A[smem desc] * B[smem desc]^T, kind::f16, cta_group::1.
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                       uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+      : "memory");
+}
+
+// 16 consecutive fp32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Shared-memory operand descriptor: K-major, 128B swizzle, 8-row groups 1024 B
+// apart (SBO), descriptor version 1.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
+  return static_cast<uint64_t>((addr & 0x3FFFFu) >> 4) | (static_cast<uint64_t>(1) << 16) |
+         (static_cast<uint64_t>(1024 >> 4) << 32) | (static_cast<uint64_t>(1) << 46) |
+         (static_cast<uint64_t>(2) << 61);
+}
+
+// Instruction descriptor: fp16 x fp16 -> fp32, both K-major, M = 128, N.
+__device__ __forceinline__ uint32_t idesc_f16(int n) {
+  return (1u << 4) | (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(kBM >> 4) << 24);
+}
+
+// Bounded wait that also gives up at once when the CTA has aborted.
+__device__ __forceinline__ bool wait_ok(uint32_t bar, uint32_t parity, uint32_t *status,
+                                        volatile int *abort_flag) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (global_timer_ns() - t0 > kWaitLimitNs) {
+      atomicOr(status, kDevWaitTimeout);
+      *abort_flag = 1;
+      return false;
+    }
+  }
+}
+
+// Work item -> (expert, token tile, feature tile).
+struct Item {
+  int e, t0, ntok, f;
+};
+
+// s_off / s_ts: the token-list offsets and tile prefix, staged in shared
+// memory.  Items are ordered (token tile, feature tile), feature fastest.
+__device__ __forceinline__ Item decode_item(const int32_t *s_off, const int32_t *s_ts, int E,
+                                            int64_t item, int ftiles) {
+  Item it;
+  const int tau = static_cast<int>(item / ftiles);
+  it.f = static_cast<int>(item % ftiles);
+  // last expert whose first tile index is <= tau
+  int lo = 0, hi = E;  // s_ts[lo] <= tau < s_ts[hi]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (s_ts[mid] <= tau) lo = mid;
+    else hi = mid;
+  }
+  it.e = lo;
+  const int tt = tau - s_ts[lo];
+  const int base = s_off[lo];
+  const int cnt = s_off[lo + 1] - base;
+  it.t0 = base + tt * kBN;
+  it.ntok = min(kBN, cnt - tt * kBN);
+  return it;
+}
+
+__device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g)); }
+
+// INT8 codes (stored q - 128) of one 16-byte chunk -> 16 fp16 weights
+// (q - zp) * s, as two 16-byte chunks of the A operand.
+__device__ __forceinline__ void dequant16(uint4 v, __half2 mz2, __half2 s2, uint4 &o0, uint4 &o1) {
+  uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  uint32_t r[8];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t u = w[i] ^ 0x80808080u;               // q in each byte
+    const uint32_t h01 = __byte_perm(u, 0x64646464u, 0x4140u);  // {1024+q0, 1024+q1}
+    const uint32_t h23 = __byte_perm(u, 0x64646464u, 0x4342u);  // {1024+q2, 1024+q3}
+    __half2 d01 = __hsub2(*reinterpret_cast<const __half2 *>(&h01), mz2);  // exact q - zp
+    __half2 d23 = __hsub2(*reinterpret_cast<const __half2 *>(&h23), mz2);
+    d01 = __hmul2(d01, s2);
+    d23 = __hmul2(d23, s2);
+    r[2 * i] = *reinterpret_cast<uint32_t *>(&d01);
+    r[2 * i + 1] = *reinterpret_cast<uint32_t *>(&d23);
+  }
+  o0 = make_uint4(r[0], r[1], r[2], r[3]);
+  o1 = make_uint4(r[4], r[5], r[6], r[7]);
+}
+
+__device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
+  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y),
+               "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
+// NT = 2: gate/up with SwiGLU epilogue (fp16 h); NT = 1: down (fp32 out).
+template <int NT>
+__global__ void __launch_bounds__(kThreads, 1)
+    moe_tc_kernel(const __grid_constant__ CUtensorMap tm_codes0,
+                  const __grid_constant__ CUtensorMap tm_codes1,
+                  const __grid_constant__ CUtensorMap tm_x, TcArgs a) {
+  using S = Smem<NT>;
+  constexpr int kAB = S::kAB, kC = S::kC;
+  extern __shared__ uint8_t smem_raw[];
+  // 1024-byte aligned base (swizzled tiles).
+  const uint32_t raw = smem_addr(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t *gbase = smem_raw + (base - raw);
+  const uint32_t sA = base + S::a_off, sB = base + S::b_off, sC = base + S::c_off;
+  const uint32_t bar0 = base + S::bar_off;
+  auto c_full = [&](int i) { return bar0 + 8 * i; };
+  auto c_free = [&](int i) { return bar0 + 8 * (kC + i); };
+  auto b_full = [&](int i) { return bar0 + 8 * (2 * kC + i); };
+  auto a_full = [&](int i) { return bar0 + 8 * (2 * kC + kAB + i); };
+  auto ab_free = [&](int i) { return bar0 + 8 * (2 * kC + 2 * kAB + i); };
+  const uint32_t acc_full = bar0 + 8 * (2 * kC + 3 * kAB);
+  const uint32_t acc_free = acc_full + 8;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + S::misc_off);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(gbase + S::misc_off + 4);
+  int32_t *s_off = reinterpret_cast<int32_t *>(gbase + S::meta_off);
+  int32_t *s_ts = s_off + a.E + 1;
+  for (int i = threadIdx.x; i <= a.E; i += blockDim.x) {
+    s_off[i] = a.offsets[i];
+    s_ts[i] = a.tile_start[i];
+  }
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  constexpr uint32_t kTmemCols = NT == 2 ? 256 : 128;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kC; ++i) {
+      mbar_init(c_full(i), 1);
+      mbar_init(c_free(i), 128);
+    }
+    for (int i = 0; i < kAB; ++i) {
+      mbar_init(b_full(i), 1);
+      mbar_init(a_full(i), 128);
+      mbar_init(ab_free(i), 1);
+    }
+    mbar_init(acc_full, 1);
+    mbar_init(acc_free, 128);
+    *abort_flag = 0;
+    mbar_fence_init();
+  }
+  if (warp == 5) tmem_alloc(smem_addr(tmem_slot), kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  const int ftiles = static_cast<int>(a.rows / kBM);
+  const int kstages = static_cast<int>(a.K / kBK);
+  const int64_t nitems = static_cast<int64_t>(s_ts[a.E]) * ftiles;
+
+  if (warp == 4) {
+    // ------------------------------------------- TMA producer: weight codes
+    if (lane == 0) {
+      int64_t gs = 0;  // global stage counter
+      for (int64_t item = blockIdx.x; item < nitems && !*abort_flag; item += gridDim.x) {
+        const Item it = decode_item(s_off, s_ts, a.E, item, ftiles);
+        for (int kb = 0; kb < kstages; ++kb, ++gs) {
+          const int c = static_cast<int>(gs % kC);
+          const uint32_t cu = static_cast<uint32_t>(gs / kC);
+          if (!wait_ok(c_free(c), (cu & 1u) ^ 1u, a.status, abort_flag)) break;
+          mbar_arrive_expect_tx(c_full(c), NT * kCTile);
+          tma_load_3d(sC + (c * NT + 0) * kCTile, &tm_codes0, kb * kBK, it.f * kBM, it.e, c_full(c));
+          if (NT == 2)
+            tma_load_3d(sC + (c * NT + 1) * kCTile, &tm_codes1, kb * kBK, it.f * kBM, it.e,
+                        c_full(c));
+        }
+      }
+      // After an abort, wait (bounded) for the copies still landing.
+      if (*abort_flag)
+        for (int64_t j = (gs > kC ? gs - kC : 0); j < gs; ++j)
+          mbar_wait_bounded(c_full(static_cast<int>(j % kC)),
+                            static_cast<uint32_t>((j / kC) & 1), a.status);
+    }
+  } else if (warp == 6) {
+    // -------------------------------------------- TMA producer: token rows
+    if (lane == 0) {
+      int64_t gs = 0;
+      for (int64_t item = blockIdx.x; item < nitems && !*abort_flag; item += gridDim.x) {
+        const Item it = decode_item(s_off, s_ts, a.E, item, ftiles);
+        const int npad = (it.ntok + 15) & ~15;
+        for (int kb = 0; kb < kstages; ++kb, ++gs) {
+          const int s = static_cast<int>(gs % kAB);
+          const uint32_t su = static_cast<uint32_t>(gs / kAB);
+          if (!wait_ok(ab_free(s), (su & 1u) ^ 1u, a.status, abort_flag)) break;
+          mbar_arrive_expect_tx(b_full(s), npad * kBK * 2);
+          for (int r = 0; r < npad; r += 16)
+            tma_load_2d(sB + s * kBTile + r * kBK * 2, &tm_x, kb * kBK, it.t0 + r, b_full(s));
+        }
+      }
+      if (*abort_flag)
+        for (int64_t j = (gs > kAB ? gs - kAB : 0); j < gs; ++j)
+          mbar_wait_bounded(b_full(static_cast<int>(j % kAB)),
+                            static_cast<uint32_t>((j / kAB) & 1), a.status);
+    }
+  } else if (warp == 5) {
+    // ------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int64_t gs = 0;
+      uint32_t nitem_done = 0;
+      for (int64_t item = blockIdx.x; item < nitems && !*abort_flag; item += gridDim.x) {
+        const Item it = decode_item(s_off, s_ts, a.E, item, ftiles);
+        const int npad = (it.ntok + 15) & ~15;
+        const uint32_t idesc = idesc_f16(npad);
+        // the previous item's epilogue has drained the accumulators
+        if (!wait_ok(acc_free, (nitem_done & 1u) ^ 1u, a.status, abort_flag)) break;
+        tc_fence_after();
+        bool ok = true;
+        for (int kb = 0; kb < kstages; ++kb, ++gs) {
+          const int s = static_cast<int>(gs % kAB);
+          const uint32_t su = static_cast<uint32_t>(gs / kAB);
+          if (!wait_ok(a_full(s), su & 1u, a.status, abort_flag) ||
+              !wait_ok(b_full(s), su & 1u, a.status, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk) {
+            const uint64_t bdesc = smem_desc_sw128(sB + s * kBTile + kk * 32);
+#pragma unroll
+            for (int t = 0; t < NT; ++t) {
+              const uint64_t adesc = smem_desc_sw128(sA + (s * NT + t) * kATile + kk * 32);
+              tc_mma(tmem + t * kBN, adesc, bdesc, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+            }
+          }
+          tc_commit(ab_free(s));
+        }
+        if (!ok) break;
+        tc_commit(acc_full);
+        ++nitem_done;
+      }
+      // After an abort, wait (bounded) for the MMAs already committed.
+      if (*abort_flag)
+        for (int64_t j = (gs > kAB ? gs - kAB : 0); j < gs; ++j)
+          mbar_wait_bounded(ab_free(static_cast<int>(j % kAB)),
+                            static_cast<uint32_t>((j / kAB) & 1), a.status);
+    }
+  } else {
+    // ------------------------------------------ dequantisation + epilogue
+    const int row = threadIdx.x;  // 0..127: weight row of the tile
+    int64_t gs = 0;
+    uint32_t nitem_done = 0;
+    for (int64_t item = blockIdx.x; item < nitems && !*abort_flag; item += gridDim.x) {
+      const Item it = decode_item(s_off, s_ts, a.E, item, ftiles);
+      const int64_t wrow = static_cast<int64_t>(it.f) * kBM + row;
+      const float *scp[NT];
+      const int32_t *zpp[NT];
+#pragma unroll
+      for (int t = 0; t < NT; ++t) {
+        scp[t] = a.sc[t] + it.e * a.gstride[t] + wrow * a.G;
+        zpp[t] = a.zp[t] + it.e * a.gstride[t] + wrow * a.G;
+      }
+      // scale / zero point of the current group and the next one (prefetch)
+      float s_nx[NT];
+      int32_t z_nx[NT];
+      __half2 s2[NT], mz2[NT];
+#pragma unroll
+      for (int t = 0; t < NT; ++t) {
+        s_nx[t] = __ldg(scp[t]);
+        z_nx[t] = __ldg(zpp[t]);
+        s2[t] = __float2half2_rn(0.0f);
+        mz2[t] = __float2half2_rn(0.0f);
+      }
+      bool ok = true;
+      for (int kb = 0; kb < kstages; ++kb, ++gs) {
+        const int k0 = kb * kBK;
+        if ((k0 & ((1 << a.group_shift) - 1)) == 0) {  // first stage of a group
+          const int gi = k0 >> a.group_shift;
+#pragma unroll
+          for (int t = 0; t < NT; ++t) {
+            s2[t] = __float2half2_rn(s_nx[t]);
+            mz2[t] = __float2half2_rn(1024.0f + static_cast<float>(z_nx[t]));
+            if (gi + 1 < a.G) {
+              s_nx[t] = __ldg(scp[t] + gi + 1);
+              z_nx[t] = __ldg(zpp[t] + gi + 1);
+            }
+          }
+        }
+        const int c = static_cast<int>(gs % kC);
+        const uint32_t cu = static_cast<uint32_t>(gs / kC);
+        const int s = static_cast<int>(gs % kAB);
+        const uint32_t su = static_cast<uint32_t>(gs / kAB);
+        bool got = wait_ok(c_full(c), cu & 1u, a.status, abort_flag) &&
+                   wait_ok(ab_free(s), (su & 1u) ^ 1u, a.status, abort_flag);
+        if (!__all_sync(0xFFFFFFFFu, got)) {  // warp-uniform exit
+          ok = false;
+          break;
+        }
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+          // codes row `row`: 64 bytes, 16-byte chunk j stored at j ^ ((row >> 1) & 3)
+          const uint32_t crow = sC + (c * NT + t) * kCTile + row * kBK;
+          const uint32_t arow = sA + (s * NT + t) * kATile + (row >> 3) * 1024 + (row & 7) * 128;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const uint4 v = lds128(crow + ((j ^ ((row >> 1) & 3)) << 4));
+            uint4 o0, o1;
+            dequant16(v, mz2[t], s2[t], o0, o1);
+            // A row: 16-byte chunk q (K 8q..8q+7) stored at q ^ (row & 7)
+            sts128(arow + (((2 * j) ^ (row & 7)) << 4), o0);
+            sts128(arow + (((2 * j + 1) ^ (row & 7)) << 4), o1);
+          }
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(a_full(s));
+        mbar_arrive(c_free(c));
+      }
+      if (!ok) break;
+      // ---------------------------------------------------- epilogue
+      if (!__all_sync(0xFFFFFFFFu, wait_ok(acc_full, nitem_done & 1u, a.status, abort_flag)))
+        break;
+      tc_fence_after();
+      const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+      const int feat = it.f * kBM + row;
+      for (int c0 = 0; c0 < it.ntok; c0 += 16) {
+        float v0[16];
+        tmem_ld16(tmem + lane_base + c0, v0);
+        if constexpr (NT == 2) {
+          float v1[16];
+          tmem_ld16(tmem + lane_base + kBN + c0, v1);
+          __half *h = static_cast<__half *>(a.out);
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            if (c0 + j < it.ntok)
+              h[static_cast<int64_t>(it.t0 + c0 + j) * a.out_ld + feat] =
+                  __float2half_rn(silu_f(v0[j]) * v1[j]);
+        } else {
+          float *o = static_cast<float *>(a.out);
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            if (c0 + j < it.ntok) o[static_cast<int64_t>(it.t0 + c0 + j) * a.out_ld + feat] = v0[j];
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(acc_free);
+      ++nitem_done;
+    }
+  }
+
+  // Teardown (every role has drained what it issued), then free TMEM.
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// Gathers the tokens of every assignment in expert-sorted order into fp16
+// rows (bf16 -> fp16 is exact for normal fp16 magnitudes).  Only the first
+// offsets[E] slots hold assignments (slots of out-of-range expert indices are
+// left out by the grouping).
+__global__ void __launch_bounds__(256) gather_x_kernel(const uint16_t *__restrict__ x, int64_t MK,
+                                                       int k, int64_t H, int E,
+                                                       const int32_t *__restrict__ offsets,
+                                                       const int32_t *__restrict__ assign,
+                                                       __half *__restrict__ xg) {
+  const int64_t H8 = H / 8;
+  const int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (t >= MK * H8) return;
+  const int64_t p = t / H8, c = t % H8;
+  if (p >= offsets[E]) return;
+  const int tok = assign[p] / k;
+  const uint4 v = __ldg(reinterpret_cast<const uint4 *>(x + tok * H) + c);
+  uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  uint32_t o[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float lo = __uint_as_float(w[i] << 16), hi = __uint_as_float(w[i] & 0xFFFF0000u);
+    __half2 h = __floats2half2_rn(lo, hi);
+    o[i] = *reinterpret_cast<uint32_t *>(&h);
+  }
+  reinterpret_cast<uint4 *>(xg + p * H)[c] = make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// ------------------------------------------------------------------ host
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// Codes of E stacked [rows, K] INT8 matrices as a 3-D map, box [64 B, 128
+// rows, 1], 64-byte swizzle.
+bool make_codes_map(CUtensorMap *m, const QMat &w, int E) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t rowbytes = static_cast<cuuint64_t>(w.cols);  // INT8
+  cuuint64_t dims[3] = {rowbytes, static_cast<cuuint64_t>(w.rows), static_cast<cuuint64_t>(E)};
+  cuuint64_t strides[2] = {rowbytes, static_cast<cuuint64_t>(w.codes_stride)};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(kBK), static_cast<cuuint32_t>(kBM), 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t *>(w.codes), dims, strides, box,
+            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// fp16 token rows [MK, K] as a 2-D map, box [64, 16], 128-byte swizzle.
+bool make_rows_map(CUtensorMap *m, const __half *p, int64_t MK, int64_t K) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(MK)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(K * 2)};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), 16};
+  cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<__half *>(p), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int NT>
+cudaError_t run_tc(const CUtensorMap &c0, const CUtensorMap &c1, const CUtensorMap &x,
+                   const TcArgs &a, cudaStream_t s) {
+  auto k = moe_tc_kernel<NT>;
+  const int bytes = Smem<NT>::bytes_for(a.E);
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e != cudaSuccess) return e;
+  k<<<sm_count(), kThreads, bytes, s>>>(c0, c1, x, a);
+  count_launch();
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool moe_tc_supported(const QMat &gate, const QMat &down, int64_t H, int64_t I) {
+  return gate.bits == 8 && down.bits == 8 && gate.group >= 64 && H % kBM == 0 && I % kBM == 0 &&
+         H % kBK == 0 && I % kBK == 0 && encode_fn() != nullptr;
+}
+
+cudaError_t launch_moe_tc(const void *x, int64_t M, int k, int E, const QMat &gate, const QMat &up,
+                          const QMat &down, const MoeWork &ws, cudaStream_t s) {
+  const int64_t MK = M * k;
+  const int64_t H = gate.cols, I = gate.rows;
+  // 1) tokens -> fp16 rows in expert order
+  {
+    const int64_t n = MK * (H / 8);
+    gather_x_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, s>>>(
+        static_cast<const uint16_t *>(x), MK, k, H, E, ws.offsets, ws.assign, ws.xg);
+    count_launch();
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  CUtensorMap mg, mu, md, mx, mh;
+  if (!make_codes_map(&mg, gate, E) || !make_codes_map(&mu, up, E) ||
+      !make_codes_map(&md, down, E) || !make_rows_map(&mx, ws.xg, MK, H) ||
+      !make_rows_map(&mh, ws.hh, MK, I))
+    return cudaErrorInvalidValue;
+  // 2) gate + up with SwiGLU -> fp16 h
+  TcArgs a{};
+  a.E = E;
+  a.k = k;
+  a.rows = I;
+  a.K = H;
+  a.G = static_cast<int>(H / gate.group);
+  a.group_shift = 0;
+  while ((1 << a.group_shift) < gate.group) ++a.group_shift;
+  a.sc[0] = gate.scales;
+  a.zp[0] = gate.zps;
+  a.gstride[0] = gate.groups_stride;
+  a.sc[1] = up.scales;
+  a.zp[1] = up.zps;
+  a.gstride[1] = up.groups_stride;
+  a.offsets = ws.offsets;
+  a.tile_start = ws.tile_start;
+  a.out = ws.hh;
+  a.out_ld = I;
+  a.status = device_status();
+  cudaError_t e = run_tc<2>(mg, mu, mx, a, s);
+  if (e != cudaSuccess) return e;
+  // 3) down -> fp32 per-assignment outputs
+  TcArgs d = a;
+  d.rows = H;
+  d.K = I;
+  d.G = static_cast<int>(I / down.group);
+  d.group_shift = 0;
+  while ((1 << d.group_shift) < down.group) ++d.group_shift;
+  d.sc[0] = down.scales;
+  d.zp[0] = down.zps;
+  d.gstride[0] = down.groups_stride;
+  d.sc[1] = nullptr;
+  d.zp[1] = nullptr;
+  d.gstride[1] = 0;
+  d.out = ws.out;
+  d.out_ld = H;
+  return run_tc<1>(md, md, mh, d, s);
+}
+
+}  // namespace qmm

@@ -238,7 +238,7 @@ int check_experts(const moe_experts *ex) {
 }
 
 struct WsLayout {
-  size_t counts, offsets, active, num_active, assign, pos, h, out, total;
+  size_t counts, offsets, active, num_active, assign, pos, h, out, tile_start, xg, total;
 };
 
 WsLayout ws_layout(int64_t M, int k, const moe_experts *ex) {
@@ -253,6 +253,8 @@ WsLayout ws_layout(int64_t M, int k, const moe_experts *ex) {
   L.pos = o;        o += round256(sizeof(int32_t) * MK);
   L.h = o;          o += round256(sizeof(float) * MK * ex->I);
   L.out = o;        o += round256(sizeof(float) * MK * ex->H);
+  L.tile_start = o; o += round256(sizeof(int32_t) * (ex->E + 1));
+  L.xg = o;         o += round256(2 * MK * ex->H);  // fp16 gathered tokens
   L.total = o;
   return L;
 }
@@ -306,15 +308,24 @@ int moe_ffn_forward(const void *x, int32_t x_dtype, int64_t M, const int32_t *to
   ws.pos = reinterpret_cast<int32_t *>(base + L.pos);
   ws.h = reinterpret_cast<float *>(base + L.h);
   ws.out = reinterpret_cast<float *>(base + L.out);
+  ws.tile_start = reinterpret_cast<int32_t *>(base + L.tile_start);
+  ws.xg = reinterpret_cast<__half *>(base + L.xg);
+  ws.hh = reinterpret_cast<__half *>(base + L.h);  // fp16 h reuses the fp32 h buffer
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const bool xb = x_dtype == QMM_BF16;
   cudaError_t e = launch_moe_dispatch(topk_idx, M, k, ex->E, ws, s);
   if (e != cudaSuccess) return cuda_fail(e, "moe_ffn_forward (dispatch)");
-  e = launch_moe_gateup(x, xb, M, k, ex->E, qmat(ex->gate), qmat(ex->up), ws, s);
-  if (e != cudaSuccess) return cuda_fail(e, "moe_ffn_forward (gate/up)");
-  e = launch_moe_down(M, k, ex->E, qmat(ex->down), ws, s);
-  if (e != cudaSuccess) return cuda_fail(e, "moe_ffn_forward (down)");
+  if (xb && moe_tc_supported(qmat(ex->gate), qmat(ex->down), ex->H, ex->I)) {
+    // bf16 activations: tensor-core grouped GEMMs (fp16 operands, fp32 accumulate)
+    e = launch_moe_tc(x, M, k, ex->E, qmat(ex->gate), qmat(ex->up), qmat(ex->down), ws, s);
+    if (e != cudaSuccess) return cuda_fail(e, "moe_ffn_forward (tensor-core experts)");
+  } else {
+    e = launch_moe_gateup(x, xb, M, k, ex->E, qmat(ex->gate), qmat(ex->up), ws, s);
+    if (e != cudaSuccess) return cuda_fail(e, "moe_ffn_forward (gate/up)");
+    e = launch_moe_down(M, k, ex->E, qmat(ex->down), ws, s);
+    if (e != cudaSuccess) return cuda_fail(e, "moe_ffn_forward (down)");
+  }
   e = launch_moe_combine(M, k, ex->H, topk_w, ws, y, y_dtype == QMM_BF16, s);
   if (e != cudaSuccess) return cuda_fail(e, "moe_ffn_forward (combine)");
   return QMM_OK;

@@ -4,6 +4,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 namespace qmm {
@@ -31,6 +32,9 @@ struct MoeWork {
   int32_t *pos;         // [M*k] position of assignment a inside `assign`
   float *h;             // [M*k, I] SwiGLU activations (fp32)
   float *out;           // [M*k, H] per-assignment expert outputs (fp32)
+  int32_t *tile_start;  // [E + 1] prefix of 128-token tiles per expert
+  __half *xg;           // [M*k, H] tokens in expert order, fp16 (tensor-core path)
+  __half *hh;           // [M*k, I] SwiGLU activations, fp16 (tensor-core path)
 };
 
 // Counts one kernel launch (for qmm_launch_count).
@@ -62,6 +66,11 @@ cudaError_t launch_moe_gateup(const void *x, bool x_bf16, int64_t M, int k, int 
 
 cudaError_t launch_moe_down(int64_t M, int k, int E, const QMat &down, const MoeWork &ws,
                             cudaStream_t s);
+
+// Tensor-core (tcgen05) path of the routed experts for bf16 activations.
+bool moe_tc_supported(const QMat &gate, const QMat &down, int64_t H, int64_t I);
+cudaError_t launch_moe_tc(const void *x, int64_t M, int k, int E, const QMat &gate, const QMat &up,
+                          const QMat &down, const MoeWork &ws, cudaStream_t s);
 
 cudaError_t launch_moe_combine(int64_t M, int k, int64_t H, const float *topk_w,
                                const MoeWork &ws, void *y, bool y_bf16, cudaStream_t s);

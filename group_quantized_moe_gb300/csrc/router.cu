@@ -198,7 +198,7 @@ __global__ void __launch_bounds__(1024) moe_dispatch_kernel(const int32_t *__res
   int32_t *cnt = sm;                 // [E]
   int32_t *cursor = sm + E;          // [E]
   int32_t *wcnt = sm + 2 * E;        // [32][E] per-warp counts of the current chunk
-  __shared__ int32_t warp_c[32], warp_f[32];
+  __shared__ int32_t warp_c[32], warp_f[32], warp_t[32];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int nthreads = blockDim.x;
   const int nwarps = nthreads >> 5;
@@ -217,53 +217,66 @@ __global__ void __launch_bounds__(1024) moe_dispatch_kernel(const int32_t *__res
   // Exclusive scan of counts (E <= blockDim: one element per thread) and of
   // the "has tokens" flags for the active-expert list.
   {
+    // Also the tile prefix: ceil(count / 128) token tiles per expert (the
+    // tensor-core path's work list).
     const int e = tid;
     const int c = (e < E) ? cnt[e] : 0;
     const int f = c > 0 ? 1 : 0;
-    int sc = c, sf = f;
+    const int tl = (c + 127) / 128;
+    int sc = c, sf = f, st = tl;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const int yc = __shfl_up_sync(0xFFFFFFFFu, sc, o);
       const int yf = __shfl_up_sync(0xFFFFFFFFu, sf, o);
+      const int yt = __shfl_up_sync(0xFFFFFFFFu, st, o);
       if (lane >= o) {
         sc += yc;
         sf += yf;
+        st += yt;
       }
     }
     if (lane == 31) {
       warp_c[warp] = sc;
       warp_f[warp] = sf;
+      warp_t[warp] = st;
     }
     __syncthreads();
     if (warp == 0) {
       int tc = lane < nwarps ? warp_c[lane] : 0;
       int tf = lane < nwarps ? warp_f[lane] : 0;
+      int tt = lane < nwarps ? warp_t[lane] : 0;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const int yc = __shfl_up_sync(0xFFFFFFFFu, tc, o);
         const int yf = __shfl_up_sync(0xFFFFFFFFu, tf, o);
+        const int yt = __shfl_up_sync(0xFFFFFFFFu, tt, o);
         if (lane >= o) {
           tc += yc;
           tf += yf;
+          tt += yt;
         }
       }
       if (lane < nwarps) {  // inclusive over warps
         warp_c[lane] = tc;
         warp_f[lane] = tf;
+        warp_t[lane] = tt;
       }
     }
     __syncthreads();
     const int exc = (warp > 0 ? warp_c[warp - 1] : 0) + sc - c;
     const int exf = (warp > 0 ? warp_f[warp - 1] : 0) + sf - f;
+    const int ext = (warp > 0 ? warp_t[warp - 1] : 0) + st - tl;
     if (e < E) {
       ws.offsets[e] = exc;
       cursor[e] = exc;
       if (f) ws.active[exf] = e;
       ws.counts[e] = c;
+      ws.tile_start[e] = ext;
     }
     if (e == E - 1) {
       ws.offsets[E] = exc + c;
       *ws.num_active = exf + f;
+      ws.tile_start[E] = ext + tl;
     }
   }
   __syncthreads();

@@ -260,14 +260,21 @@ def _small_experts(dev, E, H, I, bits, group, seed=1):
 
 
 def _moe_check(dev, x, xd, idx, w, ex, og, ou, od, y_dtype=torch.float32, what=""):
+    """fp32 activations run the fp32 CUDA-core path (strict bound); bf16
+    activations may run the fp16 tensor-core path (bf16 bar)."""
     y = q.moe_ffn_forward(xd, T(idx, dev), T(w, dev), ex, y_dtype=y_dtype)
     y = y.float().cpu().numpy().astype(np.float64)
     yref, bound = oracle.moe_ffn(x, idx, w, og, ou, od)
-    if y_dtype == torch.float32:
+    if y_dtype == torch.float32 and xd.dtype == torch.float32:
         assert_within(y, yref, bound, what)
     else:
         assert_bf16_rows(y, yref, what)
     return y
+
+
+def _bf16_x(x, dev):
+    xb = synth.to_bf16(x)
+    return synth.bf16_to_f32(xb), torch.from_numpy(xb.view(np.int16)).to(dev).view(torch.bfloat16)
 
 
 @pytest.mark.parametrize("bits,group,H,I", [(4, 64, 256, 256), (8, 128, 512, 512),
@@ -304,6 +311,33 @@ def test_moe_one_hot_expert_many_tokens(dev):
     w2 = np.full((M, 2), 0.5, np.float32)
     _moe_check(dev, x, T(x, dev), idx2, w2, ex, og, ou, od, what="two slots")
     _moe_check(dev, x[:1], T(x[:1], dev), idx2[:1], w2[:1], ex, og, ou, od, what="M=1")
+
+
+@pytest.mark.parametrize("group,H,I", [(64, 512, 256), (128, 1024, 512), (256, 1024, 1024)])
+def test_moe_tensor_core_tiles(dev, group, H, I):
+    """bf16 tokens, INT8 experts: the tensor-core path.  One expert gets 160
+    tokens (two 128-token tiles, ragged last tile), others 1-17 tokens, some
+    none; H and I span several 128-feature tiles and 64-wide K stages."""
+    E, k = 6, 2
+    ex, og, ou, od = _small_experts(dev, E, H, I, 8, group, seed=9)
+    M = 160
+    x, xd = _bf16_x(synth.normal(9, 1, M * H).reshape(M, H), dev)
+    idx = np.zeros((M, k), np.int32)
+    idx[:, 0] = 3
+    idx[:, 1] = np.where(np.arange(M) % 17 == 0, 1, np.where(np.arange(M) % 5 == 0, 5, 0))
+    w = np.full((M, k), 0.5, np.float32)
+    _moe_check(dev, x, xd, idx, w, ex, og, ou, od, what=f"tc g{group}")
+    _moe_check(dev, x, xd, idx, w, ex, og, ou, od, y_dtype=torch.bfloat16, what="tc bf16 out")
+    # a single token, and a bad index (skipped, flagged)
+    _moe_check(dev, x[:1], xd[:1], idx[:1], w[:1], ex, og, ou, od, what="tc M=1")
+    bad = idx[:7].copy()
+    bad[2, 1] = 77
+    q.qmm_device_status(clear=True)
+    y = q.moe_ffn_forward(xd[:7], T(bad, dev), T(w[:7], dev), ex).cpu().numpy()
+    assert q.qmm_device_status(clear=True) & q.QMM_DEV_BAD_EXPERT
+    w_ok = np.where(bad < E, w[:7], 0).astype(np.float32)
+    yref, _ = oracle.moe_ffn(x[:7], np.where(bad < E, bad, 0).astype(np.int32), w_ok, og, ou, od)
+    assert_bf16_rows(y, yref, "tc bad index")
 
 
 def test_moe_bad_expert_index_flagged(dev):
