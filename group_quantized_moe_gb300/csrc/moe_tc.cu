@@ -15,17 +15,22 @@
 //   gate/up: D_g, D_u in TMEM, epilogue h = silu(D_g) * D_u -> fp16 [tok, I]
 //   down:    D_d in TMEM, epilogue -> fp32 out[tok, H]
 //
-// CTA = 7 warps, one CTA per SM, persistent over work items
+// CTA = 19 warps, one CTA per SM, persistent over work items
 // (token tile of an expert, 128-feature tile):
-//   warp 4 (one lane): TMA producer of weight codes [128 rows x 64 K] into a
+//   warp 16 (one lane): TMA producer of weight codes [128 rows x 64 K] into a
 //     deep ring (64B swizzle for INT8).
-//   warp 6 (one lane): TMA producer of token rows [16 x 64 K] fp16 into the
+//   warp 18 (one lane): TMA producer of token rows [16 x 64 K] fp16 into the
 //     B stages (128B swizzle, the canonical K-major operand layout).
-//   warps 0-3 (128 threads, thread = weight row): dequantise the stage's codes
-//     to fp16, (q - zp) * s computed exactly up to the final fp16 rounding,
-//     and store them as the K-major 128B-swizzled A operand; after the last
-//     stage of an item they run the epilogue (tcgen05.ld from TMEM).
-//   warp 5: allocates TMEM; one lane issues tcgen05.mma (kind::f16, fp32
+//   warps 0-15 (512 threads; thread t handles weight row t % 128, K quarter
+//     t / 128 of each stage): dequantise the stage's codes to fp16,
+//     (q - zp) * s exact up to the final fp16 rounding, and store them with
+//     tcgen05.st straight into tensor memory, where the MMA reads its A
+//     operand (row = TMEM lane, two K values per 32-bit column); this keeps
+//     shared memory for deep TMA rings.  After the last stage of an item they
+//     run the epilogue (tcgen05.ld from TMEM; the four warpgroups take
+//     16-token column blocks in turn).  Each item's scale and zero-point
+//     lines are prefetched into L2 when the item starts.
+//   warp 17: allocates TMEM; one lane issues tcgen05.mma (kind::f16, fp32
 //     accumulate) and tcgen05.commit.
 // Every wait is bounded; on a timeout the CTA raises QMM_DEV_WAIT_TIMEOUT,
 // stops issuing work, waits (bounded) for what is in flight, frees its TMEM
@@ -46,32 +51,39 @@ namespace {
 constexpr int kBM = 128;        // weight rows per tile (MMA M)
 constexpr int kBN = 128;        // max tokens per tile (MMA N)
 constexpr int kBK = 64;         // K per stage
-constexpr int kThreads = 224;
-constexpr int kATile = kBM * kBK * 2;   // 16 KB fp16, 128B-swizzled K-major
+constexpr int kThreads = 608;
+constexpr int kDequant = 512;  // dequant / epilogue threads (warps 0-15)
+constexpr int kDequantWarps = kDequant / 32;  // one mbarrier arrival per warp
+constexpr int kACols = kBK / 2;         // TMEM columns of one A tile stage
 constexpr int kBTile = kBN * kBK * 2;   // 16 KB fp16
 constexpr int kCTile = kBM * kBK;       // 8 KB INT8 codes (64B swizzle)
 
 template <int NT>
 struct Ring;  // NT = weight tiles sharing one token tile (2: gate+up, 1: down)
+// Three independent rings: codes (TMA -> dequant), A (dequant -> MMA) and
+// B (TMA -> MMA), each with its own depth.
+// A stages live in TMEM after the accumulators: NT=2 uses 256 + 4*2*32 =
+// 512 columns, NT=1 uses 128 + 4*32 = 256.
 template <>
 struct Ring<2> {
-  static constexpr int kAB = 2, kC = 6;
+  static constexpr int kA = 4, kB = 4, kC = 8;
+  static constexpr uint32_t kTmemCols = 512;
 };
 template <>
 struct Ring<1> {
-  static constexpr int kAB = 3, kC = 8;
+  static constexpr int kA = 4, kB = 4, kC = 16;
+  static constexpr uint32_t kTmemCols = 256;
 };
 
 template <int NT>
 struct Smem {
-  static constexpr int kAB = Ring<NT>::kAB, kC = Ring<NT>::kC;
-  static constexpr int a_off = 0;
-  static constexpr int b_off = a_off + kAB * NT * kATile;
-  static constexpr int c_off = b_off + kAB * kBTile;
+  static constexpr int kA = Ring<NT>::kA, kB = Ring<NT>::kB, kC = Ring<NT>::kC;
+  static constexpr int b_off = 0;
+  static constexpr int c_off = b_off + kB * kBTile;
   static constexpr int bar_off = c_off + kC * NT * kCTile;
-  // barriers: c_full[kC], c_free[kC], b_full[kAB], a_full[kAB], ab_free[kAB],
-  // acc_full, acc_free
-  static constexpr int nbar = 2 * kC + 3 * kAB + 2;
+  // barriers: c_full[kC], c_free[kC], a_full[kA], a_free[kA], b_full[kB],
+  // b_free[kB], acc_full, acc_free
+  static constexpr int nbar = 2 * kC + 2 * kA + 2 * kB + 2;
   static constexpr int misc_off = bar_off + nbar * 8;
   static constexpr int meta_off = misc_off + 16;  // offsets[E+1], tile_start[E+1]
   static constexpr int bytes_for(int E) { return meta_off + 8 * (E + 1) + 1024; }
@@ -132,15 +144,28 @@ __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// D[tmem] (+)= A[smem desc] * B[smem desc]^T, kind::f16, cta_group::1.
-__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
-                                       uint32_t idesc, uint32_t accumulate) {
+// D[tmem] (+)= A[tmem] * B[smem desc]^T, kind::f16, cta_group::1.
+__device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                          uint32_t idesc, uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
+}
+
+// 8 consecutive 32-bit columns of this thread's TMEM lane (asynchronous;
+// tmem_wait_st() waits for all of this thread's stores).
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
 __device__ __forceinline__ void tc_commit(uint32_t bar) {
@@ -224,7 +249,7 @@ __device__ __forceinline__ Item decode_item(const int32_t *s_off, const int32_t 
 __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g)); }
 
 // INT8 codes (stored q - 128) of one 16-byte chunk -> 16 fp16 weights
-// (q - zp) * s, as two 16-byte chunks of the A operand.
+// (q - zp) * s, packed two per 32-bit word in K order.
 __device__ __forceinline__ void dequant16(uint4 v, __half2 mz2, __half2 s2, uint4 &o0, uint4 &o1) {
   uint32_t w[4] = {v.x, v.y, v.z, v.w};
   uint32_t r[8];
@@ -244,12 +269,6 @@ __device__ __forceinline__ void dequant16(uint4 v, __half2 mz2, __half2 s2, uint
   o1 = make_uint4(r[4], r[5], r[6], r[7]);
 }
 
-__device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
-  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y),
-               "r"(v.z), "r"(v.w)
-               : "memory");
-}
-
 // NT = 2: gate/up with SwiGLU epilogue (fp16 h); NT = 1: down (fp32 out).
 template <int NT>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -257,20 +276,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                   const __grid_constant__ CUtensorMap tm_codes1,
                   const __grid_constant__ CUtensorMap tm_x, TcArgs a) {
   using S = Smem<NT>;
-  constexpr int kAB = S::kAB, kC = S::kC;
+  constexpr int kA = S::kA, kB = S::kB, kC = S::kC;
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte aligned base (swizzled tiles).
   const uint32_t raw = smem_addr(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t *gbase = smem_raw + (base - raw);
-  const uint32_t sA = base + S::a_off, sB = base + S::b_off, sC = base + S::c_off;
+  const uint32_t sB = base + S::b_off, sC = base + S::c_off;
   const uint32_t bar0 = base + S::bar_off;
   auto c_full = [&](int i) { return bar0 + 8 * i; };
   auto c_free = [&](int i) { return bar0 + 8 * (kC + i); };
-  auto b_full = [&](int i) { return bar0 + 8 * (2 * kC + i); };
-  auto a_full = [&](int i) { return bar0 + 8 * (2 * kC + kAB + i); };
-  auto ab_free = [&](int i) { return bar0 + 8 * (2 * kC + 2 * kAB + i); };
-  const uint32_t acc_full = bar0 + 8 * (2 * kC + 3 * kAB);
+  auto a_full = [&](int i) { return bar0 + 8 * (2 * kC + i); };
+  auto a_free = [&](int i) { return bar0 + 8 * (2 * kC + kA + i); };
+  auto b_full = [&](int i) { return bar0 + 8 * (2 * kC + 2 * kA + i); };
+  auto b_free = [&](int i) { return bar0 + 8 * (2 * kC + 2 * kA + kB + i); };
+  const uint32_t acc_full = bar0 + 8 * (2 * kC + 2 * kA + 2 * kB);
   const uint32_t acc_free = acc_full + 8;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + S::misc_off);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(gbase + S::misc_off + 4);
@@ -282,34 +302,41 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  constexpr uint32_t kTmemCols = NT == 2 ? 256 : 128;
+  constexpr uint32_t kTmemCols = Ring<NT>::kTmemCols;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kC; ++i) {
       mbar_init(c_full(i), 1);
-      mbar_init(c_free(i), 128);
+      mbar_init(c_free(i), kDequantWarps);
     }
-    for (int i = 0; i < kAB; ++i) {
+    for (int i = 0; i < kA; ++i) {
+      mbar_init(a_full(i), kDequantWarps);
+      mbar_init(a_free(i), 1);
+    }
+    for (int i = 0; i < kB; ++i) {
       mbar_init(b_full(i), 1);
-      mbar_init(a_full(i), 128);
-      mbar_init(ab_free(i), 1);
+      mbar_init(b_free(i), 1);
     }
     mbar_init(acc_full, 1);
-    mbar_init(acc_free, 128);
+    mbar_init(acc_free, kDequantWarps);
     *abort_flag = 0;
     mbar_fence_init();
   }
-  if (warp == 5) tmem_alloc(smem_addr(tmem_slot), kTmemCols);
+  if (warp == 17) tmem_alloc(smem_addr(tmem_slot), kTmemCols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // TMEM column of A stage slot s, tile t (after the NT accumulators)
+  auto a_col = [&](int slot, int t) {
+    return static_cast<uint32_t>(NT * kBN + (slot * NT + t) * kACols);
+  };
 
   const int ftiles = static_cast<int>(a.rows / kBM);
   const int kstages = static_cast<int>(a.K / kBK);
   const int64_t nitems = static_cast<int64_t>(s_ts[a.E]) * ftiles;
 
-  if (warp == 4) {
+  if (warp == 16) {
     // ------------------------------------------- TMA producer: weight codes
     if (lane == 0) {
       int64_t gs = 0;  // global stage counter
@@ -332,7 +359,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_wait_bounded(c_full(static_cast<int>(j % kC)),
                             static_cast<uint32_t>((j / kC) & 1), a.status);
     }
-  } else if (warp == 6) {
+  } else if (warp == 18) {
     // -------------------------------------------- TMA producer: token rows
     if (lane == 0) {
       int64_t gs = 0;
@@ -340,20 +367,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         const Item it = decode_item(s_off, s_ts, a.E, item, ftiles);
         const int npad = (it.ntok + 15) & ~15;
         for (int kb = 0; kb < kstages; ++kb, ++gs) {
-          const int s = static_cast<int>(gs % kAB);
-          const uint32_t su = static_cast<uint32_t>(gs / kAB);
-          if (!wait_ok(ab_free(s), (su & 1u) ^ 1u, a.status, abort_flag)) break;
+          const int s = static_cast<int>(gs % kB);
+          const uint32_t su = static_cast<uint32_t>(gs / kB);
+          if (!wait_ok(b_free(s), (su & 1u) ^ 1u, a.status, abort_flag)) break;
           mbar_arrive_expect_tx(b_full(s), npad * kBK * 2);
           for (int r = 0; r < npad; r += 16)
             tma_load_2d(sB + s * kBTile + r * kBK * 2, &tm_x, kb * kBK, it.t0 + r, b_full(s));
         }
       }
       if (*abort_flag)
-        for (int64_t j = (gs > kAB ? gs - kAB : 0); j < gs; ++j)
-          mbar_wait_bounded(b_full(static_cast<int>(j % kAB)),
-                            static_cast<uint32_t>((j / kAB) & 1), a.status);
+        for (int64_t j = (gs > kB ? gs - kB : 0); j < gs; ++j)
+          mbar_wait_bounded(b_full(static_cast<int>(j % kB)),
+                            static_cast<uint32_t>((j / kB) & 1), a.status);
     }
-  } else if (warp == 5) {
+  } else if (warp == 17) {
     // ------------------------------------------------------ MMA issuer
     if (lane == 0) {
       int64_t gs = 0;
@@ -367,24 +394,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         bool ok = true;
         for (int kb = 0; kb < kstages; ++kb, ++gs) {
-          const int s = static_cast<int>(gs % kAB);
-          const uint32_t su = static_cast<uint32_t>(gs / kAB);
-          if (!wait_ok(a_full(s), su & 1u, a.status, abort_flag) ||
-              !wait_ok(b_full(s), su & 1u, a.status, abort_flag)) {
+          const int sa = static_cast<int>(gs % kA), sb = static_cast<int>(gs % kB);
+          const uint32_t ua = static_cast<uint32_t>(gs / kA), ub = static_cast<uint32_t>(gs / kB);
+          if (!wait_ok(b_full(sb), ub & 1u, a.status, abort_flag) ||
+              !wait_ok(a_full(sa), ua & 1u, a.status, abort_flag)) {
             ok = false;
             break;
           }
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk) {
-            const uint64_t bdesc = smem_desc_sw128(sB + s * kBTile + kk * 32);
+            const uint64_t bdesc = smem_desc_sw128(sB + sb * kBTile + kk * 32);
 #pragma unroll
-            for (int t = 0; t < NT; ++t) {
-              const uint64_t adesc = smem_desc_sw128(sA + (s * NT + t) * kATile + kk * 32);
-              tc_mma(tmem + t * kBN, adesc, bdesc, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
-            }
+            for (int t = 0; t < NT; ++t)
+              tc_mma_ts(tmem + t * kBN, tmem + a_col(sa, t) + kk * 8, bdesc, idesc,
+                        (kb > 0 || kk > 0) ? 1u : 0u);
           }
-          tc_commit(ab_free(s));
+          tc_commit(a_free(sa));
+          tc_commit(b_free(sb));
         }
         if (!ok) break;
         tc_commit(acc_full);
@@ -392,13 +419,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // After an abort, wait (bounded) for the MMAs already committed.
       if (*abort_flag)
-        for (int64_t j = (gs > kAB ? gs - kAB : 0); j < gs; ++j)
-          mbar_wait_bounded(ab_free(static_cast<int>(j % kAB)),
-                            static_cast<uint32_t>((j / kAB) & 1), a.status);
+        for (int64_t j = (gs > kA ? gs - kA : 0); j < gs; ++j)
+          mbar_wait_bounded(a_free(static_cast<int>(j % kA)),
+                            static_cast<uint32_t>((j / kA) & 1), a.status);
     }
   } else {
     // ------------------------------------------ dequantisation + epilogue
-    const int row = threadIdx.x;  // 0..127: weight row of the tile
+    const int row = threadIdx.x & (kBM - 1);  // weight row of the tile
+    const int quarter = threadIdx.x >> 7;      // K quarter of each stage (16 codes)
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     int64_t gs = 0;
     uint32_t nitem_done = 0;
     for (int64_t item = blockIdx.x; item < nitems && !*abort_flag; item += gridDim.x) {
@@ -410,6 +439,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int t = 0; t < NT; ++t) {
         scp[t] = a.sc[t] + it.e * a.gstride[t] + wrow * a.G;
         zpp[t] = a.zp[t] + it.e * a.gstride[t] + wrow * a.G;
+        // pull this row's scale / zero-point lines into L2 for the whole item
+        for (int g = 4 * quarter; g < a.G; g += 32) {
+          asm volatile("prefetch.global.L2 [%0];" ::"l"(scp[t] + g));
+          asm volatile("prefetch.global.L2 [%0];" ::"l"(zpp[t] + g));
+        }
       }
       // scale / zero point of the current group and the next one (prefetch)
       float s_nx[NT];
@@ -439,41 +473,52 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const int c = static_cast<int>(gs % kC);
         const uint32_t cu = static_cast<uint32_t>(gs / kC);
-        const int s = static_cast<int>(gs % kAB);
-        const uint32_t su = static_cast<uint32_t>(gs / kAB);
+        const int s = static_cast<int>(gs % kA);
+        const uint32_t su = static_cast<uint32_t>(gs / kA);
         bool got = wait_ok(c_full(c), cu & 1u, a.status, abort_flag) &&
-                   wait_ok(ab_free(s), (su & 1u) ^ 1u, a.status, abort_flag);
+                   wait_ok(a_free(s), (su & 1u) ^ 1u, a.status, abort_flag);
         if (!__all_sync(0xFFFFFFFFu, got)) {  // warp-uniform exit
           ok = false;
           break;
         }
+        tc_fence_after();
+        uint32_t packed[NT][8];
 #pragma unroll
         for (int t = 0; t < NT; ++t) {
-          // codes row `row`: 64 bytes, 16-byte chunk j stored at j ^ ((row >> 1) & 3)
+          // codes row `row`: 64 bytes, 16-byte chunk j stored at j ^ ((row >> 1) & 3);
+          // this thread converts chunk `quarter` (16 K values).
           const uint32_t crow = sC + (c * NT + t) * kCTile + row * kBK;
-          const uint32_t arow = sA + (s * NT + t) * kATile + (row >> 3) * 1024 + (row & 7) * 128;
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const uint4 v = lds128(crow + ((j ^ ((row >> 1) & 3)) << 4));
-            uint4 o0, o1;
-            dequant16(v, mz2[t], s2[t], o0, o1);
-            // A row: 16-byte chunk q (K 8q..8q+7) stored at q ^ (row & 7)
-            sts128(arow + (((2 * j) ^ (row & 7)) << 4), o0);
-            sts128(arow + (((2 * j + 1) ^ (row & 7)) << 4), o1);
-          }
+          const uint4 v = lds128(crow + ((quarter ^ ((row >> 1) & 3)) << 4));
+          uint4 o0, o1;
+          dequant16(v, mz2[t], s2[t], o0, o1);
+          packed[t][0] = o0.x;
+          packed[t][1] = o0.y;
+          packed[t][2] = o0.z;
+          packed[t][3] = o0.w;
+          packed[t][4] = o1.x;
+          packed[t][5] = o1.y;
+          packed[t][6] = o1.z;
+          packed[t][7] = o1.w;
         }
-        fence_proxy_async_smem();
-        mbar_arrive(a_full(s));
-        mbar_arrive(c_free(c));
+        // A[row][k] -> TMEM lane row, column k / 2 of the stage slot
+#pragma unroll
+        for (int t = 0; t < NT; ++t)
+          tmem_st8(tmem + lane_base + a_col(s, t) + quarter * 8, packed[t]);
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(a_full(s));
+          mbar_arrive(c_free(c));
+        }
       }
       if (!ok) break;
       // ---------------------------------------------------- epilogue
       if (!__all_sync(0xFFFFFFFFu, wait_ok(acc_full, nitem_done & 1u, a.status, abort_flag)))
         break;
       tc_fence_after();
-      const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
       const int feat = it.f * kBM + row;
-      for (int c0 = 0; c0 < it.ntok; c0 += 16) {
+      for (int c0 = 16 * quarter; c0 < it.ntok; c0 += 64) {
         float v0[16];
         tmem_ld16(tmem + lane_base + c0, v0);
         if constexpr (NT == 2) {
@@ -493,14 +538,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       tc_fence_before();
-      mbar_arrive(acc_free);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acc_free);
       ++nitem_done;
     }
   }
 
   // Teardown (every role has drained what it issued), then free TMEM.
   __syncthreads();
-  if (warp == 5) {
+  if (warp == 17) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
@@ -655,3 +701,4 @@ cudaError_t launch_moe_tc(const void *x, int64_t M, int k, int E, const QMat &ga
 }
 
 }  // namespace qmm
+

@@ -49,7 +49,36 @@ __global__ void __launch_bounds__(128) router_logits_kernel(const void *__restri
 #pragma unroll
     for (int e = 0; e < EB; ++e) acc[m][e] = 0.0f;
 
-  for (int64_t h = p; h < H; h += 128) {
+  // Four h-steps per iteration: all their loads issue before the FMAs, so a
+  // thread keeps 4 * (MB + EB) loads in flight (the chain order per partial
+  // is unchanged).
+  int64_t h = p;
+  for (; h + 3 * 128 < H; h += 4 * 128) {
+    float xv[4][MB], wv[4][EB];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+#pragma unroll
+      for (int m = 0; m < MB; ++m) {
+        const int64_t mm = m0 + (m < mb ? m : 0);
+        if constexpr (XBF16) {
+          const uint16_t b = static_cast<const uint16_t *>(x)[mm * H + h + 128 * u];
+          xv[u][m] = __uint_as_float(static_cast<uint32_t>(b) << 16);
+        } else {
+          xv[u][m] = __ldg(static_cast<const float *>(x) + mm * H + h + 128 * u);
+        }
+      }
+#pragma unroll
+      for (int e = 0; e < EB; ++e)
+        wv[u][e] = __ldg(wr + int64_t(e0 + (e < eb ? e : 0)) * H + h + 128 * u);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+#pragma unroll
+      for (int m = 0; m < MB; ++m)
+#pragma unroll
+        for (int e = 0; e < EB; ++e) acc[m][e] = __fmaf_rn(xv[u][m], wv[u][e], acc[m][e]);
+  }
+  for (; h < H; h += 128) {
     float xv[MB], wv[EB];
 #pragma unroll
     for (int m = 0; m < MB; ++m) {
@@ -218,7 +247,7 @@ __global__ void __launch_bounds__(1024) moe_dispatch_kernel(const int32_t *__res
   // the "has tokens" flags for the active-expert list.
   {
     // Also the tile prefix: ceil(count / 128) token tiles per expert (the
-    // tensor-core path's work list).
+    // tensor-core path's work list; 128 = its largest token tile).
     const int e = tid;
     const int c = (e < E) ? cnt[e] : 0;
     const int f = c > 0 ? 1 : 0;
