@@ -15,23 +15,28 @@
 //   gate/up: D_g, D_u in TMEM, epilogue h = silu(D_g) * D_u -> fp16 [tok, I]
 //   down:    D_d in TMEM, epilogue -> fp32 out[tok, H]
 //
-// CTA = 19 warps, one CTA per SM, persistent over work items
+// CTA = 20 warps, one CTA per SM, persistent over work items
 // (token tile of an expert, 128-feature tile):
 //   warp 16 (one lane): TMA producer of weight codes [128 rows x 64 K] into a
 //     deep ring (64B swizzle for INT8).
 //   warp 18 (one lane): TMA producer of token rows [16 x 64 K] fp16 into the
 //     B stages (128B swizzle, the canonical K-major operand layout).
-//   warps 0-15 (512 threads; thread t handles weight row t % 128, K quarter
-//     t / 128 of each stage): dequantise the stage's codes to fp16,
-//     (q - zp) * s exact up to the final fp16 rounding, and store them with
-//     tcgen05.st straight into tensor memory, where the MMA reads its A
-//     operand (row = TMEM lane, two K values per 32-bit column); this keeps
-//     shared memory for deep TMA rings.  After the last stage of an item they
-//     run the epilogue (tcgen05.ld from TMEM; the four warpgroups take
+//   warps 0-15 = four dequant warpgroups; warpgroup g converts the stages
+//     kb = g (mod 4), thread t the whole 64-K row t % 128 of each weight tile,
+//     so four stages are being converted at once (one stage's conversion is
+//     latency bound; stages pipeline).  Codes -> fp16 (q - zp) * s, exact up
+//     to the final fp16 rounding, stored with tcgen05.st straight into tensor
+//     memory, where the MMA reads its A operand (row = TMEM lane, two K values
+//     per 32-bit column); this keeps shared memory for deep TMA rings.  After
+//     an item's last stage all four run the epilogue (tcgen05.ld from TMEM,
 //     16-token column blocks in turn).  Each item's scale and zero-point
 //     lines are prefetched into L2 when the item starts.
-//   warp 17: allocates TMEM; one lane issues tcgen05.mma (kind::f16, fp32
-//     accumulate) and tcgen05.commit.
+//   warps 17 and 19: one lane each issues tcgen05.mma (kind::f16, fp32
+//     accumulate) and tcgen05.commit.  A single thread issues about one MMA
+//     per 60-100 cycles whatever N is, so with few tokens per item two
+//     issuers are needed: for gate/up each owns one accumulator (gate, up);
+//     for down they take alternate 16-K steps into two accumulators that the
+//     epilogue adds.  Warp 17 also allocates TMEM.
 // Every wait is bounded; on a timeout the CTA raises QMM_DEV_WAIT_TIMEOUT,
 // stops issuing work, waits (bounded) for what is in flight, frees its TMEM
 // and returns.
@@ -51,9 +56,8 @@ namespace {
 constexpr int kBM = 128;        // weight rows per tile (MMA M)
 constexpr int kBN = 128;        // max tokens per tile (MMA N)
 constexpr int kBK = 64;         // K per stage
-constexpr int kThreads = 608;
-constexpr int kDequant = 512;  // dequant / epilogue threads (warps 0-15)
-constexpr int kDequantWarps = kDequant / 32;  // one mbarrier arrival per warp
+constexpr int kThreads = 640;
+constexpr int kDequantWarps = 16;  // warps 0-15: 4 warpgroups, stages round-robin
 constexpr int kACols = kBK / 2;         // TMEM columns of one A tile stage
 constexpr int kBTile = kBN * kBK * 2;   // 16 KB fp16
 constexpr int kCTile = kBM * kBK;       // 8 KB INT8 codes (64B swizzle)
@@ -62,8 +66,9 @@ template <int NT>
 struct Ring;  // NT = weight tiles sharing one token tile (2: gate+up, 1: down)
 // Three independent rings: codes (TMA -> dequant), A (dequant -> MMA) and
 // B (TMA -> MMA), each with its own depth.
-// A stages live in TMEM after the accumulators: NT=2 uses 256 + 4*2*32 =
-// 512 columns, NT=1 uses 128 + 4*32 = 256.
+// TMEM: accumulators in columns [0, 256) (gate, up for NT=2; the two k-step
+// parities for NT=1), then the A stages: NT=2 uses 256 + 4*2*32 = 512
+// columns, NT=1 uses 256 + 4*32 = 384 (allocation 512).
 template <>
 struct Ring<2> {
   static constexpr int kA = 4, kB = 4, kC = 8;
@@ -72,7 +77,7 @@ struct Ring<2> {
 template <>
 struct Ring<1> {
   static constexpr int kA = 4, kB = 4, kC = 16;
-  static constexpr uint32_t kTmemCols = 256;
+  static constexpr uint32_t kTmemCols = 512;
 };
 
 template <int NT>
@@ -155,12 +160,14 @@ __device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint
       : "memory");
 }
 
-// 8 consecutive 32-bit columns of this thread's TMEM lane (asynchronous;
+// 16 consecutive 32-bit columns of this thread's TMEM lane (asynchronous;
 // tmem_wait_st() waits for all of this thread's stores).
-__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t *r) {
   asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
-      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
       : "memory");
 }
 
@@ -307,17 +314,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < kC; ++i) {
       mbar_init(c_full(i), 1);
-      mbar_init(c_free(i), kDequantWarps);
+      mbar_init(c_free(i), 4);  // one arrival per warp of the converting warpgroup
     }
     for (int i = 0; i < kA; ++i) {
-      mbar_init(a_full(i), kDequantWarps);
-      mbar_init(a_free(i), 1);
+      mbar_init(a_full(i), 4);
+      mbar_init(a_free(i), 2);  // one commit per MMA issuer
     }
     for (int i = 0; i < kB; ++i) {
       mbar_init(b_full(i), 1);
-      mbar_init(b_free(i), 1);
+      mbar_init(b_free(i), 2);
     }
-    mbar_init(acc_full, 1);
+    mbar_init(acc_full, 2);
     mbar_init(acc_free, kDequantWarps);
     *abort_flag = 0;
     mbar_fence_init();
@@ -329,7 +336,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
   // TMEM column of A stage slot s, tile t (after the NT accumulators)
   auto a_col = [&](int slot, int t) {
-    return static_cast<uint32_t>(NT * kBN + (slot * NT + t) * kACols);
+    return static_cast<uint32_t>(2 * kBN + (slot * NT + t) * kACols);
   };
 
   const int ftiles = static_cast<int>(a.rows / kBM);
@@ -380,11 +387,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_wait_bounded(b_full(static_cast<int>(j % kB)),
                             static_cast<uint32_t>((j / kB) & 1), a.status);
     }
-  } else if (warp == 17) {
-    // ------------------------------------------------------ MMA issuer
+  } else if (warp == 17 || warp == 19) {
+    // ---------------------------------------------------- MMA issuers
+    const int issuer = warp == 17 ? 0 : 1;
     if (lane == 0) {
       int64_t gs = 0;
       uint32_t nitem_done = 0;
+      const uint32_t d_tmem = tmem + issuer * kBN;
       for (int64_t item = blockIdx.x; item < nitems && !*abort_flag; item += gridDim.x) {
         const Item it = decode_item(s_off, s_ts, a.E, item, ftiles);
         const int npad = (it.ntok + 15) & ~15;
@@ -405,10 +414,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk) {
             const uint64_t bdesc = smem_desc_sw128(sB + sb * kBTile + kk * 32);
-#pragma unroll
-            for (int t = 0; t < NT; ++t)
-              tc_mma_ts(tmem + t * kBN, tmem + a_col(sa, t) + kk * 8, bdesc, idesc,
+            if constexpr (NT == 2) {
+              // issuer t owns accumulator t (gate or up)
+              tc_mma_ts(d_tmem, tmem + a_col(sa, issuer) + kk * 8, bdesc, idesc,
                         (kb > 0 || kk > 0) ? 1u : 0u);
+            } else {
+              // issuer p takes the 16-K steps of parity p into accumulator p
+              if ((kk & 1) == issuer)
+                tc_mma_ts(d_tmem, tmem + a_col(sa, 0) + kk * 8, bdesc, idesc,
+                          (kb > 0 || kk > 1) ? 1u : 0u);
+            }
           }
           tc_commit(a_free(sa));
           tc_commit(b_free(sb));
@@ -425,8 +440,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------ dequantisation + epilogue
-    const int row = threadIdx.x & (kBM - 1);  // weight row of the tile
-    const int quarter = threadIdx.x >> 7;      // K quarter of each stage (16 codes)
+    const int row = threadIdx.x & (kBM - 1);  // weight row of the tile (= TMEM lane)
+    const int wg = warp >> 2;                  // converts stages kb = wg (mod 4)
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     int64_t gs = 0;
     uint32_t nitem_done = 0;
@@ -440,35 +455,43 @@ __global__ void __launch_bounds__(kThreads, 1)
         scp[t] = a.sc[t] + it.e * a.gstride[t] + wrow * a.G;
         zpp[t] = a.zp[t] + it.e * a.gstride[t] + wrow * a.G;
         // pull this row's scale / zero-point lines into L2 for the whole item
-        for (int g = 4 * quarter; g < a.G; g += 32) {
+        for (int g = 32 * wg; g < a.G; g += 128) {
           asm volatile("prefetch.global.L2 [%0];" ::"l"(scp[t] + g));
           asm volatile("prefetch.global.L2 [%0];" ::"l"(zpp[t] + g));
         }
       }
-      // scale / zero point of the current group and the next one (prefetch)
+      // scale / zero point of this warpgroup's next stage, loaded one of its
+      // stages ahead
       float s_nx[NT];
       int32_t z_nx[NT];
-      __half2 s2[NT], mz2[NT];
 #pragma unroll
       for (int t = 0; t < NT; ++t) {
-        s_nx[t] = __ldg(scp[t]);
-        z_nx[t] = __ldg(zpp[t]);
-        s2[t] = __float2half2_rn(0.0f);
-        mz2[t] = __float2half2_rn(0.0f);
+        s_nx[t] = 0.0f;
+        z_nx[t] = 0;
+      }
+      if (wg < kstages) {
+        const int gi = (wg * kBK) >> a.group_shift;
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+          s_nx[t] = __ldg(scp[t] + gi);
+          z_nx[t] = __ldg(zpp[t] + gi);
+        }
       }
       bool ok = true;
       for (int kb = 0; kb < kstages; ++kb, ++gs) {
-        const int k0 = kb * kBK;
-        if ((k0 & ((1 << a.group_shift) - 1)) == 0) {  // first stage of a group
-          const int gi = k0 >> a.group_shift;
+        if ((kb & 3) != wg) continue;
+        __half2 s2[NT], mz2[NT];
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+          s2[t] = __float2half2_rn(s_nx[t]);
+          mz2[t] = __float2half2_rn(1024.0f + static_cast<float>(z_nx[t]));
+        }
+        if (kb + 4 < kstages) {
+          const int gi = ((kb + 4) * kBK) >> a.group_shift;
 #pragma unroll
           for (int t = 0; t < NT; ++t) {
-            s2[t] = __float2half2_rn(s_nx[t]);
-            mz2[t] = __float2half2_rn(1024.0f + static_cast<float>(z_nx[t]));
-            if (gi + 1 < a.G) {
-              s_nx[t] = __ldg(scp[t] + gi + 1);
-              z_nx[t] = __ldg(zpp[t] + gi + 1);
-            }
+            s_nx[t] = __ldg(scp[t] + gi);
+            z_nx[t] = __ldg(zpp[t] + gi);
           }
         }
         const int c = static_cast<int>(gs % kC);
@@ -482,28 +505,29 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc_fence_after();
-        uint32_t packed[NT][8];
 #pragma unroll
         for (int t = 0; t < NT; ++t) {
-          // codes row `row`: 64 bytes, 16-byte chunk j stored at j ^ ((row >> 1) & 3);
-          // this thread converts chunk `quarter` (16 K values).
+          // codes row `row`: 64 bytes, 16-byte chunk j stored at j ^ ((row >> 1) & 3)
           const uint32_t crow = sC + (c * NT + t) * kCTile + row * kBK;
-          const uint4 v = lds128(crow + ((quarter ^ ((row >> 1) & 3)) << 4));
-          uint4 o0, o1;
-          dequant16(v, mz2[t], s2[t], o0, o1);
-          packed[t][0] = o0.x;
-          packed[t][1] = o0.y;
-          packed[t][2] = o0.z;
-          packed[t][3] = o0.w;
-          packed[t][4] = o1.x;
-          packed[t][5] = o1.y;
-          packed[t][6] = o1.z;
-          packed[t][7] = o1.w;
-        }
-        // A[row][k] -> TMEM lane row, column k / 2 of the stage slot
+          uint32_t packed[32];
 #pragma unroll
-        for (int t = 0; t < NT; ++t)
-          tmem_st8(tmem + lane_base + a_col(s, t) + quarter * 8, packed[t]);
+          for (int j = 0; j < 4; ++j) {
+            const uint4 v = lds128(crow + ((j ^ ((row >> 1) & 3)) << 4));
+            uint4 o0, o1;
+            dequant16(v, mz2[t], s2[t], o0, o1);
+            packed[8 * j + 0] = o0.x;
+            packed[8 * j + 1] = o0.y;
+            packed[8 * j + 2] = o0.z;
+            packed[8 * j + 3] = o0.w;
+            packed[8 * j + 4] = o1.x;
+            packed[8 * j + 5] = o1.y;
+            packed[8 * j + 6] = o1.z;
+            packed[8 * j + 7] = o1.w;
+          }
+          // A[row][k] -> TMEM lane row, column k / 2 of the stage slot
+          tmem_st16(tmem + lane_base + a_col(s, t), packed);
+          tmem_st16(tmem + lane_base + a_col(s, t) + 16, packed + 16);
+        }
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
@@ -518,7 +542,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       tc_fence_after();
       const int feat = it.f * kBM + row;
-      for (int c0 = 16 * quarter; c0 < it.ntok; c0 += 64) {
+      for (int c0 = 16 * wg; c0 < it.ntok; c0 += 64) {
         float v0[16];
         tmem_ld16(tmem + lane_base + c0, v0);
         if constexpr (NT == 2) {
@@ -531,10 +555,13 @@ __global__ void __launch_bounds__(kThreads, 1)
               h[static_cast<int64_t>(it.t0 + c0 + j) * a.out_ld + feat] =
                   __float2half_rn(silu_f(v0[j]) * v1[j]);
         } else {
+          float v1[16];  // the other k-step parity
+          tmem_ld16(tmem + lane_base + kBN + c0, v1);
           float *o = static_cast<float *>(a.out);
 #pragma unroll
           for (int j = 0; j < 16; ++j)
-            if (c0 + j < it.ntok) o[static_cast<int64_t>(it.t0 + c0 + j) * a.out_ld + feat] = v0[j];
+            if (c0 + j < it.ntok)
+              o[static_cast<int64_t>(it.t0 + c0 + j) * a.out_ld + feat] = v0[j] + v1[j];
         }
       }
       tc_fence_before();
