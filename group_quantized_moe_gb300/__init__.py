@@ -33,7 +33,8 @@ QMM_DEV_BAD_EXPERT = 2
 
 EXPORTED = ("qmm_quantize_groupwise", "qmm_linear", "moe_route_workspace_bytes", "moe_route_topk",
             "moe_ffn_workspace_bytes", "moe_ffn_forward", "qmm_last_error", "qmm_launch_count",
-            "qmm_device_status")
+            "qmm_device_status", "moe_route_topk_noalloc")
+QMM_NOALLOC_MAX_LOGITS = 262144
 
 
 class QmmError(RuntimeError):
@@ -98,6 +99,9 @@ def lib() -> ctypes.CDLL:
             L.qmm_launch_count.restype = u64
             L.qmm_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32), i32]
             L.qmm_device_status.restype = ctypes.c_int
+            L.moe_route_topk_noalloc.argtypes = [vp, i32, i64, i64, vp, vp, i32, i32, vp, vp, vp,
+                                                 vp]
+            L.moe_route_topk_noalloc.restype = ctypes.c_int
             _lib = L
     return _lib
 
@@ -292,6 +296,29 @@ def moe_ffn_forward(x: torch.Tensor, topk_idx: torch.Tensor, topk_w: torch.Tenso
                                  ctypes.byref(desc), _ptr(y), _dtype_code(y), _ptr(workspace),
                                  workspace.numel(), _stream(stream)))
     return y
+
+
+def moe_route_topk_noalloc(x: torch.Tensor, w_router: torch.Tensor, bias: torch.Tensor | None,
+                           k: int, topk_idx=None, topk_w=None, expert_counts=None,
+                           with_counts: bool = True, stream=None):
+    """The router without a workspace, for callers that cannot allocate device
+    memory: its logits scratch is a fixed 1 MiB array inside the library
+    (M * E <= QMM_NOALLOC_MAX_LOGITS).  Outputs are allocated here only when
+    the caller passes none.  Returns (topk_idx, topk_w, expert_counts)."""
+    _require_cuda(x, w_router, bias)
+    M, H = x.shape
+    E = w_router.shape[0]
+    dev = x.device
+    if topk_idx is None:
+        topk_idx = torch.empty((M, k), dtype=torch.int32, device=dev)
+    if topk_w is None:
+        topk_w = torch.empty((M, k), dtype=torch.float32, device=dev)
+    if expert_counts is None and with_counts:
+        expert_counts = torch.empty((E,), dtype=torch.int32, device=dev)
+    _check(lib().moe_route_topk_noalloc(_ptr(x), _dtype_code(x), M, H, _ptr(w_router), _ptr(bias),
+                                        E, k, _ptr(topk_idx), _ptr(topk_w), _ptr(expert_counts),
+                                        _stream(stream)))
+    return topk_idx, topk_w, expert_counts
 
 
 def qmm_last_error() -> str:

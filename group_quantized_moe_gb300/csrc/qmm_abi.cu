@@ -66,6 +66,13 @@ int check_qshape(int bits, int group, int64_t rows, int64_t cols, const char *wh
 
 void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
+void record_error(const char *fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof(g_err), fmt, ap);
+  va_end(ap);
+}
+
 int sm_count() {
   const int d = current_device();
   if (d < 0 || d >= kMaxDevices) return 1;

@@ -84,3 +84,8 @@ int gemv_rows_per_tile(int64_t rowbytes, int64_t G, int copies);
 // Bytes of router logits for M tokens and E experts.
 size_t router_logits_bytes(int64_t M, int E);
 }  // namespace qmm
+
+namespace qmm {
+// Sets this thread's qmm_last_error() message (printf-style; "" clears it).
+void record_error(const char *fmt, ...);
+}  // namespace qmm

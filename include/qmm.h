@@ -177,6 +177,31 @@ int moe_ffn_forward(const void *x, int32_t x_dtype, int64_t M,
                     void *workspace, size_t workspace_bytes,
                     qmm_stream_t stream);
 
+/*
+ * Allocation-free router (no counterpart on the pages: it is a calling
+ * convention, not part of the method).  Computes exactly what moe_route_topk
+ * computes, with the same arguments minus the workspace, for callers that
+ * cannot create device allocations themselves -- hosts whose device memory is
+ * owned by another allocator (a serving arena, a framework plugin limited to
+ * the buffers it is handed) or loops that must not pay for cudaMalloc and its
+ * implicit synchronisation.  The caller still passes all inputs and outputs.
+ * The logits scratch is a fixed array of device memory inside the library,
+ * QMM_NOALLOC_MAX_LOGITS fp32 values (1 MiB), which every GPU that loads the
+ * library holds until the process exits; M * E above that limit returns
+ * QMM_ERR_WORKSPACE.  The first call on a device looks up the array's device
+ * address (one-time set-up; make that first call before any stream capture).
+ * All calls on a device share the array and it keeps the last call's
+ * contents (every value read is written first, so nothing needs clearing);
+ * calls whose kernels may overlap on the GPU race on it.  Nothing here calls
+ * cudaMalloc, cudaFree or any allocating routine.
+ */
+#define QMM_NOALLOC_MAX_LOGITS 262144
+
+int moe_route_topk_noalloc(const void *x, int32_t x_dtype, int64_t M, int64_t H,
+                           const float *w_router, const float *bias, int32_t E,
+                           int32_t k, int32_t *topk_idx, float *topk_w,
+                           int32_t *expert_counts, qmm_stream_t stream);
+
 /* Message for the last non-zero return on this thread ("" if none). */
 const char *qmm_last_error(void);
 
