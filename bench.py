@@ -376,6 +376,8 @@ def main():
     ap.add_argument("--only", choices=["gemv", "moe_decode", "moe_prefill"], default=None,
                     help="run one workload only (profiling)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
+    ap.add_argument("--experts", type=int, default=None,
+                    help="with --only moe_*: fewer experts (a smaller case for profiler captures)")
     args = ap.parse_args()
     peaks = load_peaks()
     metric = "fused dequant-GEMV weight GB/s & MoE layer tokens/s, % of HBM/TC roofline"
@@ -416,6 +418,9 @@ def main():
 
     if args.only in ("moe_decode", "moe_prefill"):
         r = recipes.CFG4 if args.only == "moe_decode" else recipes.CFG5
+        if args.experts:
+            import dataclasses
+            r = dataclasses.replace(r, name=f"{r.name}_e{args.experts}", E=args.experts)
         mo = run_moe(dev, r, args.steps, args.warmup)
         if rank == 0:
             print(json.dumps({"only": args.only, **mo}))
@@ -425,7 +430,7 @@ def main():
     ms_e2e = dist_max(g["ms_e2e"], world)
     value = world * g["bytes"] / (ms * 1e-3) / 1e9
     ach = g["b_vocab"] / (g["t_vocab_ms"] * 1e-3) / 1e9
-    traffic = traffic_for("gemv_kernel", ("gemv.cu", "qmm_device.cuh"),
+    traffic = traffic_for("gemv_kernel", ("gemv.cu", "stream_tile.cuh", "qmm_device.cuh"),
                           "int8_g64_k4096_n129280")
     line = {"metric": metric, "value": value, "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,

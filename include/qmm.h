@@ -58,7 +58,7 @@ enum {
   QMM_ERR_ALIGN = 3,       /* a pointer or stride is not 16-byte aligned    */
   QMM_ERR_WORKSPACE = 4,   /* workspace missing or too small                */
   QMM_ERR_CUDA = 5,        /* a CUDA runtime call or launch failed          */
-  QMM_ERR_UNSUPPORTED = 6  /* a valid configuration this build does not run */
+  QMM_ERR_UNSUPPORTED = 6  /* a valid configuration the library does not run */
 };
 
 /* Activation / output element types. */

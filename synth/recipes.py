@@ -54,22 +54,22 @@ class MoeRecipe:
     seed: int = 0
 
 
-# configs[0]: single INT8 group-64 linear.
+# Single INT8 group-64 linear (small correctness case).
 CFG1 = LinearRecipe("int8_g64_k256_n128", N=128, K=256, M=1, bits=8, group=64, stream=S_W0)
-# configs[1]: decode GEMV, INT8 group 64, 1% outliers x20; trunk projection and vocab head.
+# Decode GEMV, INT8 group 64, 1% outliers x20; trunk projection and vocab head.
 CFG2_TRUNK = LinearRecipe("int8_g64_k4096_n4096", N=4096, K=4096, M=1, bits=8, group=64,
                           stream=S_W0, outlier_p=0.01)
 CFG2_VOCAB = LinearRecipe("int8_g64_k4096_n129280", N=129280, K=4096, M=1, bits=8, group=64,
                           stream=S_W1, outlier_p=0.01)
-# configs[2]: decode GEMV, INT4 group 128.
+# Decode GEMV, INT4 group 128.
 CFG3_A = LinearRecipe("int4_g128_k4096_n4096", N=4096, K=4096, M=1, bits=4, group=128,
                       stream=S_W0)
 CFG3_B = LinearRecipe("int4_g128_k4096_n2048", N=2048, K=4096, M=1, bits=4, group=128,
                       stream=S_W1)
-# configs[3]: MoE decode layer.
+# MoE decode layer (8 tokens).
 CFG4 = MoeRecipe("moe_decode_m8_int4_g64", M=8, H=4096, I=2048, E=256, k=6, bits=4, group=64,
                  x_bf16=False, zipf_s=None)
-# configs[4]: batched-prefill MoE with Zipf(1.1) expert popularity.
+# Batched-prefill MoE (512 bf16 tokens) with Zipf(1.1) expert popularity.
 CFG5 = MoeRecipe("moe_prefill_m512_bf16_int8_g128", M=512, H=4096, I=2048, E=256, k=6, bits=8,
                  group=128, x_bf16=True, zipf_s=1.1)
 
