@@ -158,7 +158,11 @@ int qmm_linear(const void *x, int32_t x_dtype, int64_t M, const qmm_weight *w, f
                 static_cast<long long>(w->K));
   QMat q{static_cast<const uint8_t *>(w->codes), 0, w->scales, w->zps, 0, w->N, w->K,
          w->bits, w->group};
-  cudaError_t e = launch_gemv(x, x_dtype == QMM_BF16, M, q, y, static_cast<cudaStream_t>(stream));
+  cudaError_t e;
+  if (M >= 2 && M <= 8 && smallm_supported(w->bits, w->group, w->K))
+    e = launch_smallm_linear(x, x_dtype == QMM_BF16, M, q, y, static_cast<cudaStream_t>(stream));
+  else
+    e = launch_gemv(x, x_dtype == QMM_BF16, M, q, y, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "qmm_linear");
   return QMM_OK;
 }
@@ -323,14 +327,20 @@ int moe_ffn_forward(const void *x, int32_t x_dtype, int64_t M, const int32_t *to
   const bool xb = x_dtype == QMM_BF16;
   cudaError_t e = launch_moe_dispatch(topk_idx, M, k, ex->E, ws, s);
   if (e != cudaSuccess) return cuda_fail(e, "moe_ffn_forward (dispatch)");
-  if (xb && moe_tc_supported(qmat(ex->gate), qmat(ex->down), ex->H, ex->I)) {
+  // Decode batches (at most 8 tokens, so at most 8 per expert unless the
+  // caller repeats an expert within a token) use the small-M kernels.
+  const bool small_gu = M <= 8 && smallm_supported(ex->gate.bits, ex->gate.group, ex->H);
+  const bool small_dn = M <= 8 && smallm_supported(ex->down.bits, ex->down.group, ex->I);
+  if (xb && !small_gu && moe_tc_supported(qmat(ex->gate), qmat(ex->down), ex->H, ex->I)) {
     // bf16 activations: tensor-core grouped GEMMs (fp16 operands, fp32 accumulate)
     e = launch_moe_tc(x, M, k, ex->E, qmat(ex->gate), qmat(ex->up), qmat(ex->down), ws, s);
     if (e != cudaSuccess) return cuda_fail(e, "moe_ffn_forward (tensor-core experts)");
   } else {
-    e = launch_moe_gateup(x, xb, M, k, ex->E, qmat(ex->gate), qmat(ex->up), ws, s);
+    e = small_gu ? launch_smallm_gateup(x, xb, k, ex->E, qmat(ex->gate), qmat(ex->up), ws, s)
+                 : launch_moe_gateup(x, xb, M, k, ex->E, qmat(ex->gate), qmat(ex->up), ws, s);
     if (e != cudaSuccess) return cuda_fail(e, "moe_ffn_forward (gate/up)");
-    e = launch_moe_down(M, k, ex->E, qmat(ex->down), ws, s);
+    e = small_dn ? launch_smallm_down(k, ex->E, qmat(ex->down), ws, s)
+                 : launch_moe_down(M, k, ex->E, qmat(ex->down), ws, s);
     if (e != cudaSuccess) return cuda_fail(e, "moe_ffn_forward (down)");
   }
   e = launch_moe_combine(M, k, ex->H, topk_w, ws, y, y_dtype == QMM_BF16, s);

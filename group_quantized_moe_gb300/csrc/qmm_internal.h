@@ -86,6 +86,17 @@ size_t router_logits_bytes(int64_t M, int E);
 }  // namespace qmm
 
 namespace qmm {
+// Small-M fused dequantise-matmul (1..8 activation rows per matrix, more in
+// passes of 8): K in {2048, 4096}, group >= 64 with K / group a multiple of 4.
+bool smallm_supported(int bits, int group, int64_t K);
+cudaError_t launch_smallm_linear(const void *x, bool x_bf16, int64_t M, const QMat &w, float *y,
+                                 cudaStream_t s);
+cudaError_t launch_smallm_gateup(const void *x, bool x_bf16, int k, int E, const QMat &gate,
+                                 const QMat &up, const MoeWork &ws, cudaStream_t s);
+cudaError_t launch_smallm_down(int k, int E, const QMat &down, const MoeWork &ws, cudaStream_t s);
+}  // namespace qmm
+
+namespace qmm {
 // Sets this thread's qmm_last_error() message (printf-style; "" clears it).
 void record_error(const char *fmt, ...);
 }  // namespace qmm

@@ -1,0 +1,85 @@
+// smallm.cuh -- fused dequantise-matmul for a few activation rows per weight
+// matrix on the CUDA cores: the routed experts of a decode batch (gate + up
+// with the SwiGLU epilogue, then down) and qmm_linear for 2..8 rows.
+//
+// "Why I hand-wrote a DeepSeek inference engine in pure C", section 3.2
+// (the codes are dequantised inside the dot product, never written out as
+// fp32 weights) and section 3.5 (the tokens routed to one expert share one
+// pass over its weights).
+//
+// GB300 design (HBM-bound: each weight byte is used by 1..8 tokens):
+//  * One CTA of eight warps per SM.  Thread 0 streams tiles of whole weight
+//    rows -- codes, fp32 scales and int32 zero points, three 1-D bulk copies
+//    per matrix -- through a 4-stage ring of 40 KB stages, completion on one
+//    mbarrier per stage (every wait bounded).  A stage is refilled right
+//    after the CTA barrier that ends its last use, so no "empty" barrier is
+//    needed.
+//  * The eight warps split the K range of every row eight ways: lane l of
+//    warp w owns columns [(32 w + l) XPL, +XPL), XPL = K / 256 (8 or 16),
+//    and keeps those columns of up to eight activation rows in registers for
+//    as long as the CTA stays on one expert.  The slice never straddles a
+//    quantisation group, so it needs one scale and one zero point per row.
+//  * Each lane dequantises its slice of a row once and applies it to every
+//    token.  The per-lane partials of a block of rows are reduced across the
+//    warp by a butterfly that halves the values a lane carries at every step
+//    (about one shuffle per value instead of five), then across the eight
+//    warps through shared memory in a fixed order.
+//  * Each CTA takes one contiguous range of tiles, balanced by a per-tile
+//    cost that grows with the expert's token count; it therefore reads one
+//    contiguous stretch of HBM and reloads activations only when its range
+//    crosses into the next expert.
+#pragma once
+
+#include <cstdint>
+
+#include "qmm_device.cuh"
+#include "qmm_internal.h"
+
+namespace qmm {
+namespace smallm {
+
+constexpr int kCW = 8;                       // consumer warps (K split 8 ways)
+constexpr int kThreads = kCW * 32;
+constexpr int kStages = 4;
+constexpr int kStageBytes = 40960;
+constexpr int kTokMax = 8;                   // activation rows per pass
+constexpr int kRedMax = 256;                 // rows x tokens reduced per tile
+constexpr int kRingBytes = kStages * kStageBytes;
+constexpr int kRedBytes = 2 * kCW * kRedMax * 4;
+
+enum Mode { kLinear = 0, kGateUp = 1, kDown = 2 };
+
+struct Args {
+  QMat w0, w1;      // linear / down: w0; gate/up: w0 = gate, w1 = up
+  int64_t rows;     // rows of each matrix (N, I or H)
+  int64_t K;        // columns
+  int rowbytes;     // code bytes per row
+  int G;            // groups per row
+  int group;
+  int tiles;        // tiles per segment: ceil(rows / rows-per-matrix-per-tile)
+  int E;            // experts (MoE); 1 for the linear layer
+  int k;            // top-k: sorted position p holds token assign[p] / k
+  int64_t M;        // linear: activation rows
+  MoeWork ws;
+  const void *x;    // linear and gate/up: activations [*, K]
+  float *y;         // linear: output [M, rows]
+  uint32_t *status;
+};
+
+// Rows of all matrices per tile (one stage): the most whole rows, a power
+// of two, whose codes, scales and zero points fit 40 KB for group >= 64.
+template <int BITS, int XPL>
+__host__ __device__ constexpr int rows_per_tile() {
+  return (BITS == 4 ? 16 : 8) * 16 / XPL;
+}
+
+// Cost of one tile of a segment with T tokens (dequantisation ~ 2 token
+// passes, then one per token).
+__host__ __device__ __forceinline__ int tile_cost(int T) { return 2 + T; }
+
+inline int meta_bytes(int E) { return (3 * E + 2) * 4; }
+
+inline int smem_bytes(int E) { return kRingBytes + kRedBytes + meta_bytes(E); }
+
+}  // namespace smallm
+}  // namespace qmm

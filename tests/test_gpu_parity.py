@@ -357,6 +357,59 @@ def test_moe_bad_expert_index_flagged(dev):
     assert_within(y, yref, bound, "bad index")
 
 
+# ------------------------- small-M kernels (2..8 rows per matrix, K 2048 / 4096)
+
+SMALLM_SHAPES = [(8, 64, 4096), (4, 64, 4096), (8, 128, 2048), (4, 128, 2048)]
+
+
+@pytest.mark.parametrize("bits,group,K", SMALLM_SHAPES)
+@pytest.mark.parametrize("M", [2, 3, 5, 8])
+def test_linear_small_m(dev, bits, group, K, M):
+    # N = 1000 is not a multiple of the rows per tile: ragged last tile
+    _linear_case(dev, bits, group, 1000, K, M, False, outl=True)
+
+
+@pytest.mark.parametrize("bits,group,K", [(8, 64, 4096), (4, 128, 2048)])
+def test_linear_small_m_bf16(dev, bits, group, K):
+    _linear_case(dev, bits, group, 777, K, 6, True)
+
+
+@pytest.mark.parametrize("bits,group,H,I", [(4, 64, 2048, 2048), (8, 128, 4096, 2048),
+                                            (4, 128, 2048, 4096), (8, 64, 2048, 2048)])
+@pytest.mark.parametrize("bf16", [False, True])
+def test_moe_small_m(dev, bits, group, H, I, bf16):
+    """Decode-sized batches (M <= 8) on the small-M expert kernels."""
+    E, k = 8, 3
+    ex, og, ou, od = _small_experts(dev, E, H, I, bits, group, seed=4)
+    wr = synth.normal(9, 10, E * H, 0.05).reshape(E, H)
+    for M in (1, 3, 8):
+        x = synth.normal(9 + M, 1, M * H).reshape(M, H)
+        if bf16:
+            x, xd = _bf16_x(x, dev)
+        else:
+            xd = T(x, dev)
+        idx, w = oracle.topk(oracle.router_logits(x, wr, None), k)
+        _moe_check(dev, x, xd, idx, w, ex, og, ou, od, what=f"b{bits} g{group} M{M} bf16={bf16}")
+
+
+def test_moe_small_m_token_patterns(dev):
+    """Every token on the same experts (8 tokens per expert), an expert
+    repeated inside each token (16 assignments: two passes of 8), and one
+    expert with 5 tokens beside single-token experts."""
+    E, H, I = 8, 2048, 2048
+    ex, og, ou, od = _small_experts(dev, E, H, I, 4, 64, seed=5)
+    M = 8
+    x = synth.normal(12, 1, M * H).reshape(M, H)
+    w = np.tile(np.array([0.5, 0.3, 0.2], np.float32), (M, 1))
+    idx = np.tile(np.array([1, 4, 6], np.int32), (M, 1))
+    _moe_check(dev, x, T(x, dev), idx, w, ex, og, ou, od, what="8 tokens per expert")
+    idx = np.tile(np.array([2, 2, 5], np.int32), (M, 1))
+    _moe_check(dev, x, T(x, dev), idx, w, ex, og, ou, od, what="repeated expert")
+    idx = np.array([[3, m % 3, 4 + m % 4] for m in range(M)], np.int32)
+    idx[5:, 0] = 7
+    _moe_check(dev, x, T(x, dev), idx, w, ex, og, ou, od, what="mixed")
+
+
 # ----------------------------------------------- full-size MoE workloads
 
 def _full_moe(dev, r):
