@@ -319,6 +319,10 @@ def run_moe(dev, r, steps: int, warmup: int):
     n0 = q.qmm_launch_count()
     for _ in range(steps):
         flush.zero_()
+        # ~0.2 ms of device-side wait so that the host has enqueued the whole
+        # step before its start event: the events then time the GPU, not the
+        # Python launch overhead
+        torch.cuda._sleep(400000)
         evs = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
         step(evs)
         torch.cuda.synchronize()

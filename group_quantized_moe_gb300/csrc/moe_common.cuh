@@ -51,8 +51,8 @@ inline size_t meta_bytes(int E) { return static_cast<size_t>(2 * E + 1) * sizeof
 
 template <typename Kern>
 cudaError_t prep_meta(Kern k, int E) {
-  return cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              static_cast<int>(kSmemBytes + meta_bytes(E)));
+  return ensure_smem(reinterpret_cast<const void *>(k),
+                     static_cast<int>(kSmemBytes + meta_bytes(E)));
 }
 
 // Activation chunks per lane when a row of K values fits in registers (at

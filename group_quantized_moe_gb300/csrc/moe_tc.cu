@@ -655,7 +655,7 @@ cudaError_t run_tc(const CUtensorMap &c0, const CUtensorMap &c1, const CUtensorM
                    const TcArgs &a, cudaStream_t s) {
   auto k = moe_tc_kernel<NT>;
   const int bytes = Smem<NT>::bytes_for(a.E);
-  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  cudaError_t e = ensure_smem(reinterpret_cast<const void *>(k), bytes);
   if (e != cudaSuccess) return e;
   k<<<sm_count(), kThreads, bytes, s>>>(c0, c1, x, a);
   count_launch();

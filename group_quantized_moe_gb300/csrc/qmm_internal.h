@@ -46,6 +46,11 @@ int sm_count();
 // Device status word of the current device.
 uint32_t *device_status();
 
+// Raises a kernel's dynamic shared memory limit to at least `bytes` on the
+// current device (the attribute is set once per kernel and device, not on
+// every launch).
+cudaError_t ensure_smem(const void *kernel, int bytes);
+
 cudaError_t launch_quantize(const float *w, int64_t N, int64_t K, int bits, int group,
                             void *codes, float *scales, int32_t *zps, cudaStream_t s);
 

@@ -443,9 +443,8 @@ cudaError_t launch_moe_dispatch(const int32_t *idx, int64_t M, int k, int E, con
   if (threads < E) threads = ((E + 31) / 32) * 32;  // the scan needs one thread per expert
   if (threads > 1024) return cudaErrorInvalidValue;
   const size_t smem = static_cast<size_t>(2 * E + (threads / 32 + 1) * E) * sizeof(int32_t);
-  cudaError_t err = cudaFuncSetAttribute(moe_dispatch_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(moe_dispatch_smem(E)));
+  cudaError_t err = ensure_smem(reinterpret_cast<const void *>(moe_dispatch_kernel),
+                                static_cast<int>(moe_dispatch_smem(E)));
   if (err != cudaSuccess) return err;
   moe_dispatch_kernel<<<1, threads, smem, s>>>(idx, MK, E, ws, device_status());
   count_launch();

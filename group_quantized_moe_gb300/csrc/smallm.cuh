@@ -8,15 +8,15 @@
 // pass over its weights).
 //
 // GB300 design (HBM-bound: each weight byte is used by 1..8 tokens):
-//  * One CTA of eight warps per SM.  Thread 0 streams tiles of whole weight
-//    rows -- codes, fp32 scales and int32 zero points, three 1-D bulk copies
-//    per matrix -- through a 4-stage ring of 40 KB stages, completion on one
-//    mbarrier per stage (every wait bounded).  A stage is refilled right
-//    after the CTA barrier that ends its last use, so no "empty" barrier is
-//    needed.
+//  * CTAs of eight warps, one or two per SM (see Cfg).  One thread streams
+//    tiles of whole weight rows -- codes, fp32 scales and int32 zero points,
+//    three 1-D bulk copies per matrix -- through a ring of 40 KB stages,
+//    completion on one mbarrier per stage (every wait bounded).  A stage is
+//    refilled right after the CTA barrier that ends its last use, so no
+//    "empty" barrier is needed.
 //  * The eight warps split the K range of every row eight ways: lane l of
 //    warp w owns columns [(32 w + l) XPL, +XPL), XPL = K / 256 (8 or 16),
-//    and keeps those columns of up to eight activation rows in registers for
+//    and keeps those columns of its activation rows in registers for
 //    as long as the CTA stays on one expert.  The slice never straddles a
 //    quantisation group, so it needs one scale and one zero point per row.
 //  * Each lane dequantises its slice of a row once and applies it to every
@@ -38,14 +38,26 @@
 namespace qmm {
 namespace smallm {
 
-constexpr int kCW = 8;                       // consumer warps (K split 8 ways)
+constexpr int kCW = 8;                       // warps; the K range is split 8 ways
 constexpr int kThreads = kCW * 32;
-constexpr int kStages = 4;
 constexpr int kStageBytes = 40960;
-constexpr int kTokMax = 8;                   // activation rows per pass
-constexpr int kRedMax = 256;                 // rows x tokens reduced per tile
-constexpr int kRingBytes = kStages * kStageBytes;
-constexpr int kRedBytes = 2 * kCW * kRedMax * 4;
+
+// Two configurations.  TBMAX 2 (two CTAs per SM, 128 registers: two
+// activation rows per lane, more tokens in passes of two over the staged
+// tile) runs the MoE experts, where most experts of a decode batch have one
+// or two tokens and latency hiding by the second CTA matters more than the
+// repeated dequantisation of the rare larger segments.  TBMAX 8 (one CTA
+// per SM, eight rows per pass) runs the linear layer for 3..8 rows, where
+// every tile serves all M rows.
+template <int TBMAX>
+struct Cfg {
+  static constexpr int kCtas = TBMAX <= 2 ? 2 : 1;      // CTAs per SM
+  static constexpr int kStages = TBMAX <= 2 ? 2 : 4;    // ring stages per CTA
+  static constexpr int kRedMax = TBMAX * 32;            // rows x tokens per tile
+  static constexpr int kRingBytes = kStages * kStageBytes;
+  static constexpr int kRedBytes = 2 * kCW * kRedMax * 4;
+  static int smem_bytes(int E) { return kRingBytes + kRedBytes + (3 * E + 2) * 4; }
+};
 
 enum Mode { kLinear = 0, kGateUp = 1, kDown = 2 };
 
@@ -77,9 +89,9 @@ __host__ __device__ constexpr int rows_per_tile() {
 // passes, then one per token).
 __host__ __device__ __forceinline__ int tile_cost(int T) { return 2 + T; }
 
-inline int meta_bytes(int E) { return (3 * E + 2) * 4; }
-
-inline int smem_bytes(int E) { return kRingBytes + kRedBytes + meta_bytes(E); }
+// Launch with TBMAX 2 (any mode) or TBMAX 8 (the linear layer only).
+cudaError_t run_lo(int mode, bool x_bf16, const Args &a, cudaStream_t s);
+cudaError_t run_hi(int mode, bool x_bf16, const Args &a, cudaStream_t s);
 
 }  // namespace smallm
 }  // namespace qmm

@@ -1,0 +1,577 @@
+// smallm_kernel.cuh -- the small-M fused dequantise-matmul kernel template
+// (design notes in smallm.cuh), instantiated by smallm_lo.cu (two activation
+// rows per pass, two CTAs per SM) and smallm_hi.cu (eight rows per pass, one
+// CTA per SM; the linear layer with 3..8 rows).
+#pragma once
+
+#include <cstdint>
+
+#include "smallm.cuh"
+
+namespace qmm {
+namespace smallm {
+namespace {
+
+typedef unsigned long long f32x2_t;
+
+__device__ __forceinline__ uint2 lds64(uint32_t addr) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+  return v;
+}
+
+__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
+  return v;
+}
+
+// CTA barrier that also ORs a predicate over the threads, so that every
+// thread takes the same decision after it.
+__device__ __forceinline__ bool consumers_sync_or(bool p) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred a, b;\n\t"
+      "setp.ne.u32 a, %1, 0;\n\t"
+      "bar.red.or.pred b, 1, %2, a;\n\t"
+      "selp.u32 %0, 1, 0, b;\n\t}"
+      : "=r"(r)
+      : "r"(p ? 1u : 0u), "n"(kCW * 32)
+      : "memory");
+  return r != 0;
+}
+
+// Bounded wait that also gives up at once when the CTA has aborted.
+__device__ __forceinline__ bool wait_ok(uint32_t bar, uint32_t parity, uint32_t *status,
+                                        volatile int *abort_flag) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (global_timer_ns() - t0 > kWaitLimitNs) {
+      atomicOr(status, kDevWaitTimeout);
+      *abort_flag = 1;
+      return false;
+    }
+  }
+}
+
+// A byte of u placed under the exponent byte 0x4B: the fp32 value 2^23 + byte.
+template <int B>
+__device__ __forceinline__ float mag(uint32_t u) {
+  return __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7440u | B));
+}
+
+// Dot products of this lane's XPL codes of one row with TB activation rows.
+//
+// INT8: a stored byte is q - 128; xor 0x80 gives q, read as 2^23 + q.
+// INT4: a byte holds column 2j (low nibble) and 2j + 1 (high nibble).  The
+// masks 0x0F0F0F0F and 0xF0F0F0F0 leave q and 16 q in each byte, read as
+// 2^23 + q and 2^23 + 16 q; one packed subtract of (2^23 + zp, 2^23 + 16 zp)
+// gives (q - zp, 16 (q - zp)) exactly.  The odd columns' activations are
+// held divided by 16 (a power-of-two scaling), so every product is the
+// product of the pages' formula.
+// xp[t][p] holds columns (2p, 2p + 1) of activation row t.
+template <int BITS, int XPL, int TB, int TBMAX>
+__device__ __forceinline__ void row_dot(uint32_t caddr, float zf,
+                                        const f32x2_t (&xp)[TBMAX][XPL / 2], float (&d)[TB]) {
+  f32x2_t acc[TB];
+#pragma unroll
+  for (int t = 0; t < TB; ++t) acc[t] = 0ull;
+  if constexpr (BITS == 4) {
+    constexpr int NW = XPL / 8;
+    uint32_t w[NW];
+    if constexpr (NW == 2) {
+      const uint2 v = lds64(caddr);
+      w[0] = v.x;
+      w[1] = v.y;
+    } else {
+      w[0] = lds32(caddr);
+    }
+    const f32x2_t off = pack2(8388608.0f + zf, fmaf(16.0f, zf, 8388608.0f));
+#pragma unroll
+    for (int i = 0; i < NW; ++i) {
+      const uint32_t lo = w[i] & 0x0F0F0F0Fu, hi = w[i] & 0xF0F0F0F0u;
+      f32x2_t dq[4];
+      dq[0] = sub2(pack2(mag<0>(lo), mag<0>(hi)), off);
+      dq[1] = sub2(pack2(mag<1>(lo), mag<1>(hi)), off);
+      dq[2] = sub2(pack2(mag<2>(lo), mag<2>(hi)), off);
+      dq[3] = sub2(pack2(mag<3>(lo), mag<3>(hi)), off);
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+#pragma unroll
+        for (int t = 0; t < TB; ++t) acc[t] = fma2(dq[j], xp[t][4 * i + j], acc[t]);
+    }
+  } else {
+    constexpr int NW = XPL / 4;
+    uint32_t w[NW];
+    if constexpr (NW == 4) {
+      const uint4 v = lds128(caddr);
+      w[0] = v.x;
+      w[1] = v.y;
+      w[2] = v.z;
+      w[3] = v.w;
+    } else {
+      const uint2 v = lds64(caddr);
+      w[0] = v.x;
+      w[1] = v.y;
+    }
+    const float m = 8388608.0f + zf;
+    const f32x2_t off = pack2(m, m);
+#pragma unroll
+    for (int i = 0; i < NW; ++i) {
+      const uint32_t u = w[i] ^ 0x80808080u;
+      const f32x2_t d01 = sub2(pack2(mag<0>(u), mag<1>(u)), off);
+      const f32x2_t d23 = sub2(pack2(mag<2>(u), mag<3>(u)), off);
+#pragma unroll
+      for (int t = 0; t < TB; ++t) {
+        acc[t] = fma2(d01, xp[t][2 * i], acc[t]);
+        acc[t] = fma2(d23, xp[t][2 * i + 1], acc[t]);
+      }
+    }
+  }
+#pragma unroll
+  for (int t = 0; t < TB; ++t) {
+    float lo, hi;
+    unpack2(acc[t], lo, hi);
+    d[t] = lo + hi;
+  }
+}
+
+// Butterfly reduce-scatter of C values over the lanes: at offset O a lane
+// keeps one half of its values (the upper half if its bit O is set) and adds
+// the partner's copy of that half; once one value is left the remaining
+// offsets are plain sums.  With V values at the start (V <= 32, a power of
+// two), lane l ends with the full sum of value l >> (5 - log2 V).
+template <int C, int O>
+__device__ __forceinline__ void bfly(float *v, int lane) {
+  if constexpr (O >= 1) {
+    if constexpr (C > 1) {
+      constexpr int H = C / 2;
+      const bool up = (lane & O) != 0;
+#pragma unroll
+      for (int i = 0; i < H; ++i) {
+        const float send = up ? v[i] : v[i + H];
+        const float keep = up ? v[i + H] : v[i];
+        v[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, O);
+      }
+      bfly<H, O / 2>(v, lane);
+    } else {
+      v[0] += __shfl_xor_sync(0xFFFFFFFFu, v[0], O);
+      bfly<1, O / 2>(v, lane);
+    }
+  }
+}
+
+template <int V>
+__host__ __device__ constexpr int log2c() {
+  return V <= 1 ? 0 : 1 + log2c<V / 2>();
+}
+
+// One tile for TB tokens: every row of the stage against the lane's slice of
+// the activations; lane partials reduced per block of NRS rows and written
+// to this warp's row of the reduction buffer (index row * TB + token).
+template <int BITS, int XPL, int NR, int TB, int TBMAX>
+__device__ __forceinline__ void tile_compute(uint32_t stage, int rowbytes, int G, int gi,
+                                             uint32_t lane_off,
+                                             const f32x2_t (&xp)[TBMAX][XPL / 2],
+                                             float *red_w, int lane) {
+  constexpr int NRS = (NR * TB <= 32) ? NR : 32 / TB;
+  constexpr int V = NRS * TB;
+  constexpr int LV = log2c<V>();
+  const uint32_t sc0 = stage + NR * rowbytes + 4 * gi;
+  const uint32_t zp0 = sc0 + NR * G * 4;
+#pragma unroll
+  for (int sb = 0; sb < NR; sb += NRS) {
+    float v[V];
+#pragma unroll
+    for (int r = 0; r < NRS; ++r) {
+      const int row = sb + r;
+      const float s = lds_f32(sc0 + row * G * 4);
+      const float zf = static_cast<float>(lds_s32(zp0 + row * G * 4));
+      float d[TB];
+      row_dot<BITS, XPL, TB, TBMAX>(stage + row * rowbytes + lane_off, zf, xp, d);
+#pragma unroll
+      for (int t = 0; t < TB; ++t) v[r * TB + t] = s * d[t];
+    }
+    bfly<V, 16>(v, lane);
+    if ((lane & ((32 >> LV) - 1)) == 0) red_w[sb * TB + (lane >> (5 - LV))] = v[0];
+  }
+}
+
+// This lane's activation slice of up to TBMAX rows: rows[t] for t < T,
+// zeros after.  INT4 keeps odd columns divided by 16 (see row_dot).
+template <int BITS, int XPL, bool XBF16, int TBMAX>
+__device__ __forceinline__ void load_x(const void *const (&rows)[TBMAX], int T, int col0,
+                                       f32x2_t (&xp)[TBMAX][XPL / 2]) {
+  const float odd = BITS == 4 ? 0.0625f : 1.0f;
+#pragma unroll
+  for (int t = 0; t < TBMAX; ++t) {
+    float v[XPL];
+    if (t < T) {
+      if constexpr (XBF16) {
+        const uint4 *p = reinterpret_cast<const uint4 *>(
+            static_cast<const uint16_t *>(rows[t]) + col0);
+#pragma unroll
+        for (int c = 0; c < XPL / 8; ++c) {
+          const uint4 u = __ldg(p + c);
+          const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+          for (int h = 0; h < 4; ++h) {
+            v[8 * c + 2 * h] = __uint_as_float(wv[h] << 16);
+            v[8 * c + 2 * h + 1] = __uint_as_float(wv[h] & 0xFFFF0000u);
+          }
+        }
+      } else {
+        const float4 *p = reinterpret_cast<const float4 *>(static_cast<const float *>(rows[t]) + col0);
+#pragma unroll
+        for (int c = 0; c < XPL / 4; ++c) {
+          const float4 f = __ldg(p + c);
+          v[4 * c] = f.x;
+          v[4 * c + 1] = f.y;
+          v[4 * c + 2] = f.z;
+          v[4 * c + 3] = f.w;
+        }
+      }
+    } else {
+#pragma unroll
+      for (int c = 0; c < XPL; ++c) v[c] = 0.0f;
+    }
+#pragma unroll
+    for (int p = 0; p < XPL / 2; ++p) xp[t][p] = pack2(v[2 * p], v[2 * p + 1] * odd);
+  }
+}
+
+__device__ __forceinline__ float silu(float g) { return g / (1.0f + expf(-g)); }
+
+__device__ __forceinline__ int64_t ceil_div(int64_t n, int64_t d) {
+  return n <= 0 ? -((-n) / d) : (n + d - 1) / d;
+}
+
+}  // namespace
+}  // namespace smallm
+}  // namespace qmm
+
+
+namespace qmm {
+namespace smallm {
+namespace {
+
+// Segment s of the work: expert s_active[s], whose tokens sit at sorted
+// positions s_off[e] .. s_off[e + 1] (the linear layer: one segment of M
+// rows).  s_cs[s] = sum of the per-tile cost of the earlier segments.
+// Tile j of a segment covers rows [j * RT, j * RT + RT) of each matrix.
+// A segment with more than TBMAX tokens is applied TBMAX tokens at a time
+// to the same staged tile.
+struct TileIt {
+  int s;
+  int64_t j, jhi;
+  bool valid;
+};
+
+template <int BITS, int XPL, int MODE, bool XBF16, int TBMAX>
+__global__ void __launch_bounds__(kThreads, Cfg<TBMAX>::kCtas) smallm_kernel(const Args a) {
+  using C = Cfg<TBMAX>;
+  constexpr int STAGES = C::kStages, RED = C::kRedMax;
+  constexpr int NR = rows_per_tile<BITS, XPL>();
+  constexpr int RT = (MODE == kGateUp) ? NR / 2 : NR;  // rows per matrix per tile
+  constexpr int NM = (MODE == kGateUp) ? 2 : 1;
+  constexpr int LB = XPL * BITS / 8;                   // code bytes per lane per row
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ __align__(8) uint64_t full_bar[STAGES];
+  __shared__ int abort_s, nseg_s;
+  volatile int *abort_flag = &abort_s;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  float *red = reinterpret_cast<float *>(smem + C::kRingBytes);
+  int32_t *s_active = reinterpret_cast<int32_t *>(smem + C::kRingBytes + C::kRedBytes);
+  int32_t *s_off = s_active + a.E;
+  int32_t *s_cs = s_off + a.E + 1;
+  const uint32_t ring = smem_addr(smem);
+
+  // Segments: the experts with tokens, in expert order (the linear layer:
+  // one segment of M rows).
+  if constexpr (MODE == kLinear) {
+    if (threadIdx.x == 0) {
+      s_active[0] = 0;
+      s_off[0] = 0;
+      s_off[1] = static_cast<int32_t>(a.M);
+      nseg_s = 1;
+    }
+  } else {
+    const int n = *a.ws.num_active;
+    for (int i = threadIdx.x; i < n; i += blockDim.x) s_active[i] = a.ws.active[i];
+    for (int i = threadIdx.x; i <= a.E; i += blockDim.x) s_off[i] = a.ws.offsets[i];
+    if (threadIdx.x == 0) nseg_s = n;
+  }
+  if (threadIdx.x == 0) {
+    abort_s = 0;
+    for (int s = 0; s < STAGES; ++s) mbar_init(smem_addr(&full_bar[s]), 1);
+    mbar_fence_init();
+  }
+  __syncthreads();
+  if (warp == 0) {
+    // Per-tile cost prefix over the segments: a run of segments per lane,
+    // then a warp scan of the run totals.
+    const int nseg = *static_cast<volatile int *>(&nseg_s);
+    const int per = (nseg + 31) / 32;
+    const int lo = min(nseg, lane * per), hi = min(nseg, lo + per);
+    int sum = 0;
+    for (int i = lo; i < hi; ++i) {
+      const int e = s_active[i];
+      sum += tile_cost(s_off[e + 1] - s_off[e]);
+    }
+    int incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+      if (lane >= o) incl += t;
+    }
+    int run = incl - sum;
+    for (int i = lo; i < hi; ++i) {
+      s_cs[i] = run;
+      const int e = s_active[i];
+      run += tile_cost(s_off[e + 1] - s_off[e]);
+    }
+    if (lane == 31) s_cs[nseg] = incl;
+  }
+  __syncthreads();
+  const int na = nseg_s;
+
+  // This CTA's tiles: those whose start cost c satisfies
+  // blockIdx.x * total <= c * gridDim.x < (blockIdx.x + 1) * total.
+  const int64_t Gd = gridDim.x;
+  const int64_t tiles = a.tiles;
+  const int64_t total = tiles * s_cs[na];
+  const int64_t lo_c = static_cast<int64_t>(blockIdx.x) * total;
+  const int64_t hi_c = lo_c + total;
+  int s_first;
+  {
+    int l = 0, h = na;  // smallest s whose cost range ends beyond lo_c
+    while (l < h) {
+      const int m = (l + h) >> 1;
+      if (tiles * s_cs[m + 1] * Gd > lo_c) h = m;
+      else l = m + 1;
+    }
+    s_first = l;
+  }
+  // Tile range [jlo, jhi) of segment s; false once the segment starts at or
+  // beyond the end of this CTA's range.
+  auto seg_range = [&](int s, int64_t &jlo, int64_t &jhi) -> bool {
+    if (s >= na) return false;
+    const int64_t base = tiles * s_cs[s] * Gd;
+    if (base >= hi_c) return false;
+    const int e = s_active[s];
+    const int64_t c = tile_cost(s_off[e + 1] - s_off[e]) * Gd;
+    jlo = ceil_div(lo_c - base, c);
+    jhi = ceil_div(hi_c - base, c);
+    jlo = jlo < 0 ? 0 : (jlo > tiles ? tiles : jlo);
+    jhi = jhi < 0 ? 0 : (jhi > tiles ? tiles : jhi);
+    return true;
+  };
+  auto it_settle = [&](TileIt &it) {  // move to the first segment with a tile left
+    while (it.j >= it.jhi) {
+      ++it.s;
+      int64_t jlo = 0, jhi = 0;
+      if (!seg_range(it.s, jlo, jhi)) {
+        it.valid = false;
+        return;
+      }
+      it.j = jlo;
+      it.jhi = jhi;
+    }
+  };
+  auto it_begin = [&]() {
+    TileIt it{s_first, 0, 0, true};
+    if (!seg_range(it.s, it.j, it.jhi)) {
+      it.valid = false;
+      return it;
+    }
+    it_settle(it);
+    return it;
+  };
+  auto it_next = [&](TileIt &it) {
+    ++it.j;
+    it_settle(it);
+  };
+  const int64_t rows = a.rows;
+  const int rowbytes = a.rowbytes, G = a.G;
+
+  // Thread 0 streams the tiles: codes, scales and zero points of RT rows of
+  // each matrix, three bulk copies per matrix completing on the stage's
+  // barrier.
+  auto issue = [&](const TileIt &it, int st) {
+    const int e = s_active[it.s];
+    const int64_t n0 = it.j * RT;
+    const int rv = static_cast<int>(min64(RT, rows - n0));
+    const uint32_t fb = smem_addr(&full_bar[st]);
+    const uint32_t stage = ring + st * kStageBytes;
+    mbar_arrive_expect_tx(fb, static_cast<uint32_t>(NM * rv * (rowbytes + 8 * G)));
+#pragma unroll
+    for (int m = 0; m < NM; ++m) {
+      const QMat &W = m == 0 ? a.w0 : a.w1;
+      const int r0 = m * RT;
+      bulk_g2s(stage + r0 * rowbytes, W.codes + e * W.codes_stride + n0 * rowbytes,
+               static_cast<uint32_t>(rv * rowbytes), fb);
+      bulk_g2s(stage + NR * rowbytes + r0 * G * 4, W.scales + e * W.groups_stride + n0 * G,
+               static_cast<uint32_t>(rv * G * 4), fb);
+      bulk_g2s(stage + NR * rowbytes + NR * G * 4 + r0 * G * 4,
+               W.zps + e * W.groups_stride + n0 * G, static_cast<uint32_t>(rv * G * 4), fb);
+    }
+  };
+  // Every thread tracks the producer's position (it is cheap and keeps the
+  // issuing role free to rotate over the warps); thread 0 fills the ring.
+  TileIt pit = it_begin();
+  int64_t issued = 0;
+  for (int st = 0; st < STAGES && pit.valid; ++st) {
+    if (threadIdx.x == 0) issue(pit, st);
+    it_next(pit);
+    ++issued;
+  }
+
+  const int col0 = threadIdx.x * XPL;  // this lane's columns
+  const int gi = col0 / a.group;
+  const uint32_t lane_off = static_cast<uint32_t>(threadIdx.x * LB);
+  f32x2_t xp[TBMAX][XPL / 2];
+  int cur_s = -1, cur_b = -1;
+  int64_t i = 0, step = 0, pending = 0;
+  bool stop = false;
+  for (TileIt it = it_begin(); it.valid && !stop; it_next(it), ++i) {
+    pending = i;
+    const int s = it.s;
+    const int e = s_active[s];
+    const int p0 = s_off[e];
+    const int T = s_off[e + 1] - p0;
+    const int nb = (T + TBMAX - 1) / TBMAX;
+    const int st = static_cast<int>(i % STAGES);
+    const bool ok = wait_ok(smem_addr(&full_bar[st]), static_cast<uint32_t>((i / STAGES) & 1),
+                            a.status, abort_flag);
+    const uint32_t stage = ring + st * kStageBytes;
+    const int64_t n0 = it.j * RT;
+    for (int b = 0; b < nb; ++b, ++step) {
+      const int t0 = b * TBMAX;
+      const int Tb = min(TBMAX, T - t0);
+      const int TB = Tb <= 1 ? 1 : Tb <= 2 ? 2 : Tb <= 4 ? 4 : 8;
+      float *red_w = red + (step & 1) * kCW * RED + warp * RED;
+      if (ok) {
+        if (s != cur_s || b != cur_b) {
+          const void *xr[TBMAX];
+#pragma unroll
+          for (int t = 0; t < TBMAX; ++t) {
+            const int64_t tt = t0 + (t < Tb ? t : 0);
+            if constexpr (MODE == kLinear) {
+              xr[t] = XBF16 ? static_cast<const void *>(static_cast<const uint16_t *>(a.x) + tt * a.K)
+                            : static_cast<const void *>(static_cast<const float *>(a.x) + tt * a.K);
+            } else if constexpr (MODE == kGateUp) {
+              const int64_t tok = a.ws.assign[p0 + tt] / a.k;
+              xr[t] = XBF16 ? static_cast<const void *>(static_cast<const uint16_t *>(a.x) + tok * a.K)
+                            : static_cast<const void *>(static_cast<const float *>(a.x) + tok * a.K);
+            } else {
+              xr[t] = a.ws.h + (p0 + tt) * a.K;
+            }
+          }
+          load_x<BITS, XPL, (MODE != kDown) && XBF16, TBMAX>(xr, Tb, col0, xp);
+          cur_s = s;
+          cur_b = b;
+        }
+        if (TB == 1) {
+          tile_compute<BITS, XPL, NR, 1, TBMAX>(stage, rowbytes, G, gi, lane_off, xp, red_w, lane);
+        } else if (TB == 2 || TBMAX == 2) {
+          tile_compute<BITS, XPL, NR, 2, TBMAX>(stage, rowbytes, G, gi, lane_off, xp, red_w, lane);
+        } else {
+          if constexpr (TBMAX >= 8) {
+            if (TB == 4)
+              tile_compute<BITS, XPL, NR, 4, TBMAX>(stage, rowbytes, G, gi, lane_off, xp, red_w, lane);
+            else
+              tile_compute<BITS, XPL, NR, 8, TBMAX>(stage, rowbytes, G, gi, lane_off, xp, red_w, lane);
+          }
+        }
+      }
+      // Every warp has written its partials (and, after the last batch, has
+      // finished reading the stage); the OR tells all threads whether any
+      // gave up.
+      if (consumers_sync_or(!ok || *abort_flag != 0)) {
+        stop = true;
+        break;
+      }
+      if (b == nb - 1 && pit.valid) {
+        // The stage is free: lane 0 of warp i % 8 refills it with the tile
+        // STAGES ahead (the role rotates so that no warp is always late).
+        if (lane == 0 && warp == static_cast<int>(i % kCW)) {
+          fence_proxy_async_smem();
+          issue(pit, st);
+        }
+        it_next(pit);
+        ++issued;
+      }
+      // Finalise: thread q sums the eight warp partials of one (row, token)
+      // output in warp order; q = 0 starts at warp (step + 1) % 8, so the
+      // usually short list of outputs also rotates over the warps.
+      const float *rb = red + (step & 1) * kCW * RED;
+      const int q = (threadIdx.x + kThreads - 32 * static_cast<int>((step + 1) % kCW)) % kThreads;
+      if (q < RT * TB) {
+        const int r = q / TB, t = q % TB;
+        if (t < Tb && n0 + r < rows) {
+          float acc0 = 0.0f;
+#pragma unroll
+          for (int w = 0; w < kCW; ++w) acc0 += rb[w * RED + r * TB + t];
+          const int64_t pos = static_cast<int64_t>(p0) + t0 + t;
+          if constexpr (MODE == kGateUp) {
+            float acc1 = 0.0f;
+#pragma unroll
+            for (int w = 0; w < kCW; ++w) acc1 += rb[w * RED + (RT + r) * TB + t];
+            a.ws.h[pos * rows + n0 + r] = silu(acc0) * acc1;
+          } else if constexpr (MODE == kDown) {
+            a.ws.out[pos * rows + n0 + r] = acc0;
+          } else {
+            a.y[pos * rows + n0 + r] = acc0;
+          }
+        }
+      }
+    }
+  }
+  if (threadIdx.x == 0) {
+    // After an abort, wait (bounded) for the copies that may still be landing
+    // (tiles pending .. issued - 1); after a normal end they have all landed.
+    for (int64_t u = pending; u < issued; ++u)
+      mbar_wait_bounded(smem_addr(&full_bar[u % STAGES]), static_cast<uint32_t>((u / STAGES) & 1),
+                        a.status);
+  }
+  __syncthreads();
+}
+
+template <int BITS, int XPL, int MODE, bool XBF16, int TBMAX>
+cudaError_t run(const Args &a, cudaStream_t s) {
+  auto k = smallm_kernel<BITS, XPL, MODE, XBF16, TBMAX>;
+  const int smem = Cfg<TBMAX>::smem_bytes(a.E);
+  cudaError_t e = ensure_smem(reinterpret_cast<const void *>(k), smem);
+  if (e != cudaSuccess) return e;
+  k<<<Cfg<TBMAX>::kCtas * sm_count(), kThreads, smem, s>>>(a);
+  count_launch();
+  return cudaGetLastError();
+}
+
+template <int MODE, bool XBF16, int TBMAX>
+cudaError_t run_shape(const Args &a, cudaStream_t s) {
+  const int xpl = static_cast<int>(a.K / 256);
+  if (a.w0.bits == 4)
+    return xpl == 16 ? run<4, 16, MODE, XBF16, TBMAX>(a, s) : run<4, 8, MODE, XBF16, TBMAX>(a, s);
+  return xpl == 16 ? run<8, 16, MODE, XBF16, TBMAX>(a, s) : run<8, 8, MODE, XBF16, TBMAX>(a, s);
+}
+
+template <int TBMAX>
+cudaError_t run_class(int mode, bool x_bf16, const Args &a, cudaStream_t s) {
+  if (mode == kLinear)
+    return x_bf16 ? run_shape<kLinear, true, TBMAX>(a, s) : run_shape<kLinear, false, TBMAX>(a, s);
+  if constexpr (TBMAX > 2) {
+    return cudaErrorInvalidValue;  // the experts run in passes of two
+  } else {
+    if (mode == kGateUp)
+      return x_bf16 ? run_shape<kGateUp, true, TBMAX>(a, s) : run_shape<kGateUp, false, TBMAX>(a, s);
+    return run_shape<kDown, false, TBMAX>(a, s);
+  }
+}
+
+}  // namespace
+}  // namespace smallm
+}  // namespace qmm

@@ -324,7 +324,7 @@ inline void layouts(int rowbytes, int G, int RT, int copies, TileLayout *out) {
 
 template <typename Kern>
 cudaError_t prep(Kern k) {
-  return cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  return ensure_smem(reinterpret_cast<const void *>(k), kSmemBytes);
 }
 
 }  // namespace tile
