@@ -28,6 +28,7 @@ struct GemvArgs {
 
 template <int BITS, int RT, int MT, bool XBF16, bool GSM, int NCL>
 __global__ void __launch_bounds__(kWarps * 32, 1) gemv_kernel(GemvArgs a) {
+  pdl_enter();
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ __align__(8) uint64_t bars[kWarps][kSlots];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -131,9 +132,7 @@ cudaError_t run_gemv(GemvArgs a, cudaStream_t s) {
   const int64_t ntiles = (a.N + RT - 1) / RT;
   int64_t blocks = (ntiles + kWarps - 1) / kWarps;
   if (blocks > sm_count()) blocks = sm_count();
-  k<<<static_cast<unsigned>(blocks), kWarps * 32, kSmemBytes, s>>>(a);
-  count_launch();
-  return cudaGetLastError();
+  return launch_pdl(k, dim3(static_cast<unsigned>(blocks)), dim3(kWarps * 32), kSmemBytes, s, a);
 }
 
 template <int BITS, int RT, bool XBF16, bool GSM>

@@ -26,6 +26,7 @@ struct DownArgs {
 
 template <int BITS, int RT, int MT, bool GSM, int NCL>
 __global__ void __launch_bounds__(kWarps * 32, 1) moe_down_kernel(DownArgs a) {
+  pdl_enter();
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ __align__(8) uint64_t bars[kWarps][kSlots];
   constexpr int CH = (BITS == 8) ? 16 : 32;
@@ -141,9 +142,7 @@ cudaError_t run_down(DownArgs a, cudaStream_t s) {
   cudaError_t e = prep_meta(k, a.E);
   if (e != cudaSuccess) return e;
   layouts(a.L.rowbytes, a.L.G, RT, 1, &a.L);
-  k<<<sm_count(), kWarps * 32, kSmemBytes + meta_bytes(a.E), s>>>(a);
-  count_launch();
-  return cudaGetLastError();
+  return launch_pdl(k, dim3(sm_count()), dim3(kWarps * 32), kSmemBytes + meta_bytes(a.E), s, a);
 }
 
 template <int BITS, int RT, int MT, bool GSM>

@@ -35,6 +35,7 @@ __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g));
 
 template <int BITS, int RT, int MT, bool XBF16, bool GSM, int NCL>
 __global__ void __launch_bounds__(kWarps * 32, 1) moe_gateup_kernel(GateUpArgs a) {
+  pdl_enter();
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ __align__(8) uint64_t bars[kWarps][kSlots];
   constexpr int CH = (BITS == 8) ? 16 : 32;
@@ -208,9 +209,7 @@ cudaError_t run_gateup(GateUpArgs a, cudaStream_t s) {
   layouts(a.Lg.rowbytes, a.Lg.G, RT, 2, L);
   a.Lg = L[0];
   a.Lu = L[1];
-  k<<<sm_count(), kWarps * 32, kSmemBytes + meta_bytes(a.E), s>>>(a);
-  count_launch();
-  return cudaGetLastError();
+  return launch_pdl(k, dim3(sm_count()), dim3(kWarps * 32), kSmemBytes + meta_bytes(a.E), s, a);
 }
 
 template <int BITS, int RT, int MT, bool XBF16, bool GSM>

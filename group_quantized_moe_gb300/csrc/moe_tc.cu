@@ -282,6 +282,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     moe_tc_kernel(const __grid_constant__ CUtensorMap tm_codes0,
                   const __grid_constant__ CUtensorMap tm_codes1,
                   const __grid_constant__ CUtensorMap tm_x, TcArgs a) {
+  pdl_enter();
   using S = Smem<NT>;
   constexpr int kA = S::kA, kB = S::kB, kC = S::kC;
   extern __shared__ uint8_t smem_raw[];
@@ -588,6 +589,7 @@ __global__ void __launch_bounds__(256) gather_x_kernel(const uint16_t *__restric
                                                        const int32_t *__restrict__ offsets,
                                                        const int32_t *__restrict__ assign,
                                                        __half *__restrict__ xg) {
+  pdl_enter();
   const int64_t H8 = H / 8;
   const int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (t >= MK * H8) return;
@@ -657,9 +659,7 @@ cudaError_t run_tc(const CUtensorMap &c0, const CUtensorMap &c1, const CUtensorM
   const int bytes = Smem<NT>::bytes_for(a.E);
   cudaError_t e = ensure_smem(reinterpret_cast<const void *>(k), bytes);
   if (e != cudaSuccess) return e;
-  k<<<sm_count(), kThreads, bytes, s>>>(c0, c1, x, a);
-  count_launch();
-  return cudaGetLastError();
+  return launch_pdl(k, dim3(sm_count()), dim3(kThreads), bytes, s, c0, c1, x, a);
 }
 
 }  // namespace
@@ -676,10 +676,10 @@ cudaError_t launch_moe_tc(const void *x, int64_t M, int k, int E, const QMat &ga
   // 1) tokens -> fp16 rows in expert order
   {
     const int64_t n = MK * (H / 8);
-    gather_x_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, s>>>(
-        static_cast<const uint16_t *>(x), MK, k, H, E, ws.offsets, ws.assign, ws.xg);
-    count_launch();
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(gather_x_kernel, dim3(static_cast<unsigned>((n + 255) / 256)),
+                               dim3(256), 0, s, static_cast<const uint16_t *>(x), MK, k, H, E,
+                               static_cast<const int32_t *>(ws.offsets),
+                               static_cast<const int32_t *>(ws.assign), ws.xg);
     if (e != cudaSuccess) return e;
   }
   CUtensorMap mg, mu, md, mx, mh;

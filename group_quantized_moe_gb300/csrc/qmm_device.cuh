@@ -29,6 +29,25 @@ __device__ __forceinline__ uint32_t smem_addr(const void *p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// ------------------------------------------- programmatic dependent launch
+//
+// Every kernel of the library is launched with programmatic stream
+// serialization: it may be scheduled while the preceding kernel on the
+// stream is still running, waits here for that kernel's completion (and
+// memory flush) before it touches global memory, and lets the next kernel
+// be scheduled early in turn.  Without a preceding kernel (or launched
+// without the attribute) both are no-ops.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ void pdl_enter() {
+  pdl_wait();
+  pdl_launch_dependents();
+}
+
 // ---------------------------------------------------------------- mbarrier
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {

@@ -4,6 +4,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <utility>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -39,6 +40,26 @@ struct MoeWork {
 
 // Counts one kernel launch (for qmm_launch_count).
 void count_launch();
+
+// Launches `kernel` with programmatic stream serialization (see pdl_wait in
+// qmm_device.cuh) and counts the launch.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t s, Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+  count_launch();
+  return e;
+}
 
 // Number of SMs of the current device (cached per device).
 int sm_count();

@@ -35,6 +35,7 @@ __global__ void __launch_bounds__(256) quantize_kernel(const float *__restrict__
                                                        int64_t K, uint8_t *__restrict__ codes,
                                                        float *__restrict__ scales,
                                                        int32_t *__restrict__ zps) {
+  pdl_enter();
   constexpr int LPG = (GROUP / 4) < 32 ? (GROUP / 4) : 32;  // lanes per group
   constexpr int VPL = GROUP / LPG;                          // values per lane
   constexpr int NV4 = VPL / 4;                              // float4 per lane
@@ -128,10 +129,8 @@ cudaError_t launch_q(const float *w, int64_t N, int64_t K, void *codes, float *s
   const int64_t cap = static_cast<int64_t>(sm_count()) * 8;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
-  quantize_kernel<BITS, GROUP><<<static_cast<unsigned>(blocks), 256, 0, s>>>(
-      w, N, K, static_cast<uint8_t *>(codes), scales, zps);
-  count_launch();
-  return cudaGetLastError();
+  return launch_pdl(quantize_kernel<BITS, GROUP>, dim3(static_cast<unsigned>(blocks)), dim3(256), 0,
+                    s, w, N, K, static_cast<uint8_t *>(codes), scales, zps);
 }
 
 }  // namespace

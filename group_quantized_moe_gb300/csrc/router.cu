@@ -34,7 +34,12 @@ __global__ void __launch_bounds__(128) router_logits_kernel(const void *__restri
                                                             int64_t H,
                                                             const float *__restrict__ wr,
                                                             const float *__restrict__ bias, int E,
-                                                            float *__restrict__ logits) {
+                                                            float *__restrict__ logits,
+                                                            int32_t *__restrict__ counts) {
+  pdl_enter();
+  // The expert histogram is accumulated by the top-k kernel that follows.
+  if (counts && blockIdx.x == 0 && blockIdx.y == 0)
+    for (int e = threadIdx.x; e < E; e += blockDim.x) counts[e] = 0;
   __shared__ float xch[2][32][MB * EB + 1];
   const int p = threadIdx.x;  // partial index
   const int warp = p >> 5, lane = p & 31;
@@ -164,6 +169,7 @@ __global__ void __launch_bounds__(256) router_topk_kernel(const float *__restric
                                                           int32_t *__restrict__ idx,
                                                           float *__restrict__ w,
                                                           int32_t *__restrict__ counts) {
+  pdl_enter();
   const int lane = threadIdx.x & 31;
   const int64_t m = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   if (m >= M) return;
@@ -223,6 +229,7 @@ __global__ void __launch_bounds__(256) router_topk_kernel(const float *__restric
 __global__ void __launch_bounds__(1024) moe_dispatch_kernel(const int32_t *__restrict__ idx,
                                                             int64_t MK, int E, MoeWork ws,
                                                             uint32_t *status) {
+  pdl_enter();
   extern __shared__ int32_t sm[];
   int32_t *cnt = sm;                 // [E]
   int32_t *cursor = sm + E;          // [E]
@@ -353,6 +360,7 @@ __global__ void __launch_bounds__(256) moe_combine_kernel(int64_t M, int k, int6
                                                           const int32_t *__restrict__ pos,
                                                           const float *__restrict__ out,
                                                           void *__restrict__ y) {
+  pdl_enter();
   const int64_t H4 = H / 4;
   const int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (t >= M * H4) return;
@@ -382,21 +390,18 @@ __global__ void __launch_bounds__(256) moe_combine_kernel(int64_t M, int k, int6
 
 template <int MB, int EB, bool XBF16>
 cudaError_t run_logits(const void *x, int64_t M, int64_t H, const float *wr, const float *bias,
-                       int E, float *logits, cudaStream_t s) {
+                       int E, float *logits, int32_t *counts, cudaStream_t s) {
   dim3 grid((E + EB - 1) / EB, static_cast<unsigned>((M + MB - 1) / MB));
-  router_logits_kernel<MB, EB, XBF16><<<grid, 128, 0, s>>>(x, M, H, wr, bias, E, logits);
-  count_launch();
-  return cudaGetLastError();
+  return launch_pdl(router_logits_kernel<MB, EB, XBF16>, grid, dim3(128), 0, s, x, M, H, wr, bias, E,
+                    logits, counts);
 }
 
 template <int EPL>
 cudaError_t run_topk(const float *logits, int64_t M, int E, int k, int32_t *idx, float *w,
                      int32_t *counts, cudaStream_t s) {
   const int64_t threads = M * 32;
-  router_topk_kernel<EPL><<<static_cast<unsigned>((threads + 255) / 256), 256, 0, s>>>(
-      logits, M, E, k, idx, w, counts);
-  count_launch();
-  return cudaGetLastError();
+  return launch_pdl(router_topk_kernel<EPL>, dim3(static_cast<unsigned>((threads + 255) / 256)),
+                    dim3(256), 0, s, static_cast<const float *>(logits), M, E, k, idx, w, counts);
 }
 
 }  // namespace
@@ -410,17 +415,13 @@ cudaError_t launch_router(const void *x, bool x_bf16, int64_t M, int64_t H, cons
   // Small batches: fewer experts per block so that the 4 MB router matrix is
   // spread over more SMs.
   if (M <= 64) {
-    err = x_bf16 ? run_logits<8, 2, true>(x, M, H, wr, bias, E, logits, s)
-                 : run_logits<8, 2, false>(x, M, H, wr, bias, E, logits, s);
+    err = x_bf16 ? run_logits<8, 2, true>(x, M, H, wr, bias, E, logits, counts, s)
+                 : run_logits<8, 2, false>(x, M, H, wr, bias, E, logits, counts, s);
   } else {
-    err = x_bf16 ? run_logits<8, 8, true>(x, M, H, wr, bias, E, logits, s)
-                 : run_logits<8, 8, false>(x, M, H, wr, bias, E, logits, s);
+    err = x_bf16 ? run_logits<8, 8, true>(x, M, H, wr, bias, E, logits, counts, s)
+                 : run_logits<8, 8, false>(x, M, H, wr, bias, E, logits, counts, s);
   }
   if (err != cudaSuccess) return err;
-  if (counts) {
-    err = cudaMemsetAsync(counts, 0, sizeof(int32_t) * E, s);
-    if (err != cudaSuccess) return err;
-  }
   const int epl = (E + 31) / 32;
   if (epl <= 1) return run_topk<1>(logits, M, E, k, idx, w, counts, s);
   if (epl <= 2) return run_topk<2>(logits, M, E, k, idx, w, counts, s);
@@ -446,21 +447,21 @@ cudaError_t launch_moe_dispatch(const int32_t *idx, int64_t M, int k, int E, con
   cudaError_t err = ensure_smem(reinterpret_cast<const void *>(moe_dispatch_kernel),
                                 static_cast<int>(moe_dispatch_smem(E)));
   if (err != cudaSuccess) return err;
-  moe_dispatch_kernel<<<1, threads, smem, s>>>(idx, MK, E, ws, device_status());
-  count_launch();
-  return cudaGetLastError();
+  return launch_pdl(moe_dispatch_kernel, dim3(1), dim3(threads), smem, s, idx, MK, E, ws,
+                    device_status());
 }
 
 cudaError_t launch_moe_combine(int64_t M, int k, int64_t H, const float *topk_w,
                                const MoeWork &ws, void *y, bool y_bf16, cudaStream_t s) {
   const int64_t threads = M * (H / 4);
   const unsigned blocks = static_cast<unsigned>((threads + 255) / 256);
+  const int32_t *pos = ws.pos;
+  const float *out = ws.out;
   if (y_bf16)
-    moe_combine_kernel<true><<<blocks, 256, 0, s>>>(M, k, H, topk_w, ws.pos, ws.out, y);
-  else
-    moe_combine_kernel<false><<<blocks, 256, 0, s>>>(M, k, H, topk_w, ws.pos, ws.out, y);
-  count_launch();
-  return cudaGetLastError();
+    return launch_pdl(moe_combine_kernel<true>, dim3(blocks), dim3(256), 0, s, M, k, H, topk_w, pos,
+                      out, y);
+  return launch_pdl(moe_combine_kernel<false>, dim3(blocks), dim3(256), 0, s, M, k, H, topk_w, pos,
+                    out, y);
 }
 
 }  // namespace qmm

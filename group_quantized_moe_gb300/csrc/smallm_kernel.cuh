@@ -272,6 +272,7 @@ struct TileIt {
 
 template <int BITS, int XPL, int MODE, bool XBF16, int TBMAX>
 __global__ void __launch_bounds__(kThreads, Cfg<TBMAX>::kCtas) smallm_kernel(const Args a) {
+  pdl_enter();
   using C = Cfg<TBMAX>;
   constexpr int STAGES = C::kStages, RED = C::kRedMax;
   constexpr int NR = rows_per_tile<BITS, XPL>();
@@ -546,9 +547,7 @@ cudaError_t run(const Args &a, cudaStream_t s) {
   const int smem = Cfg<TBMAX>::smem_bytes(a.E);
   cudaError_t e = ensure_smem(reinterpret_cast<const void *>(k), smem);
   if (e != cudaSuccess) return e;
-  k<<<Cfg<TBMAX>::kCtas * sm_count(), kThreads, smem, s>>>(a);
-  count_launch();
-  return cudaGetLastError();
+  return launch_pdl(k, dim3(Cfg<TBMAX>::kCtas * sm_count()), dim3(kThreads), smem, s, a);
 }
 
 template <int MODE, bool XBF16, int TBMAX>
