@@ -19,8 +19,9 @@
 // (token tile of an expert, 128-feature tile):
 //   warp 16 (one lane): TMA producer of weight codes [128 rows x 64 K] into a
 //     deep ring (64B swizzle for INT8).
-//   warp 18 (one lane): TMA producer of token rows [16 x 64 K] fp16 into the
-//     B stages (128B swizzle, the canonical K-major operand layout).
+//   warp 18 (one lane): TMA producer of token rows [npad x 64 K] fp16 into
+//     the B stages (128B swizzle, the canonical K-major operand layout):
+//     16-row boxes for up to 64 tokens, one 128-row box above.
 //   warps 0-15 = four dequant warpgroups; warpgroup g converts the stages
 //     kb = g (mod 4), thread t the whole 64-K row t % 128 of each weight tile,
 //     so four stages are being converted at once (one stage's conversion is
@@ -69,14 +70,17 @@ struct Ring;  // NT = weight tiles sharing one token tile (2: gate+up, 1: down)
 // TMEM: accumulators in columns [0, 256) (gate, up for NT=2; the two k-step
 // parities for NT=1), then the A stages: NT=2 uses 256 + 4*2*32 = 512
 // columns, NT=1 uses 256 + 4*32 = 384 (allocation 512).
+// The code ring only has to cover HBM latency and the TMA queue; a deeper
+// one delays the token-tile loads queued behind it, so the token ring is the
+// deeper of the two.
 template <>
 struct Ring<2> {
-  static constexpr int kA = 4, kB = 4, kC = 8;
+  static constexpr int kA = 4, kB = 6, kC = 4;
   static constexpr uint32_t kTmemCols = 512;
 };
 template <>
 struct Ring<1> {
-  static constexpr int kA = 4, kB = 4, kC = 16;
+  static constexpr int kA = 4, kB = 6, kC = 8;
   static constexpr uint32_t kTmemCols = 512;
 };
 
@@ -281,7 +285,8 @@ template <int NT>
 __global__ void __launch_bounds__(kThreads, 1)
     moe_tc_kernel(const __grid_constant__ CUtensorMap tm_codes0,
                   const __grid_constant__ CUtensorMap tm_codes1,
-                  const __grid_constant__ CUtensorMap tm_x, TcArgs a) {
+                  const __grid_constant__ CUtensorMap tm_x,
+                  const __grid_constant__ CUtensorMap tm_x128, TcArgs a) {
   pdl_enter();
   using S = Smem<NT>;
   constexpr int kA = S::kA, kB = S::kB, kC = S::kC;
@@ -378,9 +383,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int s = static_cast<int>(gs % kB);
           const uint32_t su = static_cast<uint32_t>(gs / kB);
           if (!wait_ok(b_free(s), (su & 1u) ^ 1u, a.status, abort_flag)) break;
-          mbar_arrive_expect_tx(b_full(s), npad * kBK * 2);
-          for (int r = 0; r < npad; r += 16)
-            tma_load_2d(sB + s * kBTile + r * kBK * 2, &tm_x, kb * kBK, it.t0 + r, b_full(s));
+          if (npad > 64) {
+            // one 128-row box (rows past the item's tokens are never used)
+            mbar_arrive_expect_tx(b_full(s), kBN * kBK * 2);
+            tma_load_2d(sB + s * kBTile, &tm_x128, kb * kBK, it.t0, b_full(s));
+          } else {
+            mbar_arrive_expect_tx(b_full(s), npad * kBK * 2);
+            for (int r = 0; r < npad; r += 16)
+              tma_load_2d(sB + s * kBTile + r * kBK * 2, &tm_x, kb * kBK, it.t0 + r, b_full(s));
+          }
         }
       }
       if (*abort_flag)
@@ -639,13 +650,13 @@ bool make_codes_map(CUtensorMap *m, const QMat &w, int E) {
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// fp16 token rows [MK, K] as a 2-D map, box [64, 16], 128-byte swizzle.
-bool make_rows_map(CUtensorMap *m, const __half *p, int64_t MK, int64_t K) {
+// fp16 token rows [MK, K] as a 2-D map, box [64, box_rows], 128-byte swizzle.
+bool make_rows_map(CUtensorMap *m, const __half *p, int64_t MK, int64_t K, int box_rows) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(MK)};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(K * 2)};
-  cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), 16};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), static_cast<cuuint32_t>(box_rows)};
   cuuint32_t es[2] = {1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<__half *>(p), dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -654,12 +665,12 @@ bool make_rows_map(CUtensorMap *m, const __half *p, int64_t MK, int64_t K) {
 
 template <int NT>
 cudaError_t run_tc(const CUtensorMap &c0, const CUtensorMap &c1, const CUtensorMap &x,
-                   const TcArgs &a, cudaStream_t s) {
+                   const CUtensorMap &x128, const TcArgs &a, cudaStream_t s) {
   auto k = moe_tc_kernel<NT>;
   const int bytes = Smem<NT>::bytes_for(a.E);
   cudaError_t e = ensure_smem(reinterpret_cast<const void *>(k), bytes);
   if (e != cudaSuccess) return e;
-  return launch_pdl(k, dim3(sm_count()), dim3(kThreads), bytes, s, c0, c1, x, a);
+  return launch_pdl(k, dim3(sm_count()), dim3(kThreads), bytes, s, c0, c1, x, x128, a);
 }
 
 }  // namespace
@@ -682,10 +693,11 @@ cudaError_t launch_moe_tc(const void *x, int64_t M, int k, int E, const QMat &ga
                                static_cast<const int32_t *>(ws.assign), ws.xg);
     if (e != cudaSuccess) return e;
   }
-  CUtensorMap mg, mu, md, mx, mh;
+  CUtensorMap mg, mu, md, mx, mx128, mh, mh128;
   if (!make_codes_map(&mg, gate, E) || !make_codes_map(&mu, up, E) ||
-      !make_codes_map(&md, down, E) || !make_rows_map(&mx, ws.xg, MK, H) ||
-      !make_rows_map(&mh, ws.hh, MK, I))
+      !make_codes_map(&md, down, E) || !make_rows_map(&mx, ws.xg, MK, H, 16) ||
+      !make_rows_map(&mx128, ws.xg, MK, H, kBN) || !make_rows_map(&mh, ws.hh, MK, I, 16) ||
+      !make_rows_map(&mh128, ws.hh, MK, I, kBN))
     return cudaErrorInvalidValue;
   // 2) gate + up with SwiGLU -> fp16 h
   TcArgs a{};
@@ -707,7 +719,7 @@ cudaError_t launch_moe_tc(const void *x, int64_t M, int k, int E, const QMat &ga
   a.out = ws.hh;
   a.out_ld = I;
   a.status = device_status();
-  cudaError_t e = run_tc<2>(mg, mu, mx, a, s);
+  cudaError_t e = run_tc<2>(mg, mu, mx, mx128, a, s);
   if (e != cudaSuccess) return e;
   // 3) down -> fp32 per-assignment outputs
   TcArgs d = a;
@@ -724,7 +736,7 @@ cudaError_t launch_moe_tc(const void *x, int64_t M, int k, int E, const QMat &ga
   d.gstride[1] = 0;
   d.out = ws.out;
   d.out_ld = H;
-  return run_tc<1>(md, md, mh, d, s);
+  return run_tc<1>(md, md, mh, mh128, d, s);
 }
 
 }  // namespace qmm
