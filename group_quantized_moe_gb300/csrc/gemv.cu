@@ -28,7 +28,6 @@ struct GemvArgs {
 
 template <int BITS, int RT, int MT, bool XBF16, bool GSM, int NCL>
 __global__ void __launch_bounds__(kWarps * 32, 1) gemv_kernel(GemvArgs a) {
-  pdl_enter();
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ __align__(8) uint64_t bars[kWarps][kSlots];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -49,9 +48,15 @@ __global__ void __launch_bounds__(kWarps * 32, 1) gemv_kernel(GemvArgs a) {
     issue_rows<GSM>(slot_addr(p, s), bar_addr(p, s), a.L, a.codes, a.scales, a.zps, n0, rows);
   };
 
+  // The first weight tiles are requested before waiting for the preceding
+  // kernel: no kernel of a launch sequence writes the quantised weights
+  // (the quantiser lets no successor start early), so their HBM latency
+  // overlaps the previous kernel's tail.  Activations and outputs are only
+  // touched after the wait.
   if (lane == 0)
     for (int s = 0; s < kSlots; ++s)
       if (exists(s)) issue(s);
+  pdl_enter();
 
   // Register-resident activation row (M == 1 and K == 32 * CH * NCL).
   constexpr int CH = (BITS == 8) ? 16 : 32;

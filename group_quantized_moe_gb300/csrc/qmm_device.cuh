@@ -34,9 +34,9 @@ __device__ __forceinline__ uint32_t smem_addr(const void *p) {
 // Every kernel of the library is launched with programmatic stream
 // serialization: it may be scheduled while the preceding kernel on the
 // stream is still running, waits here for that kernel's completion (and
-// memory flush) before it touches global memory, and lets the next kernel
-// be scheduled early in turn.  Without a preceding kernel (or launched
-// without the attribute) both are no-ops.
+// memory flush) before it touches anything a preceding kernel may write,
+// and lets the next kernel be scheduled early in turn.  Without a
+// preceding kernel (or launched without the attribute) both are no-ops.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 __device__ __forceinline__ void pdl_launch_dependents() {

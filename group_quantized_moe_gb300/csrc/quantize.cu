@@ -35,7 +35,9 @@ __global__ void __launch_bounds__(256) quantize_kernel(const float *__restrict__
                                                        int64_t K, uint8_t *__restrict__ codes,
                                                        float *__restrict__ scales,
                                                        int32_t *__restrict__ zps) {
-  pdl_enter();
+  // Waits for the preceding kernel but lets no successor start early: the
+  // codes it writes may be read by a successor's early weight prefetch.
+  pdl_wait();
   constexpr int LPG = (GROUP / 4) < 32 ? (GROUP / 4) : 32;  // lanes per group
   constexpr int VPL = GROUP / LPG;                          // values per lane
   constexpr int NV4 = VPL / 4;                              // float4 per lane

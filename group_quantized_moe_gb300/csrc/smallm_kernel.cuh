@@ -272,7 +272,10 @@ struct TileIt {
 
 template <int BITS, int XPL, int MODE, bool XBF16, int TBMAX>
 __global__ void __launch_bounds__(kThreads, Cfg<TBMAX>::kCtas) smallm_kernel(const Args a) {
-  pdl_enter();
+  // The MoE modes need the routing of the preceding kernels before anything
+  // else; the linear layer first requests its leading weight tiles (see
+  // gemv_kernel) and waits just before loading activations.
+  if constexpr (MODE != kLinear) pdl_enter();
   using C = Cfg<TBMAX>;
   constexpr int STAGES = C::kStages, RED = C::kRedMax;
   constexpr int NR = rows_per_tile<BITS, XPL>();
@@ -429,6 +432,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<TBMAX>::kCtas) smallm_kernel(con
     it_next(pit);
     ++issued;
   }
+  if constexpr (MODE == kLinear) pdl_enter();
 
   const int col0 = threadIdx.x * XPL;  // this lane's columns
   const int gi = col0 / a.group;
