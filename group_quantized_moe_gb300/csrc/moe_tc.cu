@@ -70,17 +70,17 @@ struct Ring;  // NT = weight tiles sharing one token tile (2: gate+up, 1: down)
 // TMEM: accumulators in columns [0, 256) (gate, up for NT=2; the two k-step
 // parities for NT=1), then the A stages: NT=2 uses 256 + 4*2*32 = 512
 // columns, NT=1 uses 256 + 4*32 = 384 (allocation 512).
-// The code ring only has to cover HBM latency and the TMA queue; a deeper
-// one delays the token-tile loads queued behind it, so the token ring is the
-// deeper of the two.
+// The A and B rings have the same depth, so that one commit frees the A
+// and B slots of a stage together; the code ring only has to cover HBM
+// latency (a deeper one delays the token-tile loads queued behind it).
 template <>
 struct Ring<2> {
-  static constexpr int kA = 4, kB = 6, kC = 4;
+  static constexpr int kA = 4, kB = 4, kC = 4;
   static constexpr uint32_t kTmemCols = 512;
 };
 template <>
 struct Ring<1> {
-  static constexpr int kA = 4, kB = 6, kC = 8;
+  static constexpr int kA = 4, kB = 4, kC = 8;
   static constexpr uint32_t kTmemCols = 512;
 };
 
@@ -90,9 +90,9 @@ struct Smem {
   static constexpr int b_off = 0;
   static constexpr int c_off = b_off + kB * kBTile;
   static constexpr int bar_off = c_off + kC * NT * kCTile;
-  // barriers: c_full[kC], c_free[kC], a_full[kA], a_free[kA], b_full[kB],
-  // b_free[kB], acc_full, acc_free
-  static constexpr int nbar = 2 * kC + 2 * kA + 2 * kB + 2;
+  // barriers: c_full[kC], c_free[kC], a_full[kA], ab_free[kA], b_full[kB],
+  // acc_full, acc_free
+  static constexpr int nbar = 2 * kC + 2 * kA + kB + 2;
   static constexpr int misc_off = bar_off + nbar * 8;
   static constexpr int meta_off = misc_off + 16;  // offsets[E+1], tile_start[E+1]
   static constexpr int bytes_for(int E) { return meta_off + 8 * (E + 1) + 1024; }
@@ -116,21 +116,35 @@ struct TcArgs {
 
 // ------------------------------------------------------------ PTX wrappers
 
+// L2 cache policies: weight codes stream through L2 once per token tile
+// (evict first); the gathered token rows are re-read by every feature tile
+// of their expert (evict last), so the code stream must not push them out.
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ uint64_t policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, int x, int y,
-                                            int z, uint32_t bar) {
+                                            int z, uint32_t bar, uint64_t policy) {
   asm volatile(
       "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
+      ".L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar), "l"(policy)
       : "memory");
 }
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y,
-                                            uint32_t bar) {
+                                            uint32_t bar, uint64_t policy) {
   asm volatile(
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "l"(policy)
       : "memory");
 }
 
@@ -297,13 +311,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t *gbase = smem_raw + (base - raw);
   const uint32_t sB = base + S::b_off, sC = base + S::c_off;
   const uint32_t bar0 = base + S::bar_off;
+  static_assert(kA == kB, "A and B slots are freed together");
   auto c_full = [&](int i) { return bar0 + 8 * i; };
   auto c_free = [&](int i) { return bar0 + 8 * (kC + i); };
   auto a_full = [&](int i) { return bar0 + 8 * (2 * kC + i); };
-  auto a_free = [&](int i) { return bar0 + 8 * (2 * kC + kA + i); };
+  // A and B slot s are freed by one MMA commit: commits are costly for the
+  // single issuing thread.
+  auto ab_free = [&](int slot) { return bar0 + 8 * (2 * kC + kA + slot); };
   auto b_full = [&](int i) { return bar0 + 8 * (2 * kC + 2 * kA + i); };
-  auto b_free = [&](int i) { return bar0 + 8 * (2 * kC + 2 * kA + kB + i); };
-  const uint32_t acc_full = bar0 + 8 * (2 * kC + 2 * kA + 2 * kB);
+  const uint32_t acc_full = bar0 + 8 * (2 * kC + 2 * kA + kB);
   const uint32_t acc_free = acc_full + 8;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + S::misc_off);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(gbase + S::misc_off + 4);
@@ -322,14 +338,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(c_full(i), 1);
       mbar_init(c_free(i), 4);  // one arrival per warp of the converting warpgroup
     }
-    for (int i = 0; i < kA; ++i) {
-      mbar_init(a_full(i), 4);
-      mbar_init(a_free(i), 2);  // one commit per MMA issuer
-    }
-    for (int i = 0; i < kB; ++i) {
-      mbar_init(b_full(i), 1);
-      mbar_init(b_free(i), 2);
-    }
+    for (int i = 0; i < kA; ++i) mbar_init(a_full(i), 4);
+    for (int i = 0; i < kA; ++i) mbar_init(ab_free(i), 2);  // one commit per MMA issuer
+    for (int i = 0; i < kB; ++i) mbar_init(b_full(i), 1);
     mbar_init(acc_full, 2);
     mbar_init(acc_free, kDequantWarps);
     *abort_flag = 0;
@@ -352,6 +363,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 16) {
     // ------------------------------------------- TMA producer: weight codes
     if (lane == 0) {
+      const uint64_t pol = policy_evict_first();
       int64_t gs = 0;  // global stage counter
       for (int64_t item = blockIdx.x; item < nitems && !*abort_flag; item += gridDim.x) {
         const Item it = decode_item(s_off, s_ts, a.E, item, ftiles);
@@ -360,10 +372,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t cu = static_cast<uint32_t>(gs / kC);
           if (!wait_ok(c_free(c), (cu & 1u) ^ 1u, a.status, abort_flag)) break;
           mbar_arrive_expect_tx(c_full(c), NT * kCTile);
-          tma_load_3d(sC + (c * NT + 0) * kCTile, &tm_codes0, kb * kBK, it.f * kBM, it.e, c_full(c));
+          tma_load_3d(sC + (c * NT + 0) * kCTile, &tm_codes0, kb * kBK, it.f * kBM, it.e, c_full(c),
+                      pol);
           if (NT == 2)
             tma_load_3d(sC + (c * NT + 1) * kCTile, &tm_codes1, kb * kBK, it.f * kBM, it.e,
-                        c_full(c));
+                        c_full(c), pol);
         }
       }
       // After an abort, wait (bounded) for the copies still landing.
@@ -375,6 +388,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 18) {
     // -------------------------------------------- TMA producer: token rows
     if (lane == 0) {
+      const uint64_t pol = policy_evict_last();
       int64_t gs = 0;
       for (int64_t item = blockIdx.x; item < nitems && !*abort_flag; item += gridDim.x) {
         const Item it = decode_item(s_off, s_ts, a.E, item, ftiles);
@@ -382,15 +396,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kb = 0; kb < kstages; ++kb, ++gs) {
           const int s = static_cast<int>(gs % kB);
           const uint32_t su = static_cast<uint32_t>(gs / kB);
-          if (!wait_ok(b_free(s), (su & 1u) ^ 1u, a.status, abort_flag)) break;
+          if (!wait_ok(ab_free(s), (su & 1u) ^ 1u, a.status, abort_flag)) break;
           if (npad > 64) {
             // one 128-row box (rows past the item's tokens are never used)
             mbar_arrive_expect_tx(b_full(s), kBN * kBK * 2);
-            tma_load_2d(sB + s * kBTile, &tm_x128, kb * kBK, it.t0, b_full(s));
+            tma_load_2d(sB + s * kBTile, &tm_x128, kb * kBK, it.t0, b_full(s), pol);
           } else {
             mbar_arrive_expect_tx(b_full(s), npad * kBK * 2);
             for (int r = 0; r < npad; r += 16)
-              tma_load_2d(sB + s * kBTile + r * kBK * 2, &tm_x, kb * kBK, it.t0 + r, b_full(s));
+              tma_load_2d(sB + s * kBTile + r * kBK * 2, &tm_x, kb * kBK, it.t0 + r, b_full(s),
+                          pol);
           }
         }
       }
@@ -437,8 +452,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                           (kb > 0 || kk > 1) ? 1u : 0u);
             }
           }
-          tc_commit(a_free(sa));
-          tc_commit(b_free(sb));
+          tc_commit(ab_free(sa));
         }
         if (!ok) break;
         tc_commit(acc_full);
@@ -447,7 +461,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // After an abort, wait (bounded) for the MMAs already committed.
       if (*abort_flag)
         for (int64_t j = (gs > kA ? gs - kA : 0); j < gs; ++j)
-          mbar_wait_bounded(a_free(static_cast<int>(j % kA)),
+          mbar_wait_bounded(ab_free(static_cast<int>(j % kA)),
                             static_cast<uint32_t>((j / kA) & 1), a.status);
     }
   } else {
@@ -511,7 +525,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int s = static_cast<int>(gs % kA);
         const uint32_t su = static_cast<uint32_t>(gs / kA);
         bool got = wait_ok(c_full(c), cu & 1u, a.status, abort_flag) &&
-                   wait_ok(a_free(s), (su & 1u) ^ 1u, a.status, abort_flag);
+                   wait_ok(ab_free(s), (su & 1u) ^ 1u, a.status, abort_flag);
         if (!__all_sync(0xFFFFFFFFu, got)) {  // warp-uniform exit
           ok = false;
           break;
