@@ -15,29 +15,30 @@
 //   gate/up: D_g, D_u in TMEM, epilogue h = silu(D_g) * D_u -> fp16 [tok, I]
 //   down:    D_d in TMEM, epilogue -> fp32 out[tok, H]
 //
-// CTA = 20 warps, one CTA per SM, persistent over work items
+// CTA = 18 warps, one CTA per SM, persistent over work items
 // (token tile of an expert, 128-feature tile):
-//   warp 16 (one lane): TMA producer of weight codes [128 rows x 64 K] into a
-//     deep ring (64B swizzle for INT8).
-//   warp 18 (one lane): TMA producer of token rows [npad x 64 K] fp16 into
+//   warp 12 (one lane): TMA producer of weight codes [128 rows x 64 K] into a
+//     ring (64B swizzle for INT8).
+//   warp 13 (one lane): TMA producer of token rows [npad x 64 K] fp16 into
 //     the B stages (128B swizzle, the canonical K-major operand layout):
 //     16-row boxes for up to 64 tokens, one 128-row box above.
-//   warps 0-15 = four dequant warpgroups; warpgroup g converts the stages
-//     kb = g (mod 4), thread t the whole 64-K row t % 128 of each weight tile,
-//     so four stages are being converted at once (one stage's conversion is
+//   warps 0-11 = three dequant warpgroups; warpgroup g converts the stages
+//     kb = g (mod 3), thread t the whole 64-K row t % 128 of each weight tile,
+//     so three stages are being converted at once (one stage's conversion is
 //     latency bound; stages pipeline).  Codes -> fp16 (q - zp) * s, exact up
 //     to the final fp16 rounding, stored with tcgen05.st straight into tensor
 //     memory, where the MMA reads its A operand (row = TMEM lane, two K values
-//     per 32-bit column); this keeps shared memory for deep TMA rings.  After
-//     an item's last stage all four run the epilogue (tcgen05.ld from TMEM,
+//     per 32-bit column); this keeps shared memory for the TMA rings.  After
+//     an item's last stage all three run the epilogue (tcgen05.ld from TMEM,
 //     16-token column blocks in turn).  Each item's scale and zero-point
 //     lines are prefetched into L2 when the item starts.
-//   warps 17 and 19: one lane each issues tcgen05.mma (kind::f16, fp32
-//     accumulate) and tcgen05.commit.  A single thread issues about one MMA
-//     per 60-100 cycles whatever N is, so with few tokens per item two
-//     issuers are needed: for gate/up each owns one accumulator (gate, up);
-//     for down they take alternate 16-K steps into two accumulators that the
-//     epilogue adds.  Warp 17 also allocates TMEM.
+//   warps 14-17: one lane each issues tcgen05.mma (kind::f16, fp32
+//     accumulate) and one tcgen05.commit per stage, which frees the stage's
+//     A and B slots.  A single thread issues only about one MMA per 60-100
+//     cycles whatever N is, so items with few tokens split every stage's
+//     MMAs over the four issuers (four accumulators, summed in the
+//     epilogue); items with more tokens are tensor-bound and use two.
+//     Warp 14 also allocates TMEM.
 // Every wait is bounded; on a timeout the CTA raises QMM_DEV_WAIT_TIMEOUT,
 // stops issuing work, waits (bounded) for what is in flight, frees its TMEM
 // and returns.
@@ -57,8 +58,13 @@ namespace {
 constexpr int kBM = 128;        // weight rows per tile (MMA M)
 constexpr int kBN = 128;        // max tokens per tile (MMA N)
 constexpr int kBK = 64;         // K per stage
-constexpr int kThreads = 640;
-constexpr int kDequantWarps = 16;  // warps 0-15: 4 warpgroups, stages round-robin
+constexpr int kDequantGroups = 3;  // warpgroups converting stages round-robin
+constexpr int kDequantWarps = 4 * kDequantGroups;  // warps 0-11
+constexpr int kWarpCodes = kDequantWarps;          // TMA producer of weight codes
+constexpr int kWarpRows = kDequantWarps + 1;       // TMA producer of token rows
+constexpr int kWarpMma = kDequantWarps + 2;        // first of the four MMA issuers
+constexpr int kThreads = (kDequantWarps + 6) * 32;
+constexpr int kLightN = 64;  // items with at most this many (padded) tokens use 4 issuers
 constexpr int kACols = kBK / 2;         // TMEM columns of one A tile stage
 constexpr int kBTile = kBN * kBK * 2;   // 16 KB fp16
 constexpr int kCTile = kBM * kBK;       // 8 KB INT8 codes (64B swizzle)
@@ -339,14 +345,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(c_free(i), 4);  // one arrival per warp of the converting warpgroup
     }
     for (int i = 0; i < kA; ++i) mbar_init(a_full(i), 4);
-    for (int i = 0; i < kA; ++i) mbar_init(ab_free(i), 2);  // one commit per MMA issuer
+    for (int i = 0; i < kA; ++i) mbar_init(ab_free(i), 4);  // one commit per MMA issuer
     for (int i = 0; i < kB; ++i) mbar_init(b_full(i), 1);
-    mbar_init(acc_full, 2);
+    mbar_init(acc_full, 4);
     mbar_init(acc_free, kDequantWarps);
     *abort_flag = 0;
     mbar_fence_init();
   }
-  if (warp == 17) tmem_alloc(smem_addr(tmem_slot), kTmemCols);
+  if (warp == kWarpMma) tmem_alloc(smem_addr(tmem_slot), kTmemCols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -360,7 +366,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int kstages = static_cast<int>(a.K / kBK);
   const int64_t nitems = static_cast<int64_t>(s_ts[a.E]) * ftiles;
 
-  if (warp == 16) {
+  if (warp == kWarpCodes) {
     // ------------------------------------------- TMA producer: weight codes
     if (lane == 0) {
       const uint64_t pol = policy_evict_first();
@@ -385,7 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_wait_bounded(c_full(static_cast<int>(j % kC)),
                             static_cast<uint32_t>((j / kC) & 1), a.status);
     }
-  } else if (warp == 18) {
+  } else if (warp == kWarpRows) {
     // -------------------------------------------- TMA producer: token rows
     if (lane == 0) {
       const uint64_t pol = policy_evict_last();
@@ -414,42 +420,55 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_wait_bounded(b_full(static_cast<int>(j % kB)),
                             static_cast<uint32_t>((j / kB) & 1), a.status);
     }
-  } else if (warp == 17 || warp == 19) {
+  } else if (warp >= kWarpMma) {
     // ---------------------------------------------------- MMA issuers
-    const int issuer = warp == 17 ? 0 : 1;
+    // A single thread issues only about one MMA per 60-100 cycles whatever
+    // N is, so light items (at most kLightN tokens) spread each stage's MMAs
+    // over four issuers with one accumulator each (64 TMEM columns):
+    //   gate/up: issuer i -> matrix i >> 1, the 16-K steps of parity i & 1
+    //   down:    issuer i -> the 16-K step i of every stage
+    // Heavier items are tensor-bound: issuers 0 and 1 each own a 128-column
+    // accumulator (gate/up: matrix i; down: K steps of parity i), and 2, 3
+    // only take part in the commits.  The epilogue adds the partial sums.
+    const int issuer = warp - kWarpMma;
     if (lane == 0) {
       int64_t gs = 0;
       uint32_t nitem_done = 0;
-      const uint32_t d_tmem = tmem + issuer * kBN;
       for (int64_t item = blockIdx.x; item < nitems && !*abort_flag; item += gridDim.x) {
         const Item it = decode_item(s_off, s_ts, a.E, item, ftiles);
         const int npad = (it.ntok + 15) & ~15;
+        const bool light = npad <= kLightN;
+        const bool active = light || issuer < 2;
         const uint32_t idesc = idesc_f16(npad);
+        const uint32_t d_tmem = tmem + (light ? 64u : 128u) * static_cast<uint32_t>(issuer);
+        const int mat = NT == 2 ? (light ? issuer >> 1 : issuer) : 0;
         // the previous item's epilogue has drained the accumulators
         if (!wait_ok(acc_free, (nitem_done & 1u) ^ 1u, a.status, abort_flag)) break;
         tc_fence_after();
         bool ok = true;
+        uint32_t acc = 0;  // the first MMA of the item into this accumulator overwrites it
         for (int kb = 0; kb < kstages; ++kb, ++gs) {
           const int sa = static_cast<int>(gs % kA), sb = static_cast<int>(gs % kB);
           const uint32_t ua = static_cast<uint32_t>(gs / kA), ub = static_cast<uint32_t>(gs / kB);
+          // every issuer waits for the stage, so that no commit runs ahead of
+          // the slot's phase
           if (!wait_ok(b_full(sb), ub & 1u, a.status, abort_flag) ||
               !wait_ok(a_full(sa), ua & 1u, a.status, abort_flag)) {
             ok = false;
             break;
           }
           tc_fence_after();
+          if (active) {
 #pragma unroll
-          for (int kk = 0; kk < kBK / 16; ++kk) {
-            const uint64_t bdesc = smem_desc_sw128(sB + sb * kBTile + kk * 32);
-            if constexpr (NT == 2) {
-              // issuer t owns accumulator t (gate or up)
-              tc_mma_ts(d_tmem, tmem + a_col(sa, issuer) + kk * 8, bdesc, idesc,
-                        (kb > 0 || kk > 0) ? 1u : 0u);
-            } else {
-              // issuer p takes the 16-K steps of parity p into accumulator p
-              if ((kk & 1) == issuer)
-                tc_mma_ts(d_tmem, tmem + a_col(sa, 0) + kk * 8, bdesc, idesc,
-                          (kb > 0 || kk > 1) ? 1u : 0u);
+            for (int kk = 0; kk < kBK / 16; ++kk) {
+              bool mine;
+              if constexpr (NT == 2) mine = light ? ((kk & 1) == (issuer & 1)) : true;
+              else mine = light ? (kk == issuer) : ((kk & 1) == issuer);
+              if (mine) {
+                tc_mma_ts(d_tmem, tmem + a_col(sa, mat) + kk * 8,
+                          smem_desc_sw128(sB + sb * kBTile + kk * 32), idesc, acc);
+                acc = 1u;
+              }
             }
           }
           tc_commit(ab_free(sa));
@@ -467,7 +486,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ------------------------------------------ dequantisation + epilogue
     const int row = threadIdx.x & (kBM - 1);  // weight row of the tile (= TMEM lane)
-    const int wg = warp >> 2;                  // converts stages kb = wg (mod 4)
+    const int wg = warp >> 2;                  // converts stages kb = wg (mod kDequantGroups)
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     int64_t gs = 0;
     uint32_t nitem_done = 0;
@@ -481,7 +500,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         scp[t] = a.sc[t] + it.e * a.gstride[t] + wrow * a.G;
         zpp[t] = a.zp[t] + it.e * a.gstride[t] + wrow * a.G;
         // pull this row's scale / zero-point lines into L2 for the whole item
-        for (int g = 32 * wg; g < a.G; g += 128) {
+        for (int g = 32 * wg; g < a.G; g += 32 * kDequantGroups) {
           asm volatile("prefetch.global.L2 [%0];" ::"l"(scp[t] + g));
           asm volatile("prefetch.global.L2 [%0];" ::"l"(zpp[t] + g));
         }
@@ -505,15 +524,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       bool ok = true;
       for (int kb = 0; kb < kstages; ++kb, ++gs) {
-        if ((kb & 3) != wg) continue;
+        if (kb % kDequantGroups != wg) continue;
         __half2 s2[NT], mz2[NT];
 #pragma unroll
         for (int t = 0; t < NT; ++t) {
           s2[t] = __float2half2_rn(s_nx[t]);
           mz2[t] = __float2half2_rn(1024.0f + static_cast<float>(z_nx[t]));
         }
-        if (kb + 4 < kstages) {
-          const int gi = ((kb + 4) * kBK) >> a.group_shift;
+        if (kb + kDequantGroups < kstages) {
+          const int gi = ((kb + kDequantGroups) * kBK) >> a.group_shift;
 #pragma unroll
           for (int t = 0; t < NT; ++t) {
             s_nx[t] = __ldg(scp[t] + gi);
@@ -568,12 +587,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       tc_fence_after();
       const int feat = it.f * kBM + row;
-      for (int c0 = 16 * wg; c0 < it.ntok; c0 += 64) {
-        float v0[16];
-        tmem_ld16(tmem + lane_base + c0, v0);
-        if constexpr (NT == 2) {
-          float v1[16];
+      // Accumulators (see the MMA issuers): light items four of 64 columns,
+      // heavy items two of 128; partial sums are added in a fixed order.
+      const bool light = ((it.ntok + 15) & ~15) <= kLightN;
+      for (int c0 = 16 * wg; c0 < it.ntok; c0 += 16 * kDequantGroups) {
+        float v0[16], v1[16];
+        if (light) {
+          float p[16];
+          tmem_ld16(tmem + lane_base + c0, v0);
+          tmem_ld16(tmem + lane_base + 64 + c0, p);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) v0[j] += p[j];
+          tmem_ld16(tmem + lane_base + 128 + c0, v1);
+          tmem_ld16(tmem + lane_base + 192 + c0, p);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) v1[j] += p[j];
+        } else {
+          tmem_ld16(tmem + lane_base + c0, v0);
           tmem_ld16(tmem + lane_base + kBN + c0, v1);
+        }
+        if constexpr (NT == 2) {
+          // v0 = gate, v1 = up
           __half *h = static_cast<__half *>(a.out);
 #pragma unroll
           for (int j = 0; j < 16; ++j)
@@ -581,8 +615,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               h[static_cast<int64_t>(it.t0 + c0 + j) * a.out_ld + feat] =
                   __float2half_rn(silu_f(v0[j]) * v1[j]);
         } else {
-          float v1[16];  // the other k-step parity
-          tmem_ld16(tmem + lane_base + kBN + c0, v1);
+          // partial sums over disjoint K steps
           float *o = static_cast<float *>(a.out);
 #pragma unroll
           for (int j = 0; j < 16; ++j)
@@ -599,7 +632,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // Teardown (every role has drained what it issued), then free TMEM.
   __syncthreads();
-  if (warp == 17) {
+  if (warp == kWarpMma) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }

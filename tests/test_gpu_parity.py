@@ -186,6 +186,49 @@ def test_linear_vocab_head_sampled(dev):
                       f"row {n}")
 
 
+def test_linear_chain_on_one_stream(dev):
+    """Kernels overlap their launches with the preceding kernel: a layer
+    whose input is the previous layer's output must still see that output,
+    and a linear layer launched right after re-quantising its weights in
+    place must see the new codes.  Two layers back to back on one stream
+    (M = 1 GEMV and M = 3 small-M path), then an in-place re-quantisation
+    followed at once by a linear call, all without host synchronisation."""
+    K1, N1, N2 = 2048, 2048, 1000
+    w1 = _weights(N1, K1, seed=3, stream=2)
+    w2 = _weights(N2, N1, seed=3, stream=3)
+    w1b = _weights(N1, K1, seed=4, stream=2)
+    o1, o2, o1b = oracle.quantize(w1, 8, 64), oracle.quantize(w2, 4, 128), oracle.quantize(w1b, 8, 64)
+    g1 = q.qmm_quantize_groupwise(T(w1, dev), 8, 64)
+    g2 = q.qmm_quantize_groupwise(T(w2, dev), 4, 128)
+    w1b_d = T(w1b, dev)
+    d2 = np.abs(oracle.dequantize(o2).astype(np.float64))
+    for M in (1, 3):
+        x = synth.normal(11 + M, 1, M * K1).reshape(M, K1)
+        xd = T(x, dev)
+        y1 = torch.empty((M, N1), dtype=torch.float32, device=dev)
+        y2 = torch.empty((M, N2), dtype=torch.float32, device=dev)
+        torch.cuda.synchronize()
+        q.qmm_linear(xd, g1, y=y1)
+        q.qmm_linear(y1, g2, y=y2)
+        y2 = y2.cpu().numpy()
+        r1, b1 = oracle.linear_fused(x, o1), oracle.linear_bound(x, o1)
+        r2 = oracle.linear_fused(r1.astype(np.float32), o2)
+        # the first layer's error (within b1) propagates through |W2|
+        b2 = oracle.linear_bound(r1.astype(np.float32), o2) + b1 @ d2.T + 1e-6 * np.abs(r2)
+        assert_within(y2, r2, b2, f"chained layers M={M}")
+    x = synth.normal(15, 1, K1).reshape(1, K1)
+    xd = T(x, dev)
+    y_new = torch.empty((1, N1), dtype=torch.float32, device=dev)
+    torch.cuda.synchronize()
+    # three kernels back to back: linear, in-place quantise, linear
+    y_old = q.qmm_linear(xd, g1)
+    q.qmm_quantize_groupwise(w1b_d, 8, 64, out=g1)
+    q.qmm_linear(xd, g1, y=y_new)
+    y_new = y_new.cpu().numpy()
+    assert_within(y_old.cpu().numpy(), oracle.linear_fused(x, o1), oracle.linear_bound(x, o1), "old")
+    assert_within(y_new, oracle.linear_fused(x, o1b), oracle.linear_bound(x, o1b), "re-quantised")
+
+
 # -------------------------------------------------------------- router (A3)
 
 def _router_case(dev, M, E, H, k, bias_kind, bf16, wr=None, x=None):
