@@ -7,7 +7,8 @@ value = algorithmic weight bytes per step (codes + fp32 scale + int32 zero
 point per group) / device time per step, in GB/s.  The two MoE workloads
 (decode M=8 INT4 g64; batched prefill M=512 bf16 INT8 g128 with Zipf-biased
 routing) are measured in the same run and reported under "moe_decode" and
-"moe_prefill" (tokens/s and GB/s).
+"moe_prefill" (tokens/s and GB/s), the INT4 group-128 decode GEMVs under
+"gemv_int4".
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--no-moe] [--cpu-seconds S]
@@ -274,6 +275,47 @@ def run_gemv(dev, steps: int, warmup: int, world: int):
             "h2d": xh.numel() * 4, "d2h": yh.numel() * 4}
 
 
+def run_gemv_int4(dev, steps: int, warmup: int):
+    """The INT4 group-128 decode GEMVs: x[1, 4096] -> W_a[4096, 4096] -> W_b[2048, 4096],
+    back to back.  Both matrices (14.2 MB) would stay in L2, so the step rotates over
+    enough copies of the pair to exceed L2 several times over."""
+    import torch
+    import group_quantized_moe_gb300 as q
+    ra, rb = recipes.CFG3_A, recipes.CFG3_B
+    wa = torch.from_numpy(recipes.linear_weight_rows(ra)).to(dev)
+    wb = torch.from_numpy(recipes.linear_weight_rows(rb)).to(dev)
+    b_pair = weight_bytes(ra.N, ra.K, ra.bits, ra.group) + weight_bytes(rb.N, rb.K, rb.bits, rb.group)
+    copies = max(2, int(4 * 129e6 / b_pair) + 1)
+    pairs = [(q.qmm_quantize_groupwise(wa, ra.bits, ra.group),
+              q.qmm_quantize_groupwise(wb, rb.bits, rb.group)) for _ in range(copies)]
+    del wa, wb
+    x = torch.from_numpy(recipes.linear_x(ra)).to(dev)
+    y1 = torch.empty((1, ra.N), dtype=torch.float32, device=dev)
+    y2 = torch.empty((1, rb.N), dtype=torch.float32, device=dev)
+    s = torch.cuda.current_stream()
+
+    def step(i):
+        ga, gb = pairs[i % copies]
+        q.qmm_linear(x, ga, y=y1, stream=s)
+        q.qmm_linear(y1, gb, y=y2, stream=s)
+
+    for i in range(max(3, warmup)):
+        step(i)
+    torch.cuda.synchronize()
+    n = max(steps, 4 * copies)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(s)
+    for i in range(n):
+        step(i)
+    e1.record(s)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / n
+    return {"workload": "decode step: x[1,4096] -> INT4 g128 W[4096,4096] -> INT4 g128 W[2048,4096]",
+            "ms_per_step": ms, "weight_bytes_per_step": b_pair,
+            "weight_gbs": b_pair / (ms * 1e-3) / 1e9, "copies_rotated": copies,
+            "l2": f"{copies} copies of the pair rotated ({copies * b_pair / 1e6:.0f} MB vs 129 MB L2)"}
+
+
 # ------------------------------------------------------------ MoE workloads
 
 def run_moe(dev, r, steps: int, warmup: int):
@@ -461,6 +503,14 @@ def main():
             "clocks": g["clocks"],
             "e2e": {"value": world * g["bytes"] / (ms_e2e * 1e-3) / 1e9, "unit": "GB/s",
                     "h2d_bytes_per_step": g["h2d"], "d2h_bytes_per_step": g["d2h"]}}
+    if args.only is None:
+        try:
+            gi = run_gemv_int4(dev, args.steps, args.warmup)
+            gi["hbm_frac"] = gi["weight_gbs"] / peaks["hbm_gbs"]
+            line["gemv_int4"] = gi
+        except Exception as e:  # keep the headline line even if an extra fails
+            line["gemv_int4"] = {"error": f"{type(e).__name__}: {e}"}
+        torch.cuda.empty_cache()
     if not args.no_moe and args.only is None:
         extras = {}
         for key, r in (("moe_decode", recipes.CFG4), ("moe_prefill", recipes.CFG5)):

@@ -29,17 +29,16 @@ namespace {
 constexpr int kMaxK = 16;
 constexpr int kMaxE = 1024;
 
-template <int MB, int EB, bool XBF16>
+// NS > 0 (H == 128 NS): the block's router rows are loaded into registers
+// before waiting for the preceding kernel (no kernel writes router weights),
+// so their latency overlaps that kernel's tail; small batches use it.
+template <int MB, int EB, bool XBF16, int NS>
 __global__ void __launch_bounds__(128) router_logits_kernel(const void *__restrict__ x, int64_t M,
                                                             int64_t H,
                                                             const float *__restrict__ wr,
                                                             const float *__restrict__ bias, int E,
                                                             float *__restrict__ logits,
                                                             int32_t *__restrict__ counts) {
-  pdl_enter();
-  // The expert histogram is accumulated by the top-k kernel that follows.
-  if (counts && blockIdx.x == 0 && blockIdx.y == 0)
-    for (int e = threadIdx.x; e < E; e += blockDim.x) counts[e] = 0;
   __shared__ float xch[2][32][MB * EB + 1];
   const int p = threadIdx.x;  // partial index
   const int warp = p >> 5, lane = p & 31;
@@ -47,6 +46,18 @@ __global__ void __launch_bounds__(128) router_logits_kernel(const void *__restri
   const int e0 = blockIdx.x * EB;
   const int mb = static_cast<int>(min64(MB, M - m0));
   const int eb = min(EB, E - e0);
+  float wpre[NS > 0 ? NS : 1][EB];
+  if constexpr (NS > 0) {
+#pragma unroll
+    for (int j = 0; j < NS; ++j)
+#pragma unroll
+      for (int e = 0; e < EB; ++e)
+        wpre[j][e] = __ldg(wr + int64_t(e0 + (e < eb ? e : 0)) * H + p + 128 * j);
+  }
+  pdl_enter();
+  // The expert histogram is accumulated by the top-k kernel that follows.
+  if (counts && blockIdx.x == 0 && blockIdx.y == 0)
+    for (int e = threadIdx.x; e < E; e += blockDim.x) counts[e] = 0;
 
   float acc[MB][EB];
 #pragma unroll
@@ -54,10 +65,37 @@ __global__ void __launch_bounds__(128) router_logits_kernel(const void *__restri
 #pragma unroll
     for (int e = 0; e < EB; ++e) acc[m][e] = 0.0f;
 
+  if constexpr (NS > 0) {
+    // same chain order: h = p, p + 128, ... for every partial
+#pragma unroll
+    for (int j0 = 0; j0 < NS; j0 += 4) {
+      float xv[4][MB];
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+#pragma unroll
+        for (int m = 0; m < MB; ++m) {
+          const int64_t mm = m0 + (m < mb ? m : 0);
+          const int64_t hh = p + 128 * (j0 + u);
+          if constexpr (XBF16) {
+            const uint16_t b = static_cast<const uint16_t *>(x)[mm * H + hh];
+            xv[u][m] = __uint_as_float(static_cast<uint32_t>(b) << 16);
+          } else {
+            xv[u][m] = __ldg(static_cast<const float *>(x) + mm * H + hh);
+          }
+        }
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+#pragma unroll
+        for (int m = 0; m < MB; ++m)
+#pragma unroll
+          for (int e = 0; e < EB; ++e) acc[m][e] = __fmaf_rn(xv[u][m], wpre[j0 + u][e], acc[m][e]);
+    }
+  }
+
   // Four h-steps per iteration: all their loads issue before the FMAs, so a
   // thread keeps 4 * (MB + EB) loads in flight (the chain order per partial
   // is unchanged).
-  int64_t h = p;
+  int64_t h = NS > 0 ? H : p;
   for (; h + 3 * 128 < H; h += 4 * 128) {
     float xv[4][MB], wv[4][EB];
 #pragma unroll
@@ -388,12 +426,12 @@ __global__ void __launch_bounds__(256) moe_combine_kernel(int64_t M, int k, int6
   }
 }
 
-template <int MB, int EB, bool XBF16>
+template <int MB, int EB, bool XBF16, int NS = 0>
 cudaError_t run_logits(const void *x, int64_t M, int64_t H, const float *wr, const float *bias,
                        int E, float *logits, int32_t *counts, cudaStream_t s) {
   dim3 grid((E + EB - 1) / EB, static_cast<unsigned>((M + MB - 1) / MB));
-  return launch_pdl(router_logits_kernel<MB, EB, XBF16>, grid, dim3(128), 0, s, x, M, H, wr, bias, E,
-                    logits, counts);
+  return launch_pdl(router_logits_kernel<MB, EB, XBF16, NS>, grid, dim3(128), 0, s, x, M, H, wr,
+                    bias, E, logits, counts);
 }
 
 template <int EPL>
@@ -414,7 +452,11 @@ cudaError_t launch_router(const void *x, bool x_bf16, int64_t M, int64_t H, cons
   cudaError_t err;
   // Small batches: fewer experts per block so that the 4 MB router matrix is
   // spread over more SMs.
-  if (M <= 64) {
+  if (M <= 8 && H == 4096) {
+    // decode: one expert per block, its router row preloaded in registers
+    err = x_bf16 ? run_logits<8, 1, true, 32>(x, M, H, wr, bias, E, logits, counts, s)
+                 : run_logits<8, 1, false, 32>(x, M, H, wr, bias, E, logits, counts, s);
+  } else if (M <= 64) {
     err = x_bf16 ? run_logits<8, 2, true>(x, M, H, wr, bias, E, logits, counts, s)
                  : run_logits<8, 2, false>(x, M, H, wr, bias, E, logits, counts, s);
   } else {
