@@ -43,12 +43,13 @@ constexpr int kThreads = kCW * 32;
 constexpr int kStageBytes = 40960;
 
 // Two configurations.  TBMAX 2 (two CTAs per SM, 128 registers: two
-// activation rows per lane, more tokens in passes of two over the staged
-// tile) runs the MoE experts, where most experts of a decode batch have one
-// or two tokens and latency hiding by the second CTA matters more than the
-// repeated dequantisation of the rare larger segments.  TBMAX 8 (one CTA
-// per SM, eight rows per pass) runs the linear layer for 3..8 rows, where
-// every tile serves all M rows.
+// activation rows per lane in the compact integer form) runs the MoE
+// experts, where most experts of a decode batch have one or two tokens and
+// latency hiding by the second CTA matters; an expert with more tokens is
+// applied in passes of two, each pass a sweep over the CTA's tiles of that
+// expert (activations load once per pass, the tiles stream again).
+// TBMAX 8 (one CTA per SM, eight fp32 rows per pass) runs the linear layer
+// for 3..8 rows, where every tile serves all M rows.
 template <int TBMAX>
 struct Cfg {
   static constexpr int kCtas = TBMAX <= 2 ? 2 : 1;      // CTAs per SM
@@ -85,9 +86,12 @@ __host__ __device__ constexpr int rows_per_tile() {
   return (BITS == 4 ? 16 : 8) * 16 / XPL;
 }
 
-// Cost of one tile of a segment with T tokens (dequantisation ~ 2 token
-// passes, then one per token).
-__host__ __device__ __forceinline__ int tile_cost(int T) { return 2 + T; }
+// Cost of one tile of a segment with T tokens applied in passes of TBMAX:
+// every pass streams and dequantises the tile (~2 token units), then one
+// unit per token.
+__host__ __device__ __forceinline__ int tile_cost(int T, int TBMAX) {
+  return 2 * ((T + TBMAX - 1) / TBMAX) + T;
+}
 
 // Launch with TBMAX 2 (any mode) or TBMAX 8 (the linear layer only).
 cudaError_t run_lo(int mode, bool x_bf16, const Args &a, cudaStream_t s);

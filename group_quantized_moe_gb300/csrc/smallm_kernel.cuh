@@ -243,6 +243,202 @@ __device__ __forceinline__ void load_x(const void *const (&rows)[TBMAX], int T, 
   }
 }
 
+// ------------------------------------------------- integer dot-product form
+//
+// Used by the two-row configuration (the routed experts of decode batches).
+// The lane's slice of each activation row is held in 22-bit fixed point:
+// x = X 2^-F, F chosen per row and lane slice so that |X| < 2^22 (relative
+// representation error <= 2^-22 of the slice's largest |x|), split into
+// bytes X = L2 2^16 + L1 2^8 + L0 (L0, L1 unsigned, L2 signed).  Byte dot
+// products (dp4a) of the codes q with each byte plane are exact integers, so
+//   sum_k (q_k - zp) x_k = 2^-F (sum_i 2^8i A_i - zp SX),
+// A_i = sum_k q_k L_i,k and SX = sum_k X_k, with only the final combination
+// rounded.  This replaces the per-code byte permute, subtract and FMA of the
+// fp32 form by three byte products per four codes (and per token).
+
+__device__ __forceinline__ uint32_t dp4a_uu(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("dp4a.u32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
+__device__ __forceinline__ int32_t dp4a_us(uint32_t a, uint32_t b, int32_t c) {
+  int32_t d;
+  asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
+// Byte planes of this lane's slice of up to TBMAX activation rows.  Word w
+// of plane i holds, for INT8, bytes of columns 4w .. 4w+3; for INT4, word 2j
+// the even columns 8j, 8j+2, 8j+4, 8j+6 and word 2j+1 the odd ones (the
+// columns of the low and high nibbles of code word j).
+template <int BITS, int XPL, bool XBF16, int TBMAX>
+__device__ __forceinline__ void load_x_int(const void *const (&rows)[TBMAX], int T, int col0,
+                                           uint32_t (&xl)[TBMAX][3][XPL / 4],
+                                           float (&sxf)[TBMAX], float (&xsc)[TBMAX]) {
+#pragma unroll
+  for (int t = 0; t < TBMAX; ++t) {
+    float v[XPL];
+    if (t < T) {
+      if constexpr (XBF16) {
+        const uint4 *p = reinterpret_cast<const uint4 *>(
+            static_cast<const uint16_t *>(rows[t]) + col0);
+#pragma unroll
+        for (int c = 0; c < XPL / 8; ++c) {
+          const uint4 u = __ldg(p + c);
+          const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+          for (int h = 0; h < 4; ++h) {
+            v[8 * c + 2 * h] = __uint_as_float(wv[h] << 16);
+            v[8 * c + 2 * h + 1] = __uint_as_float(wv[h] & 0xFFFF0000u);
+          }
+        }
+      } else {
+        const float4 *p = reinterpret_cast<const float4 *>(static_cast<const float *>(rows[t]) + col0);
+#pragma unroll
+        for (int c = 0; c < XPL / 4; ++c) {
+          const float4 f = __ldg(p + c);
+          v[4 * c] = f.x;
+          v[4 * c + 1] = f.y;
+          v[4 * c + 2] = f.z;
+          v[4 * c + 3] = f.w;
+        }
+      }
+    } else {
+#pragma unroll
+      for (int c = 0; c < XPL; ++c) v[c] = 0.0f;
+    }
+    float mx = 0.0f;
+#pragma unroll
+    for (int c = 0; c < XPL; ++c) mx = fmaxf(mx, fabsf(v[c]));
+    // F = 21 - floor(log2 mx) puts mx 2^F in [2^21, 2^22); exponents are
+    // read from the bits (power-of-two scalings are exact).
+    const int e = mx > 0.0f ? ((__float_as_int(mx) >> 23) & 0xFF) - 127 : 0;
+    const int F = max(-126, min(127, 21 - e));
+    const float up = __int_as_float((F + 127) << 23);
+    xsc[t] = F <= 126 ? __int_as_float((127 - F) << 23) : 0.0f;  // 2^-F
+    int32_t X[XPL];
+#pragma unroll
+    for (int c = 0; c < XPL; ++c) X[c] = __float2int_rn(v[c] * up);
+    int32_t sx[3] = {0, 0, 0};
+#pragma unroll
+    for (int c = 0; c < XPL; ++c) {
+      sx[0] += X[c] & 0xFF;
+      sx[1] += (X[c] >> 8) & 0xFF;
+      sx[2] += X[c] >> 16;
+    }
+    sxf[t] = fmaf(static_cast<float>(sx[2]), 65536.0f,
+                  fmaf(static_cast<float>(sx[1]), 256.0f, static_cast<float>(sx[0])));
+#pragma unroll
+    for (int w = 0; w < XPL / 4; ++w) {
+      int c0, st;  // first column and column step of the four bytes of word w
+      if constexpr (BITS == 4) {
+        c0 = 8 * (w >> 1) + (w & 1);
+        st = 2;
+      } else {
+        c0 = 4 * w;
+        st = 1;
+      }
+#pragma unroll
+      for (int i = 0; i < 3; ++i) {
+        uint32_t word = 0;
+#pragma unroll
+        for (int b = 0; b < 4; ++b)
+          word |= (static_cast<uint32_t>(X[c0 + st * b] >> (8 * i)) & 0xFFu) << (8 * b);
+        xl[t][i][w] = word;
+      }
+    }
+  }
+}
+
+// Integer dot products of this lane's XPL codes of one row with TB rows,
+// returned as (sum_k (q_k - zp) x_k) / s.
+template <int BITS, int XPL, int TB, int TBMAX>
+__device__ __forceinline__ void row_dot_int(uint32_t caddr, float zf,
+                                            const uint32_t (&xl)[TBMAX][3][XPL / 4],
+                                            const float (&sxf)[TBMAX], const float (&xsc)[TBMAX],
+                                            float (&d)[TB]) {
+  uint32_t a0[TB], a1[TB];
+  int32_t a2[TB];
+#pragma unroll
+  for (int t = 0; t < TB; ++t) {
+    a0[t] = a1[t] = 0u;
+    a2[t] = 0;
+  }
+  constexpr int NW = XPL * BITS / 32;  // code words per lane per row
+  uint32_t w[NW];
+  if constexpr (NW == 4) {
+    const uint4 v = lds128(caddr);
+    w[0] = v.x;
+    w[1] = v.y;
+    w[2] = v.z;
+    w[3] = v.w;
+  } else if constexpr (NW == 2) {
+    const uint2 v = lds64(caddr);
+    w[0] = v.x;
+    w[1] = v.y;
+  } else {
+    w[0] = lds32(caddr);
+  }
+#pragma unroll
+  for (int j = 0; j < NW; ++j) {
+    if constexpr (BITS == 4) {
+      const uint32_t lo = w[j] & 0x0F0F0F0Fu, hi = (w[j] >> 4) & 0x0F0F0F0Fu;
+#pragma unroll
+      for (int t = 0; t < TB; ++t) {
+        a0[t] = dp4a_uu(hi, xl[t][0][2 * j + 1], dp4a_uu(lo, xl[t][0][2 * j], a0[t]));
+        a1[t] = dp4a_uu(hi, xl[t][1][2 * j + 1], dp4a_uu(lo, xl[t][1][2 * j], a1[t]));
+        a2[t] = dp4a_us(hi, xl[t][2][2 * j + 1], dp4a_us(lo, xl[t][2][2 * j], a2[t]));
+      }
+    } else {
+      const uint32_t u = w[j] ^ 0x80808080u;  // stored q - 128 -> q
+#pragma unroll
+      for (int t = 0; t < TB; ++t) {
+        a0[t] = dp4a_uu(u, xl[t][0][j], a0[t]);
+        a1[t] = dp4a_uu(u, xl[t][1][j], a1[t]);
+        a2[t] = dp4a_us(u, xl[t][2][j], a2[t]);
+      }
+    }
+  }
+#pragma unroll
+  for (int t = 0; t < TB; ++t) {
+    const float q = fmaf(static_cast<float>(a2[t]), 65536.0f,
+                         fmaf(static_cast<float>(a1[t]), 256.0f, static_cast<float>(a0[t])));
+    d[t] = fmaf(-zf, sxf[t], q) * xsc[t];
+  }
+}
+
+// tile_compute for the integer form.
+template <int BITS, int XPL, int NR, int TB, int TBMAX>
+__device__ __forceinline__ void tile_compute_int(uint32_t stage, int rowbytes, int G, int gi,
+                                                 uint32_t lane_off,
+                                                 const uint32_t (&xl)[TBMAX][3][XPL / 4],
+                                                 const float (&sxf)[TBMAX],
+                                                 const float (&xsc)[TBMAX], float *red_w,
+                                                 int lane) {
+  constexpr int NRS = (NR * TB <= 32) ? NR : 32 / TB;
+  constexpr int V = NRS * TB;
+  constexpr int LV = log2c<V>();
+  const uint32_t sc0 = stage + NR * rowbytes + 4 * gi;
+  const uint32_t zp0 = sc0 + NR * G * 4;
+#pragma unroll
+  for (int sb = 0; sb < NR; sb += NRS) {
+    float v[V];
+#pragma unroll
+    for (int r = 0; r < NRS; ++r) {
+      const int row = sb + r;
+      const float s = lds_f32(sc0 + row * G * 4);
+      const float zf = static_cast<float>(lds_s32(zp0 + row * G * 4));
+      float d[TB];
+      row_dot_int<BITS, XPL, TB, TBMAX>(stage + row * rowbytes + lane_off, zf, xl, sxf, xsc, d);
+#pragma unroll
+      for (int t = 0; t < TB; ++t) v[r * TB + t] = s * d[t];
+    }
+    bfly<V, 16>(v, lane);
+    if ((lane & ((32 >> LV) - 1)) == 0) red_w[sb * TB + (lane >> (5 - LV))] = v[0];
+  }
+}
+
 __device__ __forceinline__ float silu(float g) { return g / (1.0f + expf(-g)); }
 
 __device__ __forceinline__ int64_t ceil_div(int64_t n, int64_t d) {
@@ -262,11 +458,13 @@ namespace {
 // positions s_off[e] .. s_off[e + 1] (the linear layer: one segment of M
 // rows).  s_cs[s] = sum of the per-tile cost of the earlier segments.
 // Tile j of a segment covers rows [j * RT, j * RT + RT) of each matrix.
-// A segment with more than TBMAX tokens is applied TBMAX tokens at a time
-// to the same staged tile.
+// A segment with more than TBMAX tokens is applied in passes of TBMAX
+// tokens; each pass sweeps the CTA's tiles of the segment (the tiles are
+// streamed again, the pass's activations load once).  The work sequence is
+// (segment, pass, tile).
 struct TileIt {
-  int s;
-  int64_t j, jhi;
+  int s, b, nb;  // segment, pass, passes of the segment
+  int64_t j, jlo, jhi;
   bool valid;
 };
 
@@ -323,7 +521,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<TBMAX>::kCtas) smallm_kernel(con
     int sum = 0;
     for (int i = lo; i < hi; ++i) {
       const int e = s_active[i];
-      sum += tile_cost(s_off[e + 1] - s_off[e]);
+      sum += tile_cost(s_off[e + 1] - s_off[e], TBMAX);
     }
     int incl = sum;
 #pragma unroll
@@ -335,7 +533,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<TBMAX>::kCtas) smallm_kernel(con
     for (int i = lo; i < hi; ++i) {
       s_cs[i] = run;
       const int e = s_active[i];
-      run += tile_cost(s_off[e + 1] - s_off[e]);
+      run += tile_cost(s_off[e + 1] - s_off[e], TBMAX);
     }
     if (lane == 31) s_cs[nseg] = incl;
   }
@@ -366,31 +564,41 @@ __global__ void __launch_bounds__(kThreads, Cfg<TBMAX>::kCtas) smallm_kernel(con
     const int64_t base = tiles * s_cs[s] * Gd;
     if (base >= hi_c) return false;
     const int e = s_active[s];
-    const int64_t c = tile_cost(s_off[e + 1] - s_off[e]) * Gd;
+    const int64_t c = tile_cost(s_off[e + 1] - s_off[e], TBMAX) * Gd;
     jlo = ceil_div(lo_c - base, c);
     jhi = ceil_div(hi_c - base, c);
     jlo = jlo < 0 ? 0 : (jlo > tiles ? tiles : jlo);
     jhi = jhi < 0 ? 0 : (jhi > tiles ? tiles : jhi);
     return true;
   };
-  auto it_settle = [&](TileIt &it) {  // move to the first segment with a tile left
+  auto passes = [&](int s) {
+    const int e = s_active[s];
+    return (s_off[e + 1] - s_off[e] + TBMAX - 1) / TBMAX;
+  };
+  auto it_settle = [&](TileIt &it) {  // move to the next (segment, pass) with a tile left
     while (it.j >= it.jhi) {
+      if (++it.b < it.nb) {
+        it.j = it.jlo;
+        continue;
+      }
       ++it.s;
-      int64_t jlo = 0, jhi = 0;
-      if (!seg_range(it.s, jlo, jhi)) {
+      it.b = 0;
+      if (!seg_range(it.s, it.jlo, it.jhi)) {
         it.valid = false;
         return;
       }
-      it.j = jlo;
-      it.jhi = jhi;
+      it.nb = passes(it.s);
+      it.j = it.jlo;
     }
   };
   auto it_begin = [&]() {
-    TileIt it{s_first, 0, 0, true};
-    if (!seg_range(it.s, it.j, it.jhi)) {
+    TileIt it{s_first, 0, 0, 0, 0, 0, true};
+    if (!seg_range(it.s, it.jlo, it.jhi)) {
       it.valid = false;
       return it;
     }
+    it.nb = passes(it.s);
+    it.j = it.jlo;
     it_settle(it);
     return it;
   };
@@ -437,100 +645,111 @@ __global__ void __launch_bounds__(kThreads, Cfg<TBMAX>::kCtas) smallm_kernel(con
   const int col0 = threadIdx.x * XPL;  // this lane's columns
   const int gi = col0 / a.group;
   const uint32_t lane_off = static_cast<uint32_t>(threadIdx.x * LB);
-  f32x2_t xp[TBMAX][XPL / 2];
+  // Activation slices: fp32 pairs (eight rows per pass) or the byte planes
+  // of the integer form (two rows per pass).
+  constexpr bool kInt = TBMAX <= 2;
+  f32x2_t xp[kInt ? 1 : TBMAX][XPL / 2];
+  uint32_t xl[kInt ? TBMAX : 1][3][XPL / 4];
+  float sxf[kInt ? TBMAX : 1], xsc[kInt ? TBMAX : 1];
   int cur_s = -1, cur_b = -1;
-  int64_t i = 0, step = 0, pending = 0;
+  int64_t i = 0, pending = 0;
   bool stop = false;
   for (TileIt it = it_begin(); it.valid && !stop; it_next(it), ++i) {
     pending = i;
-    const int s = it.s;
+    const int s = it.s, b = it.b;
     const int e = s_active[s];
     const int p0 = s_off[e];
     const int T = s_off[e + 1] - p0;
-    const int nb = (T + TBMAX - 1) / TBMAX;
     const int st = static_cast<int>(i % STAGES);
     const bool ok = wait_ok(smem_addr(&full_bar[st]), static_cast<uint32_t>((i / STAGES) & 1),
                             a.status, abort_flag);
     const uint32_t stage = ring + st * kStageBytes;
     const int64_t n0 = it.j * RT;
-    for (int b = 0; b < nb; ++b, ++step) {
-      const int t0 = b * TBMAX;
-      const int Tb = min(TBMAX, T - t0);
-      const int TB = Tb <= 1 ? 1 : Tb <= 2 ? 2 : Tb <= 4 ? 4 : 8;
-      float *red_w = red + (step & 1) * kCW * RED + warp * RED;
-      if (ok) {
-        if (s != cur_s || b != cur_b) {
-          const void *xr[TBMAX];
+    const int t0 = b * TBMAX;
+    const int Tb = min(TBMAX, T - t0);
+    const int TB = Tb <= 1 ? 1 : Tb <= 2 ? 2 : Tb <= 4 ? 4 : 8;
+    float *red_w = red + (i & 1) * kCW * RED + warp * RED;
+    if (ok) {
+      if (s != cur_s || b != cur_b) {
+        const void *xr[TBMAX];
 #pragma unroll
-          for (int t = 0; t < TBMAX; ++t) {
-            const int64_t tt = t0 + (t < Tb ? t : 0);
-            if constexpr (MODE == kLinear) {
-              xr[t] = XBF16 ? static_cast<const void *>(static_cast<const uint16_t *>(a.x) + tt * a.K)
-                            : static_cast<const void *>(static_cast<const float *>(a.x) + tt * a.K);
-            } else if constexpr (MODE == kGateUp) {
-              const int64_t tok = a.ws.assign[p0 + tt] / a.k;
-              xr[t] = XBF16 ? static_cast<const void *>(static_cast<const uint16_t *>(a.x) + tok * a.K)
-                            : static_cast<const void *>(static_cast<const float *>(a.x) + tok * a.K);
-            } else {
-              xr[t] = a.ws.h + (p0 + tt) * a.K;
-            }
-          }
-          load_x<BITS, XPL, (MODE != kDown) && XBF16, TBMAX>(xr, Tb, col0, xp);
-          cur_s = s;
-          cur_b = b;
-        }
-        if (TB == 1) {
-          tile_compute<BITS, XPL, NR, 1, TBMAX>(stage, rowbytes, G, gi, lane_off, xp, red_w, lane);
-        } else if (TB == 2 || TBMAX == 2) {
-          tile_compute<BITS, XPL, NR, 2, TBMAX>(stage, rowbytes, G, gi, lane_off, xp, red_w, lane);
-        } else {
-          if constexpr (TBMAX >= 8) {
-            if (TB == 4)
-              tile_compute<BITS, XPL, NR, 4, TBMAX>(stage, rowbytes, G, gi, lane_off, xp, red_w, lane);
-            else
-              tile_compute<BITS, XPL, NR, 8, TBMAX>(stage, rowbytes, G, gi, lane_off, xp, red_w, lane);
-          }
-        }
-      }
-      // Every warp has written its partials (and, after the last batch, has
-      // finished reading the stage); the OR tells all threads whether any
-      // gave up.
-      if (consumers_sync_or(!ok || *abort_flag != 0)) {
-        stop = true;
-        break;
-      }
-      if (b == nb - 1 && pit.valid) {
-        // The stage is free: lane 0 of warp i % 8 refills it with the tile
-        // STAGES ahead (the role rotates so that no warp is always late).
-        if (lane == 0 && warp == static_cast<int>(i % kCW)) {
-          fence_proxy_async_smem();
-          issue(pit, st);
-        }
-        it_next(pit);
-        ++issued;
-      }
-      // Finalise: thread q sums the eight warp partials of one (row, token)
-      // output in warp order; q = 0 starts at warp (step + 1) % 8, so the
-      // usually short list of outputs also rotates over the warps.
-      const float *rb = red + (step & 1) * kCW * RED;
-      const int q = (threadIdx.x + kThreads - 32 * static_cast<int>((step + 1) % kCW)) % kThreads;
-      if (q < RT * TB) {
-        const int r = q / TB, t = q % TB;
-        if (t < Tb && n0 + r < rows) {
-          float acc0 = 0.0f;
-#pragma unroll
-          for (int w = 0; w < kCW; ++w) acc0 += rb[w * RED + r * TB + t];
-          const int64_t pos = static_cast<int64_t>(p0) + t0 + t;
-          if constexpr (MODE == kGateUp) {
-            float acc1 = 0.0f;
-#pragma unroll
-            for (int w = 0; w < kCW; ++w) acc1 += rb[w * RED + (RT + r) * TB + t];
-            a.ws.h[pos * rows + n0 + r] = silu(acc0) * acc1;
-          } else if constexpr (MODE == kDown) {
-            a.ws.out[pos * rows + n0 + r] = acc0;
+        for (int t = 0; t < TBMAX; ++t) {
+          const int64_t tt = t0 + (t < Tb ? t : 0);
+          if constexpr (MODE == kLinear) {
+            xr[t] = XBF16 ? static_cast<const void *>(static_cast<const uint16_t *>(a.x) + tt * a.K)
+                          : static_cast<const void *>(static_cast<const float *>(a.x) + tt * a.K);
+          } else if constexpr (MODE == kGateUp) {
+            const int64_t tok = a.ws.assign[p0 + tt] / a.k;
+            xr[t] = XBF16 ? static_cast<const void *>(static_cast<const uint16_t *>(a.x) + tok * a.K)
+                          : static_cast<const void *>(static_cast<const float *>(a.x) + tok * a.K);
           } else {
-            a.y[pos * rows + n0 + r] = acc0;
+            xr[t] = a.ws.h + (p0 + tt) * a.K;
           }
+        }
+        if constexpr (kInt)
+          load_x_int<BITS, XPL, (MODE != kDown) && XBF16, TBMAX>(xr, Tb, col0, xl, sxf, xsc);
+        else
+          load_x<BITS, XPL, (MODE != kDown) && XBF16, TBMAX>(xr, Tb, col0, xp);
+        cur_s = s;
+        cur_b = b;
+      }
+      if constexpr (kInt) {
+        if (TB == 1)
+          tile_compute_int<BITS, XPL, NR, 1, TBMAX>(stage, rowbytes, G, gi, lane_off, xl, sxf, xsc,
+                                                    red_w, lane);
+        else
+          tile_compute_int<BITS, XPL, NR, 2, TBMAX>(stage, rowbytes, G, gi, lane_off, xl, sxf, xsc,
+                                                    red_w, lane);
+      } else if (TB == 1) {
+        tile_compute<BITS, XPL, NR, 1, TBMAX>(stage, rowbytes, G, gi, lane_off, xp, red_w, lane);
+      } else if (TB == 2) {
+        tile_compute<BITS, XPL, NR, 2, TBMAX>(stage, rowbytes, G, gi, lane_off, xp, red_w, lane);
+      } else {
+        if constexpr (TBMAX >= 8) {
+          if (TB == 4)
+            tile_compute<BITS, XPL, NR, 4, TBMAX>(stage, rowbytes, G, gi, lane_off, xp, red_w, lane);
+          else
+            tile_compute<BITS, XPL, NR, 8, TBMAX>(stage, rowbytes, G, gi, lane_off, xp, red_w, lane);
+        }
+      }
+    }
+    // Every warp has written its partials and finished reading the stage;
+    // the OR tells all threads whether any gave up.
+    if (consumers_sync_or(!ok || *abort_flag != 0)) {
+      stop = true;
+      break;
+    }
+    if (pit.valid) {
+      // The stage is free: lane 0 of warp i % 8 refills it with the work
+      // item STAGES ahead (the role rotates so that no warp is always late).
+      if (lane == 0 && warp == static_cast<int>(i % kCW)) {
+        fence_proxy_async_smem();
+        issue(pit, st);
+      }
+      it_next(pit);
+      ++issued;
+    }
+    // Finalise: thread q sums the eight warp partials of one (row, token)
+    // output in warp order; q = 0 starts at warp (i + 1) % 8, so the usually
+    // short list of outputs also rotates over the warps.
+    const float *rb = red + (i & 1) * kCW * RED;
+    const int q = (threadIdx.x + kThreads - 32 * static_cast<int>((i + 1) % kCW)) % kThreads;
+    if (q < RT * TB) {
+      const int r = q / TB, t = q % TB;
+      if (t < Tb && n0 + r < rows) {
+        float acc0 = 0.0f;
+#pragma unroll
+        for (int w = 0; w < kCW; ++w) acc0 += rb[w * RED + r * TB + t];
+        const int64_t pos = static_cast<int64_t>(p0) + t0 + t;
+        if constexpr (MODE == kGateUp) {
+          float acc1 = 0.0f;
+#pragma unroll
+          for (int w = 0; w < kCW; ++w) acc1 += rb[w * RED + (RT + r) * TB + t];
+          a.ws.h[pos * rows + n0 + r] = silu(acc0) * acc1;
+        } else if constexpr (MODE == kDown) {
+          a.ws.out[pos * rows + n0 + r] = acc0;
+        } else {
+          a.y[pos * rows + n0 + r] = acc0;
         }
       }
     }
