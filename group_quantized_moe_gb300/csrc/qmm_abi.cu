@@ -175,10 +175,9 @@ int qmm_linear(const void *x, int32_t x_dtype, int64_t M, const qmm_weight *w, f
   QMat q{static_cast<const uint8_t *>(w->codes), 0, w->scales, w->zps, 0, w->N, w->K,
          w->bits, w->group};
   cudaError_t e;
-  // The small-M kernel for 2..8 rows, and for single rows of small matrices,
-  // where its finer K split shortens the latency-bound critical path.
-  const bool small = smallm_supported(w->bits, w->group, w->K) &&
-                     ((M >= 2 && M <= 8) || (M == 1 && w->N <= 16384));
+  // The small-M kernel (integer dot products, K split over the warps) for
+  // 1..8 rows of the shapes it takes; the per-warp row kernel otherwise.
+  const bool small = smallm_supported(w->bits, w->group, w->K) && M >= 1 && M <= 8;
   if (small)
     e = launch_smallm_linear(x, x_dtype == QMM_BF16, M, q, y, static_cast<cudaStream_t>(stream));
   else
