@@ -193,6 +193,200 @@ __global__ void __launch_bounds__(128) router_logits_kernel(const void *__restri
   }
 }
 
+// ---------------------------------------------------------------------------
+// Batched logits (many tokens).  The kernel above reads its operands straight
+// from L2 with no reuse inside the block, which leaves a 512-token batch
+// bound by L2 traffic.  Here a block owns a tile of kTM tokens x kTE experts
+// for all 128 partials: the tile's token rows and router rows stream through
+// shared memory in chunks of kCH columns (1-D bulk copies, a ring of kNST
+// stages), thread (p, half) keeps partial p of 8 tokens x 16 experts in
+// registers, and every staged value feeds 8 or 16 FMAs.  The summation order
+// is the one above: each partial is one fma chain in increasing h; the
+// first tree level ((P0 + P1) + (P2 + P3)) runs as two halving exchanges
+// between adjacent lanes; the last five levels run per output from shared
+// memory.
+namespace tiled {
+constexpr int kTM = 16, kTE = 16, kCH = 512, kNST = 3, kThreads = 256;
+constexpr int kTStride = 129;  // padded row of the level-1 sums in shared memory
+template <bool XBF16>
+__host__ __device__ constexpr int stage_bytes() {
+  return kTM * kCH * (XBF16 ? 2 : 4) + kTE * kCH * 4;
+}
+template <bool XBF16>
+__host__ __device__ constexpr int smem_bytes() {
+  return kNST * stage_bytes<XBF16>();
+}
+static_assert(2 * 32 * kTStride * 4 <= kNST * stage_bytes<true>(), "level-1 sums reuse the ring");
+}  // namespace tiled
+
+template <bool XBF16>
+__global__ void __launch_bounds__(tiled::kThreads, 1)
+    router_logits_tiled_kernel(const void *__restrict__ x, int64_t M, int64_t H,
+                               const float *__restrict__ wr, const float *__restrict__ bias,
+                               int E, float *__restrict__ logits, int32_t *__restrict__ counts,
+                               uint32_t *status) {
+  using namespace tiled;
+  constexpr int XB = XBF16 ? 2 : 4;
+  constexpr int SB = stage_bytes<XBF16>();
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ __align__(8) uint64_t full[kNST];
+  const int tid = threadIdx.x, p = tid & 127, half = tid >> 7;
+  const int lane = tid & 31;
+  const int64_t m0 = static_cast<int64_t>(blockIdx.y) * kTM;
+  const int e0 = blockIdx.x * kTE;
+  const int mv = static_cast<int>(min64(kTM, M - m0));
+  const int ev = min(kTE, E - e0);
+  const int nch = static_cast<int>(H / kCH);
+  const uint32_t base = smem_addr(smem);
+  auto bar = [&](int s) { return smem_addr(&full[s]); };
+
+  if (tid == 0) {
+    for (int s = 0; s < kNST; ++s) mbar_init(bar(s), 1);
+    mbar_fence_init();
+  }
+  __syncthreads();
+  // Thread 0 requests chunk c into stage c % kNST: the router rows (no
+  // kernel of this library writes them, so the first chunks go out before
+  // the wait for the preceding kernel) and the token rows.
+  auto issue_w = [&](int c) {
+    const int s = c % kNST;
+    const uint32_t ws = base + s * SB + kTM * kCH * XB;
+    mbar_arrive_expect_tx(bar(s), static_cast<uint32_t>(mv * kCH * XB + ev * kCH * 4));
+    for (int e = 0; e < ev; ++e)
+      bulk_g2s(ws + e * kCH * 4, wr + int64_t(e0 + e) * H + int64_t(c) * kCH, kCH * 4, bar(s));
+  };
+  auto issue_x = [&](int c) {
+    const int s = c % kNST;
+    const uint32_t xs = base + s * SB;
+    for (int m = 0; m < mv; ++m)
+      bulk_g2s(xs + m * kCH * XB,
+               static_cast<const uint8_t *>(x) + ((m0 + m) * H + int64_t(c) * kCH) * XB,
+               kCH * XB, bar(s));
+  };
+  const int npre = min(kNST, nch);
+  if (tid == 0)
+    for (int c = 0; c < npre; ++c) issue_w(c);
+  pdl_enter();
+  if (counts && blockIdx.x == 0 && blockIdx.y == 0)
+    for (int e = tid; e < E; e += blockDim.x) counts[e] = 0;
+  if (tid == 0)
+    for (int c = 0; c < npre; ++c) issue_x(c);
+
+  float acc[8][kTE];
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+#pragma unroll
+    for (int e = 0; e < kTE; ++e) acc[i][e] = 0.0f;
+
+  int issued = npre, c = 0;
+  bool aborted = false;
+  for (; c < nch; ++c) {
+    const int s = c % kNST;
+    const bool ok = mbar_wait_bounded(bar(s), static_cast<uint32_t>((c / kNST) & 1), status);
+    if (ok) {
+      const uint8_t *st = smem + s * SB;
+      const float *ws = reinterpret_cast<const float *>(st + kTM * kCH * XB);
+#pragma unroll
+      for (int j = 0; j < kCH / 128; ++j) {
+        const int hl = p + 128 * j;
+        float xv[8], wv[kTE];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          if constexpr (XBF16) {
+            const uint16_t b = reinterpret_cast<const uint16_t *>(st)[(8 * half + i) * kCH + hl];
+            xv[i] = __uint_as_float(static_cast<uint32_t>(b) << 16);
+          } else {
+            xv[i] = reinterpret_cast<const float *>(st)[(8 * half + i) * kCH + hl];
+          }
+        }
+#pragma unroll
+        for (int e = 0; e < kTE; ++e) wv[e] = ws[e * kCH + hl];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+#pragma unroll
+          for (int e = 0; e < kTE; ++e) acc[i][e] = __fmaf_rn(xv[i], wv[e], acc[i][e]);
+      }
+    }
+    // one barrier per chunk: every thread is done with stage s, and all
+    // learn whether any wait gave up
+    if (__syncthreads_or(!ok)) {
+      aborted = true;
+      break;
+    }
+    if (tid == 0 && issued < nch) {
+      fence_proxy_async_smem();
+      issue_w(issued);
+      issue_x(issued);
+      ++issued;
+    }
+  }
+  if (aborted) {
+    // Wait (bounded) for the copies still landing, then leave.
+    if (tid == 0)
+      for (int u = c; u < issued; ++u)
+        mbar_wait_bounded(bar(u % kNST), static_cast<uint32_t>((u / kNST) & 1), status);
+    return;
+  }
+
+  // Level 1 inside groups of four lanes (partials 4l .. 4l+3): at offset 1 a
+  // lane keeps half of its 128 values and adds the neighbour's copy of that
+  // half (P0 + P1, P2 + P3), at offset 2 half again ((P0+P1) + (P2+P3)).
+  // Lane bits (b1 b0) end with the 32 sums of value index 64 b0 + 32 b1 + i.
+  float v[8 * kTE];
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+#pragma unroll
+    for (int e = 0; e < kTE; ++e) v[i * kTE + e] = acc[i][e];
+  {
+    const bool up = (lane & 1) != 0;
+#pragma unroll
+    for (int i = 0; i < 64; ++i) {
+      const float send = up ? v[i] : v[i + 64];
+      const float keep = up ? v[i + 64] : v[i];
+      v[i] = __fadd_rn(keep, __shfl_xor_sync(0xFFFFFFFFu, send, 1));
+    }
+  }
+  {
+    const bool up = (lane & 2) != 0;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const float send = up ? v[i] : v[i + 32];
+      const float keep = up ? v[i + 32] : v[i];
+      v[i] = __fadd_rn(keep, __shfl_xor_sync(0xFFFFFFFFu, send, 2));
+    }
+  }
+  // t_l (l = p / 4) of value index vi lives at tb[half][l][vi ^ 8 (vi >> 5)]
+  // (rows padded to kTStride; the swizzle spreads the four value blocks a
+  // warp writes over distinct banks).
+  float *tb = reinterpret_cast<float *>(smem);
+  const int l = p >> 2;
+  const int vb = 64 * (lane & 1) + 32 * ((lane >> 1) & 1);
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    const int vi = vb + i;
+    tb[(half * 32 + l) * kTStride + (vi ^ ((vi >> 5) << 3))] = v[i];
+  }
+  __syncthreads();
+  {
+    // Output o = tid: token 8 half + vi / 16, expert vi % 16.
+    const int vi = p;
+    const int col = vi ^ ((vi >> 5) << 3);
+    float t[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) t[j] = tb[(half * 32 + j) * kTStride + col];
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1)
+#pragma unroll
+      for (int j = 0; j < o; ++j) t[j] = __fadd_rn(t[j], t[j + o]);
+    const int m = 8 * half + (vi >> 4), e = vi & 15;
+    if (m < mv && e < ev) {
+      float r = t[0];
+      if (bias) r = __fadd_rn(r, bias[e0 + e]);
+      logits[(m0 + m) * E + e0 + e] = r;
+    }
+  }
+}
+
 // a beats b: larger logit, or equal logit and lower index.
 __device__ __forceinline__ bool beats(float la, int a, float lb, int b) {
   return la > lb || (la == lb && a < b);
@@ -434,6 +628,19 @@ cudaError_t run_logits(const void *x, int64_t M, int64_t H, const float *wr, con
                     bias, E, logits, counts);
 }
 
+template <bool XBF16>
+cudaError_t run_logits_tiled(const void *x, int64_t M, int64_t H, const float *wr,
+                             const float *bias, int E, float *logits, int32_t *counts,
+                             cudaStream_t s) {
+  constexpr int smem = tiled::smem_bytes<XBF16>();
+  const cudaError_t err =
+      ensure_smem(reinterpret_cast<const void *>(router_logits_tiled_kernel<XBF16>), smem);
+  if (err != cudaSuccess) return err;
+  dim3 grid((E + tiled::kTE - 1) / tiled::kTE, static_cast<unsigned>((M + tiled::kTM - 1) / tiled::kTM));
+  return launch_pdl(router_logits_tiled_kernel<XBF16>, grid, dim3(tiled::kThreads), smem, s, x, M,
+                    H, wr, bias, E, logits, counts, device_status());
+}
+
 template <int EPL>
 cudaError_t run_topk(const float *logits, int64_t M, int E, int k, int32_t *idx, float *w,
                      int32_t *counts, cudaStream_t s) {
@@ -456,6 +663,10 @@ cudaError_t launch_router(const void *x, bool x_bf16, int64_t M, int64_t H, cons
     // decode: one expert per block, its router row preloaded in registers
     err = x_bf16 ? run_logits<8, 1, true, 32>(x, M, H, wr, bias, E, logits, counts, s)
                  : run_logits<8, 1, false, 32>(x, M, H, wr, bias, E, logits, counts, s);
+  } else if (M > 64 && H % tiled::kCH == 0 && (M + tiled::kTM - 1) / tiled::kTM <= 65535) {
+    // larger batches: tiles staged through shared memory
+    err = x_bf16 ? run_logits_tiled<true>(x, M, H, wr, bias, E, logits, counts, s)
+                 : run_logits_tiled<false>(x, M, H, wr, bias, E, logits, counts, s);
   } else if (M <= 64) {
     err = x_bf16 ? run_logits<8, 2, true>(x, M, H, wr, bias, E, logits, counts, s)
                  : run_logits<8, 2, false>(x, M, H, wr, bias, E, logits, counts, s);

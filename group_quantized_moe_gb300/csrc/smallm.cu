@@ -32,7 +32,7 @@ bool smallm_supported(int bits, int group, int64_t K) {
   if (bits != 4 && bits != 8) return false;
   if (K != 2048 && K != 4096) return false;
   if (group < 64 || K % group != 0 || (K / group) % 4 != 0) return false;
-  return group % (K / 256) == 0;
+  return group % 16 == 0;  // a lane's 16 (or 8) columns never straddle a group
 }
 
 cudaError_t launch_smallm_linear(const void *x, bool x_bf16, int64_t M, const QMat &w, float *y,
@@ -56,7 +56,7 @@ cudaError_t launch_smallm_gateup(const void *x, bool x_bf16, int k, int E, const
   a.k = k;
   a.ws = ws;
   a.x = x;
-  return smallm::run_lo(smallm::kGateUp, x_bf16, a, s);
+  return smallm::run_one(smallm::kGateUp, x_bf16, a, s);
 }
 
 cudaError_t launch_smallm_down(int k, int E, const QMat &down, const MoeWork &ws, cudaStream_t s) {
@@ -64,7 +64,7 @@ cudaError_t launch_smallm_down(int k, int E, const QMat &down, const MoeWork &ws
   a.E = E;
   a.k = k;
   a.ws = ws;
-  return smallm::run_lo(smallm::kDown, false, a, s);
+  return smallm::run_one(smallm::kDown, false, a, s);
 }
 
 }  // namespace qmm

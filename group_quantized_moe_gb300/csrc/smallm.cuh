@@ -14,16 +14,17 @@
 //    completion on one mbarrier per stage (every wait bounded).  A stage is
 //    refilled right after the CTA barrier that ends its last use, so no
 //    "empty" barrier is needed.
-//  * The eight warps split the K range of every row eight ways: lane l of
-//    warp w owns columns [(32 w + l) XPL, +XPL), XPL = K / 256 (8 or 16),
-//    and keeps those columns of its activation rows in registers for
-//    as long as the CTA stays on one expert.  The slice never straddles a
-//    quantisation group, so it needs one scale and one zero point per row.
+//  * KW warps split the K range of a row (K = 32 KW XPL; the 8 / KW row
+//    groups of the CTA take disjoint rows of each stage): lane l of warp w
+//    owns columns [(32 (w mod KW) + l) XPL, +XPL), XPL = 8, 16 or 32, and
+//    keeps those columns of its activation rows in registers for as long as
+//    the CTA stays on one expert.  The slice never straddles a quantisation
+//    group, so it needs one scale and one zero point per row.
 //  * Each lane dequantises its slice of a row once and applies it to every
 //    token.  The per-lane partials of a block of rows are reduced across the
 //    warp by a butterfly that halves the values a lane carries at every step
-//    (about one shuffle per value instead of five), then across the eight
-//    warps through shared memory in a fixed order.
+//    (about one shuffle per value instead of five), then across the KW
+//    warps of the row group through shared memory in a fixed order.
 //  * Each CTA takes one contiguous range of tiles, balanced by a per-tile
 //    cost that grows with the expert's token count; it therefore reads one
 //    contiguous stretch of HBM and reloads activations only when its range
@@ -42,14 +43,16 @@ constexpr int kCW = 8;                       // warps; the K range is split 8 wa
 constexpr int kThreads = kCW * 32;
 constexpr int kStageBytes = 40960;
 
-// Two configurations.  TBMAX 2 (two CTAs per SM, 128 registers: two
-// activation rows per lane in the compact integer form) runs the MoE
-// experts, where most experts of a decode batch have one or two tokens and
-// latency hiding by the second CTA matters; an expert with more tokens is
-// applied in passes of two, each pass a sweep over the CTA's tiles of that
-// expert (activations load once per pass, the tiles stream again).
-// TBMAX 8 (one CTA per SM, eight fp32 rows per pass) runs the linear layer
-// for 3..8 rows, where every tile serves all M rows.
+// Three configurations (TBMAX = activation rows per pass).  TBMAX 1 and 2
+// use two CTAs per SM (128 registers) and the compact integer form.
+// TBMAX 1 runs the routed experts: most experts of a decode batch have one
+// token, and with one row per pass a lane can hold 32 columns, which halves
+// the per-row work (scale, zero point, conversions, reduction) per code; an
+// expert with T tokens is applied in T passes, each a sweep over the CTA's
+// tiles of that expert (activations load once per pass, the tiles stream
+// again).  TBMAX 2 (16 columns per lane) runs the linear layer with 1..2
+// rows.  TBMAX 8 (one CTA per SM, eight fp32 rows per pass) runs the linear
+// layer with 3..8 rows, where every tile serves all M rows.
 template <int TBMAX>
 struct Cfg {
   static constexpr int kCtas = TBMAX <= 2 ? 2 : 1;      // CTAs per SM
@@ -80,10 +83,11 @@ struct Args {
 };
 
 // Rows of all matrices per tile (one stage): the most whole rows, a power
-// of two, whose codes, scales and zero points fit 40 KB for group >= 64.
-template <int BITS, int XPL>
+// of two, whose codes, scales and zero points fit 40 KB for group >= 64
+// (KB = K / 256).
+template <int BITS, int KB>
 __host__ __device__ constexpr int rows_per_tile() {
-  return (BITS == 4 ? 16 : 8) * 16 / XPL;
+  return (BITS == 4 ? 16 : 8) * 16 / KB;
 }
 
 // Cost of one tile of a segment with T tokens applied in passes of TBMAX:
@@ -93,7 +97,9 @@ __host__ __device__ __forceinline__ int tile_cost(int T, int TBMAX) {
   return 2 * ((T + TBMAX - 1) / TBMAX) + T;
 }
 
-// Launch with TBMAX 2 (any mode) or TBMAX 8 (the linear layer only).
+// Launch with TBMAX 1 (the routed experts), 2 (any mode) or 8 (the linear
+// layer only).
+cudaError_t run_one(int mode, bool x_bf16, const Args &a, cudaStream_t s);
 cudaError_t run_lo(int mode, bool x_bf16, const Args &a, cudaStream_t s);
 cudaError_t run_hi(int mode, bool x_bf16, const Args &a, cudaStream_t s);
 

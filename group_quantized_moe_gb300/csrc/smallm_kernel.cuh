@@ -367,7 +367,17 @@ __device__ __forceinline__ void row_dot_int(uint32_t caddr, float zf,
   }
   constexpr int NW = XPL * BITS / 32;  // code words per lane per row
   uint32_t w[NW];
-  if constexpr (NW == 4) {
+  if constexpr (NW == 8) {
+    const uint4 v0 = lds128(caddr), v1 = lds128(caddr + 16);
+    w[0] = v0.x;
+    w[1] = v0.y;
+    w[2] = v0.z;
+    w[3] = v0.w;
+    w[4] = v1.x;
+    w[5] = v1.y;
+    w[6] = v1.z;
+    w[7] = v1.w;
+  } else if constexpr (NW == 4) {
     const uint4 v = lds128(caddr);
     w[0] = v.x;
     w[1] = v.y;
@@ -400,33 +410,44 @@ __device__ __forceinline__ void row_dot_int(uint32_t caddr, float zf,
       }
     }
   }
+  // a0 + 2^8 a1 < 2^31 always (XPL <= 64); for INT4 (codes <= 15) the whole
+  // sum a0 + 2^8 a1 + 2^16 a2 stays inside int32 for XPL <= 32, so a single
+  // conversion (one rounding, as before) suffices.
 #pragma unroll
   for (int t = 0; t < TB; ++t) {
-    const float q = fmaf(static_cast<float>(a2[t]), 65536.0f,
-                         fmaf(static_cast<float>(a1[t]), 256.0f, static_cast<float>(a0[t])));
+    const int32_t a01 = static_cast<int32_t>(a0[t] + (a1[t] << 8));
+    float q;
+    if constexpr (BITS == 4) {
+      static_assert(XPL <= 32, "INT4 plane sums must fit in int32");
+      q = static_cast<float>(a01 + a2[t] * 65536);
+    } else {
+      static_assert(XPL <= 64, "INT8 plane sums a0 + 2^8 a1 must fit in int32");
+      q = fmaf(static_cast<float>(a2[t]), 65536.0f, static_cast<float>(a01));
+    }
     d[t] = fmaf(-zf, sxf[t], q) * xsc[t];
   }
 }
 
-// tile_compute for the integer form.
-template <int BITS, int XPL, int NR, int TB, int TBMAX>
+// tile_compute for the integer form, over the NRW rows row0 .. row0 + NRW - 1
+// of a stage of NR rows (the warp's row group).
+template <int BITS, int XPL, int NR, int NRW, int TB, int TBMAX>
 __device__ __forceinline__ void tile_compute_int(uint32_t stage, int rowbytes, int G, int gi,
-                                                 uint32_t lane_off,
+                                                 uint32_t lane_off, int row0,
                                                  const uint32_t (&xl)[TBMAX][3][XPL / 4],
                                                  const float (&sxf)[TBMAX],
                                                  const float (&xsc)[TBMAX], float *red_w,
                                                  int lane) {
-  constexpr int NRS = (NR * TB <= 32) ? NR : 32 / TB;
+  constexpr int NRS = (NRW * TB <= 32) ? NRW : 32 / TB;
   constexpr int V = NRS * TB;
   constexpr int LV = log2c<V>();
   const uint32_t sc0 = stage + NR * rowbytes + 4 * gi;
   const uint32_t zp0 = sc0 + NR * G * 4;
 #pragma unroll
-  for (int sb = 0; sb < NR; sb += NRS) {
+  for (int sb = 0; sb < NRW; sb += NRS) {
     float v[V];
 #pragma unroll
     for (int r = 0; r < NRS; ++r) {
-      const int row = sb + r;
+      const int row = row0 + sb + r;
       const float s = lds_f32(sc0 + row * G * 4);
       const float zf = static_cast<float>(lds_s32(zp0 + row * G * 4));
       float d[TB];
@@ -468,15 +489,25 @@ struct TileIt {
   bool valid;
 };
 
-template <int BITS, int XPL, int MODE, bool XBF16, int TBMAX>
+// KW warps split the K range of a row (K = 32 KW XPL); the kCW / KW row
+// groups of a CTA take disjoint rows of every stage (KW = 4: two groups).
+template <int BITS, int XPL, int KW, int MODE, bool XBF16, int TBMAX>
 __global__ void __launch_bounds__(kThreads, Cfg<TBMAX>::kCtas) smallm_kernel(const Args a) {
-  // The MoE modes need the routing of the preceding kernels before anything
-  // else; the linear layer first requests its leading weight tiles (see
-  // gemv_kernel) and waits just before loading activations.
-  if constexpr (MODE != kLinear) pdl_enter();
+  // Gate/up needs the routing of the immediately preceding kernel (the
+  // dispatch) before anything else.  The linear layer and the down
+  // projection first request their leading weight tiles (see gemv_kernel)
+  // and wait just before loading activations: the down projection's
+  // grouping comes from the dispatch two launches back, which has completed
+  // by the time it starts (the gate/up kernel between them starts dependents
+  // only after its own wait), and only its activations (h) come from the
+  // gate/up kernel.
+  if constexpr (MODE == kGateUp) pdl_enter();
+  static_assert(KW == kCW || (KW < kCW && TBMAX <= 2), "row groups need the integer form");
   using C = Cfg<TBMAX>;
   constexpr int STAGES = C::kStages, RED = C::kRedMax;
-  constexpr int NR = rows_per_tile<BITS, XPL>();
+  constexpr int NR = rows_per_tile<BITS, XPL * KW / kCW>();
+  constexpr int RG = kCW / KW;   // row groups
+  constexpr int NRG = NR / RG;   // rows of a stage per row group
   constexpr int RT = (MODE == kGateUp) ? NR / 2 : NR;  // rows per matrix per tile
   constexpr int NM = (MODE == kGateUp) ? 2 : 1;
   constexpr int LB = XPL * BITS / 8;                   // code bytes per lane per row
@@ -640,11 +671,13 @@ __global__ void __launch_bounds__(kThreads, Cfg<TBMAX>::kCtas) smallm_kernel(con
     it_next(pit);
     ++issued;
   }
-  if constexpr (MODE == kLinear) pdl_enter();
+  if constexpr (MODE != kGateUp) pdl_enter();
 
-  const int col0 = threadIdx.x * XPL;  // this lane's columns
+  const int kslot = (warp % KW) * 32 + lane;  // this lane's slice of K
+  const int col0 = kslot * XPL;               // its columns
   const int gi = col0 / a.group;
-  const uint32_t lane_off = static_cast<uint32_t>(threadIdx.x * LB);
+  const uint32_t lane_off = static_cast<uint32_t>(kslot * LB);
+  const int row0 = (warp / KW) * NRG;         // first stage row of this warp's group
   // Activation slices: fp32 pairs (eight rows per pass) or the byte planes
   // of the integer form (two rows per pass).
   constexpr bool kInt = TBMAX <= 2;
@@ -694,12 +727,14 @@ __global__ void __launch_bounds__(kThreads, Cfg<TBMAX>::kCtas) smallm_kernel(con
         cur_b = b;
       }
       if constexpr (kInt) {
-        if (TB == 1)
-          tile_compute_int<BITS, XPL, NR, 1, TBMAX>(stage, rowbytes, G, gi, lane_off, xl, sxf, xsc,
-                                                    red_w, lane);
-        else
-          tile_compute_int<BITS, XPL, NR, 2, TBMAX>(stage, rowbytes, G, gi, lane_off, xl, sxf, xsc,
-                                                    red_w, lane);
+        if (TBMAX == 1 || TB == 1) {
+          tile_compute_int<BITS, XPL, NR, NRG, 1, TBMAX>(stage, rowbytes, G, gi, lane_off, row0, xl,
+                                                         sxf, xsc, red_w, lane);
+        } else {
+          if constexpr (TBMAX >= 2)
+            tile_compute_int<BITS, XPL, NR, NRG, 2, TBMAX>(stage, rowbytes, G, gi, lane_off, row0,
+                                                           xl, sxf, xsc, red_w, lane);
+        }
       } else if (TB == 1) {
         tile_compute<BITS, XPL, NR, 1, TBMAX>(stage, rowbytes, G, gi, lane_off, xp, red_w, lane);
       } else if (TB == 2) {
@@ -729,22 +764,28 @@ __global__ void __launch_bounds__(kThreads, Cfg<TBMAX>::kCtas) smallm_kernel(con
       it_next(pit);
       ++issued;
     }
-    // Finalise: thread q sums the eight warp partials of one (row, token)
-    // output in warp order; q = 0 starts at warp (i + 1) % 8, so the usually
-    // short list of outputs also rotates over the warps.
+    // Finalise: thread q sums the KW warp partials of one (row, token)
+    // output in warp order (the warps of the row's group); q = 0 starts at
+    // warp (i + 1) % 8, so the usually short list of outputs also rotates
+    // over the warps.
     const float *rb = red + (i & 1) * kCW * RED;
     const int q = (threadIdx.x + kThreads - 32 * static_cast<int>((i + 1) % kCW)) % kThreads;
     if (q < RT * TB) {
       const int r = q / TB, t = q % TB;
-      if (t < Tb && n0 + r < rows) {
-        float acc0 = 0.0f;
+      // stage row R: sum over the warps of its row group, in order
+      auto row_sum = [&](int R) {
+        const int g = R / NRG;
+        const float *rr = rb + g * KW * RED + (R - g * NRG) * TB + t;
+        float acc = 0.0f;
 #pragma unroll
-        for (int w = 0; w < kCW; ++w) acc0 += rb[w * RED + r * TB + t];
+        for (int w = 0; w < KW; ++w) acc += rr[w * RED];
+        return acc;
+      };
+      if (t < Tb && n0 + r < rows) {
+        const float acc0 = row_sum(r);
         const int64_t pos = static_cast<int64_t>(p0) + t0 + t;
         if constexpr (MODE == kGateUp) {
-          float acc1 = 0.0f;
-#pragma unroll
-          for (int w = 0; w < kCW; ++w) acc1 += rb[w * RED + (RT + r) * TB + t];
+          const float acc1 = row_sum(RT + r);
           a.ws.h[pos * rows + n0 + r] = silu(acc0) * acc1;
         } else if constexpr (MODE == kDown) {
           a.ws.out[pos * rows + n0 + r] = acc0;
@@ -764,33 +805,52 @@ __global__ void __launch_bounds__(kThreads, Cfg<TBMAX>::kCtas) smallm_kernel(con
   __syncthreads();
 }
 
-template <int BITS, int XPL, int MODE, bool XBF16, int TBMAX>
+template <int BITS, int XPL, int KW, int MODE, bool XBF16, int TBMAX>
 cudaError_t run(const Args &a, cudaStream_t s) {
-  auto k = smallm_kernel<BITS, XPL, MODE, XBF16, TBMAX>;
+  auto k = smallm_kernel<BITS, XPL, KW, MODE, XBF16, TBMAX>;
   const int smem = Cfg<TBMAX>::smem_bytes(a.E);
   cudaError_t e = ensure_smem(reinterpret_cast<const void *>(k), smem);
   if (e != cudaSuccess) return e;
   return launch_pdl(k, dim3(Cfg<TBMAX>::kCtas * sm_count()), dim3(kThreads), smem, s, a);
 }
 
+// K = 4096: eight warps of 16 columns per lane.  K = 2048: the integer form
+// keeps 16 columns per lane (four warps per row, two row groups: half the
+// per-row reduction and conversion work per code of eight columns); the
+// eight-row fp32 form keeps eight warps of 8 columns (its activation rows
+// would not fit in registers at 16).
 template <int MODE, bool XBF16, int TBMAX>
 cudaError_t run_shape(const Args &a, cudaStream_t s) {
-  const int xpl = static_cast<int>(a.K / 256);
-  if (a.w0.bits == 4)
-    return xpl == 16 ? run<4, 16, MODE, XBF16, TBMAX>(a, s) : run<4, 8, MODE, XBF16, TBMAX>(a, s);
-  return xpl == 16 ? run<8, 16, MODE, XBF16, TBMAX>(a, s) : run<8, 8, MODE, XBF16, TBMAX>(a, s);
+  const bool wide = a.K == 4096;
+  if constexpr (TBMAX == 1) {
+    // routed experts, one token per pass: 32 columns per lane (K = 4096:
+    // four warps per row, two row groups; K = 2048: two warps, four groups)
+    if (a.w0.bits == 4)
+      return wide ? run<4, 32, 4, MODE, XBF16, TBMAX>(a, s) : run<4, 32, 2, MODE, XBF16, TBMAX>(a, s);
+    return wide ? run<8, 32, 4, MODE, XBF16, TBMAX>(a, s) : run<8, 32, 2, MODE, XBF16, TBMAX>(a, s);
+  } else if constexpr (TBMAX == 2) {
+    if (a.w0.bits == 4)
+      return wide ? run<4, 16, 8, MODE, XBF16, TBMAX>(a, s) : run<4, 16, 4, MODE, XBF16, TBMAX>(a, s);
+    return wide ? run<8, 16, 8, MODE, XBF16, TBMAX>(a, s) : run<8, 16, 4, MODE, XBF16, TBMAX>(a, s);
+  } else {
+    if (a.w0.bits == 4)
+      return wide ? run<4, 16, 8, MODE, XBF16, TBMAX>(a, s) : run<4, 8, 8, MODE, XBF16, TBMAX>(a, s);
+    return wide ? run<8, 16, 8, MODE, XBF16, TBMAX>(a, s) : run<8, 8, 8, MODE, XBF16, TBMAX>(a, s);
+  }
 }
 
+// TBMAX 1: the routed experts (gate/up, down); TBMAX 2 and 8: the linear
+// layer.
 template <int TBMAX>
 cudaError_t run_class(int mode, bool x_bf16, const Args &a, cudaStream_t s) {
-  if (mode == kLinear)
-    return x_bf16 ? run_shape<kLinear, true, TBMAX>(a, s) : run_shape<kLinear, false, TBMAX>(a, s);
-  if constexpr (TBMAX > 2) {
-    return cudaErrorInvalidValue;  // the experts run in passes of two
-  } else {
+  if constexpr (TBMAX == 1) {
     if (mode == kGateUp)
-      return x_bf16 ? run_shape<kGateUp, true, TBMAX>(a, s) : run_shape<kGateUp, false, TBMAX>(a, s);
-    return run_shape<kDown, false, TBMAX>(a, s);
+      return x_bf16 ? run_shape<kGateUp, true, 1>(a, s) : run_shape<kGateUp, false, 1>(a, s);
+    if (mode == kDown) return run_shape<kDown, false, 1>(a, s);
+    return cudaErrorInvalidValue;
+  } else {
+    if (mode != kLinear) return cudaErrorInvalidValue;
+    return x_bf16 ? run_shape<kLinear, true, TBMAX>(a, s) : run_shape<kLinear, false, TBMAX>(a, s);
   }
 }
 

@@ -1,5 +1,5 @@
 // smallm_lo.cu -- small-M kernels with two activation rows per pass (two
-// CTAs per SM): the MoE experts and the linear layer with 1..2 rows.
+// CTAs per SM): the linear layer with 1..2 rows.
 #include "smallm_kernel.cuh"
 
 namespace qmm {

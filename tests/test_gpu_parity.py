@@ -266,6 +266,12 @@ def _router_case(dev, M, E, H, k, bias_kind, bf16, wr=None, x=None):
     (17, 64, 4100, 16, None, True),
     (5, 8, 64, 3, None, False),
     (70, 1024, 256, 8, "zipf", False),
+    # tiles staged through shared memory (M > 64, H a multiple of 512):
+    # ragged token and expert tiles, a single chunk, fp32 and bf16 tokens
+    (100, 40, 1024, 6, None, False),
+    (129, 256, 2048, 8, "zipf", True),
+    (65, 16, 512, 4, None, True),
+    (300, 1024, 4096, 16, "zipf", False),
 ])
 def test_router(dev, M, E, H, k, bias, bf16):
     _router_case(dev, M, E, H, k, bias, bf16)
@@ -283,6 +289,9 @@ def test_router_exact_ties_lower_index_wins(dev):
     _router_case(dev, M, E, H, 6, None, False, wr=wr, x=x)
     wr2 = np.tile(wr[:1], (E, 1))  # every logit equal -> experts 0..k-1
     _router_case(dev, 2, E, H, 4, None, False, wr=wr2)
+    # the same ties through the shared-memory tiled path (M > 64)
+    x80 = np.tile(x[:1], (80, 1))
+    _router_case(dev, 80, E, H, 6, None, False, wr=wr, x=x80)
 
 
 # ----------------------------------------------------------- MoE layer (A4-A6)
@@ -406,7 +415,7 @@ SMALLM_SHAPES = [(8, 64, 4096), (4, 64, 4096), (8, 128, 2048), (4, 128, 2048)]
 
 
 @pytest.mark.parametrize("bits,group,K", SMALLM_SHAPES)
-@pytest.mark.parametrize("M", [2, 3, 5, 8])
+@pytest.mark.parametrize("M", [1, 2, 3, 5, 8])
 def test_linear_small_m(dev, bits, group, K, M):
     # N = 1000 is not a multiple of the rows per tile: ragged last tile
     _linear_case(dev, bits, group, 1000, K, M, False, outl=True)
