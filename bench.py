@@ -351,12 +351,12 @@ def run_moe(dev, r, steps: int, warmup: int):
     # router matrix and small layers could stay resident between steps).
     flush = torch.empty((256 << 20,), dtype=torch.uint8, device=dev)
 
-    def step(evs=None):
+    def step(evs=None, split=False):
         if evs:
             evs[0].record(s)
         q.moe_route_topk(x, wr_d, bias_d, k, topk_idx=idx, topk_w=tw, expert_counts=cnt,
                          workspace=rws, stream=s)
-        if evs:
+        if evs and split:
             evs[1].record(s)
         q.moe_ffn_forward(x, idx, tw, ex, y=y, workspace=fws, stream=s)
         if evs:
@@ -365,21 +365,33 @@ def run_moe(dev, r, steps: int, warmup: int):
     for _ in range(max(3, warmup)):
         step()
     torch.cuda.synchronize()
-    times, t_route, t_ffn = [], [], []
+
+    def timed(split):
+        out = []
+        for _ in range(steps):
+            flush.zero_()
+            # ~0.2 ms of device-side wait so that the host has enqueued the
+            # whole step before its start event: the events then time the
+            # GPU, not the Python launch overhead
+            torch.cuda._sleep(400000)
+            evs = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+            step(evs, split)
+            torch.cuda.synchronize()
+            out.append((evs[0].elapsed_time(evs[2]),
+                        evs[0].elapsed_time(evs[1]) if split else 0.0,
+                        evs[1].elapsed_time(evs[2]) if split else 0.0))
+        return out
+
+    # The step is timed as one region: an event between the router and the
+    # FFN would stop the FFN's launch from overlapping the router's tail.  A
+    # second pass with that event splits the time between the two.
     n0 = q.qmm_launch_count()
-    for _ in range(steps):
-        flush.zero_()
-        # ~0.2 ms of device-side wait so that the host has enqueued the whole
-        # step before its start event: the events then time the GPU, not the
-        # Python launch overhead
-        torch.cuda._sleep(400000)
-        evs = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
-        step(evs)
-        torch.cuda.synchronize()
-        times.append(evs[0].elapsed_time(evs[2]))
-        t_route.append(evs[0].elapsed_time(evs[1]))
-        t_ffn.append(evs[1].elapsed_time(evs[2]))
+    whole = timed(False)
     launches = q.qmm_launch_count() - n0
+    parts = timed(True)
+    times = [w[0] for w in whole]
+    t_route = [p[1] for p in parts]
+    t_ffn = [p[2] for p in parts]
     counts = cnt.cpu().numpy()
     touched = int((counts > 0).sum())
     hot = int((counts >= 64).sum())

@@ -65,7 +65,31 @@ __global__ void __launch_bounds__(128) router_logits_kernel(const void *__restri
 #pragma unroll
     for (int e = 0; e < EB; ++e) acc[m][e] = 0.0f;
 
-  if constexpr (NS > 0) {
+  if constexpr (NS > 0 && MB * NS <= 64) {
+    // few tokens: the thread's activation loads are independent of each
+    // other and of the chains, so they can all be in flight together (same
+    // chain order per partial)
+    float xv[NS][MB];
+#pragma unroll
+    for (int j = 0; j < NS; ++j)
+#pragma unroll
+      for (int m = 0; m < MB; ++m) {
+        const int64_t mm = m0 + (m < mb ? m : 0);
+        const int64_t hh = p + 128 * j;
+        if constexpr (XBF16) {
+          const uint16_t b = static_cast<const uint16_t *>(x)[mm * H + hh];
+          xv[j][m] = __uint_as_float(static_cast<uint32_t>(b) << 16);
+        } else {
+          xv[j][m] = __ldg(static_cast<const float *>(x) + mm * H + hh);
+        }
+      }
+#pragma unroll
+    for (int j = 0; j < NS; ++j)
+#pragma unroll
+      for (int m = 0; m < MB; ++m)
+#pragma unroll
+        for (int e = 0; e < EB; ++e) acc[m][e] = __fmaf_rn(xv[j][m], wpre[j][e], acc[m][e]);
+  } else if constexpr (NS > 0) {
     // same chain order: h = p, p + 128, ... for every partial
 #pragma unroll
     for (int j0 = 0; j0 < NS; j0 += 4) {
@@ -660,9 +684,10 @@ cudaError_t launch_router(const void *x, bool x_bf16, int64_t M, int64_t H, cons
   // Small batches: fewer experts per block so that the 4 MB router matrix is
   // spread over more SMs.
   if (M <= 8 && H == 4096) {
-    // decode: one expert per block, its router row preloaded in registers
-    err = x_bf16 ? run_logits<8, 1, true, 32>(x, M, H, wr, bias, E, logits, counts, s)
-                 : run_logits<8, 1, false, 32>(x, M, H, wr, bias, E, logits, counts, s);
+    // decode: one expert and two tokens per block, the router row preloaded
+    // in registers and all of the two token rows' loads in flight at once
+    err = x_bf16 ? run_logits<2, 1, true, 32>(x, M, H, wr, bias, E, logits, counts, s)
+                 : run_logits<2, 1, false, 32>(x, M, H, wr, bias, E, logits, counts, s);
   } else if (M > 64 && H % tiled::kCH == 0 && (M + tiled::kTM - 1) / tiled::kTM <= 65535) {
     // larger batches: tiles staged through shared memory
     err = x_bf16 ? run_logits_tiled<true>(x, M, H, wr, bias, E, logits, counts, s)
