@@ -516,6 +516,18 @@ def main():
             "clocks": g["clocks"],
             "e2e": {"value": world * g["bytes"] / (ms_e2e * 1e-3) / 1e9, "unit": "GB/s",
                     "h2d_bytes_per_step": g["h2d"], "d2h_bytes_per_step": g["d2h"]}}
+    # The extra workloads are best effort: a failure is recorded in the line,
+    # and after a CUDA error (which poisons the context) no further GPU work
+    # is attempted, so the headline line is still printed.
+    cuda_ok = True
+
+    def release():
+        nonlocal cuda_ok
+        try:
+            torch.cuda.empty_cache()
+        except Exception:  # a sticky CUDA error from the extra that just ran
+            cuda_ok = False
+
     if args.only is None:
         try:
             gi = run_gemv_int4(dev, args.steps, args.warmup)
@@ -523,10 +535,13 @@ def main():
             line["gemv_int4"] = gi
         except Exception as e:  # keep the headline line even if an extra fails
             line["gemv_int4"] = {"error": f"{type(e).__name__}: {e}"}
-        torch.cuda.empty_cache()
+        release()
     if not args.no_moe and args.only is None:
         extras = {}
         for key, r in (("moe_decode", recipes.CFG4), ("moe_prefill", recipes.CFG5)):
+            if not cuda_ok:
+                extras[key] = {"error": "skipped after a CUDA error in an earlier extra"}
+                continue
             try:
                 mo = run_moe(dev, r, max(10, min(100, args.steps // 10)), args.warmup)
                 mo["hbm_frac"] = mo["weight_gbs"] / peaks["hbm_gbs"]
@@ -534,7 +549,7 @@ def main():
                 extras[key] = mo
             except Exception as e:  # keep the headline line even if an extra fails
                 extras[key] = {"error": f"{type(e).__name__}: {e}"}
-            torch.cuda.empty_cache()
+            release()
         line.update(extras)
     if rank == 0 and not args.no_cpu:
         gbs, nbytes, spent = oracle_gemv_sample(args.cpu_seconds)
