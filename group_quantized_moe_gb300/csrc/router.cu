@@ -220,46 +220,49 @@ __global__ void __launch_bounds__(128) router_logits_kernel(const void *__restri
 // ---------------------------------------------------------------------------
 // Batched logits (many tokens).  The kernel above reads its operands straight
 // from L2 with no reuse inside the block, which leaves a 512-token batch
-// bound by L2 traffic.  Here a block owns a tile of kTM tokens x kTE experts
+// bound by L2 traffic.  Here a block owns a tile of kTM tokens x TE experts
 // for all 128 partials: the tile's token rows and router rows stream through
 // shared memory in chunks of kCH columns (1-D bulk copies, a ring of kNST
-// stages), thread (p, half) keeps partial p of 8 tokens x 16 experts in
-// registers, and every staged value feeds 8 or 16 FMAs.  The summation order
+// stages), thread (p, half) keeps partial p of 8 tokens x TE experts in
+// registers, and every staged value feeds 8 or TE FMAs.  TE = 8 keeps the
+// registers under 128 so that two blocks share an SM: the FMA chains wait on
+// shared-memory loads, and the second block's warps fill those waits.  The summation order
 // is the one above: each partial is one fma chain in increasing h; the
 // first tree level ((P0 + P1) + (P2 + P3)) runs as two halving exchanges
 // between adjacent lanes; the last five levels run per output from shared
 // memory.
 namespace tiled {
-constexpr int kTM = 16, kTE = 16, kCH = 512, kNST = 3, kThreads = 256;
-constexpr int kTStride = 129;  // padded row of the level-1 sums in shared memory
-template <bool XBF16>
+constexpr int kTM = 16, kTE = 8, kCH = 512, kNST = 3, kThreads = 256;
+template <bool XBF16, int TE>
 __host__ __device__ constexpr int stage_bytes() {
-  return kTM * kCH * (XBF16 ? 2 : 4) + kTE * kCH * 4;
+  return kTM * kCH * (XBF16 ? 2 : 4) + TE * kCH * 4;
 }
-template <bool XBF16>
+template <bool XBF16, int TE>
 __host__ __device__ constexpr int smem_bytes() {
-  return kNST * stage_bytes<XBF16>();
+  return kNST * stage_bytes<XBF16, TE>();
 }
-static_assert(2 * 32 * kTStride * 4 <= kNST * stage_bytes<true>(), "level-1 sums reuse the ring");
 }  // namespace tiled
 
-template <bool XBF16>
-__global__ void __launch_bounds__(tiled::kThreads, 1)
+template <bool XBF16, int TE>
+__global__ void __launch_bounds__(tiled::kThreads, TE <= 8 ? 2 : 1)
     router_logits_tiled_kernel(const void *__restrict__ x, int64_t M, int64_t H,
                                const float *__restrict__ wr, const float *__restrict__ bias,
                                int E, float *__restrict__ logits, int32_t *__restrict__ counts,
                                uint32_t *status) {
   using namespace tiled;
   constexpr int XB = XBF16 ? 2 : 4;
-  constexpr int SB = stage_bytes<XBF16>();
+  constexpr int SB = stage_bytes<XBF16, TE>();
+  constexpr int V = 8 * TE;          // values per thread (8 tokens x TE experts)
+  constexpr int TS = V + 1;          // padded row of the level-1 sums in shared memory
+  static_assert(2 * 32 * TS * 4 <= kNST * SB, "level-1 sums reuse the ring");
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ __align__(8) uint64_t full[kNST];
   const int tid = threadIdx.x, p = tid & 127, half = tid >> 7;
   const int lane = tid & 31;
   const int64_t m0 = static_cast<int64_t>(blockIdx.y) * kTM;
-  const int e0 = blockIdx.x * kTE;
+  const int e0 = blockIdx.x * TE;
   const int mv = static_cast<int>(min64(kTM, M - m0));
-  const int ev = min(kTE, E - e0);
+  const int ev = min(TE, E - e0);
   const int nch = static_cast<int>(H / kCH);
   const uint32_t base = smem_addr(smem);
   auto bar = [&](int s) { return smem_addr(&full[s]); };
@@ -296,11 +299,11 @@ __global__ void __launch_bounds__(tiled::kThreads, 1)
   if (tid == 0)
     for (int c = 0; c < npre; ++c) issue_x(c);
 
-  float acc[8][kTE];
+  float acc[8][TE];
 #pragma unroll
   for (int i = 0; i < 8; ++i)
 #pragma unroll
-    for (int e = 0; e < kTE; ++e) acc[i][e] = 0.0f;
+    for (int e = 0; e < TE; ++e) acc[i][e] = 0.0f;
 
   int issued = npre, c = 0;
   bool aborted = false;
@@ -313,7 +316,7 @@ __global__ void __launch_bounds__(tiled::kThreads, 1)
 #pragma unroll
       for (int j = 0; j < kCH / 128; ++j) {
         const int hl = p + 128 * j;
-        float xv[8], wv[kTE];
+        float xv[8], wv[TE];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           if constexpr (XBF16) {
@@ -324,11 +327,11 @@ __global__ void __launch_bounds__(tiled::kThreads, 1)
           }
         }
 #pragma unroll
-        for (int e = 0; e < kTE; ++e) wv[e] = ws[e * kCH + hl];
+        for (int e = 0; e < TE; ++e) wv[e] = ws[e * kCH + hl];
 #pragma unroll
         for (int i = 0; i < 8; ++i)
 #pragma unroll
-          for (int e = 0; e < kTE; ++e) acc[i][e] = __fmaf_rn(xv[i], wv[e], acc[i][e]);
+          for (int e = 0; e < TE; ++e) acc[i][e] = __fmaf_rn(xv[i], wv[e], acc[i][e]);
       }
     }
     // one barrier per chunk: every thread is done with stage s, and all
@@ -353,56 +356,58 @@ __global__ void __launch_bounds__(tiled::kThreads, 1)
   }
 
   // Level 1 inside groups of four lanes (partials 4l .. 4l+3): at offset 1 a
-  // lane keeps half of its 128 values and adds the neighbour's copy of that
+  // lane keeps half of its V values and adds the neighbour's copy of that
   // half (P0 + P1, P2 + P3), at offset 2 half again ((P0+P1) + (P2+P3)).
-  // Lane bits (b1 b0) end with the 32 sums of value index 64 b0 + 32 b1 + i.
-  float v[8 * kTE];
+  // Lane bits (b1 b0) end with the V / 4 sums of value index
+  // (V / 2) b0 + (V / 4) b1 + i.
+  float v[V];
 #pragma unroll
   for (int i = 0; i < 8; ++i)
 #pragma unroll
-    for (int e = 0; e < kTE; ++e) v[i * kTE + e] = acc[i][e];
+    for (int e = 0; e < TE; ++e) v[i * TE + e] = acc[i][e];
   {
     const bool up = (lane & 1) != 0;
 #pragma unroll
-    for (int i = 0; i < 64; ++i) {
-      const float send = up ? v[i] : v[i + 64];
-      const float keep = up ? v[i + 64] : v[i];
+    for (int i = 0; i < V / 2; ++i) {
+      const float send = up ? v[i] : v[i + V / 2];
+      const float keep = up ? v[i + V / 2] : v[i];
       v[i] = __fadd_rn(keep, __shfl_xor_sync(0xFFFFFFFFu, send, 1));
     }
   }
   {
     const bool up = (lane & 2) != 0;
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      const float send = up ? v[i] : v[i + 32];
-      const float keep = up ? v[i + 32] : v[i];
+    for (int i = 0; i < V / 4; ++i) {
+      const float send = up ? v[i] : v[i + V / 4];
+      const float keep = up ? v[i + V / 4] : v[i];
       v[i] = __fadd_rn(keep, __shfl_xor_sync(0xFFFFFFFFu, send, 2));
     }
   }
   // t_l (l = p / 4) of value index vi lives at tb[half][l][vi ^ 8 (vi >> 5)]
-  // (rows padded to kTStride; the swizzle spreads the four value blocks a
-  // warp writes over distinct banks).
+  // (rows padded to TS; the four value blocks a warp writes at one step,
+  // offsets {0, V/2, V/4, 3V/4}, land 8 banks apart after the swizzle).
   float *tb = reinterpret_cast<float *>(smem);
   const int l = p >> 2;
-  const int vb = 64 * (lane & 1) + 32 * ((lane >> 1) & 1);
+  const int vb = (V / 2) * (lane & 1) + (V / 4) * ((lane >> 1) & 1);
 #pragma unroll
-  for (int i = 0; i < 32; ++i) {
+  for (int i = 0; i < V / 4; ++i) {
     const int vi = vb + i;
-    tb[(half * 32 + l) * kTStride + (vi ^ ((vi >> 5) << 3))] = v[i];
+    tb[(half * 32 + l) * TS + (vi ^ ((vi >> 5) << 3))] = v[i];
   }
   __syncthreads();
-  {
-    // Output o = tid: token 8 half + vi / 16, expert vi % 16.
-    const int vi = p;
+  if (tid < 2 * V) {
+    // Output o = tid: half o / V, value vi = o % V = token offset vi / TE,
+    // expert vi % TE.
+    const int oh = tid / V, vi = tid % V;
     const int col = vi ^ ((vi >> 5) << 3);
     float t[32];
 #pragma unroll
-    for (int j = 0; j < 32; ++j) t[j] = tb[(half * 32 + j) * kTStride + col];
+    for (int j = 0; j < 32; ++j) t[j] = tb[(oh * 32 + j) * TS + col];
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1)
 #pragma unroll
       for (int j = 0; j < o; ++j) t[j] = __fadd_rn(t[j], t[j + o]);
-    const int m = 8 * half + (vi >> 4), e = vi & 15;
+    const int m = 8 * oh + vi / TE, e = vi % TE;
     if (m < mv && e < ev) {
       float r = t[0];
       if (bias) r = __fadd_rn(r, bias[e0 + e]);
@@ -656,12 +661,13 @@ template <bool XBF16>
 cudaError_t run_logits_tiled(const void *x, int64_t M, int64_t H, const float *wr,
                              const float *bias, int E, float *logits, int32_t *counts,
                              cudaStream_t s) {
-  constexpr int smem = tiled::smem_bytes<XBF16>();
+  constexpr int TE = tiled::kTE;
+  constexpr int smem = tiled::smem_bytes<XBF16, TE>();
   const cudaError_t err =
-      ensure_smem(reinterpret_cast<const void *>(router_logits_tiled_kernel<XBF16>), smem);
+      ensure_smem(reinterpret_cast<const void *>(router_logits_tiled_kernel<XBF16, TE>), smem);
   if (err != cudaSuccess) return err;
-  dim3 grid((E + tiled::kTE - 1) / tiled::kTE, static_cast<unsigned>((M + tiled::kTM - 1) / tiled::kTM));
-  return launch_pdl(router_logits_tiled_kernel<XBF16>, grid, dim3(tiled::kThreads), smem, s, x, M,
+  dim3 grid((E + TE - 1) / TE, static_cast<unsigned>((M + tiled::kTM - 1) / tiled::kTM));
+  return launch_pdl(router_logits_tiled_kernel<XBF16, TE>, grid, dim3(tiled::kThreads), smem, s, x, M,
                     H, wr, bias, E, logits, counts, device_status());
 }
 
