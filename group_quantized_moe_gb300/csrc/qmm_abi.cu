@@ -268,7 +268,8 @@ int check_experts(const moe_experts *ex) {
 }
 
 struct WsLayout {
-  size_t counts, offsets, active, num_active, assign, pos, h, out, tile_start, xg, total;
+  size_t counts, offsets, active, num_active, assign, pos, h, out, tile_start, xg, light,
+      num_light, total;
 };
 
 WsLayout ws_layout(int64_t M, int k, const moe_experts *ex) {
@@ -285,6 +286,8 @@ WsLayout ws_layout(int64_t M, int k, const moe_experts *ex) {
   L.out = o;        o += round256(sizeof(float) * MK * ex->H);
   L.tile_start = o; o += round256(sizeof(int32_t) * (ex->E + 1));
   L.xg = o;         o += round256(2 * MK * ex->H);  // fp16 gathered tokens
+  L.light = o;      o += round256(sizeof(int32_t) * ex->E);
+  L.num_light = o;  o += 256;
   L.total = o;
   return L;
 }
@@ -341,19 +344,40 @@ int moe_ffn_forward(const void *x, int32_t x_dtype, int64_t M, const int32_t *to
   ws.tile_start = reinterpret_cast<int32_t *>(base + L.tile_start);
   ws.xg = reinterpret_cast<__half *>(base + L.xg);
   ws.hh = reinterpret_cast<__half *>(base + L.h);  // fp16 h reuses the fp32 h buffer
+  ws.active_light = reinterpret_cast<int32_t *>(base + L.light);
+  ws.num_light = reinterpret_cast<int32_t *>(base + L.num_light);
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const bool xb = x_dtype == QMM_BF16;
-  cudaError_t e = launch_moe_dispatch(topk_idx, M, k, ex->E, ws, s);
-  if (e != cudaSuccess) return cuda_fail(e, "moe_ffn_forward (dispatch)");
   // Decode batches (at most 8 tokens, so at most 8 per expert unless the
   // caller repeats an expert within a token) use the small-M kernels.
   const bool small_gu = M <= 8 && smallm_supported(ex->gate.bits, ex->gate.group, ex->H);
   const bool small_dn = M <= 8 && smallm_supported(ex->down.bits, ex->down.group, ex->I);
-  if (xb && !small_gu && moe_tc_supported(qmat(ex->gate), qmat(ex->down), ex->H, ex->I)) {
+  const bool tc = xb && !small_gu && moe_tc_supported(qmat(ex->gate), qmat(ex->down), ex->H, ex->I);
+  // On the tensor-core path, experts with a single token skip the dequantise
+  // -> fp16 -> MMA pipeline (a 16-row token tile for one token) and stream
+  // their weights through the small-M integer kernels instead.
+  const int light_max = (tc && smallm_supported(ex->gate.bits, ex->gate.group, ex->H) &&
+                         smallm_supported(ex->down.bits, ex->down.group, ex->I))
+                            ? 1
+                            : 0;
+  cudaError_t e = launch_moe_dispatch(topk_idx, M, k, ex->E, light_max, ws, s);
+  if (e != cudaSuccess) return cuda_fail(e, "moe_ffn_forward (dispatch)");
+  if (tc) {
     // bf16 activations: tensor-core grouped GEMMs (fp16 operands, fp32 accumulate)
     e = launch_moe_tc(x, M, k, ex->E, qmat(ex->gate), qmat(ex->up), qmat(ex->down), ws, s);
     if (e != cudaSuccess) return cuda_fail(e, "moe_ffn_forward (tensor-core experts)");
+    if (light_max > 0) {
+      // the single-token experts (they write the fp32 h buffer that the
+      // tensor-core kernels' fp16 h shares, after those have finished)
+      MoeWork wl = ws;
+      wl.active = ws.active_light;
+      wl.num_active = ws.num_light;
+      e = launch_smallm_gateup(x, xb, k, ex->E, qmat(ex->gate), qmat(ex->up), wl, s);
+      if (e != cudaSuccess) return cuda_fail(e, "moe_ffn_forward (single-token gate/up)");
+      e = launch_smallm_down(k, ex->E, qmat(ex->down), wl, s);
+      if (e != cudaSuccess) return cuda_fail(e, "moe_ffn_forward (single-token down)");
+    }
   } else {
     e = small_gu ? launch_smallm_gateup(x, xb, k, ex->E, qmat(ex->gate), qmat(ex->up), ws, s)
                  : launch_moe_gateup(x, xb, M, k, ex->E, qmat(ex->gate), qmat(ex->up), ws, s);

@@ -33,7 +33,9 @@ struct MoeWork {
   int32_t *pos;         // [M*k] position of assignment a inside `assign`
   float *h;             // [M*k, I] SwiGLU activations (fp32)
   float *out;           // [M*k, H] per-assignment expert outputs (fp32)
-  int32_t *tile_start;  // [E + 1] prefix of 128-token tiles per expert
+  int32_t *tile_start;  // [E + 1] prefix of 128-token tiles per expert (light experts: none)
+  int32_t *active_light;  // [E] experts with 1..light_max tokens, ascending
+  int32_t *num_light;     // [1]
   __half *xg;           // [M*k, H] tokens in expert order, fp16 (tensor-core path)
   __half *hh;           // [M*k, I] SwiGLU activations, fp16 (tensor-core path)
 };
@@ -83,7 +85,7 @@ cudaError_t launch_router(const void *x, bool x_bf16, int64_t M, int64_t H,
                           float *logits_scratch, int32_t *idx, float *w, int32_t *counts,
                           cudaStream_t s);
 
-cudaError_t launch_moe_dispatch(const int32_t *idx, int64_t M, int k, int E,
+cudaError_t launch_moe_dispatch(const int32_t *idx, int64_t M, int k, int E, int light_max,
                                 const MoeWork &ws, cudaStream_t s);
 
 cudaError_t launch_moe_gateup(const void *x, bool x_bf16, int64_t M, int k, int E,

@@ -487,15 +487,18 @@ __global__ void __launch_bounds__(256) router_topk_kernel(const float *__restric
 // Grouping by expert (one block): counts, exclusive offsets, the ascending
 // list of experts with tokens, and the assignments a = m*k + i sorted by
 // (expert, a) -- a stable counting sort, so the layout is deterministic.
+// Experts with at most light_max tokens (light_max > 0) also go to a second
+// ascending list and get no 128-token tiles in the tile prefix: the
+// tensor-core path skips them and the small-M kernels take them.
 __global__ void __launch_bounds__(1024) moe_dispatch_kernel(const int32_t *__restrict__ idx,
-                                                            int64_t MK, int E, MoeWork ws,
-                                                            uint32_t *status) {
+                                                            int64_t MK, int E, int light_max,
+                                                            MoeWork ws, uint32_t *status) {
   pdl_enter();
   extern __shared__ int32_t sm[];
   int32_t *cnt = sm;                 // [E]
   int32_t *cursor = sm + E;          // [E]
   int32_t *wcnt = sm + 2 * E;        // [32][E] per-warp counts of the current chunk
-  __shared__ int32_t warp_c[32], warp_f[32], warp_t[32];
+  __shared__ int32_t warp_c[32], warp_f[32], warp_t[32], warp_l[32];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int nthreads = blockDim.x;
   const int nwarps = nthreads >> 5;
@@ -519,60 +522,71 @@ __global__ void __launch_bounds__(1024) moe_dispatch_kernel(const int32_t *__res
     const int e = tid;
     const int c = (e < E) ? cnt[e] : 0;
     const int f = c > 0 ? 1 : 0;
-    const int tl = (c + 127) / 128;
-    int sc = c, sf = f, st = tl;
+    const int lf = (c > 0 && c <= light_max) ? 1 : 0;
+    const int tl = lf ? 0 : (c + 127) / 128;
+    int sc = c, sf = f, st = tl, sl = lf;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const int yc = __shfl_up_sync(0xFFFFFFFFu, sc, o);
       const int yf = __shfl_up_sync(0xFFFFFFFFu, sf, o);
       const int yt = __shfl_up_sync(0xFFFFFFFFu, st, o);
+      const int yl = __shfl_up_sync(0xFFFFFFFFu, sl, o);
       if (lane >= o) {
         sc += yc;
         sf += yf;
         st += yt;
+        sl += yl;
       }
     }
     if (lane == 31) {
       warp_c[warp] = sc;
       warp_f[warp] = sf;
       warp_t[warp] = st;
+      warp_l[warp] = sl;
     }
     __syncthreads();
     if (warp == 0) {
       int tc = lane < nwarps ? warp_c[lane] : 0;
       int tf = lane < nwarps ? warp_f[lane] : 0;
       int tt = lane < nwarps ? warp_t[lane] : 0;
+      int tg = lane < nwarps ? warp_l[lane] : 0;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const int yc = __shfl_up_sync(0xFFFFFFFFu, tc, o);
         const int yf = __shfl_up_sync(0xFFFFFFFFu, tf, o);
         const int yt = __shfl_up_sync(0xFFFFFFFFu, tt, o);
+        const int yl = __shfl_up_sync(0xFFFFFFFFu, tg, o);
         if (lane >= o) {
           tc += yc;
           tf += yf;
           tt += yt;
+          tg += yl;
         }
       }
       if (lane < nwarps) {  // inclusive over warps
         warp_c[lane] = tc;
         warp_f[lane] = tf;
         warp_t[lane] = tt;
+        warp_l[lane] = tg;
       }
     }
     __syncthreads();
     const int exc = (warp > 0 ? warp_c[warp - 1] : 0) + sc - c;
     const int exf = (warp > 0 ? warp_f[warp - 1] : 0) + sf - f;
     const int ext = (warp > 0 ? warp_t[warp - 1] : 0) + st - tl;
+    const int exl = (warp > 0 ? warp_l[warp - 1] : 0) + sl - lf;
     if (e < E) {
       ws.offsets[e] = exc;
       cursor[e] = exc;
       if (f) ws.active[exf] = e;
+      if (lf) ws.active_light[exl] = e;
       ws.counts[e] = c;
       ws.tile_start[e] = ext;
     }
     if (e == E - 1) {
       ws.offsets[E] = exc + c;
       *ws.num_active = exf + f;
+      *ws.num_light = exl + lf;
       ws.tile_start[E] = ext + tl;
     }
   }
@@ -720,8 +734,8 @@ size_t moe_dispatch_smem(int E) {
   return static_cast<size_t>(2 * E + 33 * E) * sizeof(int32_t);
 }
 
-cudaError_t launch_moe_dispatch(const int32_t *idx, int64_t M, int k, int E, const MoeWork &ws,
-                                cudaStream_t s) {
+cudaError_t launch_moe_dispatch(const int32_t *idx, int64_t M, int k, int E, int light_max,
+                                const MoeWork &ws, cudaStream_t s) {
   const int64_t MK = M * k;
   int threads = 1024;
   if (MK < 1024) threads = static_cast<int>(((MK + 31) / 32) * 32);
@@ -731,8 +745,8 @@ cudaError_t launch_moe_dispatch(const int32_t *idx, int64_t M, int k, int E, con
   cudaError_t err = ensure_smem(reinterpret_cast<const void *>(moe_dispatch_kernel),
                                 static_cast<int>(moe_dispatch_smem(E)));
   if (err != cudaSuccess) return err;
-  return launch_pdl(moe_dispatch_kernel, dim3(1), dim3(threads), smem, s, idx, MK, E, ws,
-                    device_status());
+  return launch_pdl(moe_dispatch_kernel, dim3(1), dim3(threads), smem, s, idx, MK, E, light_max,
+                    ws, device_status());
 }
 
 cudaError_t launch_moe_combine(int64_t M, int k, int64_t H, const float *topk_w,
