@@ -354,12 +354,13 @@ int moe_ffn_forward(const void *x, int32_t x_dtype, int64_t M, const int32_t *to
   const bool small_gu = M <= 8 && smallm_supported(ex->gate.bits, ex->gate.group, ex->H);
   const bool small_dn = M <= 8 && smallm_supported(ex->down.bits, ex->down.group, ex->I);
   const bool tc = xb && !small_gu && moe_tc_supported(qmat(ex->gate), qmat(ex->down), ex->H, ex->I);
-  // On the tensor-core path, experts with a single token skip the dequantise
-  // -> fp16 -> MMA pipeline (a 16-row token tile for one token) and stream
-  // their weights through the small-M integer kernels instead.
+  // On the tensor-core path, experts with one or two tokens skip the
+  // dequantise -> fp16 -> MMA pipeline (a 16-row token tile for two tokens at
+  // most) and stream their weights through the small-M integer kernels, both
+  // tokens in one pass.
   const int light_max = (tc && smallm_supported(ex->gate.bits, ex->gate.group, ex->H) &&
                          smallm_supported(ex->down.bits, ex->down.group, ex->I))
-                            ? 1
+                            ? 2
                             : 0;
   cudaError_t e = launch_moe_dispatch(topk_idx, M, k, ex->E, light_max, ws, s);
   if (e != cudaSuccess) return cuda_fail(e, "moe_ffn_forward (dispatch)");
@@ -368,15 +369,16 @@ int moe_ffn_forward(const void *x, int32_t x_dtype, int64_t M, const int32_t *to
     e = launch_moe_tc(x, M, k, ex->E, qmat(ex->gate), qmat(ex->up), qmat(ex->down), ws, s);
     if (e != cudaSuccess) return cuda_fail(e, "moe_ffn_forward (tensor-core experts)");
     if (light_max > 0) {
-      // the single-token experts (they write the fp32 h buffer that the
-      // tensor-core kernels' fp16 h shares, after those have finished)
+      // the experts with one or two tokens (they write the fp32 h buffer
+      // that the tensor-core kernels' fp16 h shares, after those have
+      // finished with it)
       MoeWork wl = ws;
       wl.active = ws.active_light;
       wl.num_active = ws.num_light;
-      e = launch_smallm_gateup(x, xb, k, ex->E, qmat(ex->gate), qmat(ex->up), wl, s);
-      if (e != cudaSuccess) return cuda_fail(e, "moe_ffn_forward (single-token gate/up)");
-      e = launch_smallm_down(k, ex->E, qmat(ex->down), wl, s);
-      if (e != cudaSuccess) return cuda_fail(e, "moe_ffn_forward (single-token down)");
+      e = launch_smallm_gateup(x, xb, k, ex->E, qmat(ex->gate), qmat(ex->up), wl, s, light_max);
+      if (e != cudaSuccess) return cuda_fail(e, "moe_ffn_forward (few-token gate/up)");
+      e = launch_smallm_down(k, ex->E, qmat(ex->down), wl, s, light_max);
+      if (e != cudaSuccess) return cuda_fail(e, "moe_ffn_forward (few-token down)");
     }
   } else {
     e = small_gu ? launch_smallm_gateup(x, xb, k, ex->E, qmat(ex->gate), qmat(ex->up), ws, s)

@@ -119,9 +119,14 @@ namespace qmm {
 bool smallm_supported(int bits, int group, int64_t K);
 cudaError_t launch_smallm_linear(const void *x, bool x_bf16, int64_t M, const QMat &w, float *y,
                                  cudaStream_t s);
+// rows_per_pass: 1 (one token per pass, 32 columns per lane: decode batches)
+// or 2 (two tokens per pass, 16 columns per lane: the experts of a prefill
+// batch with at most two tokens).
 cudaError_t launch_smallm_gateup(const void *x, bool x_bf16, int k, int E, const QMat &gate,
-                                 const QMat &up, const MoeWork &ws, cudaStream_t s);
-cudaError_t launch_smallm_down(int k, int E, const QMat &down, const MoeWork &ws, cudaStream_t s);
+                                 const QMat &up, const MoeWork &ws, cudaStream_t s,
+                                 int rows_per_pass = 1);
+cudaError_t launch_smallm_down(int k, int E, const QMat &down, const MoeWork &ws, cudaStream_t s,
+                               int rows_per_pass = 1);
 }  // namespace qmm
 
 namespace qmm {
