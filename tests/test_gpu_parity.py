@@ -444,6 +444,30 @@ def test_moe_small_m(dev, bits, group, H, I, bf16):
         _moe_check(dev, x, xd, idx, w, ex, og, ou, od, what=f"b{bits} g{group} M{M} bf16={bf16}")
 
 
+def test_moe_tensor_core_few_token_experts(dev):
+    """bf16 tokens with M > 8 on the tensor-core path, H = I = 2048: experts with one
+    or two tokens run on the small-M kernels (two tokens per pass), the others on the
+    tensor cores, in the same call."""
+    E, k, H, I, M = 8, 2, 2048, 2048, 24
+    ex, og, ou, od = _small_experts(dev, E, H, I, 8, 128, seed=13)
+    x, xd = _bf16_x(synth.normal(13, 1, M * H).reshape(M, H), dev)
+    idx = np.zeros((M, k), np.int32)
+    idx[:, 0] = 0                  # 24 tokens: tensor cores
+    idx[:, 1] = 4                  # 17 tokens: tensor cores
+    idx[0, 1] = 1                  # one token
+    idx[1:3, 1] = 2                # two tokens
+    idx[3:6, 1] = 3                # three tokens: tensor cores
+    idx[6, 1] = 7                  # one token
+    w = np.tile(np.array([0.6, 0.4], np.float32), (M, 1))
+    _moe_check(dev, x, xd, idx, w, ex, og, ou, od, what="split fp32 out")
+    _moe_check(dev, x, xd, idx, w, ex, og, ou, od, y_dtype=torch.bfloat16, what="split bf16 out")
+    # every expert light (k = 1: expert 0 gets two tokens, the others one), so
+    # the tensor-core launches find no work items
+    idx2 = (np.arange(9, dtype=np.int32) % E).reshape(9, 1)
+    w2 = np.ones((9, 1), np.float32)
+    _moe_check(dev, x[:9], xd[:9], idx2, w2, ex, og, ou, od, what="all light")
+
+
 def test_moe_small_m_token_patterns(dev):
     """Every token on the same experts (8 tokens per expert), an expert
     repeated inside each token (16 assignments: two passes of 8), and one
