@@ -17,7 +17,10 @@
 // router rows as coalesced 512-byte rows per step.  The tree runs in the
 // order above: adjacent-partial sums by xor shuffles 1 and 2, the o = 16 and
 // o = 8 stages across warps through shared memory, the rest by xor shuffles
-// 16, 8, 4 inside warp 0.
+// 16, 8, 4 inside warp 0.  Decode batches (M <= 8) use two tokens and one
+// expert per block with the router row preloaded; batches above 64 tokens
+// stage 16-token x 8-expert tiles through shared memory
+// (router_logits_tiled_kernel).
 #include <cstdint>
 
 #include "qmm_device.cuh"
@@ -65,7 +68,8 @@ __global__ void __launch_bounds__(128) router_logits_kernel(const void *__restri
 #pragma unroll
     for (int e = 0; e < EB; ++e) acc[m][e] = 0.0f;
 
-  if constexpr (NS > 0 && MB * NS <= 64) {
+  static_assert(NS == 0 || MB * NS <= 64, "preloaded rows are for a few tokens");
+  if constexpr (NS > 0) {
     // few tokens: the thread's activation loads are independent of each
     // other and of the chains, so they can all be in flight together (same
     // chain order per partial)
@@ -89,31 +93,6 @@ __global__ void __launch_bounds__(128) router_logits_kernel(const void *__restri
       for (int m = 0; m < MB; ++m)
 #pragma unroll
         for (int e = 0; e < EB; ++e) acc[m][e] = __fmaf_rn(xv[j][m], wpre[j][e], acc[m][e]);
-  } else if constexpr (NS > 0) {
-    // same chain order: h = p, p + 128, ... for every partial
-#pragma unroll
-    for (int j0 = 0; j0 < NS; j0 += 4) {
-      float xv[4][MB];
-#pragma unroll
-      for (int u = 0; u < 4; ++u)
-#pragma unroll
-        for (int m = 0; m < MB; ++m) {
-          const int64_t mm = m0 + (m < mb ? m : 0);
-          const int64_t hh = p + 128 * (j0 + u);
-          if constexpr (XBF16) {
-            const uint16_t b = static_cast<const uint16_t *>(x)[mm * H + hh];
-            xv[u][m] = __uint_as_float(static_cast<uint32_t>(b) << 16);
-          } else {
-            xv[u][m] = __ldg(static_cast<const float *>(x) + mm * H + hh);
-          }
-        }
-#pragma unroll
-      for (int u = 0; u < 4; ++u)
-#pragma unroll
-        for (int m = 0; m < MB; ++m)
-#pragma unroll
-          for (int e = 0; e < EB; ++e) acc[m][e] = __fmaf_rn(xv[u][m], wpre[j0 + u][e], acc[m][e]);
-    }
   }
 
   // Four h-steps per iteration: all their loads issue before the FMAs, so a
