@@ -205,19 +205,47 @@ __device__ __forceinline__ void tc_commit(uint32_t bar) {
       : "memory");
 }
 
-// 16 consecutive fp32 columns of this thread's TMEM lane.
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
-  uint32_t r[16];
+// 16 columns at each of two TMEM addresses of this thread's lane, both loads
+// in flight before the single wait (one asm statement, so no use of the
+// outputs can be scheduled before the wait).
+__device__ __forceinline__ void tmem_ld16x2(uint32_t a0, uint32_t a1, float (&v0)[16],
+                                            float (&v1)[16]) {
+  uint32_t r[32];
   asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
-      "%11, %12, %13, %14, %15}, [%16];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-        "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%32];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%33];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(a0), "r"(a1)
+      : "memory");
 #pragma unroll
-  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+  for (int i = 0; i < 16; ++i) {
+    v0[i] = __uint_as_float(r[i]);
+    v1[i] = __uint_as_float(r[16 + i]);
+  }
+}
+
+// The same for four addresses.
+__device__ __forceinline__ void tmem_ld16x4(uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                            float (&v0)[16], float (&v1)[16], float (&v2)[16],
+                                            float (&v3)[16]) {
+  uint32_t r[64];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%64];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%65];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47}, [%66];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [%67];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    v0[i] = __uint_as_float(r[i]);
+    v1[i] = __uint_as_float(r[16 + i]);
+    v2[i] = __uint_as_float(r[32 + i]);
+    v3[i] = __uint_as_float(r[48 + i]);
+  }
 }
 
 // Shared-memory operand descriptor: K-major, 128B swizzle, 8-row groups 1024 B
@@ -277,7 +305,12 @@ __device__ __forceinline__ Item decode_item(const int32_t *s_off, const int32_t 
   return it;
 }
 
-__device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g)); }
+// SwiGLU's silu for an fp16 result: the fast exponential and division (a few
+// ulp of fp32) are far inside fp16 rounding; the exponent is clamped so that
+// the divisor stays finite (silu(g) for g < -80 is below 1e-33).
+__device__ __forceinline__ float silu_f(float g) {
+  return __fdividef(g, 1.0f + __expf(fminf(-g, 80.0f)));
+}
 
 // INT8 codes (stored q - 128) of one 16-byte chunk -> 16 fp16 weights
 // (q - zp) * s, packed two per 32-bit word in K order.
@@ -593,18 +626,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int c0 = 16 * wg; c0 < it.ntok; c0 += 16 * kDequantGroups) {
         float v0[16], v1[16];
         if (light) {
-          float p[16];
-          tmem_ld16(tmem + lane_base + c0, v0);
-          tmem_ld16(tmem + lane_base + 64 + c0, p);
+          float p0[16], p1[16];
+          tmem_ld16x4(tmem + lane_base + c0, tmem + lane_base + 64 + c0,
+                      tmem + lane_base + 128 + c0, tmem + lane_base + 192 + c0, v0, p0, v1, p1);
 #pragma unroll
-          for (int j = 0; j < 16; ++j) v0[j] += p[j];
-          tmem_ld16(tmem + lane_base + 128 + c0, v1);
-          tmem_ld16(tmem + lane_base + 192 + c0, p);
-#pragma unroll
-          for (int j = 0; j < 16; ++j) v1[j] += p[j];
+          for (int j = 0; j < 16; ++j) {
+            v0[j] += p0[j];
+            v1[j] += p1[j];
+          }
         } else {
-          tmem_ld16(tmem + lane_base + c0, v0);
-          tmem_ld16(tmem + lane_base + kBN + c0, v1);
+          tmem_ld16x2(tmem + lane_base + c0, tmem + lane_base + kBN + c0, v0, v1);
         }
         if constexpr (NT == 2) {
           // v0 = gate, v1 = up
