@@ -1,6 +1,7 @@
 // smallm.cuh -- fused dequantise-matmul for a few activation rows per weight
-// matrix on the CUDA cores: the routed experts of a decode batch (gate + up
-// with the SwiGLU epilogue, then down) and qmm_linear for 2..8 rows.
+// matrix on the CUDA cores: the routed experts of a decode batch and the
+// one- or two-token experts of a prefill batch (gate + up with the SwiGLU
+// epilogue, then down), and qmm_linear for 1..8 rows.
 //
 // "Why I hand-wrote a DeepSeek inference engine in pure C", section 3.2
 // (the codes are dequantised inside the dot product, never written out as
@@ -45,14 +46,16 @@ constexpr int kStageBytes = 40960;
 
 // Three configurations (TBMAX = activation rows per pass).  TBMAX 1 and 2
 // use two CTAs per SM (128 registers) and the compact integer form.
-// TBMAX 1 runs the routed experts: most experts of a decode batch have one
+// TBMAX 1 runs the routed experts of decode batches: most of them have one
 // token, and with one row per pass a lane can hold 32 columns, which halves
 // the per-row work (scale, zero point, conversions, reduction) per code; an
 // expert with T tokens is applied in T passes, each a sweep over the CTA's
 // tiles of that expert (activations load once per pass, the tiles stream
 // again).  TBMAX 2 (16 columns per lane) runs the linear layer with 1..2
-// rows.  TBMAX 8 (one CTA per SM, eight fp32 rows per pass) runs the linear
-// layer with 3..8 rows, where every tile serves all M rows.
+// rows and the experts of a prefill batch that have one or two tokens (both
+// tokens in one pass, so the weights stream once).  TBMAX 8 (one CTA per SM,
+// eight fp32 rows per pass) runs the linear layer with 3..8 rows, where every
+// tile serves all M rows.
 template <int TBMAX>
 struct Cfg {
   static constexpr int kCtas = TBMAX <= 2 ? 2 : 1;      // CTAs per SM
