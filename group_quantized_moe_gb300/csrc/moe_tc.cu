@@ -23,7 +23,8 @@
 //     the B stages (128B swizzle, the canonical K-major operand layout):
 //     16-row boxes for up to 64 tokens, one 128-row box above.
 //   warps 0-11 = three dequant warpgroups; warpgroup g converts the stages
-//     kb = g (mod 3), thread t the whole 64-K row t % 128 of each weight tile,
+//     whose global number is g (mod 3), thread t the whole 64-K row t % 128
+//     of each weight tile,
 //     so three stages are being converted at once (one stage's conversion is
 //     latency bound; stages pipeline).  Codes -> fp16 (q - zp) * s, exact up
 //     to the final fp16 rounding, stored with tcgen05.st straight into tensor
@@ -77,18 +78,27 @@ struct Ring;  // NT = weight tiles sharing one token tile (2: gate+up, 1: down)
 // parities for NT=1), then the A stages: NT=2 uses 256 + 4*2*32 = 512
 // columns, NT=1 uses 256 + 4*32 = 384 (allocation 512).
 // The A and B rings have the same depth, so that one commit frees the A
-// and B slots of a stage together; the code ring only has to cover HBM
-// latency (a deeper one delays the token-tile loads queued behind it).
+// and B slots of a stage together.  The code ring's depth is a multiple of
+// the three dequant warpgroups: stage gs goes to code slot gs mod kC and to
+// warpgroup gs mod 3, so every use of a slot belongs to the same warpgroup,
+// in order.  Its wait on the slot's barrier can then never see a phase two
+// uses old (which the parity test would take as complete: with a depth that
+// is not a multiple of 3, a warpgroup that runs ahead could read a slot whose
+// copy is still landing and arrive on the wrong phase of its free barrier).
+// Three warpgroups hold three slots while they convert, so the ring also
+// needs more than three slots to keep loads in flight.
 template <>
 struct Ring<2> {
-  static constexpr int kA = 4, kB = 4, kC = 4;
+  static constexpr int kA = 4, kB = 4, kC = 6;
   static constexpr uint32_t kTmemCols = 512;
 };
 template <>
 struct Ring<1> {
-  static constexpr int kA = 4, kB = 4, kC = 8;
+  static constexpr int kA = 4, kB = 4, kC = 9;
   static constexpr uint32_t kTmemCols = 512;
 };
+static_assert(Ring<2>::kC % kDequantGroups == 0 && Ring<1>::kC % kDequantGroups == 0,
+              "each code slot must belong to one dequant warpgroup");
 
 template <int NT>
 struct Smem {
@@ -538,6 +548,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           asm volatile("prefetch.global.L2 [%0];" ::"l"(zpp[t] + g));
         }
       }
+      // this warpgroup's first stage of the item (stages are dealt by their
+      // global number gs)
+      const int kb0 = static_cast<int>((wg - gs % kDequantGroups + kDequantGroups) % kDequantGroups);
       // scale / zero point of this warpgroup's next stage, loaded one of its
       // stages ahead
       float s_nx[NT];
@@ -547,8 +560,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         s_nx[t] = 0.0f;
         z_nx[t] = 0;
       }
-      if (wg < kstages) {
-        const int gi = (wg * kBK) >> a.group_shift;
+      if (kb0 < kstages) {
+        const int gi = (kb0 * kBK) >> a.group_shift;
 #pragma unroll
         for (int t = 0; t < NT; ++t) {
           s_nx[t] = __ldg(scp[t] + gi);
@@ -557,7 +570,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       bool ok = true;
       for (int kb = 0; kb < kstages; ++kb, ++gs) {
-        if (kb % kDequantGroups != wg) continue;
+        if (static_cast<int>(gs % kDequantGroups) != wg) continue;
         __half2 s2[NT], mz2[NT];
 #pragma unroll
         for (int t = 0; t < NT; ++t) {
