@@ -362,8 +362,14 @@ int moe_ffn_forward(const void *x, int32_t x_dtype, int64_t M, const int32_t *to
                          smallm_supported(ex->down.bits, ex->down.group, ex->I))
                             ? 2
                             : 0;
-  cudaError_t e = launch_moe_dispatch(topk_idx, M, k, ex->E, light_max, ws, s);
-  if (e != cudaSuccess) return cuda_fail(e, "moe_ffn_forward (dispatch)");
+  // Decode batches on the small-M kernels group their (at most 128)
+  // assignments themselves; everything else goes through the dispatch kernel.
+  const bool self_grouped = !tc && small_gu && small_dn;
+  cudaError_t e = cudaSuccess;
+  if (!self_grouped) {
+    e = launch_moe_dispatch(topk_idx, M, k, ex->E, light_max, ws, s);
+    if (e != cudaSuccess) return cuda_fail(e, "moe_ffn_forward (dispatch)");
+  }
   if (tc) {
     // bf16 activations: tensor-core grouped GEMMs (fp16 operands, fp32 accumulate)
     e = launch_moe_tc(x, M, k, ex->E, qmat(ex->gate), qmat(ex->up), qmat(ex->down), ws, s);
@@ -380,12 +386,17 @@ int moe_ffn_forward(const void *x, int32_t x_dtype, int64_t M, const int32_t *to
       e = launch_smallm_down(k, ex->E, qmat(ex->down), wl, s, light_max);
       if (e != cudaSuccess) return cuda_fail(e, "moe_ffn_forward (few-token down)");
     }
-  } else {
-    e = small_gu ? launch_smallm_gateup(x, xb, k, ex->E, qmat(ex->gate), qmat(ex->up), ws, s)
-                 : launch_moe_gateup(x, xb, M, k, ex->E, qmat(ex->gate), qmat(ex->up), ws, s);
+  } else if (self_grouped) {
+    const int64_t MK = M * k;
+    e = launch_smallm_gateup(x, xb, k, ex->E, qmat(ex->gate), qmat(ex->up), ws, s, 1, topk_idx,
+                             MK);
     if (e != cudaSuccess) return cuda_fail(e, "moe_ffn_forward (gate/up)");
-    e = small_dn ? launch_smallm_down(k, ex->E, qmat(ex->down), ws, s)
-                 : launch_moe_down(M, k, ex->E, qmat(ex->down), ws, s);
+    e = launch_smallm_down(k, ex->E, qmat(ex->down), ws, s, 1, topk_idx, MK);
+    if (e != cudaSuccess) return cuda_fail(e, "moe_ffn_forward (down)");
+  } else {
+    e = launch_moe_gateup(x, xb, M, k, ex->E, qmat(ex->gate), qmat(ex->up), ws, s);
+    if (e != cudaSuccess) return cuda_fail(e, "moe_ffn_forward (gate/up)");
+    e = launch_moe_down(M, k, ex->E, qmat(ex->down), ws, s);
     if (e != cudaSuccess) return cuda_fail(e, "moe_ffn_forward (down)");
   }
   e = launch_moe_combine(M, k, ex->H, topk_w, ws, y, y_dtype == QMM_BF16, s);

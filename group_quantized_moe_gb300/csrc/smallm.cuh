@@ -63,7 +63,11 @@ struct Cfg {
   static constexpr int kRedMax = TBMAX * 32;            // rows x tokens per tile
   static constexpr int kRingBytes = kStages * kStageBytes;
   static constexpr int kRedBytes = 2 * kCW * kRedMax * 4;
-  static int smem_bytes(int E) { return kRingBytes + kRedBytes + (3 * E + 2) * 4; }
+  // segments (3 E + 2 ints), and for the in-CTA grouping of a decode batch
+  // the assignments' experts and sorted order (2 MK) and the counts (E)
+  static int smem_bytes(int E, int64_t MK) {
+    return kRingBytes + kRedBytes + (3 * E + 2) * 4 + static_cast<int>(2 * MK + E) * 4;
+  }
 };
 
 enum Mode { kLinear = 0, kGateUp = 1, kDown = 2 };
@@ -80,6 +84,12 @@ struct Args {
   int k;            // top-k: sorted position p holds token assign[p] / k
   int64_t M;        // linear: activation rows
   MoeWork ws;
+  // Decode batches: the expert kernels group the M k assignments themselves
+  // from the top-k indices (no dispatch kernel); gate/up's CTA 0 writes the
+  // sorted position of every assignment to pos_out for the combine.
+  const int32_t *idx;  // [M k] expert of each assignment, or NULL (use ws)
+  int64_t MK;
+  int32_t *pos_out;
   const void *x;    // linear and gate/up: activations [*, K]
   float *y;         // linear: output [M, rows]
   uint32_t *status;

@@ -520,6 +520,10 @@ __global__ void __launch_bounds__(kThreads, Cfg<TBMAX>::kCtas) smallm_kernel(con
   int32_t *s_active = reinterpret_cast<int32_t *>(smem + C::kRingBytes + C::kRedBytes);
   int32_t *s_off = s_active + a.E;
   int32_t *s_cs = s_off + a.E + 1;
+  int32_t *s_idx = s_cs + a.E + 1;   // in-CTA grouping: expert of each assignment
+  int32_t *s_asg = s_idx + a.MK;     //   sorted position -> assignment
+  int32_t *s_cnt = s_asg + a.MK;     //   tokens per expert
+  __shared__ int32_t scan_w[kCW][2];
   const uint32_t ring = smem_addr(smem);
 
   // Segments: the experts with tokens, in expert order (the linear layer:
@@ -530,6 +534,81 @@ __global__ void __launch_bounds__(kThreads, Cfg<TBMAX>::kCtas) smallm_kernel(con
       s_off[0] = 0;
       s_off[1] = static_cast<int32_t>(a.M);
       nseg_s = 1;
+    }
+  } else if (a.idx) {
+    // Decode batch: group the assignments by expert here (a stable counting
+    // sort, the dispatch kernel's order: expert, then assignment).
+    const int MK = static_cast<int>(a.MK), E = a.E;
+    for (int t = threadIdx.x; t < MK; t += blockDim.x) {
+      const int e = a.idx[t];
+      const bool valid = e >= 0 && e < E;
+      s_idx[t] = valid ? e : -1;
+      if (!valid && MODE == kGateUp && blockIdx.x == 0) atomicOr(a.status, kDevBadExpert);
+    }
+    for (int e = threadIdx.x; e < E; e += blockDim.x) s_cnt[e] = 0;
+    __syncthreads();
+    for (int t = threadIdx.x; t < MK; t += blockDim.x)
+      if (s_idx[t] >= 0) atomicAdd(&s_cnt[s_idx[t]], 1);
+    __syncthreads();
+    {
+      // exclusive scans of the counts and of the "has tokens" flags: four
+      // consecutive experts per thread (E <= 1024), then warp and block scans
+      constexpr int PER = 1024 / kThreads;
+      const int e0 = PER * threadIdx.x;
+      int c[PER], f[PER], sc = 0, sf = 0;
+#pragma unroll
+      for (int u = 0; u < PER; ++u) {
+        c[u] = e0 + u < E ? s_cnt[e0 + u] : 0;
+        f[u] = c[u] > 0 ? 1 : 0;
+        sc += c[u];
+        sf += f[u];
+      }
+      int ic = sc, jf = sf;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int yc = __shfl_up_sync(0xFFFFFFFFu, ic, o);
+        const int yf = __shfl_up_sync(0xFFFFFFFFu, jf, o);
+        if (lane >= o) {
+          ic += yc;
+          jf += yf;
+        }
+      }
+      if (lane == 31) {
+        scan_w[warp][0] = ic;
+        scan_w[warp][1] = jf;
+      }
+      __syncthreads();
+      int bc = 0, bf = 0;
+      for (int w = 0; w < warp; ++w) {
+        bc += scan_w[w][0];
+        bf += scan_w[w][1];
+      }
+      int xc = bc + ic - sc, xf = bf + jf - sf;
+#pragma unroll
+      for (int u = 0; u < PER; ++u) {
+        if (e0 + u < E) {
+          s_off[e0 + u] = xc;
+          if (f[u]) s_active[xf] = e0 + u;
+        }
+        xc += c[u];
+        xf += f[u];
+      }
+      if (threadIdx.x == kThreads - 1) {
+        s_off[E] = xc;
+        nseg_s = xf;
+      }
+    }
+    __syncthreads();
+    for (int t = threadIdx.x; t < MK; t += blockDim.x) {
+      const int e = s_idx[t];
+      int p = -1;
+      if (e >= 0) {
+        int r = 0;
+        for (int u = 0; u < t; ++u) r += s_idx[u] == e ? 1 : 0;
+        p = s_off[e] + r;
+        s_asg[p] = t;
+      }
+      if (a.pos_out && blockIdx.x == 0) a.pos_out[t] = p;
     }
   } else {
     const int n = *a.ws.num_active;
@@ -712,7 +791,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<TBMAX>::kCtas) smallm_kernel(con
             xr[t] = XBF16 ? static_cast<const void *>(static_cast<const uint16_t *>(a.x) + tt * a.K)
                           : static_cast<const void *>(static_cast<const float *>(a.x) + tt * a.K);
           } else if constexpr (MODE == kGateUp) {
-            const int64_t tok = a.ws.assign[p0 + tt] / a.k;
+            const int64_t tok = (a.idx ? s_asg[p0 + tt] : a.ws.assign[p0 + tt]) / a.k;
             xr[t] = XBF16 ? static_cast<const void *>(static_cast<const uint16_t *>(a.x) + tok * a.K)
                           : static_cast<const void *>(static_cast<const float *>(a.x) + tok * a.K);
           } else {
@@ -808,7 +887,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<TBMAX>::kCtas) smallm_kernel(con
 template <int BITS, int XPL, int KW, int MODE, bool XBF16, int TBMAX>
 cudaError_t run(const Args &a, cudaStream_t s) {
   auto k = smallm_kernel<BITS, XPL, KW, MODE, XBF16, TBMAX>;
-  const int smem = Cfg<TBMAX>::smem_bytes(a.E);
+  const int smem = Cfg<TBMAX>::smem_bytes(a.E, a.idx ? a.MK : 0);
   cudaError_t e = ensure_smem(reinterpret_cast<const void *>(k), smem);
   if (e != cudaSuccess) return e;
   return launch_pdl(k, dim3(Cfg<TBMAX>::kCtas * sm_count()), dim3(kThreads), smem, s, a);
