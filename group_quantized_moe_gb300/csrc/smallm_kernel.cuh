@@ -721,24 +721,34 @@ __global__ void __launch_bounds__(kThreads, Cfg<TBMAX>::kCtas) smallm_kernel(con
 
   // Thread 0 streams the tiles: codes, scales and zero points of RT rows of
   // each matrix, three bulk copies per matrix completing on the stage's
-  // barrier.
+  // barrier.  Experts: a tile that a later pass of its segment reads again
+  // (an expert with more tokens than one pass takes) keeps the normal L2
+  // priority; every other read is the tile's last and goes in as "evict
+  // first", so the tiles still to be re-read stay in L2 while the rest of
+  // the weights stream past them.
   auto issue = [&](const TileIt &it, int st) {
     const int e = s_active[it.s];
     const int64_t n0 = it.j * RT;
     const int rv = static_cast<int>(min64(RT, rows - n0));
     const uint32_t fb = smem_addr(&full_bar[st]);
     const uint32_t stage = ring + st * kStageBytes;
+    const bool hint = MODE != kLinear && it.b + 1 >= it.nb;
+    const uint64_t pol = hint ? l2_evict_first_policy() : 0ull;
+    auto copy = [&](uint32_t dst, const void *src, int bytes) {
+      if (hint)
+        bulk_g2s_hint(dst, src, static_cast<uint32_t>(bytes), fb, pol);
+      else
+        bulk_g2s(dst, src, static_cast<uint32_t>(bytes), fb);
+    };
     mbar_arrive_expect_tx(fb, static_cast<uint32_t>(NM * rv * (rowbytes + 8 * G)));
 #pragma unroll
     for (int m = 0; m < NM; ++m) {
       const QMat &W = m == 0 ? a.w0 : a.w1;
       const int r0 = m * RT;
-      bulk_g2s(stage + r0 * rowbytes, W.codes + e * W.codes_stride + n0 * rowbytes,
-               static_cast<uint32_t>(rv * rowbytes), fb);
-      bulk_g2s(stage + NR * rowbytes + r0 * G * 4, W.scales + e * W.groups_stride + n0 * G,
-               static_cast<uint32_t>(rv * G * 4), fb);
-      bulk_g2s(stage + NR * rowbytes + NR * G * 4 + r0 * G * 4,
-               W.zps + e * W.groups_stride + n0 * G, static_cast<uint32_t>(rv * G * 4), fb);
+      copy(stage + r0 * rowbytes, W.codes + e * W.codes_stride + n0 * rowbytes, rv * rowbytes);
+      copy(stage + NR * rowbytes + r0 * G * 4, W.scales + e * W.groups_stride + n0 * G, rv * G * 4);
+      copy(stage + NR * rowbytes + NR * G * 4 + r0 * G * 4, W.zps + e * W.groups_stride + n0 * G,
+           rv * G * 4);
     }
   };
   // Every thread tracks the producer's position (it is cheap and keeps the
