@@ -70,3 +70,20 @@ def test_reference_arm_under_torchrun_prints_once_from_rank0():
     assert d["impl"] == "reference"
     assert d["cpu_baseline"]["kind"] == "oracle"
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["value"] > 0
+
+
+def test_cpu_baseline_parallel_oracle_processes():
+    """The multi-core baseline runs the unchanged oracle in spawned processes
+    from a common start; its figure counts every worker's bytes over the
+    wall-clock span, and the single-thread figure is kept beside it."""
+    sys.path.insert(0, ROOT)
+    import bench
+    gbs, nbytes, span = bench.oracle_gemv_parallel(0.3, 2, setup_s=3.0)
+    per_block = bench.weight_bytes(1024, 4096, 8, 64)
+    assert gbs > 0 and nbytes % per_block == 0 and nbytes >= 2 * per_block
+    assert 0.3 <= span < 3.0
+    d = bench.cpu_baseline(0.2)
+    assert d["kind"] == "oracle" and d["unit"] == "GB/s"
+    assert d["single_thread"]["cores"] == 1 and d["single_thread"]["value"] > 0
+    if bench.host_cores() > 2:
+        assert d["cores"] == bench.host_cores() - 1 and "parallel_error" not in d
