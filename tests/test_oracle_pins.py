@@ -163,6 +163,163 @@ def test_linear_brute_force_tiny():
             assert y[n] == pytest.approx(acc, rel=1e-13, abs=1e-15)
 
 
+# --------------------------- tolerance bounds ----------------------------
+# The per-output fp32 tolerance of a linear output is 1e-5 * sum_k |x_k w^_k|
+# + 1e-6; the MoE tolerance propagates it through SwiGLU and the down
+# projection.  They decide every fp32 parity verdict, so they are pinned by
+# special cases and properties, not by their formula.
+
+
+@pytest.mark.parametrize("bits", [8, 4])
+def test_linear_bound_one_hot_reads_one_weight(bits):
+    """x = c e_k: the bound is 1e-5 |c w^[n,k]| + 1e-6 for every row n (a
+    wrong index, a transposed operand or a wrong factor changes it)."""
+    N, K = 5, 128
+    qw = oracle.quantize(_weights(21, 1, N, K, outliers=True), bits, 32)
+    wh = oracle.dequantize(qw).astype(np.float64)
+    for k, c in ((0, 2.0), (77, -0.5), (127, 8.0)):
+        x = np.zeros(K, np.float32)
+        x[k] = c
+        b = oracle.linear_bound(x, qw)[0]
+        np.testing.assert_allclose(b, 1e-5 * np.abs(c * wh[:, k]) + 1e-6, rtol=1e-14, atol=0)
+
+
+def test_linear_bound_sign_invariance_and_dominance():
+    """Flipping the signs of x leaves the bound unchanged (it sums absolute
+    products); it dominates 1e-5 |y| + 1e-6 (triangle inequality), with
+    equality when every product x_k w^_k is non-negative."""
+    N, K = 4, 256
+    qw = oracle.quantize(_weights(22, 1, N, K), 8, 64)
+    wh = oracle.dequantize(qw).astype(np.float64)
+    x = synth.normal(22, 2, K)
+    flip = np.where(synth.normal(22, 3, K) > 0, 1.0, -1.0).astype(np.float32)
+    b = oracle.linear_bound(x, qw)[0]
+    np.testing.assert_array_equal(oracle.linear_bound(x * flip, qw)[0], b)
+    y = oracle.linear_fused(x, qw)[0]
+    assert (b - 1e-6 >= 1e-5 * np.abs(y) * (1 - 1e-12)).all()
+    assert (b - 1e-6 > 2 * 1e-5 * np.abs(y)).any()  # mixed signs: strictly looser
+    for n in range(N):
+        xs = (np.abs(x) * np.where(wh[n] >= 0, 1.0, -1.0)).astype(np.float32)
+        bn = oracle.linear_bound(xs, qw)[0, n]
+        yn = oracle.linear_fused(xs, qw)[0, n]
+        assert bn - 1e-6 == pytest.approx(1e-5 * yn, rel=1e-12)
+
+
+def test_linear_bound_covers_a_plain_fp32_gemv():
+    """The tolerance exists for fp32 implementations: a plain fp32 GEMV of
+    the dequantised weights (sequential fp32 accumulation, the worst common
+    order) stays within it, and the bound is not orders of magnitude loose."""
+    N, K = 16, 4096
+    qw = oracle.quantize(_weights(23, 1, N, K, outliers=True), 8, 64)
+    wh = oracle.dequantize(qw)
+    x = synth.normal(23, 2, K)
+    y = oracle.linear_fused(x, qw)[0]
+    b = oracle.linear_bound(x, qw)[0]
+    y32 = np.zeros(N, np.float32)
+    for k in range(K):
+        y32 = (y32 + x[k] * wh[:, k]).astype(np.float32)
+    err = np.abs(y32.astype(np.float64) - y)
+    assert (err <= b).all()
+    sabs = (b - 1e-6) / 1e-5
+    assert (b < 1e-3 * sabs + 1e-6).all()
+
+
+def _moe_case(seed, k=2, M=3, E=4, H=64, I=32):
+    gate, up, down = _experts(seed, E, H, I, 8, 32)
+    x = synth.normal(seed, 1, M * H).reshape(M, H)
+    idx = np.array([[(m + i) % E for i in range(k)] for m in range(M)], np.int32)
+    return x, idx, gate, up, down
+
+
+def test_moe_bound_homogeneous_and_additive_in_routing_weights():
+    """With no routing-weight error (dw = 0) every slot adds |w_i| times its
+    own propagated bound: scaling w by c scales the bound (less the 1e-6
+    floor) by |c|, and the slots' contributions add."""
+    x, idx, gate, up, down = _moe_case(31)
+    w = np.array([[0.75, 0.25], [0.5, 0.5], [0.125, 0.875]], np.float32)
+    _, b = oracle.moe_ffn(x, idx, w, gate, up, down)
+    _, b2 = oracle.moe_ffn(x, idx, (-2 * w).astype(np.float32), gate, up, down)
+    np.testing.assert_allclose(b2 - 1e-6, 2 * (b - 1e-6), rtol=1e-12)
+    w0 = w.copy()
+    w0[:, 1] = 0
+    w1 = w.copy()
+    w1[:, 0] = 0
+    _, ba = oracle.moe_ffn(x, idx, w0, gate, up, down)
+    _, bb = oracle.moe_ffn(x, idx, w1, gate, up, down)
+    np.testing.assert_allclose(b - 1e-6, (ba - 1e-6) + (bb - 1e-6), rtol=1e-12)
+
+
+def test_moe_bound_routing_weight_term():
+    """The routing-weight error dw adds dw |o_i| per slot, o_i the slot's
+    expert output (read off with one-hot weights), not dw |sum_i o_i|."""
+    x, idx, gate, up, down = _moe_case(32)
+    w = np.array([[0.6, 0.4], [0.3, 0.7], [0.9, 0.1]], np.float32)
+    dw = 2e-6
+    _, b0 = oracle.moe_ffn(x, idx, w, gate, up, down)
+    _, b1 = oracle.moe_ffn(x, idx, w, gate, up, down, dw=dw)
+    e0 = np.zeros_like(w)
+    e0[:, 0] = 1
+    e1 = np.zeros_like(w)
+    e1[:, 1] = 1
+    o0, _ = oracle.moe_ffn(x, idx, e0, gate, up, down)
+    o1, _ = oracle.moe_ffn(x, idx, e1, gate, up, down)
+    np.testing.assert_allclose(b1 - b0, dw * (np.abs(o0) + np.abs(o1)), rtol=1e-9, atol=1e-20)
+
+
+def test_moe_bound_first_order_propagation_through_swiglu():
+    """One expert, one slot, w = 1, and a diagonal down matrix (each group
+    holds one nonzero and zeros, which the quantiser keeps exactly): output n
+    depends on h_n = silu(g_n) u_n alone, so its bound is 1e-6 + 1e-5 |wd h_n|
+    + |wd| dh_n + 1e-6, where dh_n, the first-order error of h_n, must equal
+    the largest change of silu(g) u when g and u move by their own linear
+    bounds (found here by perturbation, not by a derivative formula), plus
+    the 1e-6 |h_n| of h's own rounding."""
+    H = I = 64
+    gate = [oracle.quantize(_weights(34, 1, I, H), 8, 32)]
+    up = [oracle.quantize(_weights(34, 2, I, H), 8, 32)]
+    v = np.array([0.02 * (1 + n % 5) * (-1) ** n for n in range(H)], np.float32)
+    down = [oracle.quantize(np.diag(v).astype(np.float32), 8, 32)]
+    wd = oracle.dequantize(down[0]).astype(np.float64)
+    np.testing.assert_array_equal(wd - np.diag(np.diag(wd)), 0)
+    assert (np.abs(np.diag(wd) - v) <= 1e-3 * np.abs(v)).all()
+    x = synth.normal(34, 3, 2 * H).reshape(2, H)
+    y, b = oracle.moe_ffn(x, np.zeros((2, 1), np.int32), np.ones((2, 1), np.float32),
+                          gate, up, down)
+    g, u = oracle.linear_fused(x, gate[0]), oracle.linear_fused(x, up[0])
+    dg, du = oracle.linear_bound(x, gate[0]), oracle.linear_bound(x, up[0])
+    h = _silu(g) * u
+    moved = [np.abs(_silu(g + sg * dg) * (u + su * du) - h) for sg in (1, -1) for su in (1, -1)]
+    dh = np.max(moved, axis=0) + 1e-6 * np.abs(h)
+    d = np.abs(np.diag(wd))
+    np.testing.assert_allclose(y, np.diag(wd)[None, :] * h, rtol=1e-12)
+    expect = 1e-6 + 1e-5 * d[None, :] * np.abs(h) + d[None, :] * dh + 1e-6
+    np.testing.assert_allclose(b, expect, rtol=1e-4)
+
+
+def test_moe_bound_covers_an_fp32_layer():
+    """An fp32 evaluation of the same layer (fp32 GEMVs of the dequantised
+    weights, SwiGLU and the combine in fp32) stays within the MoE bound, and
+    the bound is not orders of magnitude above the error scale it models."""
+    E, H, I, k, M = 4, 1024, 512, 2, 3
+    gate, up, down = _experts(33, E, H, I, 8, 64)
+    x = synth.normal(33, 1, M * H).reshape(M, H)
+    idx = np.array([[0, 1], [2, 3], [1, 3]], np.int32)
+    w = np.array([[0.7, 0.3], [0.45, 0.55], [0.2, 0.8]], np.float32)
+    y, b = oracle.moe_ffn(x, idx, w, gate, up, down)
+    deq = lambda q: oracle.dequantize(q)
+    for m in range(M):
+        acc = np.zeros(H, np.float32)
+        for i in range(k):
+            e = idx[m, i]
+            g = (deq(gate[e]) @ x[m]).astype(np.float32)
+            u = (deq(up[e]) @ x[m]).astype(np.float32)
+            h = (g / (np.float32(1) + np.exp(-g)) * u).astype(np.float32)
+            acc = (acc + w[m, i] * (deq(down[e]) @ h)).astype(np.float32)
+        err = np.abs(acc.astype(np.float64) - y[m])
+        assert (err <= b[m]).all()
+        assert (b[m] < 1e-2 * (np.abs(y[m]).max() + 1e-3)).all()
+
+
 # --------------------------- router ------------------------------------
 
 
