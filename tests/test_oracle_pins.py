@@ -419,6 +419,42 @@ def test_router_expert_permutation_equivariance():
     np.testing.assert_array_equal(wp, w)
 
 
+def test_router_summation_order_worked_examples():
+    """The logit's fixed fp32 order, worked by hand: partial p is one fma
+    chain over h = p, p + 128, ...; level 1 sums (P0 + P1) + (P2 + P3) per four
+    partials; then t_l += t_{l+o} for o = 16, 8, 4, 2, 1; the bias is added
+    last.  Each row puts exact products where only that order gives the
+    stated logit (2^24 + 1 rounds to 2^24: a tie, to even)."""
+    H, big = 256, np.float32(2.0 ** 24)
+    wr = np.ones((2, H), np.float32)
+    a = np.float32(1 + 2.0 ** -12)
+    wr[1, 128] = a
+    x = np.zeros((5, H), np.float32)
+    # A: x0 w0 = -1, x128 w128 = (1 + 2^-12)^2 = 1 + 2^-11 + 2^-24.  One fma
+    # on -1 keeps 2^-11 + 2^-24 exactly; a rounded product first gives 2^-11.
+    x[0, 0], x[0, 128] = -1, a
+    # B: 2^24 (h = 0), -2^24 (h = 1), 1 (h = 128).  With 128 partials h = 128
+    # joins partial 0: 2^24 + 1 -> 2^24, then 2^24 - 2^24 = 0.  (127 partials
+    # would put h = 128 with h = 1: -2^24 + 1 exactly, logit 1.)
+    x[1, 0], x[1, 1], x[1, 128] = big, -big, 1
+    # C: P0..P3 = 2^24, 1, 1, -2^24.  (P0 + P1) + (P2 + P3) = 2^24 + (1 - 2^24)
+    # = 1; ((P0 + P1) + P2) + P3 = 0.
+    x[2, 0:4] = [big, 1, 1, -big]
+    # D: t0 = 2^24, t8 = -2^24, t16 = 1, t24 = 1 (partials 0, 32, 64, 96).  o =
+    # 16: t0 = 2^24 + 1 -> 2^24, t8 = -2^24 + 1; o = 8: t0 = 1.  A sequential
+    # or reversed (o = 1 first) tree gives 2.
+    x[3, 0], x[3, 32], x[3, 64], x[3, 96] = big, -big, 1, 1
+    # E: 2^24 - 2^24 = 0 in the tree; the bias (1) comes after it.  Added into
+    # partial 0 instead it would vanish in 2^24 + 1.
+    x[4, 0], x[4, 1] = big, -big
+    lg = oracle.router_logits(x, wr, None)
+    assert lg[0, 1] == np.float32(2.0 ** -11 + 2.0 ** -24)
+    assert lg[0, 0] == np.float32(2.0 ** -12)
+    assert lg[1:, 0].tolist() == [0.0, 1.0, 1.0, 0.0]
+    lb = oracle.router_logits(x, wr, np.array([1.0, 0.0], np.float32))
+    assert lb[1:, 0].tolist() == [1.0, 2.0, 2.0, 1.0]
+
+
 def test_router_partial_order_is_fixed():
     """The summation order is part of the definition: reversing the columns
     generally changes low bits (shows the test above is not vacuous) but
