@@ -95,7 +95,10 @@ def test_quantize_bit_exact(dev, bits, group, N, K, outl):
 @pytest.mark.parametrize("bits", [8, 4])
 def test_quantize_degenerate_groups(dev, bits):
     """Constant groups (zero, positive, negative), a group whose range is one
-    ulp (conversions saturate), and a mix with ordinary groups."""
+    ulp (conversions saturate), a mix with ordinary groups, and exact half
+    ties: codes and a zero point that round away from zero, and a maximum
+    that reaches 2^bits after rounding and is clamped (the worked examples
+    of the oracle's pins, padded with zeros inside their range)."""
     K, group = 256, 32
     rows = [np.zeros(K), np.full(K, 0.5), np.full(K, -3.0),
             np.where(np.arange(K) % 2 == 0, 100.0, np.nextafter(np.float32(100.0), np.float32(200))),
@@ -104,6 +107,12 @@ def test_quantize_degenerate_groups(dev, bits):
     mix[:32] = 7.25
     mix[64:96] = 0.0
     rows.append(mix)
+    ties8 = np.zeros(K)
+    ties8[:6] = [0, 255, 0.5, 2.5, 127.5, 254.5]
+    ties8[32:36] = [-2.5, 252.5, 0.5, -0.5]
+    ties4 = np.zeros(K)
+    ties4[:4] = [-0.5, 14.5, 2.5, 6.5]
+    rows += [ties8, ties4]
     w = np.stack(rows).astype(np.float32)
     g = q.qmm_quantize_groupwise(T(w, dev), bits, group)
     assert_quant_equal(g, oracle.quantize(w, bits, group))
