@@ -20,6 +20,9 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "qmm_oracle.c")
 _HDR = os.path.join(_HERE, "qmm_oracle.h")
 _LIB_PATH = os.path.join(_HERE, "libqmm_oracle.so")
+# A prebuilt variant of the same source (the tests' sanitizer build) may be
+# named in QMM_ORACLE_LIB; it is loaded as it is.
+_LIB_OVERRIDE = os.environ.get("QMM_ORACLE_LIB")
 _lock = threading.Lock()
 _lib = None
 
@@ -48,8 +51,7 @@ def _load():
     global _lib
     with _lock:
         if _lib is None:
-            build()
-            lib = ctypes.CDLL(_LIB_PATH)
+            lib = ctypes.CDLL(_LIB_OVERRIDE or build())
             i32, i64, vp, dbl = ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p, ctypes.c_double
             pqw = ctypes.POINTER(_QW)
             lib.orc_quantize.argtypes = [vp, i64, i64, ctypes.c_int, ctypes.c_int, vp, vp, vp]
