@@ -17,6 +17,7 @@ import synth
 from synth import recipes
 import group_quantized_moe_gb300 as q
 from group_quantized_moe_gb300 import build_lib
+from parity_checks import assert_bf16_rows, assert_within
 
 pytestmark = pytest.mark.gpu
 
@@ -47,27 +48,6 @@ def assert_quant_equal(gq, oq):
     np.testing.assert_array_equal(gq.scales.cpu().numpy().view(np.uint32),
                                   oq.scales.view(np.uint32))
     np.testing.assert_array_equal(gq.zps.cpu().numpy(), oq.zps)
-
-
-def assert_within(y, ref, bound, what=""):
-    y = np.asarray(y, dtype=np.float64)
-    err = np.abs(y - ref)
-    bad = err > bound
-    assert not bad.any(), (f"{what}: {bad.sum()} of {bad.size} outside tolerance; worst "
-                           f"err/bound {float((err / bound).max()):.3g}")
-
-
-def assert_bf16_rows(y, yref, what=""):
-    """bf16-path bar: per row, relative L2 error <= 1e-2 and the same arg-max,
-    except rows whose oracle top-2 gap is below 1e-2 * max|y_ref| (a near tie
-    that output rounding alone can flip)."""
-    y = np.asarray(y, dtype=np.float64)
-    rel = np.linalg.norm(y - yref, axis=1) / np.linalg.norm(yref, axis=1)
-    assert (rel <= 1e-2).all(), (what, float(rel.max()))
-    top2 = np.sort(yref, axis=1)[:, -2:]
-    near_tie = (top2[:, 1] - top2[:, 0]) < 1e-2 * np.abs(yref).max(axis=1)
-    same = np.argmax(y, axis=1) == np.argmax(yref, axis=1)
-    assert (same | near_tie).all(), (what, np.where(~(same | near_tie))[0])
 
 
 def _weights(N, K, seed=0, stream=2, outl=False, sigma=0.02):
