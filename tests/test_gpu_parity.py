@@ -475,6 +475,25 @@ def test_moe_small_m_token_patterns(dev):
     _moe_check(dev, x, T(x, dev), idx, w, ex, og, ou, od, what="mixed")
 
 
+def test_moe_decode_bad_expert_index_flagged(dev):
+    """Decode batches group their assignments inside the expert kernels: an
+    out-of-range index there is also skipped (its slot contributes nothing)
+    and flagged as QMM_DEV_BAD_EXPERT."""
+    E, H, I = 8, 2048, 2048
+    ex, og, ou, od = _small_experts(dev, E, H, I, 4, 64, seed=6)
+    M = 4
+    x = synth.normal(13, 1, M * H).reshape(M, H)
+    idx = np.array([[0, 5, 2], [8, 1, 2], [3, -1, 5], [7, 6, 1]], np.int32)
+    w = np.array([[0.5, 0.3, 0.2], [0.4, 0.4, 0.2], [0.6, 0.3, 0.1], [0.2, 0.3, 0.5]], np.float32)
+    q.qmm_device_status(clear=True)
+    y = q.moe_ffn_forward(T(x, dev), T(idx, dev), T(w, dev), ex).cpu().numpy()
+    assert q.qmm_device_status(clear=True) & q.QMM_DEV_BAD_EXPERT
+    ok = (idx >= 0) & (idx < E)
+    yref, bound = oracle.moe_ffn(x, np.where(ok, idx, 0).astype(np.int32),
+                                 np.where(ok, w, 0).astype(np.float32), og, ou, od)
+    assert_within(y, yref, bound, "decode bad index")
+
+
 # ----------------------------------------------- full-size MoE workloads
 
 def _full_moe(dev, r):
