@@ -143,6 +143,24 @@ def _require_cuda(*ts):
             raise ValueError("tensors must be contiguous")
 
 
+def _need(t, numel: int, dtypes, name: str) -> None:
+    """A buffer the kernels read or write must hold exactly the elements they
+    touch, of a matching type: the library sees only its address, so a short
+    buffer would be overrun and a buffer of another type misread.  (A raw
+    integer address is the caller's responsibility.)"""
+    if t is None or not isinstance(t, torch.Tensor):
+        return
+    if t.dtype not in dtypes:
+        raise TypeError(f"{name} has dtype {t.dtype}, expected "
+                        + " or ".join(str(d) for d in dtypes))
+    if t.numel() != numel:
+        raise ValueError(f"{name} has {t.numel()} elements, expected {numel}")
+
+
+def _nbytes(t) -> int:
+    return t.numel() * t.element_size()
+
+
 @dataclass
 class QWeight:
     """A quantised W[N, K] on the device: codes (int8 [N, K] or uint8
@@ -172,13 +190,30 @@ def alloc_qweight(N: int, K: int, bits: int, group: int, device="cuda") -> QWeig
                    torch.empty((N, G), dtype=torch.int32, device=device))
 
 
+def _check_qweight(w: QWeight, name: str = "w") -> None:
+    """codes int8 or uint8 [N K bits / 8], scales fp32 and zps int32 [N K / group]
+    (a descriptor the library rejects anyway is left to its own check)."""
+    if w.bits not in (4, 8) or w.group <= 0 or w.K % w.group:
+        return
+    G = w.K // w.group
+    _need(w.codes, w.N * w.K * w.bits // 8, (torch.int8, torch.uint8), f"{name}.codes")
+    _need(w.scales, w.N * G, (torch.float32,), f"{name}.scales")
+    _need(w.zps, w.N * G, (torch.int32,), f"{name}.zps")
+
+
 def qmm_quantize_groupwise(w: torch.Tensor, bits: int, group: int, out: QWeight | None = None,
                            stream=None) -> QWeight:
     """Group-wise quantisation of fp32 w[N, K] (see include/qmm.h)."""
-    _require_cuda(w)
     if w.dtype != torch.float32 or w.dim() != 2:
         raise TypeError("w must be a 2-D float32 tensor")
     N, K = w.shape
+    if out is not None:
+        if (out.N, out.K, out.bits, out.group) != (N, K, bits, group):
+            raise ValueError(f"out describes N={out.N} K={out.K} bits={out.bits} "
+                             f"group={out.group}, the call N={N} K={K} bits={bits} group={group}")
+        _check_qweight(out, "out")
+        _require_cuda(out.codes, out.scales, out.zps)
+    _require_cuda(w)
     if out is None:
         out = alloc_qweight(N, K, bits, group, device=w.device)
     _check(lib().qmm_quantize_groupwise(_ptr(w), N, K, bits, group, _ptr(out.codes),
@@ -189,9 +224,13 @@ def qmm_quantize_groupwise(w: torch.Tensor, bits: int, group: int, out: QWeight 
 def qmm_linear(x: torch.Tensor, w: QWeight, y: torch.Tensor | None = None,
                stream=None) -> torch.Tensor:
     """y[M, N] = x[M, K] . deq(W)^T (fp32 output)."""
-    _require_cuda(x)
+    if x.dim() == 0 or x.shape[-1] != w.K:
+        raise ValueError(f"x has shape {tuple(x.shape)}: its last dimension must be K = {w.K}")
     x2 = x.reshape(-1, w.K) if x.dim() != 2 else x
     M = x2.shape[0]
+    _check_qweight(w)
+    _need(y, M * w.N, (torch.float32,), "y")
+    _require_cuda(x, w.codes, w.scales, w.zps, y)
     if y is None:
         y = torch.empty((M, w.N), dtype=torch.float32, device=x.device)
     desc = w._c()
@@ -204,14 +243,30 @@ def moe_route_workspace_bytes(M: int, E: int) -> int:
     return int(lib().moe_route_workspace_bytes(M, E))
 
 
+def _check_route(x, w_router, bias, k, topk_idx, topk_w, expert_counts):
+    """x [M, H] fp32 or bf16, w_router fp32 [E, H], bias fp32 [E], outputs
+    topk_idx int32 and topk_w fp32 [M, k], expert_counts int32 [E]."""
+    if x.dim() != 2 or w_router.dim() != 2:
+        raise ValueError("x must be [M, H] and w_router [E, H]")
+    M, H = x.shape
+    E = w_router.shape[0]
+    _dtype_code(x)
+    _need(w_router, E * H, (torch.float32,), "w_router")
+    _need(bias, E, (torch.float32,), "bias")
+    _need(topk_idx, M * k, (torch.int32,), "topk_idx")
+    _need(topk_w, M * k, (torch.float32,), "topk_w")
+    _need(expert_counts, E, (torch.int32,), "expert_counts")
+    _require_cuda(x, w_router, bias, topk_idx, topk_w, expert_counts)
+    return M, H, E
+
+
 def moe_route_topk(x: torch.Tensor, w_router: torch.Tensor, bias: torch.Tensor | None, k: int,
                    topk_idx=None, topk_w=None, expert_counts=None, workspace=None,
                    with_counts: bool = True, stream=None):
     """Router: fixed-order fp32 logits, top-k (lower index wins ties) and
     renormalised softmax weights.  Returns (topk_idx, topk_w, expert_counts)."""
-    _require_cuda(x, w_router, bias)
-    M, H = x.shape
-    E = w_router.shape[0]
+    M, H, E = _check_route(x, w_router, bias, k, topk_idx, topk_w, expert_counts)
+    _require_cuda(workspace)
     dev = x.device
     if topk_idx is None:
         topk_idx = torch.empty((M, k), dtype=torch.int32, device=dev)
@@ -224,7 +279,7 @@ def moe_route_topk(x: torch.Tensor, w_router: torch.Tensor, bias: torch.Tensor |
         workspace = torch.empty((nbytes,), dtype=torch.uint8, device=dev)
     _check(lib().moe_route_topk(_ptr(x), _dtype_code(x), M, H, _ptr(w_router), _ptr(bias), E, k,
                                 _ptr(topk_idx), _ptr(topk_w), _ptr(expert_counts),
-                                _ptr(workspace), workspace.numel(), _stream(stream)))
+                                _ptr(workspace), _nbytes(workspace), _stream(stream)))
     return topk_idx, topk_w, expert_counts
 
 
@@ -273,6 +328,24 @@ def alloc_experts(E: int, H: int, I: int, bits: int, group: int, device="cuda") 
     return MoeExperts(E, H, I, bits, group, *g, *u, *d)
 
 
+def _check_experts(ex: MoeExperts) -> None:
+    """Stacked expert buffers: codes int8 or uint8 [E, rows, cols bits / 8],
+    scales fp32 and zps int32 [E, rows, cols / group], rows x cols = I x H for
+    gate and up, H x I for down (what the library's checks cannot see)."""
+    if ex.bits not in (4, 8) or ex.group <= 0 or ex.H % ex.group or ex.I % ex.group:
+        return
+    for which in ("gate", "up", "down"):
+        rows, cols = (ex.I, ex.H) if which != "down" else (ex.H, ex.I)
+        _need(getattr(ex, f"{which}_codes"), ex.E * rows * cols * ex.bits // 8,
+              (torch.int8, torch.uint8), f"{which}_codes")
+        _need(getattr(ex, f"{which}_scales"), ex.E * rows * (cols // ex.group), (torch.float32,),
+              f"{which}_scales")
+        _need(getattr(ex, f"{which}_zps"), ex.E * rows * (cols // ex.group), (torch.int32,),
+              f"{which}_zps")
+    _require_cuda(*(getattr(ex, f"{w}_{p}") for w in ("gate", "up", "down")
+                    for p in ("codes", "scales", "zps")))
+
+
 def moe_ffn_workspace_bytes(M: int, k: int, experts: MoeExperts) -> int:
     desc = experts._c()
     return int(lib().moe_ffn_workspace_bytes(M, k, ctypes.byref(desc)))
@@ -283,9 +356,16 @@ def moe_ffn_forward(x: torch.Tensor, topk_idx: torch.Tensor, topk_w: torch.Tenso
                     y_dtype: torch.dtype = torch.float32, workspace: torch.Tensor | None = None,
                     stream=None) -> torch.Tensor:
     """Routed SwiGLU MoE layer: y[m] = sum_i w[m,i] FFN_{idx[m,i]}(x[m])."""
-    _require_cuda(x, topk_idx, topk_w)
+    if x.dim() != 2 or x.shape[1] != experts.H or topk_idx.dim() != 2:
+        raise ValueError(f"x must be [M, H = {experts.H}] and topk_idx [M, k]")
     M, H = x.shape
     k = topk_idx.shape[1]
+    _dtype_code(x)
+    _need(topk_idx, M * k, (torch.int32,), "topk_idx")
+    _need(topk_w, M * k, (torch.float32,), "topk_w")
+    _need(y, M * H, (torch.float32, torch.bfloat16), "y")
+    _check_experts(experts)
+    _require_cuda(x, topk_idx, topk_w, y, workspace)
     if y is None:
         y = torch.empty((M, H), dtype=y_dtype, device=x.device)
     desc = experts._c()
@@ -294,7 +374,7 @@ def moe_ffn_forward(x: torch.Tensor, topk_idx: torch.Tensor, topk_w: torch.Tenso
         workspace = torch.empty((nbytes,), dtype=torch.uint8, device=x.device)
     _check(lib().moe_ffn_forward(_ptr(x), _dtype_code(x), M, _ptr(topk_idx), _ptr(topk_w), k,
                                  ctypes.byref(desc), _ptr(y), _dtype_code(y), _ptr(workspace),
-                                 workspace.numel(), _stream(stream)))
+                                 _nbytes(workspace), _stream(stream)))
     return y
 
 
@@ -305,9 +385,7 @@ def moe_route_topk_noalloc(x: torch.Tensor, w_router: torch.Tensor, bias: torch.
     memory: its logits scratch is a fixed 1 MiB array inside the library
     (M * E <= QMM_NOALLOC_MAX_LOGITS).  Outputs are allocated here only when
     the caller passes none.  Returns (topk_idx, topk_w, expert_counts)."""
-    _require_cuda(x, w_router, bias)
-    M, H = x.shape
-    E = w_router.shape[0]
+    M, H, E = _check_route(x, w_router, bias, k, topk_idx, topk_w, expert_counts)
     dev = x.device
     if topk_idx is None:
         topk_idx = torch.empty((M, k), dtype=torch.int32, device=dev)
