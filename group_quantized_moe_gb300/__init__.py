@@ -10,6 +10,7 @@ library's CUDA kernels; there is no other implementation behind these names.
 from __future__ import annotations
 
 import ctypes
+import operator
 import os
 import threading
 from dataclasses import dataclass
@@ -190,15 +191,29 @@ def alloc_qweight(N: int, K: int, bits: int, group: int, device="cuda") -> QWeig
                    torch.empty((N, G), dtype=torch.int32, device=device))
 
 
-def _check_qweight(w: QWeight, name: str = "w") -> None:
+def _checked(obj, tensors) -> bool:
+    """True if obj was validated with exactly these tensor objects (weights are
+    checked once, not on every call: each check costs host time per launch)."""
+    c = obj.__dict__.get("_checked_with")
+    return c is not None and len(c) == len(tensors) and all(map(operator.is_, c, tensors))
+
+
+def _mark_checked(obj, tensors) -> None:
+    obj.__dict__["_checked_with"] = tuple(tensors)
+
+
+def _qweight_tensors(w: QWeight):
+    return (w.codes, w.scales, w.zps)
+
+
+def _qweight_sizes(w: QWeight, name: str = "w") -> None:
     """codes int8 or uint8 [N K bits / 8], scales fp32 and zps int32 [N K / group]
     (a descriptor the library rejects anyway is left to its own check)."""
-    if w.bits not in (4, 8) or w.group <= 0 or w.K % w.group:
-        return
-    G = w.K // w.group
-    _need(w.codes, w.N * w.K * w.bits // 8, (torch.int8, torch.uint8), f"{name}.codes")
-    _need(w.scales, w.N * G, (torch.float32,), f"{name}.scales")
-    _need(w.zps, w.N * G, (torch.int32,), f"{name}.zps")
+    if w.bits in (4, 8) and w.group > 0 and w.K % w.group == 0:
+        G = w.K // w.group
+        _need(w.codes, w.N * w.K * w.bits // 8, (torch.int8, torch.uint8), f"{name}.codes")
+        _need(w.scales, w.N * G, (torch.float32,), f"{name}.scales")
+        _need(w.zps, w.N * G, (torch.int32,), f"{name}.zps")
 
 
 def qmm_quantize_groupwise(w: torch.Tensor, bits: int, group: int, out: QWeight | None = None,
@@ -211,9 +226,10 @@ def qmm_quantize_groupwise(w: torch.Tensor, bits: int, group: int, out: QWeight 
         if (out.N, out.K, out.bits, out.group) != (N, K, bits, group):
             raise ValueError(f"out describes N={out.N} K={out.K} bits={out.bits} "
                              f"group={out.group}, the call N={N} K={K} bits={bits} group={group}")
-        _check_qweight(out, "out")
-        _require_cuda(out.codes, out.scales, out.zps)
+        _qweight_sizes(out, "out")
     _require_cuda(w)
+    if out is not None:
+        _require_cuda(*_qweight_tensors(out))
     if out is None:
         out = alloc_qweight(N, K, bits, group, device=w.device)
     _check(lib().qmm_quantize_groupwise(_ptr(w), N, K, bits, group, _ptr(out.codes),
@@ -228,12 +244,28 @@ def qmm_linear(x: torch.Tensor, w: QWeight, y: torch.Tensor | None = None,
         raise ValueError(f"x has shape {tuple(x.shape)}: its last dimension must be K = {w.K}")
     x2 = x.reshape(-1, w.K) if x.dim() != 2 else x
     M = x2.shape[0]
-    _check_qweight(w)
+    # A weight is checked once; its descriptor is kept with the check, keyed by
+    # the tensor objects and their addresses (this runs on every call, and a
+    # decode-size launch is only a few microseconds of GPU time).
+    c = w.__dict__.get("_desc_for")
+    codes, scales, zps = w.codes, w.scales, w.zps
+    shape = (w.bits, w.group, w.N, w.K)
+    known = (c is not None and c[0] is codes and c[1] is scales and c[2] is zps
+             and c[3] == codes.data_ptr() and c[4] == scales.data_ptr() and c[5] == zps.data_ptr()
+             and c[7] == shape)
+    if not known:
+        _qweight_sizes(w)
     _need(y, M * w.N, (torch.float32,), "y")
-    _require_cuda(x, w.codes, w.scales, w.zps, y)
+    _require_cuda(x, y)
+    if known:
+        desc = c[6]
+    else:
+        _require_cuda(codes, scales, zps)
+        desc = w._c()
+        w.__dict__["_desc_for"] = (codes, scales, zps, codes.data_ptr(), scales.data_ptr(),
+                                   zps.data_ptr(), desc, shape)
     if y is None:
         y = torch.empty((M, w.N), dtype=torch.float32, device=x.device)
-    desc = w._c()
     _check(lib().qmm_linear(_ptr(x2), _dtype_code(x2), M, ctypes.byref(desc), _ptr(y),
                             _stream(stream)))
     return y
@@ -328,7 +360,12 @@ def alloc_experts(E: int, H: int, I: int, bits: int, group: int, device="cuda") 
     return MoeExperts(E, H, I, bits, group, *g, *u, *d)
 
 
-def _check_experts(ex: MoeExperts) -> None:
+def _experts_tensors(ex: MoeExperts):
+    return tuple(getattr(ex, f"{w}_{p}") for w in ("gate", "up", "down")
+                 for p in ("codes", "scales", "zps"))
+
+
+def _experts_sizes(ex: MoeExperts) -> None:
     """Stacked expert buffers: codes int8 or uint8 [E, rows, cols bits / 8],
     scales fp32 and zps int32 [E, rows, cols / group], rows x cols = I x H for
     gate and up, H x I for down (what the library's checks cannot see)."""
@@ -342,8 +379,6 @@ def _check_experts(ex: MoeExperts) -> None:
               f"{which}_scales")
         _need(getattr(ex, f"{which}_zps"), ex.E * rows * (cols // ex.group), (torch.int32,),
               f"{which}_zps")
-    _require_cuda(*(getattr(ex, f"{w}_{p}") for w in ("gate", "up", "down")
-                    for p in ("codes", "scales", "zps")))
 
 
 def moe_ffn_workspace_bytes(M: int, k: int, experts: MoeExperts) -> int:
@@ -364,8 +399,14 @@ def moe_ffn_forward(x: torch.Tensor, topk_idx: torch.Tensor, topk_w: torch.Tenso
     _need(topk_idx, M * k, (torch.int32,), "topk_idx")
     _need(topk_w, M * k, (torch.float32,), "topk_w")
     _need(y, M * H, (torch.float32, torch.bfloat16), "y")
-    _check_experts(experts)
+    ts = _experts_tensors(experts)
+    known = _checked(experts, ts)
+    if not known:
+        _experts_sizes(experts)
     _require_cuda(x, topk_idx, topk_w, y, workspace)
+    if not known:
+        _require_cuda(*ts)
+        _mark_checked(experts, ts)
     if y is None:
         y = torch.empty((M, H), dtype=y_dtype, device=x.device)
     desc = experts._c()

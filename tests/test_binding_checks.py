@@ -133,3 +133,36 @@ def test_moe_rejects(bad):
     with pytest.raises(exc) as e:
         q.moe_ffn_forward(x, idx, w, ex, y=y)
     assert DEVICE_MSG not in str(e.value)
+
+
+def test_linear_weight_check_is_cached_and_invalidated(monkeypatch):
+    """A weight is checked once and its descriptor kept; swapping one of its
+    tensors or changing its shape fields runs the check again (the library
+    and the device check are stubbed: this is the binding's own logic)."""
+    calls = []
+
+    class FakeLib:
+        def qmm_linear(self, *a):
+            calls.append(a)
+            return q.QMM_OK
+
+    fake = FakeLib()
+    monkeypatch.setattr(q, "lib", lambda: fake)
+    monkeypatch.setattr(q, "_require_cuda", lambda *ts: None)
+    monkeypatch.setattr(q, "_stream", lambda s: 0)
+    sizes = []
+    real_sizes = q._qweight_sizes
+    monkeypatch.setattr(q, "_qweight_sizes", lambda w, name="w": (sizes.append(1), real_sizes(w, name)))
+    w, x, y = _qw(), torch.zeros(2, 256), torch.zeros(2, 64)
+    for _ in range(3):
+        q.qmm_linear(x, w, y=y)
+    assert len(calls) == 3 and len(sizes) == 1
+    w.codes = torch.zeros(64, 255, dtype=torch.int8)  # another tensor, the wrong size
+    with pytest.raises(ValueError, match="codes"):
+        q.qmm_linear(x, w, y=y)
+    w.codes = torch.zeros(64, 256, dtype=torch.int8)
+    q.qmm_linear(x, w, y=y)
+    assert len(sizes) == 3
+    w.N = 65  # shape fields changed under the same tensors
+    with pytest.raises(ValueError):
+        q.qmm_linear(x, w, y=torch.zeros(2, 65))
