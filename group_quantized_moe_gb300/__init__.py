@@ -191,17 +191,6 @@ def alloc_qweight(N: int, K: int, bits: int, group: int, device="cuda") -> QWeig
                    torch.empty((N, G), dtype=torch.int32, device=device))
 
 
-def _checked(obj, tensors) -> bool:
-    """True if obj was validated with exactly these tensor objects (weights are
-    checked once, not on every call: each check costs host time per launch)."""
-    c = obj.__dict__.get("_checked_with")
-    return c is not None and len(c) == len(tensors) and all(map(operator.is_, c, tensors))
-
-
-def _mark_checked(obj, tensors) -> None:
-    obj.__dict__["_checked_with"] = tuple(tensors)
-
-
 def _qweight_tensors(w: QWeight):
     return (w.codes, w.scales, w.zps)
 
@@ -399,19 +388,27 @@ def moe_ffn_forward(x: torch.Tensor, topk_idx: torch.Tensor, topk_w: torch.Tenso
     _need(topk_idx, M * k, (torch.int32,), "topk_idx")
     _need(topk_w, M * k, (torch.float32,), "topk_w")
     _need(y, M * H, (torch.float32, torch.bfloat16), "y")
+    # The experts are checked once and their descriptor kept, keyed by the
+    # tensor objects, their addresses and the shape fields (building it costs
+    # more host time than the rest of the call).
     ts = _experts_tensors(experts)
-    known = _checked(experts, ts)
+    shape = (experts.E, experts.H, experts.I, experts.bits, experts.group)
+    c = experts.__dict__.get("_desc_for")
+    known = (c is not None and c[2] == shape and all(map(operator.is_, c[0], ts))
+             and c[1] == tuple(t.data_ptr() for t in ts))
     if not known:
         _experts_sizes(experts)
     _require_cuda(x, topk_idx, topk_w, y, workspace)
-    if not known:
+    if known:
+        desc = c[3]
+    else:
         _require_cuda(*ts)
-        _mark_checked(experts, ts)
+        desc = experts._c()
+        experts.__dict__["_desc_for"] = (ts, tuple(t.data_ptr() for t in ts), shape, desc)
     if y is None:
         y = torch.empty((M, H), dtype=y_dtype, device=x.device)
-    desc = experts._c()
-    nbytes = int(lib().moe_ffn_workspace_bytes(M, k, ctypes.byref(desc)))
-    if workspace is None:
+    if workspace is None:  # a caller's workspace is size-checked by the library
+        nbytes = int(lib().moe_ffn_workspace_bytes(M, k, ctypes.byref(desc)))
         workspace = torch.empty((nbytes,), dtype=torch.uint8, device=x.device)
     _check(lib().moe_ffn_forward(_ptr(x), _dtype_code(x), M, _ptr(topk_idx), _ptr(topk_w), k,
                                  ctypes.byref(desc), _ptr(y), _dtype_code(y), _ptr(workspace),

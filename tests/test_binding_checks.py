@@ -166,3 +166,34 @@ def test_linear_weight_check_is_cached_and_invalidated(monkeypatch):
     w.N = 65  # shape fields changed under the same tensors
     with pytest.raises(ValueError):
         q.qmm_linear(x, w, y=torch.zeros(2, 65))
+
+
+def test_moe_experts_descriptor_is_cached_and_invalidated(monkeypatch):
+    calls = []
+
+    class FakeLib:
+        def moe_ffn_workspace_bytes(self, *a):
+            return 1 << 16
+
+        def moe_ffn_forward(self, *a):
+            calls.append(a)
+            return q.QMM_OK
+
+    fake = FakeLib()
+    monkeypatch.setattr(q, "lib", lambda: fake)
+    monkeypatch.setattr(q, "_require_cuda", lambda *ts: None)
+    monkeypatch.setattr(q, "_stream", lambda s: 0)
+    built = []
+    real_c = q.MoeExperts._c
+    monkeypatch.setattr(q.MoeExperts, "_c", lambda self: (built.append(1), real_c(self))[1])
+    ex, M, k = _experts(), 5, 2
+    x, idx, w = torch.zeros(M, 256), torch.zeros(M, k, dtype=torch.int32), torch.zeros(M, k)
+    for _ in range(3):
+        q.moe_ffn_forward(x, idx, w, ex)
+    assert len(calls) == 3 and len(built) == 1
+    ex.down_codes = torch.zeros(4, 256, 32, dtype=torch.uint8)  # another tensor, the wrong size
+    with pytest.raises(ValueError, match="down_codes"):
+        q.moe_ffn_forward(x, idx, w, ex)
+    ex.down_codes = torch.zeros(4, 256, 64, dtype=torch.uint8)
+    q.moe_ffn_forward(x, idx, w, ex)
+    assert len(built) == 2
