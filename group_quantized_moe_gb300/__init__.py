@@ -295,9 +295,8 @@ def moe_route_topk(x: torch.Tensor, w_router: torch.Tensor, bias: torch.Tensor |
         topk_w = torch.empty((M, k), dtype=torch.float32, device=dev)
     if expert_counts is None and with_counts:
         expert_counts = torch.empty((E,), dtype=torch.int32, device=dev)
-    nbytes = moe_route_workspace_bytes(M, E)
-    if workspace is None:
-        workspace = torch.empty((nbytes,), dtype=torch.uint8, device=dev)
+    if workspace is None:  # a caller's workspace is size-checked by the library
+        workspace = torch.empty((moe_route_workspace_bytes(M, E),), dtype=torch.uint8, device=dev)
     _check(lib().moe_route_topk(_ptr(x), _dtype_code(x), M, H, _ptr(w_router), _ptr(bias), E, k,
                                 _ptr(topk_idx), _ptr(topk_w), _ptr(expert_counts),
                                 _ptr(workspace), _nbytes(workspace), _stream(stream)))
