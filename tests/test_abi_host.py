@@ -4,6 +4,8 @@ documented status codes before touching the device."""
 import ctypes
 import os
 import re
+import shutil
+import subprocess
 
 import pytest
 
@@ -217,3 +219,38 @@ def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
         q.lib()
     monkeypatch.undo()
     importlib.reload(q)
+
+
+def test_header_is_plain_c_and_a_c_program_links(tmp_path, L):
+    """The boundary is a C ABI: include/qmm.h compiles as C99 with warnings as
+    errors, and a C program linked against libqmm.so calls the entry points
+    that need no GPU (no launch happens: M = 0 is a no-op by contract)."""
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("gcc not found")
+    src = tmp_path / "use_qmm.c"
+    src.write_text(r'''
+#include <stdio.h>
+#include <string.h>
+#include "qmm.h"
+int main(void) {
+  qmm_weight w;
+  memset(&w, 0, sizeof w);
+  w.bits = 8; w.group = 64; w.N = 128; w.K = 256;
+  if (qmm_linear(NULL, QMM_F32, 0, &w, NULL, NULL) != QMM_OK) return 1;
+  if (qmm_linear(NULL, 7, 1, &w, NULL, NULL) != QMM_ERR_INVALID_ARG) return 2;
+  if (strlen(qmm_last_error()) == 0) return 3;
+  if (moe_route_workspace_bytes(8, 256) < (size_t)8 * 256 * 4) return 4;
+  printf("ok %llu\n", (unsigned long long)qmm_launch_count());
+  return 0;
+}
+''')
+    exe = tmp_path / "use_qmm"
+    libdir = os.path.dirname(build_lib.LIB)
+    r = subprocess.run([gcc, "-std=c99", "-Wall", "-Wextra", "-Werror", "-pedantic",
+                        "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe),
+                        "-L", libdir, "-lqmm", f"-Wl,-rpath,{libdir}"],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0 and r.stdout.startswith("ok"), (r.returncode, r.stdout, r.stderr)
