@@ -70,6 +70,8 @@ def _load():
             lib.orc_moe_ffn.argtypes = [vp, i64, i64, i64, vp, vp, i32, i32,
                                         pqw, pqw, pqw, dbl, vp, vp]
             lib.orc_moe_ffn.restype = ctypes.c_int
+            lib.orc_load_stats.argtypes = [vp, i64, i32, i32, i64, vp]
+            lib.orc_load_stats.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -202,3 +204,15 @@ def moe_ffn(x: np.ndarray, idx: np.ndarray, w: np.ndarray, gate, up, down,
     if rc != 0:
         raise ValueError(f"orc_moe_ffn failed ({rc})")
     return y, bound
+
+
+def load_stats(idx: np.ndarray, E: int, threshold: int):
+    """Routing load check: (stats int64 [4] = largest count, its expert, experts
+    touched, total selections; flag = largest count > threshold)."""
+    idx = _c(idx, np.int32)
+    M, k = idx.shape
+    stats = np.zeros(4, dtype=np.int64)
+    flag = _load().orc_load_stats(idx.ctypes.data, M, k, E, threshold, stats.ctypes.data)
+    if flag < 0:
+        raise MemoryError("orc_load_stats")
+    return stats, bool(flag)

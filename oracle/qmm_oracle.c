@@ -275,6 +275,34 @@ void orc_topk(const float *logits, int64_t M, int32_t E, int32_t k,
   free(p);
 }
 
+/* Routing load check [P1 section 3.5, last paragraph: when one expert is
+ * chosen more often than a threshold the engine warns, because grouped expert
+ * work then degenerates towards serial work].  Counts how often each expert
+ * appears among the M x k selected indices (indices outside [0, E) are not
+ * counted), then stats = {largest count, the lowest expert index with that
+ * count, number of experts chosen at least once, number of counted
+ * selections}.  Returns 1 when the largest count exceeds `threshold`. */
+int orc_load_stats(const int32_t *idx, int64_t M, int32_t k, int32_t E,
+                   int64_t threshold, int64_t *stats) {
+  int64_t *count = (int64_t *)calloc((size_t)E, sizeof(int64_t));
+  if (!count) return -1;
+  for (int64_t a = 0; a < M * k; ++a)
+    if (idx[a] >= 0 && idx[a] < E) count[idx[a]] += 1;
+  int64_t best = 0, total = 0, touched = 0;
+  int32_t arg = 0;
+  for (int32_t e = 0; e < E; ++e) {
+    if (count[e] > best) { best = count[e]; arg = e; }
+    if (count[e] > 0) touched += 1;
+    total += count[e];
+  }
+  free(count);
+  stats[0] = best;
+  stats[1] = arg;
+  stats[2] = touched;
+  stats[3] = total;
+  return best > threshold ? 1 : 0;
+}
+
 /* ------------------------------------------------------------------ */
 /* Routed SwiGLU MoE FFN [P1 section 3.5, P2 Trace 2]                  */
 /* ------------------------------------------------------------------ */

@@ -33,6 +33,8 @@ void orc_router_logits(const float *x, int64_t M, int64_t H, const float *wr,
                        const float *bias, int32_t E, float *logits);
 void orc_topk(const float *logits, int64_t M, int32_t E, int32_t k, int32_t *idx,
               float *w);
+int orc_load_stats(const int32_t *idx, int64_t M, int32_t k, int32_t E,
+                   int64_t threshold, int64_t *stats);
 /* gate/up/down: arrays of E descriptors (only experts named in idx are read).
  * dw: bound on |w_gpu - w_oracle| of the routing weights (0 when both sides
  * use the same weights).  y and bound are [M, H] doubles. */

@@ -529,3 +529,25 @@ def test_moe_linear_in_routing_weights_and_token_order():
     p = np.array([2, 0, 3, 1])
     y3, _ = oracle.moe_ffn(x[p], idx[p], w[p], gate, up, down)
     np.testing.assert_array_equal(y3, y[p])
+
+
+# ------------------------------------------------------- routing load check
+
+def test_load_stats_worked_examples():
+    """The load check of the engine's MoE layer (the warning when one expert
+    is chosen more often than a threshold), worked by hand."""
+    # 3 tokens, k = 2, E = 5: expert 2 three times, 1 twice, 3 once
+    idx = np.array([[1, 2], [2, 3], [2, 1]], np.int32)
+    st, flag = oracle.load_stats(idx, 5, 2)
+    assert st.tolist() == [3, 2, 3, 6] and flag
+    st, flag = oracle.load_stats(idx, 5, 3)
+    assert st.tolist() == [3, 2, 3, 6] and not flag
+    # equal largest counts: the lower expert index is reported
+    st, _ = oracle.load_stats(np.array([[4, 1], [1, 4]], np.int32), 5, 10)
+    assert st.tolist() == [2, 1, 2, 4]
+    # an index outside [0, E) is not counted
+    st, flag = oracle.load_stats(np.array([[0, 7], [-1, 0]], np.int32), 5, 1)
+    assert st.tolist() == [2, 0, 1, 2] and flag
+    # every token on one expert: the largest count is M
+    st, _ = oracle.load_stats(np.full((9, 1), 3, np.int32), 8, 100)
+    assert st.tolist() == [9, 3, 1, 9]
