@@ -308,6 +308,16 @@ def run_gemv_int4(dev, steps: int, warmup: int):
         step(i)
     torch.cuda.synchronize()
     n = max(steps, 4 * copies)
+    # Each step is ~14 MB of weights (a few microseconds of GPU time), about
+    # what the host needs to issue its two calls: a device-side wait long
+    # enough for the host to queue all n steps precedes the start event, so
+    # that the events time the GPU, not the Python issue rate.
+    t0 = time.perf_counter()
+    for i in range(4):
+        step(i)
+    torch.cuda.synchronize()
+    issue_s = (time.perf_counter() - t0) / 4
+    torch.cuda._sleep(int(min(4e9, 2.0e9 * 1.5 * issue_s * n + 2e6)))
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(s)
     for i in range(n):
@@ -318,6 +328,7 @@ def run_gemv_int4(dev, steps: int, warmup: int):
     return {"workload": "decode step: x[1,4096] -> INT4 g128 W[4096,4096] -> INT4 g128 W[2048,4096]",
             "ms_per_step": ms, "weight_bytes_per_step": b_pair,
             "weight_gbs": b_pair / (ms * 1e-3) / 1e9, "copies_rotated": copies,
+            "queued": f"{n} steps queued behind a device-side wait before the start event",
             "l2": f"{copies} copies of the pair rotated ({copies * b_pair / 1e6:.0f} MB vs 129 MB L2)"}
 
 
@@ -399,6 +410,9 @@ def run_moe(dev, r, steps: int, warmup: int):
     touched = int((counts > 0).sum())
     hot = int((counts >= 64).sum())
     ms = float(np.mean(times))
+    tc_subset = None
+    if r.x_bf16 and hot > 0:
+        tc_subset = run_tc_subset(dev, r, ex, x, idx, counts, steps, flush)
     per_expert = weight_bytes(r.I, r.H, r.bits, r.group) * 2 + weight_bytes(r.H, r.I, r.bits, r.group)
     bytes_ = touched * per_expert + r.E * r.H * 4
     flops = 2.0 * M * k * 3 * r.H * r.I + 2.0 * M * r.E * r.H
@@ -408,7 +422,134 @@ def run_moe(dev, r, steps: int, warmup: int):
             "flops": flops, "tflops": flops / (ms * 1e-3) / 1e12, "distinct_experts": touched,
             "experts_ge64_tokens": hot, "max_tokens_per_expert": int(counts.max()),
             "gpu_launches": int(launches), "setup_s": round(setup_s, 1),
-            "l2": "256 MB written between steps"}
+            "l2": "256 MB written between steps", "tc_subset": tc_subset}
+
+
+def run_tc_subset(dev, r, ex, x, idx, counts, steps: int, flush):
+    """The tensor-bound part of the prefill layer alone: the assignments of the
+    experts with 64 or more tokens, as a routing with one expert per row (each
+    of those experts gets exactly its tokens of the full layer).  The timed
+    call is the whole moe_ffn_forward on that routing, so besides the two
+    tensor-core GEMM launches it includes the grouping, the token gather, the
+    SwiGLU row conversion and the combine (a lower bound on the tensor-core
+    kernels' own rate)."""
+    import torch
+    import group_quantized_moe_gb300 as q
+    idx_np = idx.cpu().numpy()
+    hot = counts >= 64
+    toks, slots = np.nonzero(hot[idx_np])
+    m_sub = len(toks)
+    x_sub = x[torch.from_numpy(toks).to(dev)].contiguous()
+    i_sub = torch.from_numpy(idx_np[toks, slots].reshape(-1, 1).astype(np.int32)).to(dev)
+    w_sub = torch.ones((m_sub, 1), dtype=torch.float32, device=dev)
+    y_sub = torch.empty((m_sub, r.H), dtype=torch.bfloat16, device=dev)
+    ws = torch.empty((q.moe_ffn_workspace_bytes(m_sub, 1, ex),), dtype=torch.uint8, device=dev)
+    s = torch.cuda.current_stream()
+
+    def call():
+        q.moe_ffn_forward(x_sub, i_sub, w_sub, ex, y=y_sub, workspace=ws, stream=s)
+
+    for _ in range(3):
+        call()
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(steps):
+        flush.zero_()
+        torch.cuda._sleep(400000)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        call()
+        e1.record(s)
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1))
+    ms = float(np.mean(times))
+    flops = 2.0 * 3 * r.H * r.I * m_sub
+    peaks = load_peaks()
+    return {"experts": int(hot.sum()), "assignments": int(m_sub), "ms": ms,
+            "flops": flops, "tflops": flops / (ms * 1e-3) / 1e12,
+            "tc_frac": flops / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"],
+            "peak_tflops": peaks["bf16_tflops"], "peak": "bf16 burst (the call runs < 1 ms)",
+            "timed": "whole moe_ffn_forward call on the experts with >= 64 tokens"}
+
+
+def run_linear_batched(dev, steps: int):
+    """Batches of 16 and 64 bf16 rows through the 4096x4096 INT8 g64 trunk
+    matrix on the tensor-core linear path (qmm_linear_batched), rotated over
+    enough copies of the matrix to exceed L2, each step after a device-side
+    wait so that the events time the GPU."""
+    import torch
+    import group_quantized_moe_gb300 as q
+    r = recipes.CFG2_TRUNK
+    w = torch.from_numpy(recipes.linear_weight_rows(r)).to(dev)
+    wb = weight_bytes(r.N, r.K, r.bits, r.group)
+    copies = max(2, int(4 * 129e6 / wb) + 1)
+    mats = [q.qmm_quantize_groupwise(w, r.bits, r.group) for _ in range(copies)]
+    del w
+    s = torch.cuda.current_stream()
+    peaks = load_peaks()
+    out = {}
+    for M in (16, 64):
+        x = torch.from_numpy(synth.to_bf16(synth.normal(5, 1, M * r.K)).view(np.int16)) \
+            .to(dev).view(torch.bfloat16).reshape(M, r.K)
+        y = torch.empty((M, r.N), dtype=torch.float32, device=dev)
+        ws = torch.empty((q.qmm_linear_batched_workspace_bytes(M, mats[0]),), dtype=torch.uint8,
+                         device=dev)
+        for i in range(3):
+            q.qmm_linear_batched(x, mats[i % copies], y=y, workspace=ws, stream=s)
+        torch.cuda.synchronize()
+        n = max(steps, 4 * copies)
+        torch.cuda._sleep(int(min(4e9, 2.0e9 * 1.5 * 20e-6 * n + 2e6)))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        for i in range(n):
+            q.qmm_linear_batched(x, mats[i % copies], y=y, workspace=ws, stream=s)
+        e1.record(s)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / n
+        gbs = wb / (ms * 1e-3) / 1e9
+        out[f"M{M}"] = {"ms_per_call": ms, "weight_gbs": gbs, "hbm_frac": gbs / peaks["hbm_gbs"],
+                        "tflops": 2.0 * M * r.N * r.K / (ms * 1e-3) / 1e12}
+    out["workload"] = "bf16 x[M,4096] -> INT8 g64 W[4096,4096], tensor cores (qmm_linear_batched)"
+    out["l2"] = f"{copies} copies of the matrix rotated"
+    return out
+
+
+def run_cfg1(dev, steps: int):
+    """Latency of the single small linear layer (INT8 g64, K = 256, N = 128,
+    M = 1): one call after a device-side wait (the call's own device time),
+    and back-to-back calls (the rate at which the stream retires them)."""
+    import torch
+    import group_quantized_moe_gb300 as q
+    r = recipes.CFG1
+    w = torch.from_numpy(recipes.linear_weight_rows(r)).to(dev)
+    qw = q.qmm_quantize_groupwise(w, r.bits, r.group)
+    x = torch.from_numpy(recipes.linear_x(r)).to(dev)
+    y = torch.empty((1, r.N), dtype=torch.float32, device=dev)
+    s = torch.cuda.current_stream()
+    for _ in range(5):
+        q.qmm_linear(x, qw, y=y, stream=s)
+    torch.cuda.synchronize()
+    single = []
+    for _ in range(max(10, min(steps, 200))):
+        torch.cuda._sleep(20000)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        q.qmm_linear(x, qw, y=y, stream=s)
+        e1.record(s)
+        torch.cuda.synchronize()
+        single.append(e0.elapsed_time(e1) * 1e3)
+    n = max(100, steps)
+    torch.cuda._sleep(2000000)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(s)
+    for _ in range(n):
+        q.qmm_linear(x, qw, y=y, stream=s)
+    e1.record(s)
+    torch.cuda.synchronize()
+    return {"workload": "single INT8 g64 linear: x[1,256] -> W[128,256]",
+            "latency_us": float(np.median(single)), "latency_us_min": float(np.min(single)),
+            "back_to_back_us": e0.elapsed_time(e1) * 1e3 / n,
+            "weight_bytes": weight_bytes(r.N, r.K, r.bits, r.group)}
 
 
 # ------------------------------------------------------------ oracle (CPU)
@@ -471,6 +612,58 @@ def oracle_gemv_parallel(seconds: float, workers: int, setup_s: float = 4.0):
     nbytes = sum(b for b, _, _ in res)
     span = max(e for _, _, e in res) - min(s for _, s, _ in res)
     return nbytes / span / 1e9, nbytes, span
+
+
+def _oracle_moe_worker(task):
+    """One process of the MoE baseline: quantise the experts its tokens pick
+    (set-up, untimed), wait for the common start, then run the oracle's router
+    (fixed-order logits, top-k) and routed SwiGLU layer token by token, over
+    its tokens in turn, for `seconds` (at least one pass).  Returns (tokens,
+    start, end) on the wall clock."""
+    name, toks, start_at, seconds = task
+    import oracle
+    r = recipes.MOES[name]
+    x, _ = recipes.moe_x(r)
+    wr, bias = recipes.moe_router(r)
+    xs = x[toks]
+    idx, _ = oracle.topk(oracle.router_logits(xs, wr, bias), r.k)
+    og, ou, od = [None] * r.E, [None] * r.E, [None] * r.E
+    for e in sorted(set(int(v) for v in idx.reshape(-1))):
+        og[e] = oracle.quantize(recipes.moe_expert_rows(r, "gate", e), r.bits, r.group)
+        ou[e] = oracle.quantize(recipes.moe_expert_rows(r, "up", e), r.bits, r.group)
+        od[e] = oracle.quantize(recipes.moe_expert_rows(r, "down", e), r.bits, r.group)
+    while time.time() < start_at:
+        time.sleep(0.005)
+    t0 = time.time()
+    done, i = 0, 0
+    while True:
+        j = i % len(toks)
+        ii, ww = oracle.topk(oracle.router_logits(xs[j:j + 1], wr, bias), r.k)
+        oracle.moe_ffn(xs[j:j + 1], ii, ww, og, ou, od, with_bound=False)
+        done += 1
+        i += 1
+        if i >= len(toks) and time.time() - t0 >= seconds:
+            break
+    return done, t0, time.time()
+
+
+def oracle_moe_parallel(r, seconds: float, workers: int, setup_s: float = 12.0) -> dict:
+    """The oracle's MoE layer (router + routed experts, token by token) in
+    `workers` spawned processes at once, one token of the workload each (the
+    first `workers` tokens); tokens/s = tokens done / wall-clock span."""
+    import multiprocessing as mp
+    workers = max(1, min(workers, r.M))
+    start_at = time.time() + setup_s
+    tasks = [(r.name, [w], start_at, seconds) for w in range(workers)]
+    ctx = mp.get_context("spawn")
+    with ctx.Pool(workers) as pool:
+        res = pool.map_async(_oracle_moe_worker, tasks).get(timeout=setup_s + 20 * seconds + 300)
+    n = sum(d for d, _, _ in res)
+    span = max(e for _, _, e in res) - min(t for _, t, _ in res)
+    return {"value": n / span, "unit": "tokens/s", "cores": workers, "kind": "oracle",
+            "sample": f"{workers} processes, one single-threaded oracle each on one token of the "
+                      f"workload (router + {r.k} routed experts, fp64 accumulation), "
+                      f"{n} tokens in {span:.2f} s of wall clock from a common start"}
 
 
 _REF: dict = {}
@@ -678,6 +871,16 @@ def main():
         except Exception as e:  # keep the headline line even if an extra fails
             line["gemv_int4"] = {"error": f"{type(e).__name__}: {e}"}
         release()
+    if args.only is None:
+        try:
+            line["cfg1_linear"] = run_cfg1(dev, args.steps)
+        except Exception as e:  # keep the headline line even if an extra fails
+            line["cfg1_linear"] = {"error": f"{type(e).__name__}: {e}"}
+        try:
+            line["linear_batched"] = run_linear_batched(dev, args.steps)
+        except Exception as e:  # keep the headline line even if an extra fails
+            line["linear_batched"] = {"error": f"{type(e).__name__}: {e}"}
+        release()
     if not args.no_moe and args.only is None:
         extras = {}
         for key, r in (("moe_decode", recipes.CFG4), ("moe_prefill", recipes.CFG5)):
@@ -695,6 +898,13 @@ def main():
         line.update(extras)
     if rank == 0 and not args.no_cpu:
         line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
+        workers = max(1, host_cores() - 1)
+        for key, r in (("moe_decode", recipes.CFG4), ("moe_prefill", recipes.CFG5)):
+            if isinstance(line.get(key), dict) and "error" not in line[key]:
+                try:
+                    line[key]["cpu_baseline"] = oracle_moe_parallel(r, 2.0, workers)
+                except Exception as e:  # the GPU figures stand without it
+                    line[key]["cpu_baseline"] = {"error": f"{type(e).__name__}: {e}"}
     if rank == 0:
         print(json.dumps(line))
     if world > 1:

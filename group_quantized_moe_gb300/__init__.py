@@ -31,10 +31,13 @@ QMM_F32 = 0
 QMM_BF16 = 1
 QMM_DEV_WAIT_TIMEOUT = 1
 QMM_DEV_BAD_EXPERT = 2
+QMM_DEV_EXPERT_OVERLOAD = 4
 
 EXPORTED = ("qmm_quantize_groupwise", "qmm_linear", "moe_route_workspace_bytes", "moe_route_topk",
             "moe_ffn_workspace_bytes", "moe_ffn_forward", "qmm_last_error", "qmm_launch_count",
-            "qmm_device_status", "moe_route_topk_noalloc")
+            "qmm_device_status", "moe_route_topk_noalloc", "moe_route_load_stats",
+            "qmm_diag_wait_timeout", "qmm_linear_batched_workspace_bytes",
+            "qmm_linear_batched")
 QMM_NOALLOC_MAX_LOGITS = 262144
 
 
@@ -82,7 +85,7 @@ def lib() -> ctypes.CDLL:
                                      ctypes.c_void_p, ctypes.c_size_t)
             L.qmm_quantize_groupwise.argtypes = [vp, i64, i64, i32, i32, vp, vp, vp, vp]
             L.qmm_quantize_groupwise.restype = ctypes.c_int
-            L.qmm_linear.argtypes = [vp, i32, i64, ctypes.POINTER(_Weight), vp, vp]
+            L.qmm_linear.argtypes = [vp, i32, i64, ctypes.POINTER(_Weight), vp, i32, vp]
             L.qmm_linear.restype = ctypes.c_int
             L.moe_route_workspace_bytes.argtypes = [i64, i32]
             L.moe_route_workspace_bytes.restype = sz
@@ -103,6 +106,15 @@ def lib() -> ctypes.CDLL:
             L.moe_route_topk_noalloc.argtypes = [vp, i32, i64, i64, vp, vp, i32, i32, vp, vp, vp,
                                                  vp]
             L.moe_route_topk_noalloc.restype = ctypes.c_int
+            L.moe_route_load_stats.argtypes = [vp, i32, i64, vp, vp]
+            L.moe_route_load_stats.restype = ctypes.c_int
+            L.qmm_diag_wait_timeout.argtypes = [u64, vp]
+            L.qmm_diag_wait_timeout.restype = ctypes.c_int
+            L.qmm_linear_batched_workspace_bytes.argtypes = [i64, ctypes.POINTER(_Weight)]
+            L.qmm_linear_batched_workspace_bytes.restype = sz
+            L.qmm_linear_batched.argtypes = [vp, i32, i64, ctypes.POINTER(_Weight), vp, i32, vp,
+                                             sz, vp]
+            L.qmm_linear_batched.restype = ctypes.c_int
             _lib = L
     return _lib
 
@@ -227,8 +239,9 @@ def qmm_quantize_groupwise(w: torch.Tensor, bits: int, group: int, out: QWeight 
 
 
 def qmm_linear(x: torch.Tensor, w: QWeight, y: torch.Tensor | None = None,
-               stream=None) -> torch.Tensor:
-    """y[M, N] = x[M, K] . deq(W)^T (fp32 output)."""
+               y_dtype: torch.dtype = torch.float32, stream=None) -> torch.Tensor:
+    """y[M, N] = x[M, K] . deq(W)^T (fp32 or bf16 output: the dtype of y when
+    given, else y_dtype)."""
     if x.dim() == 0 or x.shape[-1] != w.K:
         raise ValueError(f"x has shape {tuple(x.shape)}: its last dimension must be K = {w.K}")
     x2 = x.reshape(-1, w.K) if x.dim() != 2 else x
@@ -244,7 +257,7 @@ def qmm_linear(x: torch.Tensor, w: QWeight, y: torch.Tensor | None = None,
              and c[7] == shape)
     if not known:
         _qweight_sizes(w)
-    _need(y, M * w.N, (torch.float32,), "y")
+    _need(y, M * w.N, (torch.float32, torch.bfloat16), "y")
     _require_cuda(x, y)
     if known:
         desc = c[6]
@@ -254,9 +267,39 @@ def qmm_linear(x: torch.Tensor, w: QWeight, y: torch.Tensor | None = None,
         w.__dict__["_desc_for"] = (codes, scales, zps, codes.data_ptr(), scales.data_ptr(),
                                    zps.data_ptr(), desc, shape)
     if y is None:
-        y = torch.empty((M, w.N), dtype=torch.float32, device=x.device)
+        y = torch.empty((M, w.N), dtype=y_dtype, device=x.device)
     _check(lib().qmm_linear(_ptr(x2), _dtype_code(x2), M, ctypes.byref(desc), _ptr(y),
-                            _stream(stream)))
+                            _dtype_code(y), _stream(stream)))
+    return y
+
+
+def qmm_linear_batched_workspace_bytes(M: int, w: QWeight) -> int:
+    desc = w._c()
+    return int(lib().qmm_linear_batched_workspace_bytes(M, ctypes.byref(desc)))
+
+
+def qmm_linear_batched(x: torch.Tensor, w: QWeight, y: torch.Tensor | None = None,
+                       y_dtype: torch.dtype = torch.float32, workspace: torch.Tensor | None = None,
+                       stream=None) -> torch.Tensor:
+    """qmm_linear for batches of rows: bf16 rows (M >= 9, INT8, group >= 64)
+    run on the tensor cores (see include/qmm.h); everything else is
+    qmm_linear."""
+    if x.dim() == 0 or x.shape[-1] != w.K:
+        raise ValueError(f"x has shape {tuple(x.shape)}: its last dimension must be K = {w.K}")
+    x2 = x.reshape(-1, w.K) if x.dim() != 2 else x
+    M = x2.shape[0]
+    _qweight_sizes(w)
+    _need(y, M * w.N, (torch.float32, torch.bfloat16), "y")
+    _require_cuda(x, y, workspace, *_qweight_tensors(w))
+    desc = w._c()
+    if y is None:
+        y = torch.empty((M, w.N), dtype=y_dtype, device=x.device)
+    if workspace is None:  # a caller's workspace is size-checked by the library
+        nbytes = int(lib().qmm_linear_batched_workspace_bytes(M, ctypes.byref(desc)))
+        workspace = torch.empty((nbytes,), dtype=torch.uint8, device=x.device)
+    _check(lib().qmm_linear_batched(_ptr(x2), _dtype_code(x2), M, ctypes.byref(desc), _ptr(y),
+                                    _dtype_code(y), _ptr(workspace), _nbytes(workspace),
+                                    _stream(stream)))
     return y
 
 
@@ -434,6 +477,29 @@ def moe_route_topk_noalloc(x: torch.Tensor, w_router: torch.Tensor, bias: torch.
                                         E, k, _ptr(topk_idx), _ptr(topk_w), _ptr(expert_counts),
                                         _stream(stream)))
     return topk_idx, topk_w, expert_counts
+
+
+def moe_route_load_stats(expert_counts: torch.Tensor, threshold: int, stats=None,
+                         stream=None) -> torch.Tensor:
+    """Load statistics of a routing histogram (int32 [E]): int64 [4] = largest
+    count, its expert, experts touched, total; sets QMM_DEV_EXPERT_OVERLOAD in
+    the device status word when the largest count exceeds `threshold`."""
+    if expert_counts.dim() != 1:
+        raise ValueError("expert_counts must be 1-D [E]")
+    E = expert_counts.shape[0]
+    _need(expert_counts, E, (torch.int32,), "expert_counts")
+    _need(stats, 4, (torch.int64,), "stats")
+    _require_cuda(expert_counts, stats)
+    if stats is None:
+        stats = torch.empty((4,), dtype=torch.int64, device=expert_counts.device)
+    _check(lib().moe_route_load_stats(_ptr(expert_counts), E, int(threshold), _ptr(stats),
+                                      _stream(stream)))
+    return stats
+
+
+def qmm_diag_wait_timeout(limit_ns: int, stream=None) -> None:
+    """Runs the bounded-wait diagnostic kernel (see include/qmm.h)."""
+    _check(lib().qmm_diag_wait_timeout(int(limit_ns), _stream(stream)))
 
 
 def qmm_last_error() -> str:

@@ -22,7 +22,8 @@ struct GemvArgs {
   int K;
   int group_shift;
   TileLayout L;
-  float *y;
+  void *y;          // [M, N] fp32, or bf16 when y_bf16
+  bool y_bf16;
   uint32_t *status;
 };
 
@@ -95,7 +96,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1) gemv_kernel(GemvArgs a) {
       if (lane == 0) {
 #pragma unroll
         for (int r = 0; r < RT; ++r)
-          if (r < rows) a.y[n0 + r] = yr[r];
+          if (r < rows) store_y(a.y, n0 + r, yr[r], a.y_bf16);
       }
     } else
     for (int64_t m0 = 0; m0 < a.M; m0 += MT) {
@@ -117,7 +118,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1) gemv_kernel(GemvArgs a) {
         for (int r = 0; r < RT; ++r)
 #pragma unroll
           for (int m = 0; m < MT; ++m)
-            if (r < rows && m < mt) a.y[(m0 + m) * a.N + n0 + r] = yacc[r][m];
+            if (r < rows && m < mt) store_y(a.y, (m0 + m) * a.N + n0 + r, yacc[r][m], a.y_bf16);
       }
     }
     __syncwarp();
@@ -175,7 +176,7 @@ int gemv_rows_per_tile(int64_t rowbytes, int64_t G, int copies) {
   return rows_per_tile(static_cast<int>(rowbytes), static_cast<int>(G), G % 4 == 0, copies);
 }
 
-cudaError_t launch_gemv(const void *x, bool x_bf16, int64_t M, const QMat &w, float *y,
+cudaError_t launch_gemv(const void *x, bool x_bf16, int64_t M, const QMat &w, void *y, bool y_bf16,
                         cudaStream_t s) {
   GemvArgs a;
   a.x = x;
@@ -189,6 +190,7 @@ cudaError_t launch_gemv(const void *x, bool x_bf16, int64_t M, const QMat &w, fl
   a.L.rowbytes = static_cast<int>(w.cols * w.bits / 8);
   a.L.G = static_cast<int>(w.cols / w.group);
   a.y = y;
+  a.y_bf16 = y_bf16;
   a.status = device_status();
   const bool gsm = a.L.G % 4 == 0;
   int rt = rows_per_tile(a.L.rowbytes, a.L.G, gsm, 1);

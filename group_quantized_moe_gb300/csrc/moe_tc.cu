@@ -64,7 +64,8 @@ constexpr int kDequantWarps = 4 * kDequantGroups;  // warps 0-11
 constexpr int kWarpCodes = kDequantWarps;          // TMA producer of weight codes
 constexpr int kWarpRows = kDequantWarps + 1;       // TMA producer of token rows
 constexpr int kWarpMma = kDequantWarps + 2;        // first of the four MMA issuers
-constexpr int kThreads = (kDequantWarps + 6) * 32;
+constexpr int kWarpRexp = kDequantWarps + 6;       // row exponents, one item ahead
+constexpr int kThreads = (kDequantWarps + 7) * 32;
 constexpr int kLightN = 64;  // items with at most this many (padded) tokens use 4 issuers
 constexpr int kACols = kBK / 2;         // TMEM columns of one A tile stage
 constexpr int kBTile = kBN * kBK * 2;   // 16 KB fp16
@@ -107,10 +108,11 @@ struct Smem {
   static constexpr int c_off = b_off + kB * kBTile;
   static constexpr int bar_off = c_off + kC * NT * kCTile;
   // barriers: c_full[kC], c_free[kC], a_full[kA], ab_free[kA], b_full[kB],
-  // acc_full, acc_free
-  static constexpr int nbar = 2 * kC + 2 * kA + kB + 2;
+  // acc_full, acc_free, rexp_full[2], rexp_free[2]
+  static constexpr int nbar = 2 * kC + 2 * kA + kB + 2 + 4;
   static constexpr int misc_off = bar_off + nbar * 8;
-  static constexpr int meta_off = misc_off + 16;  // offsets[E+1], tile_start[E+1]
+  static constexpr int rexp_off = misc_off + 16;  // int32 [2 slots][NT][128 rows]
+  static constexpr int meta_off = rexp_off + 2 * NT * kBM * 4;  // offsets[E+1], tile_start[E+1]
   static constexpr int bytes_for(int E) { return meta_off + 8 * (E + 1) + 1024; }
 };
 
@@ -125,9 +127,17 @@ struct TcArgs {
   int64_t gstride[2];    // elements between experts
   const int32_t *offsets;      // [E + 1] token-list offsets (sorted order)
   const int32_t *tile_start;   // [E + 1] prefix of 128-token tiles per expert
-  void *out;             // gate/up: fp16 h [MK, I]; down: fp32 out [MK, H]
+  const float *colscale;       // [MK] power of two that undoes the scaling of
+                               // each fp16 token row (gate/up: x, down: h)
+  float *out;            // gate/up: fp32 h [MK, I]; down: fp32 out [MK, H]
   int64_t out_ld;        // elements per output row
   uint32_t *status;
+  // Linear layer (one matrix, M token rows, rows = N may be ragged): lin_M > 0
+  // replaces offsets / tile_start ({0, M} and one expert); the K range is
+  // split nsplit ways, split s writing its partial sums at out + s out_split.
+  int lin_M;
+  int nsplit;
+  int64_t out_split;
 };
 
 // ------------------------------------------------------------ PTX wrappers
@@ -289,16 +299,19 @@ __device__ __forceinline__ bool wait_ok(uint32_t bar, uint32_t parity, uint32_t 
 
 // Work item -> (expert, token tile, feature tile).
 struct Item {
-  int e, t0, ntok, f;
+  int e, t0, ntok, f, ks;
 };
 
 // s_off / s_ts: the token-list offsets and tile prefix, staged in shared
-// memory.  Items are ordered (token tile, feature tile), feature fastest.
+// memory.  Items are ordered (token tile, feature tile, K split), the split
+// fastest.
 __device__ __forceinline__ Item decode_item(const int32_t *s_off, const int32_t *s_ts, int E,
-                                            int64_t item, int ftiles) {
+                                            int64_t item, int ftiles, int nsplit) {
   Item it;
-  const int tau = static_cast<int>(item / ftiles);
-  it.f = static_cast<int>(item % ftiles);
+  const int64_t tf = item / nsplit;
+  it.ks = static_cast<int>(item % nsplit);
+  const int tau = static_cast<int>(tf / ftiles);
+  it.f = static_cast<int>(tf % ftiles);
   // last expert whose first tile index is <= tau
   int lo = 0, hi = E;  // s_ts[lo] <= tau < s_ts[hi]
   while (hi - lo > 1) {
@@ -315,9 +328,10 @@ __device__ __forceinline__ Item decode_item(const int32_t *s_off, const int32_t 
   return it;
 }
 
-// SwiGLU's silu for an fp16 result: the fast exponential and division (a few
-// ulp of fp32) are far inside fp16 rounding; the exponent is clamped so that
-// the divisor stays finite (silu(g) for g < -80 is below 1e-33).
+// SwiGLU's silu for a result that is rounded to fp16 before the down GEMM:
+// the fast exponential and division (a few ulp of fp32) are far inside fp16
+// rounding; the exponent is clamped so that the divisor stays finite (silu(g)
+// for g < -80 is below 1e-33 |g|).
 __device__ __forceinline__ float silu_f(float g) {
   return __fdividef(g, 1.0f + __expf(fminf(-g, 80.0f)));
 }
@@ -343,7 +357,40 @@ __device__ __forceinline__ void dequant16(uint4 v, __half2 mz2, __half2 s2, uint
   o1 = make_uint4(r[4], r[5], r[6], r[7]);
 }
 
-// NT = 2: gate/up with SwiGLU epilogue (fp16 h); NT = 1: down (fp32 out).
+// The same for a group outside the fast form's exact range: each weight
+// (q - zp) s' formed as the oracle forms it in fp32 (the difference in 64
+// bits, one conversion, one product) and rounded to fp16 once.
+__device__ __forceinline__ void dequant16_exact(uint4 v, int32_t zp, float s, uint4 &o0,
+                                                uint4 &o1) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  uint32_t r[8];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t u = w[i] ^ 0x80808080u;
+    float f[4];
+#pragma unroll
+    for (int b = 0; b < 4; ++b)
+      f[b] = __ll2float_rn(static_cast<int64_t>((u >> (8 * b)) & 0xFFu) - zp) * s;
+    __half2 d01 = __floats2half2_rn(f[0], f[1]);
+    __half2 d23 = __floats2half2_rn(f[2], f[3]);
+    r[2 * i] = *reinterpret_cast<uint32_t *>(&d01);
+    r[2 * i + 1] = *reinterpret_cast<uint32_t *>(&d23);
+  }
+  o0 = make_uint4(r[0], r[1], r[2], r[3]);
+  o1 = make_uint4(r[4], r[5], r[6], r[7]);
+}
+
+// 2^s and 2^-s for the power of two s that puts a positive magnitude m into
+// [2^14, 2^15) (s clamped to [-126, 126], so that both are normal fp32; m = 0
+// gives the largest s).  Read from m's exponent bits.
+__device__ __forceinline__ void pow2_to_fp16_range(float m, float &up, float &down) {
+  const int e = ((__float_as_int(m) >> 23) & 0xFF) - 127;
+  const int sh = max(-126, min(126, 14 - e));
+  up = __int_as_float((127 + sh) << 23);
+  down = __int_as_float((127 - sh) << 23);
+}
+
+// NT = 2: gate/up with SwiGLU epilogue (fp32 h); NT = 1: down (fp32 out).
 template <int NT>
 __global__ void __launch_bounds__(kThreads, 1)
     moe_tc_kernel(const __grid_constant__ CUtensorMap tm_codes0,
@@ -370,13 +417,26 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto b_full = [&](int i) { return bar0 + 8 * (2 * kC + 2 * kA + i); };
   const uint32_t acc_full = bar0 + 8 * (2 * kC + 2 * kA + kB);
   const uint32_t acc_free = acc_full + 8;
+  // row-exponent slots: filled by the exponent warp one item ahead
+  auto rexp_full = [&](int i) { return acc_free + 8 + 8 * i; };
+  auto rexp_free = [&](int i) { return acc_free + 24 + 8 * i; };
+  int32_t *s_rexp = reinterpret_cast<int32_t *>(gbase + S::rexp_off);
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + S::misc_off);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(gbase + S::misc_off + 4);
   int32_t *s_off = reinterpret_cast<int32_t *>(gbase + S::meta_off);
   int32_t *s_ts = s_off + a.E + 1;
-  for (int i = threadIdx.x; i <= a.E; i += blockDim.x) {
-    s_off[i] = a.offsets[i];
-    s_ts[i] = a.tile_start[i];
+  if (a.lin_M > 0) {
+    if (threadIdx.x == 0) {  // one "expert" holding the M rows of x
+      s_off[0] = 0;
+      s_off[1] = a.lin_M;
+      s_ts[0] = 0;
+      s_ts[1] = (a.lin_M + kBN - 1) / kBN;
+    }
+  } else {
+    for (int i = threadIdx.x; i <= a.E; i += blockDim.x) {
+      s_off[i] = a.offsets[i];
+      s_ts[i] = a.tile_start[i];
+    }
   }
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -392,6 +452,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < kB; ++i) mbar_init(b_full(i), 1);
     mbar_init(acc_full, 4);
     mbar_init(acc_free, kDequantWarps);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(rexp_full(i), 32);             // every lane of the exponent warp
+      mbar_init(rexp_free(i), kDequantWarps);  // one arrival per dequant warp
+    }
     *abort_flag = 0;
     mbar_fence_init();
   }
@@ -405,9 +469,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     return static_cast<uint32_t>(2 * kBN + (slot * NT + t) * kACols);
   };
 
-  const int ftiles = static_cast<int>(a.rows / kBM);
-  const int kstages = static_cast<int>(a.K / kBK);
-  const int64_t nitems = static_cast<int64_t>(s_ts[a.E]) * ftiles;
+  const int ftiles = static_cast<int>((a.rows + kBM - 1) / kBM);  // last tile may be ragged
+  const int kps = static_cast<int>(a.K / kBK) / a.nsplit;          // stages per item
+  const int64_t nitems = static_cast<int64_t>(s_ts[a.E]) * ftiles * a.nsplit;
 
   if (warp == kWarpCodes) {
     // ------------------------------------------- TMA producer: weight codes
@@ -415,8 +479,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t pol = policy_evict_first();
       int64_t gs = 0;  // global stage counter
       for (int64_t item = blockIdx.x; item < nitems && !*abort_flag; item += gridDim.x) {
-        const Item it = decode_item(s_off, s_ts, a.E, item, ftiles);
-        for (int kb = 0; kb < kstages; ++kb, ++gs) {
+        const Item it = decode_item(s_off, s_ts, a.E, item, ftiles, a.nsplit);
+        for (int kb = it.ks * kps; kb < (it.ks + 1) * kps; ++kb, ++gs) {
           const int c = static_cast<int>(gs % kC);
           const uint32_t cu = static_cast<uint32_t>(gs / kC);
           if (!wait_ok(c_free(c), (cu & 1u) ^ 1u, a.status, abort_flag)) break;
@@ -440,9 +504,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t pol = policy_evict_last();
       int64_t gs = 0;
       for (int64_t item = blockIdx.x; item < nitems && !*abort_flag; item += gridDim.x) {
-        const Item it = decode_item(s_off, s_ts, a.E, item, ftiles);
+        const Item it = decode_item(s_off, s_ts, a.E, item, ftiles, a.nsplit);
         const int npad = (it.ntok + 15) & ~15;
-        for (int kb = 0; kb < kstages; ++kb, ++gs) {
+        for (int kb = it.ks * kps; kb < (it.ks + 1) * kps; ++kb, ++gs) {
           const int s = static_cast<int>(gs % kB);
           const uint32_t su = static_cast<uint32_t>(gs / kB);
           if (!wait_ok(ab_free(s), (su & 1u) ^ 1u, a.status, abort_flag)) break;
@@ -463,6 +527,47 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_wait_bounded(b_full(static_cast<int>(j % kB)),
                             static_cast<uint32_t>((j / kB) & 1), a.status);
     }
+  } else if (warp == kWarpRexp) {
+    // ------------------------------------------------ row exponents
+    // For every item in turn, the power of two r of each weight row (and
+    // matrix) that puts the row's largest dequantised magnitude,
+    // max over groups of s max(|zp|, |255 - zp|), into [2^14, 2^15), so that
+    // every (q - zp) s 2^r is finite in fp16 and uses its full precision
+    // whatever the weights' size.  Written to a two-slot ring one item ahead
+    // of the dequant warpgroups (lane l takes rows l, l + 32, l + 64, l + 96).
+    int64_t n = 0;
+    for (int64_t item = blockIdx.x; item < nitems && !*abort_flag; item += gridDim.x, ++n) {
+      const int slot = static_cast<int>(n & 1);
+      const uint32_t use = static_cast<uint32_t>(n >> 1);
+      if (!__all_sync(0xFFFFFFFFu, wait_ok(rexp_free(slot), (use & 1u) ^ 1u, a.status, abort_flag)))
+        break;
+      const Item it = decode_item(s_off, s_ts, a.E, item, ftiles, a.nsplit);
+#pragma unroll
+      for (int t = 0; t < NT; ++t) {
+        for (int rr = lane; rr < kBM; rr += 32) {
+          const int64_t wrow = static_cast<int64_t>(it.f) * kBM + rr;
+          const float *sp = a.sc[t] + it.e * a.gstride[t] + wrow * a.G;
+          const int32_t *zq = a.zp[t] + it.e * a.gstride[t] + wrow * a.G;
+          float m = 0.0f;
+          // rows past the matrix (a ragged last tile) read nothing
+          for (int g = 0; g < (wrow < a.rows ? a.G : 0); g += 4) {
+            const float4 s4 = __ldg(reinterpret_cast<const float4 *>(sp + g));
+            const int4 z4 = __ldg(reinterpret_cast<const int4 *>(zq + g));
+            const float sv[4] = {s4.x, s4.y, s4.z, s4.w};
+            const int32_t zv[4] = {z4.x, z4.y, z4.z, z4.w};
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              // max(|zp|, |255 - zp|) = |zp - 127.5| + 127.5
+              const float zw = fabsf(static_cast<float>(zv[u]) - 127.5f) + 127.5f;
+              m = fmaxf(m, sv[u] * zw);
+            }
+          }
+          const int e = ((__float_as_int(m) >> 23) & 0xFF) - 127;
+          s_rexp[(slot * NT + t) * kBM + rr] = max(-126, min(126, 14 - e));
+        }
+      }
+      mbar_arrive(rexp_full(slot));
+    }
   } else if (warp >= kWarpMma) {
     // ---------------------------------------------------- MMA issuers
     // A single thread issues only about one MMA per 60-100 cycles whatever
@@ -478,7 +583,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int64_t gs = 0;
       uint32_t nitem_done = 0;
       for (int64_t item = blockIdx.x; item < nitems && !*abort_flag; item += gridDim.x) {
-        const Item it = decode_item(s_off, s_ts, a.E, item, ftiles);
+        const Item it = decode_item(s_off, s_ts, a.E, item, ftiles, a.nsplit);
         const int npad = (it.ntok + 15) & ~15;
         const bool light = npad <= kLightN;
         const bool active = light || issuer < 2;
@@ -490,7 +595,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         bool ok = true;
         uint32_t acc = 0;  // the first MMA of the item into this accumulator overwrites it
-        for (int kb = 0; kb < kstages; ++kb, ++gs) {
+        for (int kb = 0; kb < kps; ++kb, ++gs) {
           const int sa = static_cast<int>(gs % kA), sb = static_cast<int>(gs % kB);
           const uint32_t ua = static_cast<uint32_t>(gs / kA), ub = static_cast<uint32_t>(gs / kB);
           // every issuer waits for the stage, so that no commit runs ahead of
@@ -534,7 +639,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int64_t gs = 0;
     uint32_t nitem_done = 0;
     for (int64_t item = blockIdx.x; item < nitems && !*abort_flag; item += gridDim.x) {
-      const Item it = decode_item(s_off, s_ts, a.E, item, ftiles);
+      const Item it = decode_item(s_off, s_ts, a.E, item, ftiles, a.nsplit);
       const int64_t wrow = static_cast<int64_t>(it.f) * kBM + row;
       const float *scp[NT];
       const int32_t *zpp[NT];
@@ -542,15 +647,31 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int t = 0; t < NT; ++t) {
         scp[t] = a.sc[t] + it.e * a.gstride[t] + wrow * a.G;
         zpp[t] = a.zp[t] + it.e * a.gstride[t] + wrow * a.G;
-        // pull this row's scale / zero-point lines into L2 for the whole item
-        for (int g = 32 * wg; g < a.G; g += 32 * kDequantGroups) {
-          asm volatile("prefetch.global.L2 [%0];" ::"l"(scp[t] + g));
-          asm volatile("prefetch.global.L2 [%0];" ::"l"(zpp[t] + g));
-        }
       }
-      // this warpgroup's first stage of the item (stages are dealt by their
-      // global number gs)
-      const int kb0 = static_cast<int>((wg - gs % kDequantGroups + kDequantGroups) % kDequantGroups);
+      // Row scale 2^r of each matrix (from the exponent warp) and its inverse,
+      // which the epilogue applies.
+      float rup[NT], rdn[NT];
+      {
+        const int slot = static_cast<int>(nitem_done & 1u);
+        const uint32_t use = nitem_done >> 1;
+        if (!__all_sync(0xFFFFFFFFu, wait_ok(rexp_full(slot), use & 1u, a.status, abort_flag)))
+          break;
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+          const int sh = s_rexp[(slot * NT + t) * kBM + row];
+          rup[t] = __int_as_float((127 + sh) << 23);
+          rdn[t] = __int_as_float((127 - sh) << 23);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(rexp_free(slot));
+      }
+      // the item's stages [kbs, kbe); this warpgroup's first one (stages are
+      // dealt by their global number gs); a row past the matrix (a ragged
+      // last tile) dequantises to zero and reads no scales
+      const int kbs = it.ks * kps, kbe = kbs + kps;
+      const bool row_ok = wrow < a.rows;
+      const int kb0 =
+          kbs + static_cast<int>((wg - gs % kDequantGroups + kDequantGroups) % kDequantGroups);
       // scale / zero point of this warpgroup's next stage, loaded one of its
       // stages ahead
       float s_nx[NT];
@@ -560,7 +681,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         s_nx[t] = 0.0f;
         z_nx[t] = 0;
       }
-      if (kb0 < kstages) {
+      if (kb0 < kbe && row_ok) {
         const int gi = (kb0 * kBK) >> a.group_shift;
 #pragma unroll
         for (int t = 0; t < NT; ++t) {
@@ -569,15 +690,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       bool ok = true;
-      for (int kb = 0; kb < kstages; ++kb, ++gs) {
+      for (int kb = kbs; kb < kbe; ++kb, ++gs) {
         if (static_cast<int>(gs % kDequantGroups) != wg) continue;
+        // Fast form (q - zp exact in fp16, times the fp16 scale) while the
+        // zero point keeps 1024 + zp and every q - zp (|.| <= 2048) exact in
+        // fp16 and the scaled scale is a normal fp16; the exact form otherwise.
         __half2 s2[NT], mz2[NT];
+        float sx[NT];
+        int32_t zx[NT];
+        bool fast[NT];
 #pragma unroll
         for (int t = 0; t < NT; ++t) {
-          s2[t] = __float2half2_rn(s_nx[t]);
-          mz2[t] = __float2half2_rn(1024.0f + static_cast<float>(z_nx[t]));
+          sx[t] = s_nx[t] * rup[t];
+          zx[t] = z_nx[t];
+          fast[t] = zx[t] >= -1793 && zx[t] <= 1024 && sx[t] >= 6.103515625e-05f;
+          s2[t] = __float2half2_rn(sx[t]);
+          mz2[t] = __float2half2_rn(1024.0f + static_cast<float>(zx[t]));
         }
-        if (kb + kDequantGroups < kstages) {
+        if (kb + kDequantGroups < kbe && row_ok) {
           const int gi = ((kb + kDequantGroups) * kBK) >> a.group_shift;
 #pragma unroll
           for (int t = 0; t < NT; ++t) {
@@ -605,7 +735,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int j = 0; j < 4; ++j) {
             const uint4 v = lds128(crow + ((j ^ ((row >> 1) & 3)) << 4));
             uint4 o0, o1;
-            dequant16(v, mz2[t], s2[t], o0, o1);
+            if (fast[t])
+              dequant16(v, mz2[t], s2[t], o0, o1);
+            else
+              dequant16_exact(v, zx[t], sx[t], o0, o1);
             packed[8 * j + 0] = o0.x;
             packed[8 * j + 1] = o0.y;
             packed[8 * j + 2] = o0.z;
@@ -650,21 +783,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else {
           tmem_ld16x2(tmem + lane_base + c0, tmem + lane_base + kBN + c0, v0, v1);
         }
+        // accumulators x (token row's 2^c) x (weight row's 2^-r): exact
+        // power-of-two rescaling back to the true products
+        const float *cs = a.colscale + it.t0 + c0;
+        float *const outp = a.out + it.ks * a.out_split;
+        const bool feat_ok = feat < a.rows;
         if constexpr (NT == 2) {
-          // v0 = gate, v1 = up
-          __half *h = static_cast<__half *>(a.out);
+          // v0 = gate, v1 = up; h in fp32 (rounded to fp16 with its own row
+          // scale once every feature tile of the token is done)
 #pragma unroll
           for (int j = 0; j < 16; ++j)
-            if (c0 + j < it.ntok)
-              h[static_cast<int64_t>(it.t0 + c0 + j) * a.out_ld + feat] =
-                  __float2half_rn(silu_f(v0[j]) * v1[j]);
+            if (c0 + j < it.ntok && feat_ok) {
+              const float c = __ldg(cs + j);
+              outp[static_cast<int64_t>(it.t0 + c0 + j) * a.out_ld + feat] =
+                  silu_f(v0[j] * c * rdn[0]) * (v1[j] * c * rdn[1]);
+            }
         } else {
           // partial sums over disjoint K steps
-          float *o = static_cast<float *>(a.out);
 #pragma unroll
           for (int j = 0; j < 16; ++j)
-            if (c0 + j < it.ntok)
-              o[static_cast<int64_t>(it.t0 + c0 + j) * a.out_ld + feat] = v0[j] + v1[j];
+            if (c0 + j < it.ntok && feat_ok)
+              outp[static_cast<int64_t>(it.t0 + c0 + j) * a.out_ld + feat] =
+                  (v0[j] + v1[j]) * __ldg(cs + j) * rdn[0];
         }
       }
       tc_fence_before();
@@ -682,32 +822,104 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// Largest of the per-thread values v over a 256-thread block (every thread
+// gets it).
+__device__ __forceinline__ uint32_t block_max_u32(uint32_t v) {
+  __shared__ uint32_t part[8];
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) v = max(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+  if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = v;
+  __syncthreads();
+  v = part[0];
+#pragma unroll
+  for (int w = 1; w < 8; ++w) v = max(v, part[w]);
+  return v;
+}
+
 // Gathers the tokens of every assignment in expert-sorted order into fp16
-// rows (bf16 -> fp16 is exact for normal fp16 magnitudes).  Only the first
-// offsets[E] slots hold assignments (slots of out-of-range expert indices are
-// left out by the grouping).
-__global__ void __launch_bounds__(256) gather_x_kernel(const uint16_t *__restrict__ x, int64_t MK,
-                                                       int k, int64_t H, int E,
+// rows (one block per sorted position p).  Each row is scaled by the power
+// of two 2^s that puts its largest magnitude into [2^14, 2^15), so that
+// bf16 -> fp16 is exact for every element within 2^28 of the row's largest
+// and never overflows, whatever the tokens' size; xs[p] = 2^-s undoes it in
+// the epilogue.  Only the first offsets[E] positions hold assignments
+// (out-of-range expert indices are left out by the grouping).  Without an
+// assignment list (a linear layer) position p is row p of x's nrows rows.
+__global__ void __launch_bounds__(256) gather_x_kernel(const uint16_t *__restrict__ x, int k,
+                                                       int64_t H, int E,
                                                        const int32_t *__restrict__ offsets,
                                                        const int32_t *__restrict__ assign,
-                                                       __half *__restrict__ xg) {
+                                                       int64_t nrows, __half *__restrict__ xg,
+                                                       float *__restrict__ xs) {
   pdl_enter();
+  const int64_t p = blockIdx.x;
+  if (p >= (assign ? static_cast<int64_t>(offsets[E]) : nrows)) return;
+  const int64_t tok = assign ? assign[p] / k : p;
+  const uint4 *src = reinterpret_cast<const uint4 *>(x + tok * H);
   const int64_t H8 = H / 8;
-  const int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (t >= MK * H8) return;
-  const int64_t p = t / H8, c = t % H8;
-  if (p >= offsets[E]) return;
-  const int tok = assign[p] / k;
-  const uint4 v = __ldg(reinterpret_cast<const uint4 *>(x + tok * H) + c);
-  uint32_t w[4] = {v.x, v.y, v.z, v.w};
-  uint32_t o[4];
+  // magnitudes as bit patterns: non-negative floats order like integers
+  uint32_t mb = 0;
+  for (int64_t c = threadIdx.x; c < H8; c += blockDim.x) {
+    const uint4 v = __ldg(src + c);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float lo = __uint_as_float(w[i] << 16), hi = __uint_as_float(w[i] & 0xFFFF0000u);
-    __half2 h = __floats2half2_rn(lo, hi);
-    o[i] = *reinterpret_cast<uint32_t *>(&h);
+    for (int i = 0; i < 4; ++i) mb = max(mb, max((w[i] << 16) & 0x7FFF0000u, w[i] & 0x7FFF0000u));
   }
-  reinterpret_cast<uint4 *>(xg + p * H)[c] = make_uint4(o[0], o[1], o[2], o[3]);
+  mb = block_max_u32(mb);
+  float up, down;
+  pow2_to_fp16_range(__uint_as_float(mb), up, down);
+  if (threadIdx.x == 0) xs[p] = down;
+  for (int64_t c = threadIdx.x; c < H8; c += blockDim.x) {
+    const uint4 v = __ldg(src + c);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float lo = __uint_as_float(w[i] << 16), hi = __uint_as_float(w[i] & 0xFFFF0000u);
+      __half2 h = __floats2half2_rn(lo * up, hi * up);
+      o[i] = *reinterpret_cast<uint32_t *>(&h);
+    }
+    reinterpret_cast<uint4 *>(xg + p * H)[c] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
+// Rounds the tensor-core experts' fp32 SwiGLU rows to fp16 for the down GEMM
+// (one block per sorted position p), each row scaled like the token rows
+// above; hs[p] undoes the scaling.  Rows of experts without token tiles (the
+// few-token experts, which run on the small-M kernels) are skipped.
+__global__ void __launch_bounds__(256) h_convert_kernel(const float *__restrict__ h, int64_t I,
+                                                        int E, const int32_t *__restrict__ offsets,
+                                                        const int32_t *__restrict__ tile_start,
+                                                        __half *__restrict__ hh,
+                                                        float *__restrict__ hs) {
+  pdl_enter();
+  const int p = blockIdx.x;
+  if (p >= offsets[E]) return;
+  int lo = 0, hi = E;  // the expert of position p: offsets[lo] <= p < offsets[hi]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (offsets[mid] <= p) lo = mid;
+    else hi = mid;
+  }
+  if (tile_start[lo + 1] == tile_start[lo]) return;
+  const float4 *src = reinterpret_cast<const float4 *>(h + static_cast<int64_t>(p) * I);
+  const int64_t I4 = I / 4;
+  uint32_t mb = 0;
+  for (int64_t c = threadIdx.x; c < I4; c += blockDim.x) {
+    const float4 v = src[c];
+    mb = max(mb, max(max(__float_as_uint(v.x) & 0x7FFFFFFFu, __float_as_uint(v.y) & 0x7FFFFFFFu),
+                     max(__float_as_uint(v.z) & 0x7FFFFFFFu, __float_as_uint(v.w) & 0x7FFFFFFFu)));
+  }
+  mb = block_max_u32(mb);
+  float up, down;
+  pow2_to_fp16_range(__uint_as_float(mb), up, down);
+  if (threadIdx.x == 0) hs[p] = down;
+  for (int64_t c = threadIdx.x; c < I4; c += blockDim.x) {
+    const float4 v = src[c];
+    __half2 a = __floats2half2_rn(v.x * up, v.y * up);
+    __half2 b = __floats2half2_rn(v.z * up, v.w * up);
+    reinterpret_cast<uint2 *>(hh + static_cast<int64_t>(p) * I)[c] =
+        make_uint2(*reinterpret_cast<uint32_t *>(&a), *reinterpret_cast<uint32_t *>(&b));
+  }
 }
 
 // ------------------------------------------------------------------ host
@@ -764,7 +976,107 @@ cudaError_t run_tc(const CUtensorMap &c0, const CUtensorMap &c1, const CUtensorM
   return launch_pdl(k, dim3(sm_count()), dim3(kThreads), bytes, s, c0, c1, x, x128, a);
 }
 
+// y = the sum of the nsplit partial results of the split K range, added in
+// split order (deterministic), written as fp32 or bf16.
+template <bool YBF16>
+__global__ void __launch_bounds__(256) split_reduce_kernel(const float *__restrict__ part,
+                                                           int nsplit, int64_t n, void *y) {
+  pdl_enter();
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  float acc = part[i];
+  for (int sidx = 1; sidx < nsplit; ++sidx) acc += part[sidx * n + i];
+  if constexpr (YBF16)
+    static_cast<__nv_bfloat16 *>(y)[i] = __float2bfloat16_rn(acc);
+  else
+    static_cast<float *>(y)[i] = acc;
+}
+
+// K splits of a linear layer with M rows on the tensor cores: enough work
+// items for two per SM, at least four 64-wide K stages per split, and a
+// divisor of the stage count.
+int linear_tc_splits(int64_t M, int64_t N, int64_t K) {
+  const int64_t items = ((M + kBN - 1) / kBN) * ((N + kBM - 1) / kBM);
+  const int kst = static_cast<int>(K / kBK);
+  int want = static_cast<int>((2 * sm_count() + items - 1) / items);
+  want = want < 1 ? 1 : want;
+  int best = 1;
+  for (int d = 1; d <= kst / 4; ++d)
+    if (kst % d == 0 && d <= want) best = d;
+  return best;
+}
+
 }  // namespace
+
+bool linear_tc_supported(const QMat &w) {
+  return w.bits == 8 && w.group >= 64 && w.cols % kBK == 0 && (w.cols / w.group) % 4 == 0 &&
+         w.rows >= 1 && encode_fn() != nullptr;
+}
+
+size_t linear_tc_workspace_bytes(int64_t M, const QMat &w) {
+  const int S = linear_tc_splits(M, w.rows, w.cols);
+  auto r256 = [](size_t v) { return (v + 255) & ~static_cast<size_t>(255); };
+  return r256(2 * static_cast<size_t>(M) * w.cols) + r256(4 * static_cast<size_t>(M)) +
+         r256(4 * static_cast<size_t>(S) * M * w.rows);
+}
+
+cudaError_t launch_linear_tc(const void *x, int64_t M, const QMat &w, void *y, bool y_bf16,
+                             void *workspace, cudaStream_t s) {
+  const int64_t N = w.rows, K = w.cols;
+  const int S = linear_tc_splits(M, N, K);
+  auto r256 = [](size_t v) { return (v + 255) & ~static_cast<size_t>(255); };
+  uint8_t *base = static_cast<uint8_t *>(workspace);
+  __half *xg = reinterpret_cast<__half *>(base);
+  float *xs = reinterpret_cast<float *>(base + r256(2 * static_cast<size_t>(M) * K));
+  float *part = reinterpret_cast<float *>(base + r256(2 * static_cast<size_t>(M) * K) +
+                                          r256(4 * static_cast<size_t>(M)));
+  // 1) rows of x -> scaled fp16 rows
+  cudaError_t e = launch_pdl(gather_x_kernel, dim3(static_cast<unsigned>(M)), dim3(256), 0, s,
+                             static_cast<const uint16_t *>(x), 1, K, 1,
+                             static_cast<const int32_t *>(nullptr),
+                             static_cast<const int32_t *>(nullptr), M, xg, xs);
+  if (e != cudaSuccess) return e;
+  CUtensorMap mw, mx, mx128;
+  QMat w1 = w;
+  w1.codes_stride = N * K;  // one matrix: any positive stride of whole 16-byte units
+  if (!make_codes_map(&mw, w1, 1) || !make_rows_map(&mx, xg, M, K, 16) ||
+      !make_rows_map(&mx128, xg, M, K, kBN))
+    return cudaErrorInvalidValue;
+  // 2) the GEMM: partial sums of each K split (fp32 y directly when there is
+  // one split)
+  const bool direct = S == 1 && !y_bf16;
+  TcArgs a{};
+  a.E = 1;
+  a.k = 1;
+  a.rows = N;
+  a.K = K;
+  a.G = static_cast<int>(K / w.group);
+  a.group_shift = 0;
+  while ((1 << a.group_shift) < w.group) ++a.group_shift;
+  a.sc[0] = w.scales;
+  a.zp[0] = w.zps;
+  a.gstride[0] = 0;
+  a.sc[1] = nullptr;
+  a.zp[1] = nullptr;
+  a.gstride[1] = 0;
+  a.colscale = xs;
+  a.out = direct ? static_cast<float *>(y) : part;
+  a.out_ld = N;
+  a.status = device_status();
+  a.lin_M = static_cast<int>(M);
+  a.nsplit = S;
+  a.out_split = M * N;
+  e = run_tc<1>(mw, mw, mx, mx128, a, s);
+  if (e != cudaSuccess || direct) return e;
+  // 3) the splits added in order
+  const int64_t n = M * N;
+  const unsigned blocks = static_cast<unsigned>((n + 255) / 256);
+  if (y_bf16)
+    return launch_pdl(split_reduce_kernel<true>, dim3(blocks), dim3(256), 0, s,
+                      static_cast<const float *>(part), S, n, y);
+  return launch_pdl(split_reduce_kernel<false>, dim3(blocks), dim3(256), 0, s,
+                    static_cast<const float *>(part), S, n, y);
+}
 
 bool moe_tc_supported(const QMat &gate, const QMat &down, int64_t H, int64_t I) {
   return gate.bits == 8 && down.bits == 8 && gate.group >= 64 && H % kBM == 0 && I % kBM == 0 &&
@@ -775,13 +1087,12 @@ cudaError_t launch_moe_tc(const void *x, int64_t M, int k, int E, const QMat &ga
                           const QMat &down, const MoeWork &ws, cudaStream_t s) {
   const int64_t MK = M * k;
   const int64_t H = gate.cols, I = gate.rows;
-  // 1) tokens -> fp16 rows in expert order
+  // 1) tokens -> scaled fp16 rows in expert order
   {
-    const int64_t n = MK * (H / 8);
-    cudaError_t e = launch_pdl(gather_x_kernel, dim3(static_cast<unsigned>((n + 255) / 256)),
-                               dim3(256), 0, s, static_cast<const uint16_t *>(x), MK, k, H, E,
+    cudaError_t e = launch_pdl(gather_x_kernel, dim3(static_cast<unsigned>(MK)), dim3(256), 0, s,
+                               static_cast<const uint16_t *>(x), k, H, E,
                                static_cast<const int32_t *>(ws.offsets),
-                               static_cast<const int32_t *>(ws.assign), ws.xg);
+                               static_cast<const int32_t *>(ws.assign), MK, ws.xg, ws.xs);
     if (e != cudaSuccess) return e;
   }
   CUtensorMap mg, mu, md, mx, mx128, mh, mh128;
@@ -790,7 +1101,7 @@ cudaError_t launch_moe_tc(const void *x, int64_t M, int k, int E, const QMat &ga
       !make_rows_map(&mx128, ws.xg, MK, H, kBN) || !make_rows_map(&mh, ws.hh, MK, I, 16) ||
       !make_rows_map(&mh128, ws.hh, MK, I, kBN))
     return cudaErrorInvalidValue;
-  // 2) gate + up with SwiGLU -> fp16 h
+  // 2) gate + up with SwiGLU -> fp32 h
   TcArgs a{};
   a.E = E;
   a.k = k;
@@ -807,12 +1118,21 @@ cudaError_t launch_moe_tc(const void *x, int64_t M, int k, int E, const QMat &ga
   a.gstride[1] = up.groups_stride;
   a.offsets = ws.offsets;
   a.tile_start = ws.tile_start;
-  a.out = ws.hh;
+  a.colscale = ws.xs;
+  a.out = ws.h;
   a.out_ld = I;
   a.status = device_status();
+  a.lin_M = 0;
+  a.nsplit = 1;
+  a.out_split = 0;
   cudaError_t e = run_tc<2>(mg, mu, mx, mx128, a, s);
   if (e != cudaSuccess) return e;
-  // 3) down -> fp32 per-assignment outputs
+  // 3) h -> scaled fp16 rows
+  e = launch_pdl(h_convert_kernel, dim3(static_cast<unsigned>(MK)), dim3(256), 0, s,
+                 static_cast<const float *>(ws.h), I, E, static_cast<const int32_t *>(ws.offsets),
+                 static_cast<const int32_t *>(ws.tile_start), ws.hh, ws.hs);
+  if (e != cudaSuccess) return e;
+  // 4) down -> fp32 per-assignment outputs
   TcArgs d = a;
   d.rows = H;
   d.K = I;
@@ -825,6 +1145,7 @@ cudaError_t launch_moe_tc(const void *x, int64_t M, int k, int E, const QMat &ga
   d.sc[1] = nullptr;
   d.zp[1] = nullptr;
   d.gstride[1] = 0;
+  d.colscale = ws.hs;
   d.out = ws.out;
   d.out_ld = H;
   return run_tc<1>(md, md, mh, mh128, d, s);

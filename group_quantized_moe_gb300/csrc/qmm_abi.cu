@@ -152,22 +152,24 @@ int qmm_quantize_groupwise(const float *w, int64_t N, int64_t K, int32_t bits, i
   return QMM_OK;
 }
 
-int qmm_linear(const void *x, int32_t x_dtype, int64_t M, const qmm_weight *w, float *y,
-               qmm_stream_t stream) {
+int qmm_linear(const void *x, int32_t x_dtype, int64_t M, const qmm_weight *w, void *y,
+               int32_t y_dtype, qmm_stream_t stream) {
   g_err[0] = '\0';
   if (!w) return fail(QMM_ERR_INVALID_ARG, "qmm_linear: weight descriptor is NULL");
   int rc = check_qshape(w->bits, w->group, w->N, w->K, "qmm_linear");
   if (rc) return rc;
   if (x_dtype != QMM_F32 && x_dtype != QMM_BF16)
     return fail(QMM_ERR_INVALID_ARG, "qmm_linear: x_dtype must be QMM_F32 or QMM_BF16");
+  if (y_dtype != QMM_F32 && y_dtype != QMM_BF16)
+    return fail(QMM_ERR_INVALID_ARG, "qmm_linear: y_dtype must be QMM_F32 or QMM_BF16");
   if (M < 0) return fail(QMM_ERR_SHAPE, "qmm_linear: negative M");
   if (M == 0 || w->N == 0) return QMM_OK;
   if (!x || !y || !w->codes || !w->scales || !w->zps)
     return fail(QMM_ERR_INVALID_ARG, "qmm_linear: null pointer");
   if (!aligned16(x) || !aligned16(w->codes) || !aligned16(w->scales) || !aligned16(w->zps))
     return fail(QMM_ERR_ALIGN, "qmm_linear: x, codes, scales and zps must be 16-byte aligned");
-  if ((reinterpret_cast<uintptr_t>(y) & 3u) != 0)
-    return fail(QMM_ERR_ALIGN, "qmm_linear: y must be 4-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(y) & (y_dtype == QMM_BF16 ? 1u : 3u)) != 0)
+    return fail(QMM_ERR_ALIGN, "qmm_linear: y must be aligned to its element size");
   const int64_t rowbytes = w->K * w->bits / 8;
   if (gemv_rows_per_tile(rowbytes, w->K / w->group, 1) < 1)
     return fail(QMM_ERR_UNSUPPORTED, "qmm_linear: K=%lld is longer than one weight tile holds",
@@ -179,15 +181,64 @@ int qmm_linear(const void *x, int32_t x_dtype, int64_t M, const qmm_weight *w, f
   // 1..8 rows of the shapes it takes; the per-warp row kernel otherwise.
   const bool small = smallm_supported(w->bits, w->group, w->K) && M >= 1 && M <= 8;
   if (small)
-    e = launch_smallm_linear(x, x_dtype == QMM_BF16, M, q, y, static_cast<cudaStream_t>(stream));
+    e = launch_smallm_linear(x, x_dtype == QMM_BF16, M, q, y, y_dtype == QMM_BF16,
+                             static_cast<cudaStream_t>(stream));
   else
-    e = launch_gemv(x, x_dtype == QMM_BF16, M, q, y, static_cast<cudaStream_t>(stream));
+    e = launch_gemv(x, x_dtype == QMM_BF16, M, q, y, y_dtype == QMM_BF16,
+                    static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "qmm_linear");
+  return QMM_OK;
+}
+
+// Rows from which bf16 activations take the tensor-core linear path.
+constexpr int64_t kLinearTcMinRows = 9;
+
+size_t qmm_linear_batched_workspace_bytes(int64_t M, const qmm_weight *w) {
+  if (!w || M < kLinearTcMinRows || M > 2147483647 || w->N <= 0 || w->K <= 0 || w->group <= 0)
+    return 256;
+  QMat q{static_cast<const uint8_t *>(w->codes), 0, w->scales, w->zps, 0, w->N, w->K,
+         w->bits, w->group};
+  if (!linear_tc_supported(q)) return 256;
+  return linear_tc_workspace_bytes(M, q);
+}
+
+int qmm_linear_batched(const void *x, int32_t x_dtype, int64_t M, const qmm_weight *w, void *y,
+                       int32_t y_dtype, void *workspace, size_t workspace_bytes,
+                       qmm_stream_t stream) {
+  g_err[0] = '\0';
+  if (!w) return fail(QMM_ERR_INVALID_ARG, "qmm_linear_batched: weight descriptor is NULL");
+  QMat q{static_cast<const uint8_t *>(w->codes), 0, w->scales, w->zps, 0, w->N, w->K,
+         w->bits, w->group};
+  const bool tc = x_dtype == QMM_BF16 && M >= kLinearTcMinRows && M <= 2147483647 &&
+                  check_qshape(w->bits, w->group, w->N, w->K, "qmm_linear_batched") == QMM_OK &&
+                  w->N > 0 && linear_tc_supported(q);
+  g_err[0] = '\0';
+  if (!tc)  // the CUDA-core paths of qmm_linear (the workspace is not used)
+    return qmm_linear(x, x_dtype, M, w, y, y_dtype, stream);
+  if (y_dtype != QMM_F32 && y_dtype != QMM_BF16)
+    return fail(QMM_ERR_INVALID_ARG, "qmm_linear_batched: y_dtype must be QMM_F32 or QMM_BF16");
+  if (!x || !y || !w->codes || !w->scales || !w->zps)
+    return fail(QMM_ERR_INVALID_ARG, "qmm_linear_batched: null pointer");
+  if (!aligned16(x) || !aligned16(w->codes) || !aligned16(w->scales) || !aligned16(w->zps))
+    return fail(QMM_ERR_ALIGN, "qmm_linear_batched: x, codes, scales and zps must be 16-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(y) & (y_dtype == QMM_BF16 ? 1u : 3u)) != 0)
+    return fail(QMM_ERR_ALIGN, "qmm_linear_batched: y must be aligned to its element size");
+  const size_t need = linear_tc_workspace_bytes(M, q);
+  if (!workspace || workspace_bytes < need)
+    return fail(QMM_ERR_WORKSPACE, "qmm_linear_batched: workspace needs %zu bytes", need);
+  if (!aligned256(workspace))
+    return fail(QMM_ERR_ALIGN, "qmm_linear_batched: workspace must be 256-byte aligned");
+  cudaError_t e = launch_linear_tc(x, M, q, y, y_dtype == QMM_BF16, workspace,
+                                   static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "qmm_linear_batched");
   return QMM_OK;
 }
 
 size_t moe_route_workspace_bytes(int64_t M, int32_t E) {
   if (M <= 0 || E <= 0) return 256;
+  // sizes the router refuses (M >= 2^31 or E > 1024) cannot be given a
+  // workspace: report the largest size so that no allocation succeeds
+  if (M > kMaxRouteTokens || E > 1024) return SIZE_MAX;
   return round256(router_logits_bytes(M, E));
 }
 
@@ -203,6 +254,8 @@ int moe_route_topk(const void *x, int32_t x_dtype, int64_t M, int64_t H, const f
     return fail(QMM_ERR_INVALID_ARG, "moe_route_topk: k must be in [1, min(E, 16)]");
   if (M < 0 || H <= 0 || H % 4 != 0)
     return fail(QMM_ERR_SHAPE, "moe_route_topk: need M >= 0 and H a positive multiple of 4");
+  if (M > kMaxRouteTokens || H > kMaxRouteWidth)
+    return fail(QMM_ERR_UNSUPPORTED, "moe_route_topk: need M < 2^31 and H <= 2^24");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (M == 0) {
     if (expert_counts) {
@@ -223,6 +276,28 @@ int moe_route_topk(const void *x, int32_t x_dtype, int64_t M, int64_t H, const f
   cudaError_t e = launch_router(x, x_dtype == QMM_BF16, M, H, w_router, bias, E, k,
                                 static_cast<float *>(workspace), topk_idx, topk_w, expert_counts, s);
   if (e != cudaSuccess) return cuda_fail(e, "moe_route_topk");
+  return QMM_OK;
+}
+
+int moe_route_load_stats(const int32_t *expert_counts, int32_t E, int64_t threshold,
+                         int64_t *stats, qmm_stream_t stream) {
+  g_err[0] = '\0';
+  if (E < 1 || E > 1024) return fail(QMM_ERR_INVALID_ARG, "moe_route_load_stats: E must be in [1, 1024]");
+  if (!expert_counts || !stats) return fail(QMM_ERR_INVALID_ARG, "moe_route_load_stats: null pointer");
+  if ((reinterpret_cast<uintptr_t>(expert_counts) & 3u) || (reinterpret_cast<uintptr_t>(stats) & 7u))
+    return fail(QMM_ERR_ALIGN, "moe_route_load_stats: counts and stats must be aligned to their elements");
+  cudaError_t e = launch_load_stats(expert_counts, E, threshold, stats,
+                                    static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "moe_route_load_stats");
+  return QMM_OK;
+}
+
+int qmm_diag_wait_timeout(uint64_t limit_ns, qmm_stream_t stream) {
+  g_err[0] = '\0';
+  if (limit_ns < 1 || limit_ns > 10000000000ull)
+    return fail(QMM_ERR_INVALID_ARG, "qmm_diag_wait_timeout: limit must be in [1 ns, 10 s]");
+  cudaError_t e = launch_wait_timeout(limit_ns, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "qmm_diag_wait_timeout");
   return QMM_OK;
 }
 
@@ -269,7 +344,7 @@ int check_experts(const moe_experts *ex) {
 
 struct WsLayout {
   size_t counts, offsets, active, num_active, assign, pos, h, out, tile_start, xg, light,
-      num_light, total;
+      num_light, hh, xs, hs, total;
 };
 
 WsLayout ws_layout(int64_t M, int k, const moe_experts *ex) {
@@ -288,6 +363,9 @@ WsLayout ws_layout(int64_t M, int k, const moe_experts *ex) {
   L.xg = o;         o += round256(2 * MK * ex->H);  // fp16 gathered tokens
   L.light = o;      o += round256(sizeof(int32_t) * ex->E);
   L.num_light = o;  o += 256;
+  L.hh = o;         o += round256(2 * MK * ex->I);  // fp16 SwiGLU activations
+  L.xs = o;         o += round256(sizeof(float) * MK);
+  L.hs = o;         o += round256(sizeof(float) * MK);
   L.total = o;
   return L;
 }
@@ -343,7 +421,9 @@ int moe_ffn_forward(const void *x, int32_t x_dtype, int64_t M, const int32_t *to
   ws.out = reinterpret_cast<float *>(base + L.out);
   ws.tile_start = reinterpret_cast<int32_t *>(base + L.tile_start);
   ws.xg = reinterpret_cast<__half *>(base + L.xg);
-  ws.hh = reinterpret_cast<__half *>(base + L.h);  // fp16 h reuses the fp32 h buffer
+  ws.hh = reinterpret_cast<__half *>(base + L.hh);
+  ws.xs = reinterpret_cast<float *>(base + L.xs);
+  ws.hs = reinterpret_cast<float *>(base + L.hs);
   ws.active_light = reinterpret_cast<int32_t *>(base + L.light);
   ws.num_light = reinterpret_cast<int32_t *>(base + L.num_light);
 
@@ -375,9 +455,8 @@ int moe_ffn_forward(const void *x, int32_t x_dtype, int64_t M, const int32_t *to
     e = launch_moe_tc(x, M, k, ex->E, qmat(ex->gate), qmat(ex->up), qmat(ex->down), ws, s);
     if (e != cudaSuccess) return cuda_fail(e, "moe_ffn_forward (tensor-core experts)");
     if (light_max > 0) {
-      // the experts with one or two tokens (they write the fp32 h buffer
-      // that the tensor-core kernels' fp16 h shares, after those have
-      // finished with it)
+      // the experts with one or two tokens (their rows of the fp32 h
+      // buffer are disjoint from the tensor-core experts' rows)
       MoeWork wl = ws;
       wl.active = ws.active_light;
       wl.num_active = ws.num_light;

@@ -13,6 +13,7 @@ namespace qmm {
 // Status bits (mirrors the public QMM_DEV_* values).
 constexpr uint32_t kDevWaitTimeout = 1u;
 constexpr uint32_t kDevBadExpert = 2u;
+constexpr uint32_t kDevExpertOverload = 4u;
 
 // Upper bound of any single wait inside a kernel (ns of %globaltimer).
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
@@ -80,14 +81,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Waits for the phase with the given parity to complete.  Gives up after
-// kWaitLimitNs, sets kDevWaitTimeout in *status and returns false.
+// limit_ns (kWaitLimitNs unless a caller passes another), sets
+// kDevWaitTimeout in *status and returns false.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
-                                                  uint32_t *status) {
+                                                  uint32_t *status,
+                                                  uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
-    if (global_timer_ns() - t0 > kWaitLimitNs) {
+    if (global_timer_ns() - t0 > limit_ns) {
       atomicOr(status, kDevWaitTimeout);
       return false;
     }
@@ -227,6 +230,14 @@ __device__ __forceinline__ float4 load_x4(const void *base, int64_t idx) {
   } else {
     return ldg_f4(reinterpret_cast<const float *>(base) + idx);
   }
+}
+
+// Output element i of a linear layer, fp32 or rounded to bf16 (nearest even).
+__device__ __forceinline__ void store_y(void *y, int64_t i, float v, bool bf16) {
+  if (bf16)
+    static_cast<__nv_bfloat16 *>(y)[i] = __float2bfloat16_rn(v);
+  else
+    static_cast<float *>(y)[i] = v;
 }
 
 __device__ __forceinline__ float warp_sum(float v) {

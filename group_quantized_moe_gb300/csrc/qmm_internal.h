@@ -38,6 +38,8 @@ struct MoeWork {
   int32_t *num_light;     // [1]
   __half *xg;           // [M*k, H] tokens in expert order, fp16 (tensor-core path)
   __half *hh;           // [M*k, I] SwiGLU activations, fp16 (tensor-core path)
+  float *xs;            // [M*k] power of two that undoes the scaling of xg's row
+  float *hs;            // [M*k] the same for hh's row
 };
 
 // Counts one kernel launch (for qmm_launch_count).
@@ -77,8 +79,8 @@ cudaError_t ensure_smem(const void *kernel, int bytes);
 cudaError_t launch_quantize(const float *w, int64_t N, int64_t K, int bits, int group,
                             void *codes, float *scales, int32_t *zps, cudaStream_t s);
 
-cudaError_t launch_gemv(const void *x, bool x_bf16, int64_t M, const QMat &w, float *y,
-                        cudaStream_t s);
+cudaError_t launch_gemv(const void *x, bool x_bf16, int64_t M, const QMat &w, void *y,
+                        bool y_bf16, cudaStream_t s);
 
 cudaError_t launch_router(const void *x, bool x_bf16, int64_t M, int64_t H,
                           const float *wr, const float *bias, int E, int k,
@@ -100,6 +102,14 @@ bool moe_tc_supported(const QMat &gate, const QMat &down, int64_t H, int64_t I);
 cudaError_t launch_moe_tc(const void *x, int64_t M, int k, int E, const QMat &gate, const QMat &up,
                           const QMat &down, const MoeWork &ws, cudaStream_t s);
 
+// Linear layer with bf16 rows on the tensor cores (INT8, group >= 64):
+// workspace bytes for M rows, and the launch (gather, GEMM with K splits,
+// ordered reduction of the splits).
+bool linear_tc_supported(const QMat &w);
+size_t linear_tc_workspace_bytes(int64_t M, const QMat &w);
+cudaError_t launch_linear_tc(const void *x, int64_t M, const QMat &w, void *y, bool y_bf16,
+                             void *workspace, cudaStream_t s);
+
 cudaError_t launch_moe_combine(int64_t M, int k, int64_t H, const float *topk_w,
                                const MoeWork &ws, void *y, bool y_bf16, cudaStream_t s);
 
@@ -111,14 +121,18 @@ namespace qmm {
 int gemv_rows_per_tile(int64_t rowbytes, int64_t G, int copies);
 // Bytes of router logits for M tokens and E experts.
 size_t router_logits_bytes(int64_t M, int E);
+// Largest token count and width the router takes (every size computed from
+// them then fits in 64 bits and every grid in 2^31 blocks).
+constexpr int64_t kMaxRouteTokens = 2147483647;
+constexpr int64_t kMaxRouteWidth = int64_t(1) << 24;
 }  // namespace qmm
 
 namespace qmm {
 // Small-M fused dequantise-matmul (1..8 activation rows per matrix, more in
 // passes of 8): K in {2048, 4096}, group >= 64 with K / group a multiple of 4.
 bool smallm_supported(int bits, int group, int64_t K);
-cudaError_t launch_smallm_linear(const void *x, bool x_bf16, int64_t M, const QMat &w, float *y,
-                                 cudaStream_t s);
+cudaError_t launch_smallm_linear(const void *x, bool x_bf16, int64_t M, const QMat &w, void *y,
+                                 bool y_bf16, cudaStream_t s);
 // rows_per_pass: 1 (one token per pass, 32 columns per lane: decode batches)
 // or 2 (two tokens per pass, 16 columns per lane: the experts of a prefill
 // batch with at most two tokens).
@@ -137,4 +151,9 @@ cudaError_t launch_smallm_down(int k, int E, const QMat &down, const MoeWork &ws
 namespace qmm {
 // Sets this thread's qmm_last_error() message (printf-style; "" clears it).
 void record_error(const char *fmt, ...);
+// Routing load statistics over an expert histogram (E <= 1024).
+cudaError_t launch_load_stats(const int32_t *counts, int E, int64_t threshold, int64_t *stats,
+                              cudaStream_t s);
+// One thread waiting on a barrier nothing completes, bounded by limit_ns.
+cudaError_t launch_wait_timeout(uint64_t limit_ns, cudaStream_t s);
 }  // namespace qmm

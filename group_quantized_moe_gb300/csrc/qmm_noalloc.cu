@@ -14,6 +14,7 @@
 // contents.  The router writes every logit it later reads, so nothing has to
 // be cleared first; two calls whose kernels overlap on the GPU (different
 // streams, no ordering between them) race on the array and must be avoided.
+#include <atomic>
 #include <cstdint>
 #include <mutex>
 
@@ -29,25 +30,33 @@ constexpr int64_t kNoallocLogits = QMM_NOALLOC_MAX_LOGITS;
 static __device__ __align__(256) float g_noalloc_logits[kNoallocLogits];
 
 constexpr int kMaxDevices = 64;
-float *g_scratch_ptr[kMaxDevices] = {nullptr};
+std::atomic<float *> g_scratch_ptr[kMaxDevices] = {};
 std::mutex g_noalloc_mu;
 
 // Device address of the scratch array on the current device, looked up once
 // per device with that device current (in host code the array's name is only
-// a host-side stand-in, not a device address).
+// a host-side stand-in, not a device address).  Later calls read the cached
+// address without taking the lock.  The address belongs to the device's
+// primary context: after cudaDeviceReset it is stale, so a process that
+// resets a device must not call this entry point on it again.
 cudaError_t scratch_for_current_device(float **out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lk(g_noalloc_mu);
-  if (!g_scratch_ptr[dev]) {
-    void *p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_noalloc_logits);
-    if (e != cudaSuccess) return e;
-    g_scratch_ptr[dev] = static_cast<float *>(p);
+  float *p = g_scratch_ptr[dev].load(std::memory_order_acquire);
+  if (!p) {
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    p = g_scratch_ptr[dev].load(std::memory_order_relaxed);
+    if (!p) {
+      void *a = nullptr;
+      e = cudaGetSymbolAddress(&a, g_noalloc_logits);
+      if (e != cudaSuccess) return e;
+      p = static_cast<float *>(a);
+      g_scratch_ptr[dev].store(p, std::memory_order_release);
+    }
   }
-  *out = g_scratch_ptr[dev];
+  *out = p;
   return cudaSuccess;
 }
 
@@ -77,12 +86,17 @@ int moe_route_topk_noalloc(const void *x, int32_t x_dtype, int64_t M, int64_t H,
              "moe_route_topk_noalloc: need M >= 0 and H a positive multiple of 4");
     return QMM_ERR_SHAPE;
   }
-  if (M * static_cast<int64_t>(E) > qmm::kNoallocLogits) {
+  if (H > qmm::kMaxRouteWidth) {
+    qmm::record_error("moe_route_topk_noalloc: need H <= 2^24");
+    return QMM_ERR_UNSUPPORTED;
+  }
+  // M > limit / E rather than M * E > limit: the product of a huge M could
+  // wrap around.
+  if (M > qmm::kNoallocLogits / E) {
     qmm::record_error(
-             "moe_route_topk_noalloc: M * E = %lld exceeds the built-in scratch of %lld "
-             "logits; use moe_route_topk with a workspace",
-             static_cast<long long>(M * static_cast<int64_t>(E)),
-             static_cast<long long>(qmm::kNoallocLogits));
+             "moe_route_topk_noalloc: M = %lld tokens times E = %d experts exceeds the "
+             "built-in scratch of %lld logits; use moe_route_topk with a workspace",
+             static_cast<long long>(M), E, static_cast<long long>(qmm::kNoallocLogits));
     return QMM_ERR_WORKSPACE;
   }
   cudaStream_t s = static_cast<cudaStream_t>(stream);

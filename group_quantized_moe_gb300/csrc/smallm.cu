@@ -35,15 +35,18 @@ bool smallm_supported(int bits, int group, int64_t K) {
   return group % 16 == 0;  // a lane's 16 (or 8) columns never straddle a group
 }
 
-cudaError_t launch_smallm_linear(const void *x, bool x_bf16, int64_t M, const QMat &w, float *y,
-                                 cudaStream_t s) {
+cudaError_t launch_smallm_linear(const void *x, bool x_bf16, int64_t M, const QMat &w, void *y,
+                                 bool y_bf16, cudaStream_t s) {
   smallm::Args a = smallm::base_args(w, 1);
   a.E = 1;
   a.k = 1;
   a.M = M;
   a.x = x;
   a.y = y;
-  // One segment of M rows: the class its token count selects.
+  a.y_bf16 = y_bf16;
+  // One segment of M rows: the class its token count selects (one row: 32
+  // columns per lane, which spreads the per-row work over twice the codes).
+  if (M == 1) return smallm::run_one(smallm::kLinear, x_bf16, a, s);
   return M <= 2 ? smallm::run_lo(smallm::kLinear, x_bf16, a, s)
                 : smallm::run_hi(smallm::kLinear, x_bf16, a, s);
 }

@@ -45,17 +45,18 @@ constexpr int kThreads = kCW * 32;
 constexpr int kStageBytes = 40960;
 
 // Three configurations (TBMAX = activation rows per pass).  TBMAX 1 and 2
-// use two CTAs per SM (128 registers) and the compact integer form.
-// TBMAX 1 runs the routed experts of decode batches: most of them have one
-// token, and with one row per pass a lane can hold 32 columns, which halves
-// the per-row work (scale, zero point, conversions, reduction) per code; an
-// expert with T tokens is applied in T passes, each a sweep over the CTA's
-// tiles of that expert (activations load once per pass, the tiles stream
-// again).  TBMAX 2 (16 columns per lane) runs the linear layer with 1..2
-// rows and the experts of a prefill batch that have one or two tokens (both
-// tokens in one pass, so the weights stream once).  TBMAX 8 (one CTA per SM,
-// eight fp32 rows per pass) runs the linear layer with 3..8 rows, where every
-// tile serves all M rows.
+// use two CTAs per SM (128 registers) and integer byte dot products of the
+// codes with the activations held as balanced digits (smallm_kernel.cuh).
+// TBMAX 1 runs the linear layer with one row and the routed experts of
+// decode batches: most of them have one token, and with one row per pass a
+// lane can hold 32 columns, which halves the per-row work (scale, zero
+// point, conversions, reduction) per code; an expert with T tokens is
+// applied in T passes, each a sweep over the CTA's tiles of that expert
+// (activations load once per pass, the tiles stream again).  TBMAX 2 (16
+// columns per lane) runs the linear layer with two rows and the experts of a
+// prefill batch that have one or two tokens (both tokens in one pass, so the
+// weights stream once).  TBMAX 8 (one CTA per SM, eight fp32 rows per pass)
+// runs the linear layer with 3..8 rows, where every tile serves all M rows.
 template <int TBMAX>
 struct Cfg {
   static constexpr int kCtas = TBMAX <= 2 ? 2 : 1;      // CTAs per SM
@@ -63,10 +64,15 @@ struct Cfg {
   static constexpr int kRedMax = TBMAX * 32;            // rows x tokens per tile
   static constexpr int kRingBytes = kStages * kStageBytes;
   static constexpr int kRedBytes = 2 * kCW * kRedMax * 4;
+  // the two low activation digits of the one- and two-row configurations
+  // (TBMAX rows x 2 digits x XPL / 4 words per lane, XPL = 32 / TBMAX), read
+  // only by warps that need all five digits
+  static constexpr int kLowBytes = TBMAX <= 2 ? kCW * 32 * 2 * 8 * 4 : 0;
   // segments (3 E + 2 ints), and for the in-CTA grouping of a decode batch
   // the assignments' experts and sorted order (2 MK) and the counts (E)
   static int smem_bytes(int E, int64_t MK) {
-    return kRingBytes + kRedBytes + (3 * E + 2) * 4 + static_cast<int>(2 * MK + E) * 4;
+    return kRingBytes + kRedBytes + kLowBytes + (3 * E + 2) * 4 +
+           static_cast<int>(2 * MK + E) * 4;
   }
 };
 
@@ -91,7 +97,8 @@ struct Args {
   int64_t MK;
   int32_t *pos_out;
   const void *x;    // linear and gate/up: activations [*, K]
-  float *y;         // linear: output [M, rows]
+  void *y;          // linear: output [M, rows], fp32 or (y_bf16) bf16
+  bool y_bf16;
   uint32_t *status;
 };
 

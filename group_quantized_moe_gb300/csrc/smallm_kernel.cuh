@@ -1,7 +1,8 @@
 // smallm_kernel.cuh -- the small-M fused dequantise-matmul kernel template
-// (design notes in smallm.cuh), instantiated by smallm_lo.cu (two activation
-// rows per pass, two CTAs per SM) and smallm_hi.cu (eight rows per pass, one
-// CTA per SM; the linear layer with 3..8 rows).
+// (design notes in smallm.cuh), instantiated by smallm_one.cu (one
+// activation row per pass), smallm_lo.cu (two rows per pass; both two CTAs
+// per SM, balanced-digit integer arithmetic) and smallm_hi.cu (eight fp32
+// rows per pass, one CTA per SM; the linear layer with 3..8 rows).
 #pragma once
 
 #include <cstdint>
@@ -24,6 +25,35 @@ __device__ __forceinline__ uint32_t lds32(uint32_t addr) {
   uint32_t v;
   asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
   return v;
+}
+
+// NW consecutive 32-bit words of shared memory (one lane's codes of a row).
+template <int NW>
+__device__ __forceinline__ void lds_words(uint32_t addr, uint32_t (&w)[NW]) {
+  if constexpr (NW == 8) {
+    const uint4 v0 = lds128(addr), v1 = lds128(addr + 16);
+    w[0] = v0.x;
+    w[1] = v0.y;
+    w[2] = v0.z;
+    w[3] = v0.w;
+    w[4] = v1.x;
+    w[5] = v1.y;
+    w[6] = v1.z;
+    w[7] = v1.w;
+  } else if constexpr (NW == 4) {
+    const uint4 v = lds128(addr);
+    w[0] = v.x;
+    w[1] = v.y;
+    w[2] = v.z;
+    w[3] = v.w;
+  } else if constexpr (NW == 2) {
+    const uint2 v = lds64(addr);
+    w[0] = v.x;
+    w[1] = v.y;
+  } else {
+    static_assert(NW == 1, "1, 2, 4 or 8 words");
+    w[0] = lds32(addr);
+  }
 }
 
 // CTA barrier that also ORs a predicate over the threads, so that every
@@ -82,13 +112,7 @@ __device__ __forceinline__ void row_dot(uint32_t caddr, float zf,
   if constexpr (BITS == 4) {
     constexpr int NW = XPL / 8;
     uint32_t w[NW];
-    if constexpr (NW == 2) {
-      const uint2 v = lds64(caddr);
-      w[0] = v.x;
-      w[1] = v.y;
-    } else {
-      w[0] = lds32(caddr);
-    }
+    lds_words<NW>(caddr, w);
     const f32x2_t off = pack2(8388608.0f + zf, fmaf(16.0f, zf, 8388608.0f));
 #pragma unroll
     for (int i = 0; i < NW; ++i) {
@@ -106,17 +130,7 @@ __device__ __forceinline__ void row_dot(uint32_t caddr, float zf,
   } else {
     constexpr int NW = XPL / 4;
     uint32_t w[NW];
-    if constexpr (NW == 4) {
-      const uint4 v = lds128(caddr);
-      w[0] = v.x;
-      w[1] = v.y;
-      w[2] = v.z;
-      w[3] = v.w;
-    } else {
-      const uint2 v = lds64(caddr);
-      w[0] = v.x;
-      w[1] = v.y;
-    }
+    lds_words<NW>(caddr, w);
     const float m = 8388608.0f + zf;
     const f32x2_t off = pack2(m, m);
 #pragma unroll
@@ -169,274 +183,15 @@ __host__ __device__ constexpr int log2c() {
   return V <= 1 ? 0 : 1 + log2c<V / 2>();
 }
 
-// One tile for TB tokens: every row of the stage against the lane's slice of
-// the activations; lane partials reduced per block of NRS rows and written
-// to this warp's row of the reduction buffer (index row * TB + token).
-template <int BITS, int XPL, int NR, int TB, int TBMAX>
+// One tile for TB tokens: the NRW rows row0 .. row0 + NRW - 1 of a stage of
+// NR rows (the warp's row group) against the lane's slice of the
+// activations; lane partials reduced per block of NRS rows and written to
+// this warp's row of the reduction buffer (index row * TB + token).
+template <int BITS, int XPL, int NR, int NRW, int TB, int TBMAX>
 __device__ __forceinline__ void tile_compute(uint32_t stage, int rowbytes, int G, int gi,
-                                             uint32_t lane_off,
+                                             uint32_t lane_off, int row0,
                                              const f32x2_t (&xp)[TBMAX][XPL / 2],
                                              float *red_w, int lane) {
-  constexpr int NRS = (NR * TB <= 32) ? NR : 32 / TB;
-  constexpr int V = NRS * TB;
-  constexpr int LV = log2c<V>();
-  const uint32_t sc0 = stage + NR * rowbytes + 4 * gi;
-  const uint32_t zp0 = sc0 + NR * G * 4;
-#pragma unroll
-  for (int sb = 0; sb < NR; sb += NRS) {
-    float v[V];
-#pragma unroll
-    for (int r = 0; r < NRS; ++r) {
-      const int row = sb + r;
-      const float s = lds_f32(sc0 + row * G * 4);
-      const float zf = static_cast<float>(lds_s32(zp0 + row * G * 4));
-      float d[TB];
-      row_dot<BITS, XPL, TB, TBMAX>(stage + row * rowbytes + lane_off, zf, xp, d);
-#pragma unroll
-      for (int t = 0; t < TB; ++t) v[r * TB + t] = s * d[t];
-    }
-    bfly<V, 16>(v, lane);
-    if ((lane & ((32 >> LV) - 1)) == 0) red_w[sb * TB + (lane >> (5 - LV))] = v[0];
-  }
-}
-
-// This lane's activation slice of up to TBMAX rows: rows[t] for t < T,
-// zeros after.  INT4 keeps odd columns divided by 16 (see row_dot).
-template <int BITS, int XPL, bool XBF16, int TBMAX>
-__device__ __forceinline__ void load_x(const void *const (&rows)[TBMAX], int T, int col0,
-                                       f32x2_t (&xp)[TBMAX][XPL / 2]) {
-  const float odd = BITS == 4 ? 0.0625f : 1.0f;
-#pragma unroll
-  for (int t = 0; t < TBMAX; ++t) {
-    float v[XPL];
-    if (t < T) {
-      if constexpr (XBF16) {
-        const uint4 *p = reinterpret_cast<const uint4 *>(
-            static_cast<const uint16_t *>(rows[t]) + col0);
-#pragma unroll
-        for (int c = 0; c < XPL / 8; ++c) {
-          const uint4 u = __ldg(p + c);
-          const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-          for (int h = 0; h < 4; ++h) {
-            v[8 * c + 2 * h] = __uint_as_float(wv[h] << 16);
-            v[8 * c + 2 * h + 1] = __uint_as_float(wv[h] & 0xFFFF0000u);
-          }
-        }
-      } else {
-        const float4 *p = reinterpret_cast<const float4 *>(static_cast<const float *>(rows[t]) + col0);
-#pragma unroll
-        for (int c = 0; c < XPL / 4; ++c) {
-          const float4 f = __ldg(p + c);
-          v[4 * c] = f.x;
-          v[4 * c + 1] = f.y;
-          v[4 * c + 2] = f.z;
-          v[4 * c + 3] = f.w;
-        }
-      }
-    } else {
-#pragma unroll
-      for (int c = 0; c < XPL; ++c) v[c] = 0.0f;
-    }
-#pragma unroll
-    for (int p = 0; p < XPL / 2; ++p) xp[t][p] = pack2(v[2 * p], v[2 * p + 1] * odd);
-  }
-}
-
-// ------------------------------------------------- integer dot-product form
-//
-// Used by the two-row configuration (the routed experts of decode batches).
-// The lane's slice of each activation row is held in 22-bit fixed point:
-// x = X 2^-F, F chosen per row and lane slice so that |X| < 2^22 (relative
-// representation error <= 2^-22 of the slice's largest |x|), split into
-// bytes X = L2 2^16 + L1 2^8 + L0 (L0, L1 unsigned, L2 signed).  Byte dot
-// products (dp4a) of the codes q with each byte plane are exact integers, so
-//   sum_k (q_k - zp) x_k = 2^-F (sum_i 2^8i A_i - zp SX),
-// A_i = sum_k q_k L_i,k and SX = sum_k X_k, with only the final combination
-// rounded.  This replaces the per-code byte permute, subtract and FMA of the
-// fp32 form by three byte products per four codes (and per token).
-
-__device__ __forceinline__ uint32_t dp4a_uu(uint32_t a, uint32_t b, uint32_t c) {
-  uint32_t d;
-  asm("dp4a.u32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
-  return d;
-}
-
-__device__ __forceinline__ int32_t dp4a_us(uint32_t a, uint32_t b, int32_t c) {
-  int32_t d;
-  asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
-  return d;
-}
-
-// Byte planes of this lane's slice of up to TBMAX activation rows.  Word w
-// of plane i holds, for INT8, bytes of columns 4w .. 4w+3; for INT4, word 2j
-// the even columns 8j, 8j+2, 8j+4, 8j+6 and word 2j+1 the odd ones (the
-// columns of the low and high nibbles of code word j).
-template <int BITS, int XPL, bool XBF16, int TBMAX>
-__device__ __forceinline__ void load_x_int(const void *const (&rows)[TBMAX], int T, int col0,
-                                           uint32_t (&xl)[TBMAX][3][XPL / 4],
-                                           float (&sxf)[TBMAX], float (&xsc)[TBMAX]) {
-#pragma unroll
-  for (int t = 0; t < TBMAX; ++t) {
-    float v[XPL];
-    if (t < T) {
-      if constexpr (XBF16) {
-        const uint4 *p = reinterpret_cast<const uint4 *>(
-            static_cast<const uint16_t *>(rows[t]) + col0);
-#pragma unroll
-        for (int c = 0; c < XPL / 8; ++c) {
-          const uint4 u = __ldg(p + c);
-          const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-          for (int h = 0; h < 4; ++h) {
-            v[8 * c + 2 * h] = __uint_as_float(wv[h] << 16);
-            v[8 * c + 2 * h + 1] = __uint_as_float(wv[h] & 0xFFFF0000u);
-          }
-        }
-      } else {
-        const float4 *p = reinterpret_cast<const float4 *>(static_cast<const float *>(rows[t]) + col0);
-#pragma unroll
-        for (int c = 0; c < XPL / 4; ++c) {
-          const float4 f = __ldg(p + c);
-          v[4 * c] = f.x;
-          v[4 * c + 1] = f.y;
-          v[4 * c + 2] = f.z;
-          v[4 * c + 3] = f.w;
-        }
-      }
-    } else {
-#pragma unroll
-      for (int c = 0; c < XPL; ++c) v[c] = 0.0f;
-    }
-    float mx = 0.0f;
-#pragma unroll
-    for (int c = 0; c < XPL; ++c) mx = fmaxf(mx, fabsf(v[c]));
-    // F = 21 - floor(log2 mx) puts mx 2^F in [2^21, 2^22); exponents are
-    // read from the bits (power-of-two scalings are exact).
-    const int e = mx > 0.0f ? ((__float_as_int(mx) >> 23) & 0xFF) - 127 : 0;
-    const int F = max(-126, min(127, 21 - e));
-    const float up = __int_as_float((F + 127) << 23);
-    xsc[t] = F <= 126 ? __int_as_float((127 - F) << 23) : 0.0f;  // 2^-F
-    int32_t X[XPL];
-#pragma unroll
-    for (int c = 0; c < XPL; ++c) X[c] = __float2int_rn(v[c] * up);
-    int32_t sx[3] = {0, 0, 0};
-#pragma unroll
-    for (int c = 0; c < XPL; ++c) {
-      sx[0] += X[c] & 0xFF;
-      sx[1] += (X[c] >> 8) & 0xFF;
-      sx[2] += X[c] >> 16;
-    }
-    sxf[t] = fmaf(static_cast<float>(sx[2]), 65536.0f,
-                  fmaf(static_cast<float>(sx[1]), 256.0f, static_cast<float>(sx[0])));
-#pragma unroll
-    for (int w = 0; w < XPL / 4; ++w) {
-      int c0, st;  // first column and column step of the four bytes of word w
-      if constexpr (BITS == 4) {
-        c0 = 8 * (w >> 1) + (w & 1);
-        st = 2;
-      } else {
-        c0 = 4 * w;
-        st = 1;
-      }
-#pragma unroll
-      for (int i = 0; i < 3; ++i) {
-        uint32_t word = 0;
-#pragma unroll
-        for (int b = 0; b < 4; ++b)
-          word |= (static_cast<uint32_t>(X[c0 + st * b] >> (8 * i)) & 0xFFu) << (8 * b);
-        xl[t][i][w] = word;
-      }
-    }
-  }
-}
-
-// Integer dot products of this lane's XPL codes of one row with TB rows,
-// returned as (sum_k (q_k - zp) x_k) / s.
-template <int BITS, int XPL, int TB, int TBMAX>
-__device__ __forceinline__ void row_dot_int(uint32_t caddr, float zf,
-                                            const uint32_t (&xl)[TBMAX][3][XPL / 4],
-                                            const float (&sxf)[TBMAX], const float (&xsc)[TBMAX],
-                                            float (&d)[TB]) {
-  uint32_t a0[TB], a1[TB];
-  int32_t a2[TB];
-#pragma unroll
-  for (int t = 0; t < TB; ++t) {
-    a0[t] = a1[t] = 0u;
-    a2[t] = 0;
-  }
-  constexpr int NW = XPL * BITS / 32;  // code words per lane per row
-  uint32_t w[NW];
-  if constexpr (NW == 8) {
-    const uint4 v0 = lds128(caddr), v1 = lds128(caddr + 16);
-    w[0] = v0.x;
-    w[1] = v0.y;
-    w[2] = v0.z;
-    w[3] = v0.w;
-    w[4] = v1.x;
-    w[5] = v1.y;
-    w[6] = v1.z;
-    w[7] = v1.w;
-  } else if constexpr (NW == 4) {
-    const uint4 v = lds128(caddr);
-    w[0] = v.x;
-    w[1] = v.y;
-    w[2] = v.z;
-    w[3] = v.w;
-  } else if constexpr (NW == 2) {
-    const uint2 v = lds64(caddr);
-    w[0] = v.x;
-    w[1] = v.y;
-  } else {
-    w[0] = lds32(caddr);
-  }
-#pragma unroll
-  for (int j = 0; j < NW; ++j) {
-    if constexpr (BITS == 4) {
-      const uint32_t lo = w[j] & 0x0F0F0F0Fu, hi = (w[j] >> 4) & 0x0F0F0F0Fu;
-#pragma unroll
-      for (int t = 0; t < TB; ++t) {
-        a0[t] = dp4a_uu(hi, xl[t][0][2 * j + 1], dp4a_uu(lo, xl[t][0][2 * j], a0[t]));
-        a1[t] = dp4a_uu(hi, xl[t][1][2 * j + 1], dp4a_uu(lo, xl[t][1][2 * j], a1[t]));
-        a2[t] = dp4a_us(hi, xl[t][2][2 * j + 1], dp4a_us(lo, xl[t][2][2 * j], a2[t]));
-      }
-    } else {
-      const uint32_t u = w[j] ^ 0x80808080u;  // stored q - 128 -> q
-#pragma unroll
-      for (int t = 0; t < TB; ++t) {
-        a0[t] = dp4a_uu(u, xl[t][0][j], a0[t]);
-        a1[t] = dp4a_uu(u, xl[t][1][j], a1[t]);
-        a2[t] = dp4a_us(u, xl[t][2][j], a2[t]);
-      }
-    }
-  }
-  // a0 + 2^8 a1 < 2^31 always (XPL <= 64); for INT4 (codes <= 15) the whole
-  // sum a0 + 2^8 a1 + 2^16 a2 stays inside int32 for XPL <= 32, so a single
-  // conversion (one rounding, as before) suffices.
-#pragma unroll
-  for (int t = 0; t < TB; ++t) {
-    const int32_t a01 = static_cast<int32_t>(a0[t] + (a1[t] << 8));
-    float q;
-    if constexpr (BITS == 4) {
-      static_assert(XPL <= 32, "INT4 plane sums must fit in int32");
-      q = static_cast<float>(a01 + a2[t] * 65536);
-    } else {
-      static_assert(XPL <= 64, "INT8 plane sums a0 + 2^8 a1 must fit in int32");
-      q = fmaf(static_cast<float>(a2[t]), 65536.0f, static_cast<float>(a01));
-    }
-    d[t] = fmaf(-zf, sxf[t], q) * xsc[t];
-  }
-}
-
-// tile_compute for the integer form, over the NRW rows row0 .. row0 + NRW - 1
-// of a stage of NR rows (the warp's row group).
-template <int BITS, int XPL, int NR, int NRW, int TB, int TBMAX>
-__device__ __forceinline__ void tile_compute_int(uint32_t stage, int rowbytes, int G, int gi,
-                                                 uint32_t lane_off, int row0,
-                                                 const uint32_t (&xl)[TBMAX][3][XPL / 4],
-                                                 const float (&sxf)[TBMAX],
-                                                 const float (&xsc)[TBMAX], float *red_w,
-                                                 int lane) {
   constexpr int NRS = (NRW * TB <= 32) ? NRW : 32 / TB;
   constexpr int V = NRS * TB;
   constexpr int LV = log2c<V>();
@@ -451,7 +206,382 @@ __device__ __forceinline__ void tile_compute_int(uint32_t stage, int rowbytes, i
       const float s = lds_f32(sc0 + row * G * 4);
       const float zf = static_cast<float>(lds_s32(zp0 + row * G * 4));
       float d[TB];
-      row_dot_int<BITS, XPL, TB, TBMAX>(stage + row * rowbytes + lane_off, zf, xl, sxf, xsc, d);
+      row_dot<BITS, XPL, TB, TBMAX>(stage + row * rowbytes + lane_off, zf, xp, d);
+#pragma unroll
+      for (int t = 0; t < TB; ++t) v[r * TB + t] = s * d[t];
+    }
+    bfly<V, 16>(v, lane);
+    if ((lane & ((32 >> LV) - 1)) == 0) red_w[sb * TB + (lane >> (5 - LV))] = v[0];
+  }
+}
+
+// This lane's activation slice of up to TBMAX rows: rows[t] for t < T,
+// zeros after.  INT4 keeps odd columns divided by 16 (see row_dot).
+// The XPL activations of this lane's slice of one row as fp32 (bf16 is
+// widened exactly); zeros when `use` is false (a token slot past the pass).
+template <bool XBF16, int XPL>
+__device__ __forceinline__ void load_slice(const void *row, bool use, int col0, float (&v)[XPL]) {
+  if (use) {
+    if constexpr (XBF16) {
+      const uint4 *p = reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(row) + col0);
+#pragma unroll
+      for (int c = 0; c < XPL / 8; ++c) {
+        const uint4 u = __ldg(p + c);
+        const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          v[8 * c + 2 * h] = __uint_as_float(wv[h] << 16);
+          v[8 * c + 2 * h + 1] = __uint_as_float(wv[h] & 0xFFFF0000u);
+        }
+      }
+    } else {
+      const float4 *p = reinterpret_cast<const float4 *>(static_cast<const float *>(row) + col0);
+#pragma unroll
+      for (int c = 0; c < XPL / 4; ++c) {
+        const float4 f = __ldg(p + c);
+        v[4 * c] = f.x;
+        v[4 * c + 1] = f.y;
+        v[4 * c + 2] = f.z;
+        v[4 * c + 3] = f.w;
+      }
+    }
+  } else {
+#pragma unroll
+    for (int c = 0; c < XPL; ++c) v[c] = 0.0f;
+  }
+}
+
+template <int BITS, int XPL, bool XBF16, int TBMAX>
+__device__ __forceinline__ void load_x(const void *const (&rows)[TBMAX], int T, int col0,
+                                       f32x2_t (&xp)[TBMAX][XPL / 2]) {
+  const float odd = BITS == 4 ? 0.0625f : 1.0f;
+#pragma unroll
+  for (int t = 0; t < TBMAX; ++t) {
+    float v[XPL];
+    load_slice<XBF16, XPL>(rows[t], t < T, col0, v);
+#pragma unroll
+    for (int p = 0; p < XPL / 2; ++p) xp[t][p] = pack2(v[2 * p], v[2 * p + 1] * odd);
+  }
+}
+
+__device__ __forceinline__ int32_t dp4a_us(uint32_t a, uint32_t b, int32_t c) {
+  int32_t d;
+  asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
+// ------------------------------------------- balanced-digit integer form
+//
+// Each activation of the lane's slice is held as one 38-bit integer,
+// x = X 2^-F with F chosen so that the slice's largest |x| times 2^F lies in
+// [2^37, 2^38): every activation within 2^14 of the slice's largest is exact
+// (its fp32 ulp is a multiple of 2^-F) and every other one is within
+// 2^-38 of the largest.  X is split into five balanced byte digits,
+// X = sum_i L_i 2^8i with L_i in [-128, 127] (each digit is the residue of
+// the remaining value in [-128, 128) and the next one takes the carry), so
+// that a small |X| has small digits and the zero digits of a small value stay
+// zero.  Per row, with the codes centred (INT8: the stored q - 128; INT4: the
+// nibble q) and z' the zero point centred the same way,
+//   c_i = sum_k (q_k - zp) L_i,k = sum_k q'_k L_i,k - z' sum_k L_i,k
+// is an exact 32-bit integer (one signed byte dot product per four codes and
+// digit, the zero point applied once per digit), and
+//   sum_k (q_k - zp) x_k = 2^-F sum_i 256^i c_i
+// is formed in fp32 from the most significant digit down (Horner's rule, one
+// rounding per step).  Balanced digits keep every partial sum within twice
+// sum_k |(q_k - zp) X_k|, so the rounding stays relative to the terms of
+// the dot product itself however strongly its terms cancel.  A zero point
+// beyond +-2^17 of the centre (single-signed groups far from zero) forms the
+// c_i in 64 bits instead.
+
+constexpr int kDigits = 5;
+// A slice whose largest |x| exceeds this many times the mean |x| of the
+// warp's columns makes the warp use all five digits.
+constexpr float kWideRatio = 128.0f;
+
+__device__ __forceinline__ int32_t dp4a_ss(uint32_t a, uint32_t b, int32_t c) {
+  int32_t d;
+  asm("dp4a.s32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
+// Shared-memory address of 16-byte unit u of low digit p (0 or 1) of row t
+// in this warp's low-digit area: consecutive lanes hold consecutive units,
+// so a warp's 16-byte accesses are free of bank conflicts.
+template <int XPL, int TBMAX>
+__device__ __forceinline__ uint32_t low_addr(uint32_t low, int t, int p, int u, int lane) {
+  constexpr int NU = XPL / 16;  // 16-byte units per digit and row
+  return low + static_cast<uint32_t>((((t * 2 + p) * NU + u) * 32 + lane) * 16);
+}
+
+__device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
+  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y),
+               "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
+// Fills the digit planes of this lane's slice of up to TBMAX rows (zeros
+// after T) and returns, the same in every lane of the warp, whether some
+// lane's slice of some row is wide: its largest |x| more than kWideRatio
+// times the mean |x| over the warp's columns of that row.  X is formed as
+// X = 2^16 Xh + Xl with Xh = round(x 2^(F-16)) (22 bits) and Xl the rounded
+// remainder (|Xl| <= 2^15), so all arithmetic stays in 32 bits; the two low
+// digits (from Xl, with their carry into Xh) are formed only when the warp
+// needs them.
+template <int BITS, int XPL, bool XBF16, int TBMAX>
+__device__ __forceinline__ bool load_x_digits(const void *const (&rows)[TBMAX], int T, int col0,
+                                              uint32_t (&xl)[TBMAX][3][XPL / 4],
+                                              uint32_t low, int lane,
+                                              int32_t (&sl)[TBMAX][kDigits],
+                                              float (&xsc)[TBMAX]) {
+  // raw slice words: XPL fp32 values, or XPL / 2 words of two bf16 each
+  // (expanded when used, which keeps fewer registers live)
+  constexpr int RW = XBF16 ? XPL / 2 : XPL;
+  auto val = [](const uint32_t (&raw)[RW], int c) {
+    if constexpr (XBF16)
+      return __uint_as_float((c & 1) ? (raw[c >> 1] & 0xFFFF0000u) : (raw[c >> 1] << 16));
+    else
+      return __uint_as_float(raw[c]);
+  };
+  // the lane's slice of row t (zeros for t >= T)
+  auto load = [&](int t, uint32_t (&raw)[RW]) {
+    if (t < T) {
+      const uint4 *p = reinterpret_cast<const uint4 *>(
+          static_cast<const uint8_t *>(rows[t]) + static_cast<int64_t>(col0) * (XBF16 ? 2 : 4));
+#pragma unroll
+      for (int c = 0; c < RW / 4; ++c) {
+        const uint4 u = __ldg(p + c);
+        raw[4 * c] = u.x;
+        raw[4 * c + 1] = u.y;
+        raw[4 * c + 2] = u.z;
+        raw[4 * c + 3] = u.w;
+      }
+    } else {
+#pragma unroll
+      for (int c = 0; c < RW; ++c) raw[c] = 0u;
+    }
+  };
+  float mxs[TBMAX];
+  bool wide = false;
+  uint32_t raw[TBMAX][RW];
+#pragma unroll
+  for (int t = 0; t < TBMAX; ++t) load(t, raw[t]);
+#pragma unroll
+  for (int t = 0; t < TBMAX; ++t) {
+    float mx = 0.0f, sa = 0.0f;
+#pragma unroll
+    for (int c = 0; c < XPL; ++c) {
+      mx = fmaxf(mx, fabsf(val(raw[t], c)));
+      sa += fabsf(val(raw[t], c));
+    }
+    mxs[t] = mx;
+    const float warp_sa = warp_sum(sa);  // sum of |x| over the warp's 32 XPL columns
+    wide = wide || mx * static_cast<float>(32 * XPL) > kWideRatio * warp_sa;
+    // an infinity reaches mx, a NaN the sum (fmaxf skips NaNs)
+    xsc[t] = (mx <= 3.40282347e38f && sa == sa) ? 0.0f : __int_as_float(0x7FC00000);
+  }
+  wide = __any_sync(0xFFFFFFFFu, wide);
+#pragma unroll
+  for (int t = 0; t < TBMAX; ++t) {
+    // F = 37 - floor(log2 mx) (exponent bits; power-of-two scalings exact)
+    const float mx = mxs[t];
+    const int e = mx > 0.0f ? ((__float_as_int(mx) >> 23) & 0xFF) - 127 : 0;
+    const int F = max(-110, min(126, 37 - e));
+    const float uph = __int_as_float((F - 16 + 127) << 23);  // 2^(F-16)
+    // 2^-F; a NaN or infinite activation makes the slice's results NaN, as
+    // they would be in fp32 arithmetic (its digits would be meaningless)
+    xsc[t] = xsc[t] == 0.0f ? __int_as_float((127 - F) << 23) : xsc[t];
+    int32_t sum[kDigits];
+#pragma unroll
+    for (int i = 0; i < kDigits; ++i) sum[i] = 0;
+    // word w holds, for INT8, columns 4w .. 4w + 3; for INT4, word 2j the
+    // even columns 8j, 8j + 2, 8j + 4, 8j + 6 and word 2j + 1 the odd ones
+#pragma unroll
+    // A balanced digit of v is the low byte of v read as a signed byte,
+    // d = v - 256 ((v + 128) >> 8), and the rest (v + 128) >> 8 carries on;
+    // the words hold the digits' low bytes (their two's complement).
+    auto pack4 = [](const int32_t (&v)[4]) {
+      return __byte_perm(__byte_perm(v[0], v[1], 0x0040), __byte_perm(v[2], v[3], 0x0040),
+                         0x5410);
+    };
+    uint32_t lw[2][4];  // the low digits' words, four at a time to shared memory
+#pragma unroll
+    for (int w = 0; w < XPL / 4; ++w) {
+      const int c0 = BITS == 4 ? 8 * (w >> 1) + (w & 1) : 4 * w;
+      const int st = BITS == 4 ? 2 : 1;
+      int32_t v2[4], v3[4], v4[4];
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        const float xs = val(raw[t], c0 + st * b) * uph;  // exact
+        int32_t xh = __float2int_rn(xs);                  // |xh| <= 2^22
+        if (wide) {
+          // remainder in units of 2^-F: |.| <= 2^15, exact in fp32
+          const int32_t xl16 = __float2int_rn((xs - static_cast<float>(xh)) * 65536.0f);
+          const int32_t c1 = (xl16 + 128) >> 8;   // in [-128, 128]
+          const int32_t c2 = (c1 + 128) >> 8;     // carry into xh: 0 or +-1
+          v2[b] = xl16;                            // digit 0 = low byte of xl16
+          v3[b] = c1;                              // digit 1 = low byte of c1
+          xh += c2;
+        }
+        v4[b] = xh;
+      }
+      if (wide) {
+        lw[0][w & 3] = pack4(v2);
+        lw[1][w & 3] = pack4(v3);
+        // a digit sum is the byte dot product of its word with ones
+        sum[0] = dp4a_ss(lw[0][w & 3], 0x01010101u, sum[0]);
+        sum[1] = dp4a_ss(lw[1][w & 3], 0x01010101u, sum[1]);
+        if ((w & 3) == 3) {
+#pragma unroll
+          for (int p = 0; p < 2; ++p)
+            sts128(low_addr<XPL, TBMAX>(low, t, p, w >> 2, lane),
+                   make_uint4(lw[p][0], lw[p][1], lw[p][2], lw[p][3]));
+        }
+      }
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        const int32_t xh = v4[b];
+        const int32_t c3 = (xh + 128) >> 8;
+        const int32_t c4 = (c3 + 128) >> 8;   // the top digit, |.| <= 65
+        v2[b] = xh;
+        v3[b] = c3;
+        v4[b] = c4;
+      }
+      xl[t][0][w] = pack4(v2);
+      xl[t][1][w] = pack4(v3);
+      xl[t][2][w] = pack4(v4);
+#pragma unroll
+      for (int i = 0; i < 3; ++i) sum[i + 2] = dp4a_ss(xl[t][i][w], 0x01010101u, sum[i + 2]);
+    }
+#pragma unroll
+    for (int i = 0; i < kDigits; ++i) sl[t][i] = sum[i];
+  }
+  return wide;
+}
+
+// Exact digit sums c_i = a_i - z' SL_i of one row and token, combined into
+// sum_k (q_k - zp) X_k in fp32 from the top digit down (digits D0..4).
+template <int D0>
+__device__ __forceinline__ float combine_digits(const int32_t (&a)[kDigits], int32_t zc,
+                                                const int32_t (&sl)[kDigits]) {
+  // Bounds (XPL <= 32): |a_i| <= 32 * 255 * 128 < 2^21, |sum L_i| <= 2^12,
+  // |sum (L_i + 256 L_i+1)| <= 2^20.  With |z'| <= 1024 the pairs
+  // c_i + 256 c_i+1 = (a_i + 256 a_i+1) - z' (sum L_i + 256 sum L_i+1) are
+  // exact in 32 bits (|.| < 2^31); otherwise every c_i is formed in 64 bits.
+  if (zc >= -1024 && zc <= 1024) {
+    // pairs of digits (2, 3) and (0, 1), then the top digit
+    const int32_t c4 = a[4] - zc * sl[4];
+    const int32_t c23 = (a[2] + 256 * a[3]) - zc * (sl[2] + 256 * sl[3]);
+    float f = fmaf(static_cast<float>(c4), 65536.0f, static_cast<float>(c23));
+    if constexpr (D0 == 0) {
+      const int32_t c01 = (a[0] + 256 * a[1]) - zc * (sl[0] + 256 * sl[1]);
+      f = fmaf(f, 65536.0f, static_cast<float>(c01));
+    }
+    return f;
+  }
+  float cf[kDigits];
+#pragma unroll
+  for (int i = D0; i < kDigits; ++i)
+    cf[i] = __ll2float_rn(static_cast<int64_t>(a[i]) - static_cast<int64_t>(zc) * sl[i]);
+  float f = cf[kDigits - 1];
+#pragma unroll
+  for (int i = kDigits - 2; i >= D0; --i) f = fmaf(f, 256.0f, cf[i]);
+  return f;
+}
+
+// Balanced-digit dot products of this lane's XPL codes of one row with TB
+// rows, returned as sum_k (q_k - zp) x_k.  The three top digits (held in
+// registers) serve every row; a wide warp adds the two low digits (from
+// shared memory), one row at a time.
+template <bool WIDE, int BITS, int XPL, int TB, int TBMAX>
+__device__ __forceinline__ void row_dot_digits(uint32_t caddr, int32_t zp,
+                                               const uint32_t (&xl)[TBMAX][3][XPL / 4],
+                                               uint32_t low, int lane,
+                                               const int32_t (&sl)[TBMAX][kDigits],
+                                               const float (&xsc)[TBMAX], float (&d)[TB]) {
+  static_assert(XPL <= 32, "digit sums must fit in 32 bits");
+  constexpr int NW = XPL * BITS / 32;  // code words per lane per row
+  uint32_t w[NW];
+  lds_words<NW>(caddr, w);
+  const int32_t zc = BITS == 8 ? zp - 128 : zp;
+  // one code word against one digit word (INT4: the word's low nibbles
+  // against the even columns' digits, its high nibbles against the odd ones)
+  auto dot = [&](int j, const uint32_t *dw, int32_t acc) {
+    if constexpr (BITS == 4) {
+      const uint32_t lo = w[j] & 0x0F0F0F0Fu, hi = (w[j] >> 4) & 0x0F0F0F0Fu;
+      return dp4a_us(hi, dw[2 * j + 1], dp4a_us(lo, dw[2 * j], acc));
+    } else {
+      return dp4a_ss(w[j], dw[j], acc);  // the stored bytes are the centred codes q - 128
+    }
+  };
+  if constexpr (!WIDE) {
+    int32_t a[TB][kDigits];
+#pragma unroll
+    for (int t = 0; t < TB; ++t)
+#pragma unroll
+      for (int i = 0; i < kDigits; ++i) a[t][i] = 0;
+#pragma unroll
+    for (int j = 0; j < NW; ++j)
+#pragma unroll
+      for (int t = 0; t < TB; ++t)
+#pragma unroll
+        for (int i = 0; i < 3; ++i) a[t][i + 2] = dot(j, xl[t][i], a[t][i + 2]);
+#pragma unroll
+    for (int t = 0; t < TB; ++t)
+      // the top three digits are X rounded to a multiple of 2^16 (balanced
+      // digits: the dropped |L1 2^8 + L0| is at most 2^15 + 2^7)
+      d[t] = combine_digits<2>(a[t], zc, sl[t]) * (xsc[t] * 65536.0f);
+  } else {
+#pragma unroll
+    for (int t = 0; t < TB; ++t) {
+      int32_t a[kDigits] = {0, 0, 0, 0, 0};
+#pragma unroll
+      for (int j = 0; j < NW; ++j)
+#pragma unroll
+        for (int i = 0; i < 3; ++i) a[i + 2] = dot(j, xl[t][i], a[i + 2]);
+#pragma unroll
+      for (int p = 0; p < 2; ++p) {
+        uint32_t lw[XPL / 4];
+#pragma unroll
+        for (int u = 0; u < XPL / 16; ++u) {
+          const uint4 v = lds128(low_addr<XPL, TBMAX>(low, t, p, u, lane));
+          lw[4 * u] = v.x;
+          lw[4 * u + 1] = v.y;
+          lw[4 * u + 2] = v.z;
+          lw[4 * u + 3] = v.w;
+        }
+#pragma unroll
+        for (int j = 0; j < NW; ++j) a[p] = dot(j, lw, a[p]);
+      }
+      d[t] = combine_digits<0>(a, zc, sl[t]) * xsc[t];
+    }
+  }
+}
+
+template <bool WIDE, int BITS, int XPL, int NR, int NRW, int TB, int TBMAX>
+__device__ __forceinline__ void tile_compute_digits(uint32_t stage, int rowbytes, int G, int gi,
+                                                    uint32_t lane_off, int row0,
+                                                    const uint32_t (&xl)[TBMAX][3][XPL / 4],
+                                                    uint32_t low,
+                                                    const int32_t (&sl)[TBMAX][kDigits],
+                                                    const float (&xsc)[TBMAX], float *red_w,
+                                                    int lane) {
+  // at most 16 row x token values per butterfly (fewer live registers)
+  constexpr int NRS = (NRW * TB <= 16) ? NRW : 16 / TB;
+  constexpr int V = NRS * TB;
+  constexpr int LV = log2c<V>();
+  const uint32_t sc0 = stage + NR * rowbytes + 4 * gi;
+  const uint32_t zp0 = sc0 + NR * G * 4;
+#pragma unroll
+  for (int sb = 0; sb < NRW; sb += NRS) {
+    float v[V];
+#pragma unroll
+    for (int r = 0; r < NRS; ++r) {
+      const int row = row0 + sb + r;
+      const float s = lds_f32(sc0 + row * G * 4);
+      const int32_t zp = lds_s32(zp0 + row * G * 4);
+      float d[TB];
+      row_dot_digits<WIDE, BITS, XPL, TB, TBMAX>(stage + row * rowbytes + lane_off, zp, xl, low,
+                                                 lane, sl, xsc, d);
 #pragma unroll
       for (int t = 0; t < TB; ++t) v[r * TB + t] = s * d[t];
     }
@@ -502,7 +632,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<TBMAX>::kCtas) smallm_kernel(con
   // only after its own wait), and only its activations (h) come from the
   // gate/up kernel.
   if constexpr (MODE == kGateUp) pdl_enter();
-  static_assert(KW == kCW || (KW < kCW && TBMAX <= 2), "row groups need the integer form");
+  static_assert(KW == kCW || (KW < kCW && TBMAX <= 2), "row groups: one or two rows per pass");
   using C = Cfg<TBMAX>;
   constexpr int STAGES = C::kStages, RED = C::kRedMax;
   constexpr int NR = rows_per_tile<BITS, XPL * KW / kCW>();
@@ -517,7 +647,8 @@ __global__ void __launch_bounds__(kThreads, Cfg<TBMAX>::kCtas) smallm_kernel(con
   volatile int *abort_flag = &abort_s;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   float *red = reinterpret_cast<float *>(smem + C::kRingBytes);
-  int32_t *s_active = reinterpret_cast<int32_t *>(smem + C::kRingBytes + C::kRedBytes);
+  int32_t *s_active =
+      reinterpret_cast<int32_t *>(smem + C::kRingBytes + C::kRedBytes + C::kLowBytes);
   int32_t *s_off = s_active + a.E;
   int32_t *s_cs = s_off + a.E + 1;
   int32_t *s_idx = s_cs + a.E + 1;   // in-CTA grouping: expert of each assignment
@@ -767,13 +898,53 @@ __global__ void __launch_bounds__(kThreads, Cfg<TBMAX>::kCtas) smallm_kernel(con
   const int gi = col0 / a.group;
   const uint32_t lane_off = static_cast<uint32_t>(kslot * LB);
   const int row0 = (warp / KW) * NRG;         // first stage row of this warp's group
-  // Activation slices: fp32 pairs (eight rows per pass) or the byte planes
-  // of the integer form (two rows per pass).
-  constexpr bool kInt = TBMAX <= 2;
-  f32x2_t xp[kInt ? 1 : TBMAX][XPL / 2];
-  uint32_t xl[kInt ? TBMAX : 1][3][XPL / 4];
-  float sxf[kInt ? TBMAX : 1], xsc[kInt ? TBMAX : 1];
+  // Activation slices: the balanced digits (one or two rows per pass) or
+  // fp32 pairs (eight rows per pass).
+  constexpr bool kD = TBMAX <= 2;
+  f32x2_t xp[kD ? 1 : TBMAX][XPL / 2];
+  uint32_t xl[kD ? TBMAX : 1][3][XPL / 4];  // the three top digits
+  // this warp's area for the two low digits
+  const uint32_t low = ring + C::kRingBytes + C::kRedBytes + warp * (C::kLowBytes / kCW);
+  float xsc[kD ? TBMAX : 1];
+  int32_t sld[kD ? TBMAX : 1][kDigits];
+  bool wide = false;  // digit form: this warp's slices need all five digits
   int cur_s = -1, cur_b = -1;
+  // The activations of pass b of segment s, in this lane's slice (every lane
+  // of the CTA takes part: the digit form reduces over the warp).
+  auto load_act = [&](int s, int b) {
+    const int e = s_active[s];
+    const int p0 = s_off[e];
+    const int t0 = b * TBMAX;
+    const int Tb = min(TBMAX, s_off[e + 1] - p0 - t0);
+    const void *xr[TBMAX];
+#pragma unroll
+    for (int t = 0; t < TBMAX; ++t) {
+      const int64_t tt = t0 + (t < Tb ? t : 0);
+      if constexpr (MODE == kLinear) {
+        xr[t] = XBF16 ? static_cast<const void *>(static_cast<const uint16_t *>(a.x) + tt * a.K)
+                      : static_cast<const void *>(static_cast<const float *>(a.x) + tt * a.K);
+      } else if constexpr (MODE == kGateUp) {
+        const int64_t tok = (a.idx ? s_asg[p0 + tt] : a.ws.assign[p0 + tt]) / a.k;
+        xr[t] = XBF16 ? static_cast<const void *>(static_cast<const uint16_t *>(a.x) + tok * a.K)
+                      : static_cast<const void *>(static_cast<const float *>(a.x) + tok * a.K);
+      } else {
+        xr[t] = a.ws.h + (p0 + tt) * a.K;
+      }
+    }
+    if constexpr (kD)
+      wide = load_x_digits<BITS, XPL, (MODE != kDown) && XBF16, TBMAX>(xr, Tb, col0, xl, low, lane,
+                                                                        sld, xsc);
+    else
+      load_x<BITS, XPL, (MODE != kDown) && XBF16, TBMAX>(xr, Tb, col0, xp);
+    cur_s = s;
+    cur_b = b;
+  };
+  // The first pass's activations are read before the first weight stage is
+  // waited for, so that their latency overlaps the stage's copy.
+  {
+    const TileIt it0 = it_begin();
+    if (it0.valid) load_act(it0.s, it0.b);
+  }
   int64_t i = 0, pending = 0;
   bool stop = false;
   for (TileIt it = it_begin(); it.valid && !stop; it_next(it), ++i) {
@@ -783,8 +954,11 @@ __global__ void __launch_bounds__(kThreads, Cfg<TBMAX>::kCtas) smallm_kernel(con
     const int p0 = s_off[e];
     const int T = s_off[e + 1] - p0;
     const int st = static_cast<int>(i % STAGES);
-    const bool ok = wait_ok(smem_addr(&full_bar[st]), static_cast<uint32_t>((i / STAGES) & 1),
-                            a.status, abort_flag);
+    // warp-uniform, so that every lane takes part in the warp's shuffles
+    const bool ok = __all_sync(0xFFFFFFFFu,
+                               wait_ok(smem_addr(&full_bar[st]),
+                                       static_cast<uint32_t>((i / STAGES) & 1), a.status,
+                                       abort_flag));
     const uint32_t stage = ring + st * kStageBytes;
     const int64_t n0 = it.j * RT;
     const int t0 = b * TBMAX;
@@ -792,48 +966,45 @@ __global__ void __launch_bounds__(kThreads, Cfg<TBMAX>::kCtas) smallm_kernel(con
     const int TB = Tb <= 1 ? 1 : Tb <= 2 ? 2 : Tb <= 4 ? 4 : 8;
     float *red_w = red + (i & 1) * kCW * RED + warp * RED;
     if (ok) {
-      if (s != cur_s || b != cur_b) {
-        const void *xr[TBMAX];
-#pragma unroll
-        for (int t = 0; t < TBMAX; ++t) {
-          const int64_t tt = t0 + (t < Tb ? t : 0);
-          if constexpr (MODE == kLinear) {
-            xr[t] = XBF16 ? static_cast<const void *>(static_cast<const uint16_t *>(a.x) + tt * a.K)
-                          : static_cast<const void *>(static_cast<const float *>(a.x) + tt * a.K);
-          } else if constexpr (MODE == kGateUp) {
-            const int64_t tok = (a.idx ? s_asg[p0 + tt] : a.ws.assign[p0 + tt]) / a.k;
-            xr[t] = XBF16 ? static_cast<const void *>(static_cast<const uint16_t *>(a.x) + tok * a.K)
-                          : static_cast<const void *>(static_cast<const float *>(a.x) + tok * a.K);
-          } else {
-            xr[t] = a.ws.h + (p0 + tt) * a.K;
+      if (s != cur_s || b != cur_b) load_act(s, b);
+      if constexpr (kD) {
+        if (TBMAX == 1 || TB == 1) {
+          if (wide)
+            tile_compute_digits<true, BITS, XPL, NR, NRG, 1, TBMAX>(stage, rowbytes, G, gi, lane_off,
+                                                                    row0, xl, low, sld, xsc, red_w,
+                                                                    lane);
+          else
+            tile_compute_digits<false, BITS, XPL, NR, NRG, 1, TBMAX>(stage, rowbytes, G, gi,
+                                                                     lane_off, row0, xl, low, sld,
+                                                                     xsc, red_w, lane);
+        } else {
+          if constexpr (TBMAX >= 2) {
+            if (wide)
+              tile_compute_digits<true, BITS, XPL, NR, NRG, 2, TBMAX>(stage, rowbytes, G, gi,
+                                                                      lane_off, row0, xl, low, sld,
+                                                                      xsc, red_w, lane);
+            else
+              tile_compute_digits<false, BITS, XPL, NR, NRG, 2, TBMAX>(stage, rowbytes, G, gi,
+                                                                       lane_off, row0, xl, low,
+                                                                       sld, xsc, red_w, lane);
           }
         }
-        if constexpr (kInt)
-          load_x_int<BITS, XPL, (MODE != kDown) && XBF16, TBMAX>(xr, Tb, col0, xl, sxf, xsc);
-        else
-          load_x<BITS, XPL, (MODE != kDown) && XBF16, TBMAX>(xr, Tb, col0, xp);
-        cur_s = s;
-        cur_b = b;
-      }
-      if constexpr (kInt) {
-        if (TBMAX == 1 || TB == 1) {
-          tile_compute_int<BITS, XPL, NR, NRG, 1, TBMAX>(stage, rowbytes, G, gi, lane_off, row0, xl,
-                                                         sxf, xsc, red_w, lane);
-        } else {
-          if constexpr (TBMAX >= 2)
-            tile_compute_int<BITS, XPL, NR, NRG, 2, TBMAX>(stage, rowbytes, G, gi, lane_off, row0,
-                                                           xl, sxf, xsc, red_w, lane);
-        }
-      } else if (TB == 1) {
-        tile_compute<BITS, XPL, NR, 1, TBMAX>(stage, rowbytes, G, gi, lane_off, xp, red_w, lane);
-      } else if (TB == 2) {
-        tile_compute<BITS, XPL, NR, 2, TBMAX>(stage, rowbytes, G, gi, lane_off, xp, red_w, lane);
+      } else if (TBMAX == 1 || TB == 1) {
+        tile_compute<BITS, XPL, NR, NRG, 1, TBMAX>(stage, rowbytes, G, gi, lane_off, row0, xp, red_w,
+                                                   lane);
       } else {
+        if constexpr (TBMAX >= 2) {
+          if (TB == 2)
+            tile_compute<BITS, XPL, NR, NRG, 2, TBMAX>(stage, rowbytes, G, gi, lane_off, row0, xp,
+                                                       red_w, lane);
+        }
         if constexpr (TBMAX >= 8) {
           if (TB == 4)
-            tile_compute<BITS, XPL, NR, 4, TBMAX>(stage, rowbytes, G, gi, lane_off, xp, red_w, lane);
-          else
-            tile_compute<BITS, XPL, NR, 8, TBMAX>(stage, rowbytes, G, gi, lane_off, xp, red_w, lane);
+            tile_compute<BITS, XPL, NR, NRG, 4, TBMAX>(stage, rowbytes, G, gi, lane_off, row0, xp,
+                                                       red_w, lane);
+          else if (TB == 8)
+            tile_compute<BITS, XPL, NR, NRG, 8, TBMAX>(stage, rowbytes, G, gi, lane_off, row0, xp,
+                                                       red_w, lane);
         }
       }
     }
@@ -879,7 +1050,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<TBMAX>::kCtas) smallm_kernel(con
         } else if constexpr (MODE == kDown) {
           a.ws.out[pos * rows + n0 + r] = acc0;
         } else {
-          a.y[pos * rows + n0 + r] = acc0;
+          store_y(a.y, pos * rows + n0 + r, acc0, a.y_bf16);
         }
       }
     }
@@ -903,7 +1074,7 @@ cudaError_t run(const Args &a, cudaStream_t s) {
   return launch_pdl(k, dim3(Cfg<TBMAX>::kCtas * sm_count()), dim3(kThreads), smem, s, a);
 }
 
-// K = 4096: eight warps of 16 columns per lane.  K = 2048: the integer form
+// K = 4096: eight warps of 16 columns per lane.  K = 2048: the digit form
 // keeps 16 columns per lane (four warps per row, two row groups: half the
 // per-row reduction and conversion work per code of eight columns); the
 // eight-row fp32 form keeps eight warps of 8 columns (its activation rows
@@ -912,8 +1083,9 @@ template <int MODE, bool XBF16, int TBMAX>
 cudaError_t run_shape(const Args &a, cudaStream_t s) {
   const bool wide = a.K == 4096;
   if constexpr (TBMAX == 1) {
-    // routed experts, one token per pass: 32 columns per lane (K = 4096:
-    // four warps per row, two row groups; K = 2048: two warps, four groups)
+    // one row (linear) or token (routed experts) per pass: 32 columns per
+    // lane (K = 4096: four warps per row, two row groups; K = 2048: two
+    // warps, four groups)
     if (a.w0.bits == 4)
       return wide ? run<4, 32, 4, MODE, XBF16, TBMAX>(a, s) : run<4, 32, 2, MODE, XBF16, TBMAX>(a, s);
     return wide ? run<8, 32, 4, MODE, XBF16, TBMAX>(a, s) : run<8, 32, 2, MODE, XBF16, TBMAX>(a, s);
@@ -936,6 +1108,8 @@ cudaError_t run_class(int mode, bool x_bf16, const Args &a, cudaStream_t s) {
     if (mode == kGateUp)
       return x_bf16 ? run_shape<kGateUp, true, 1>(a, s) : run_shape<kGateUp, false, 1>(a, s);
     if (mode == kDown) return run_shape<kDown, false, 1>(a, s);
+    if (mode == kLinear)
+      return x_bf16 ? run_shape<kLinear, true, 1>(a, s) : run_shape<kLinear, false, 1>(a, s);
     return cudaErrorInvalidValue;
   } else {
     if (mode == kLinear)

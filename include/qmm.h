@@ -69,8 +69,10 @@ enum {
   QMM_DEV_WAIT_TIMEOUT = 1u, /* an asynchronous copy or MMA did not complete
                                 within the kernel's time limit; that kernel's
                                 output is incomplete                        */
-  QMM_DEV_BAD_EXPERT = 2u    /* topk_idx held an index outside [0, E); that
+  QMM_DEV_BAD_EXPERT = 2u,   /* topk_idx held an index outside [0, E); that
                                 assignment contributed nothing              */
+  QMM_DEV_EXPERT_OVERLOAD = 4u /* moe_route_load_stats found an expert chosen
+                                more often than its threshold             */
 };
 
 typedef void *qmm_stream_t; /* a cudaStream_t */
@@ -102,12 +104,43 @@ int qmm_quantize_groupwise(const float *w, int64_t N, int64_t K, int32_t bits,
 /*
  * Fused dequantise-matmul [P1 sections 3.2-3.3]:
  *   y[m, n] = sum_k x[m, k] * (q[n, k] - zp[n, k/g]) * s[n, k/g]
- * x: [M, K] fp32 or bf16 (x_dtype), y: [M, N] fp32.  The codes are
+ * x: [M, K] fp32 or bf16 (x_dtype), y: [M, N] fp32 or bf16 (y_dtype; a bf16
+ * output is the fp32 result rounded to nearest even).  The codes are
  * dequantised in registers inside the inner loop; accumulation in fp32.
- * M == 0 or N == 0 is a no-op.
+ * Error: fp32 rounding, of order 2^-24 relative to sum_k |x_k w^_k|; with one
+ * or two rows and K in {2048, 4096} (integer byte dot products of the codes
+ * with fixed-point activations) also the activations' representation: each
+ * lane's slice of 16 or 32 activations is held to 2^-22 of its largest |x|,
+ * or to 2^-38 when that largest exceeds 128 times the mean |x| around it (a
+ * "massive" channel).  The library's tests hold every output to
+ * 1e-5 * sum_k |x_k w^_k| + 1e-6.  A NaN or infinite activation gives NaN
+ * outputs.  M == 0 or N == 0 is a no-op.
  */
 int qmm_linear(const void *x, int32_t x_dtype, int64_t M, const qmm_weight *w,
-               float *y, qmm_stream_t stream);
+               void *y, int32_t y_dtype, qmm_stream_t stream);
+
+/*
+ * The same linear layer for batches of rows [P1 sections 3.2-3.3; P3: reusing
+ * each weight read for many tokens is the batched-prefill piece the pages'
+ * engines lack].  With bf16 activations, M >= 9, INT8 codes, group >= 64,
+ * K a multiple of 64 and K / group a multiple of 4, it runs on the tensor
+ * cores: each row of x is copied to fp16 scaled by the power of two that
+ * puts its largest |x| into [2^14, 2^15), each weight row is dequantised to
+ * fp16 with its own power-of-two scale (inexact zero points as
+ * (float)(q - zp) * s rounded once), fp32 accumulation, the K range split so
+ * that every SM gets work and the splits' partial sums added in a fixed
+ * order (results are reproducible bit for bit).  Accuracy: the fp16 operand
+ * rounding, a relative L2 error per row within 1e-2 of the exact result.
+ * Any other call is qmm_linear's (workspace unused).  N may be any positive
+ * size.  workspace: device scratch of at least
+ * qmm_linear_batched_workspace_bytes(M, w) bytes, 256-byte aligned (the fp16
+ * rows and, with more than one split, the partial sums).
+ */
+size_t qmm_linear_batched_workspace_bytes(int64_t M, const qmm_weight *w);
+
+int qmm_linear_batched(const void *x, int32_t x_dtype, int64_t M, const qmm_weight *w,
+                       void *y, int32_t y_dtype, void *workspace, size_t workspace_bytes,
+                       qmm_stream_t stream);
 
 /*
  * MoE router [P1 sections 3.4-3.5]:
@@ -123,7 +156,8 @@ int qmm_linear(const void *x, int32_t x_dtype, int64_t M, const qmm_weight *w,
  * expert.  x: [M, H] fp32 or bf16; w_router: [E, H] fp32; bias: [E] fp32 or
  * NULL.  workspace: device scratch of at least moe_route_workspace_bytes(M, E)
  * bytes (holds the logits), 256-byte aligned.  Requires 1 <= k <= min(E, 16),
- * E <= 1024, H % 4 == 0.
+ * E <= 1024, H % 4 == 0, M < 2^31 and H <= 2^24 (moe_route_workspace_bytes
+ * returns SIZE_MAX for sizes beyond these).
  */
 size_t moe_route_workspace_bytes(int64_t M, int32_t E);
 
@@ -168,8 +202,24 @@ size_t moe_ffn_workspace_bytes(int64_t M, int32_t k, const moe_experts *ex);
  * (y_dtype).  topk_idx / topk_w: [M, k] as produced by moe_route_topk.
  * workspace: device scratch of at least moe_ffn_workspace_bytes(M, k, ex)
  * bytes, 256-byte aligned; its contents on entry do not matter.
- * Every expert runs on the fp32 CUDA-core path (dequantisation in registers,
- * fp32 accumulation).
+ *
+ * Which arithmetic runs (all of it on the GPU):
+ *  - fp32 activations, any M, and bf16 activations with M <= 8 (decode): the
+ *    CUDA-core kernels, codes dequantised in registers, fp32 accumulation;
+ *    every output is within 1e-5 * sum |x w^| + 1e-6 per linear stage of the
+ *    exact result (propagated through SwiGLU and the weighted sum).
+ *  - bf16 activations with M > 8 and INT8 experts (batched prefill, H and I
+ *    multiples of 128, group >= 64): experts with three or more tokens run on
+ *    the tensor cores with fp16 operands and fp32 accumulation.  Each token
+ *    row, each SwiGLU row and each weight row is scaled by its own power of
+ *    two so that its largest magnitude lies in [2^14, 2^15) (no overflow,
+ *    fp16's full 11-bit precision for every value within 2^28 of its row's
+ *    largest, for tokens and weights of any fp32 magnitude); groups whose
+ *    zero point lies outside [-1793, 1024] (q - zp not exact in fp16) are
+ *    dequantised as (float)(q - zp) * s rounded once to fp16.  Accuracy: per
+ *    token row a relative L2 error within 1e-2 of the exact result (the
+ *    operands' fp16 rounding, about 2^-11 relative per value).  Experts
+ *    with one or two tokens in such a batch run on the CUDA-core kernels.
  */
 int moe_ffn_forward(const void *x, int32_t x_dtype, int64_t M,
                     const int32_t *topk_idx, const float *topk_w, int32_t k,
@@ -189,7 +239,9 @@ int moe_ffn_forward(const void *x, int32_t x_dtype, int64_t M,
  * QMM_NOALLOC_MAX_LOGITS fp32 values (1 MiB), which every GPU that loads the
  * library holds until the process exits; M * E above that limit returns
  * QMM_ERR_WORKSPACE.  The first call on a device looks up the array's device
- * address (one-time set-up; make that first call before any stream capture).
+ * address (one-time set-up; make that first call before any stream capture;
+ * after cudaDeviceReset the looked-up address is stale, so do not call this
+ * entry point again on a device the process has reset).
  * All calls on a device share the array and it keeps the last call's
  * contents (every value read is written first, so nothing needs clearing);
  * calls whose kernels may overlap on the GPU race on it.  Nothing here calls
@@ -201,6 +253,35 @@ int moe_route_topk_noalloc(const void *x, int32_t x_dtype, int64_t M, int64_t H,
                            const float *w_router, const float *bias, int32_t E,
                            int32_t k, int32_t *topk_idx, float *topk_w,
                            int32_t *expert_counts, qmm_stream_t stream);
+
+/*
+ * Routing load statistics [P1 section 3.5, last paragraph: grouped expert
+ * work degrades towards serial when one expert gets most tokens, so the
+ * engine checks how often each expert was chosen and warns above a
+ * threshold].  Reads expert_counts[E] (device, int32, e.g. the histogram
+ * moe_route_topk writes) and writes stats[4] (device, int64): the largest
+ * count, its expert (the lowest index among equal counts), the number of
+ * experts with at least one token and the sum of the counts (M * k for a
+ * histogram of M tokens and k slots).  The imbalance of the routing is
+ * stats[0] * stats[2] / stats[3] (largest over mean count per touched
+ * expert).  When the largest count exceeds `threshold`, QMM_DEV_EXPERT_OVERLOAD
+ * is set in the device status word.  Requires 1 <= E <= 1024; asynchronous on
+ * `stream`.
+ */
+int moe_route_load_stats(const int32_t *expert_counts, int32_t E, int64_t threshold,
+                         int64_t *stats, qmm_stream_t stream);
+
+/*
+ * Diagnostic of the library's bounded waits (no counterpart on the pages).
+ * Launches one kernel whose single thread waits on a barrier that nothing
+ * completes, using the same bounded wait as the library's kernels but with a
+ * limit of limit_ns (1 ns .. 10 s; the kernels themselves use 2 s).  When the
+ * limit passes, the wait gives up, QMM_DEV_WAIT_TIMEOUT is set in the device
+ * status word and the kernel returns; nothing else is in flight, so the
+ * device stays usable.  It shows that an expired wait is reported rather than
+ * hanging the GPU.
+ */
+int qmm_diag_wait_timeout(uint64_t limit_ns, qmm_stream_t stream);
 
 /* Message for the last non-zero return on this thread ("" if none). */
 const char *qmm_last_error(void);

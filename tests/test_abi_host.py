@@ -82,7 +82,7 @@ def _w(bits=8, group=64, N=128, K=256, codes=P, scales=P, zps=P):
 def test_linear_rejects(Lfake, kw, code):
     L = Lfake
     w = _w(**kw)
-    rc = L.qmm_linear(P2, q.QMM_F32, 1, ctypes.byref(w), P2, None)
+    rc = L.qmm_linear(P2, q.QMM_F32, 1, ctypes.byref(w), P2, q.QMM_F32, None)
     assert rc == code, q.qmm_last_error()
     assert q.qmm_last_error()
 
@@ -90,19 +90,19 @@ def test_linear_rejects(Lfake, kw, code):
 def test_linear_rejects_bad_dtype_and_x(Lfake):
     L = Lfake
     w = _w()
-    assert L.qmm_linear(P2, 7, 1, ctypes.byref(w), P2, None) == q.QMM_ERR_INVALID_ARG
-    assert L.qmm_linear(P2 + 4, q.QMM_F32, 1, ctypes.byref(w), P2, None) == q.QMM_ERR_ALIGN
-    assert L.qmm_linear(None, q.QMM_F32, 1, ctypes.byref(w), P2, None) == q.QMM_ERR_INVALID_ARG
-    assert L.qmm_linear(P2, q.QMM_F32, 1, None, P2, None) == q.QMM_ERR_INVALID_ARG
-    assert L.qmm_linear(P2, q.QMM_F32, -1, ctypes.byref(w), P2, None) == q.QMM_ERR_SHAPE
+    assert L.qmm_linear(P2, 7, 1, ctypes.byref(w), P2, q.QMM_F32, None) == q.QMM_ERR_INVALID_ARG
+    assert L.qmm_linear(P2 + 4, q.QMM_F32, 1, ctypes.byref(w), P2, q.QMM_F32, None) == q.QMM_ERR_ALIGN
+    assert L.qmm_linear(None, q.QMM_F32, 1, ctypes.byref(w), P2, q.QMM_F32, None) == q.QMM_ERR_INVALID_ARG
+    assert L.qmm_linear(P2, q.QMM_F32, 1, None, P2, q.QMM_F32, None) == q.QMM_ERR_INVALID_ARG
+    assert L.qmm_linear(P2, q.QMM_F32, -1, ctypes.byref(w), P2, q.QMM_F32, None) == q.QMM_ERR_SHAPE
 
 
 def test_linear_empty_is_noop(Lfake):
     L = Lfake
     w = _w()
-    assert L.qmm_linear(None, q.QMM_F32, 0, ctypes.byref(w), None, None) == q.QMM_OK
+    assert L.qmm_linear(None, q.QMM_F32, 0, ctypes.byref(w), None, q.QMM_F32, None) == q.QMM_OK
     w0 = _w(N=0)
-    assert L.qmm_linear(None, q.QMM_F32, 3, ctypes.byref(w0), None, None) == q.QMM_OK
+    assert L.qmm_linear(None, q.QMM_F32, 3, ctypes.byref(w0), None, q.QMM_F32, None) == q.QMM_OK
 
 
 def test_quantize_rejects(Lfake):
@@ -143,6 +143,29 @@ def test_router_rejects(Lfake):
     assert call(ws=None) == q.QMM_ERR_WORKSPACE
     assert call(ws=P2 + 16) == q.QMM_ERR_ALIGN
     assert call(M=0, x=None, idx=None, w=None) == q.QMM_OK
+    # sizes whose workspace or grid would not fit are refused before any
+    # product of them is formed
+    assert call(M=1 << 31) == q.QMM_ERR_UNSUPPORTED
+    assert call(M=(1 << 62) + 1) == q.QMM_ERR_UNSUPPORTED
+    assert call(H=(1 << 24) + 4) == q.QMM_ERR_UNSUPPORTED
+    assert q.moe_route_workspace_bytes(1 << 31, 256) == 2 ** 64 - 1
+    assert q.moe_route_workspace_bytes((1 << 62) + 1, 256) == 2 ** 64 - 1
+
+
+def test_noalloc_router_rejects(Lfake):
+    """The allocation-free router checks the built-in scratch size before it
+    touches the device: M * E beyond it, including an M whose product with E
+    would wrap around 64 bits, is refused."""
+    L = Lfake
+    f = L.moe_route_topk_noalloc
+    lim = q.QMM_NOALLOC_MAX_LOGITS
+    assert f(P, q.QMM_F32, lim // 256 + 1, 4096, P, None, 256, 6, P2, P2, None, None) == \
+        q.QMM_ERR_WORKSPACE
+    assert f(P, q.QMM_F32, (1 << 62) + 1, 4096, P, None, 256, 6, P2, P2, None, None) == \
+        q.QMM_ERR_WORKSPACE
+    assert f(P, q.QMM_F32, 2, 4096, P, None, 256, 17, P2, P2, None, None) == q.QMM_ERR_INVALID_ARG
+    assert f(P, q.QMM_F32, 2, 4094, P, None, 256, 6, P2, P2, None, None) == q.QMM_ERR_SHAPE
+    assert f(P + 8, q.QMM_F32, 2, 4096, P, None, 256, 6, P2, P2, None, None) == q.QMM_ERR_ALIGN
 
 
 def _experts(E=8, H=256, I=256, bits=4, group=64, **over):
@@ -237,8 +260,8 @@ int main(void) {
   qmm_weight w;
   memset(&w, 0, sizeof w);
   w.bits = 8; w.group = 64; w.N = 128; w.K = 256;
-  if (qmm_linear(NULL, QMM_F32, 0, &w, NULL, NULL) != QMM_OK) return 1;
-  if (qmm_linear(NULL, 7, 1, &w, NULL, NULL) != QMM_ERR_INVALID_ARG) return 2;
+  if (qmm_linear(NULL, QMM_F32, 0, &w, NULL, QMM_F32, NULL) != QMM_OK) return 1;
+  if (qmm_linear(NULL, 7, 1, &w, NULL, QMM_F32, NULL) != QMM_ERR_INVALID_ARG) return 2;
   if (strlen(qmm_last_error()) == 0) return 3;
   if (moe_route_workspace_bytes(8, 256) < (size_t)8 * 256 * 4) return 4;
   printf("ok %llu\n", (unsigned long long)qmm_launch_count());

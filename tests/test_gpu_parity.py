@@ -18,6 +18,7 @@ from synth import recipes
 import group_quantized_moe_gb300 as q
 from group_quantized_moe_gb300 import build_lib
 from parity_checks import assert_bf16_rows, assert_within
+import oracle_pool
 
 pytestmark = pytest.mark.gpu
 
@@ -535,7 +536,8 @@ def test_moe_decode_full_size(dev):
 @pytest.mark.slow
 def test_moe_prefill_full_size_sampled(dev):
     """Batched-prefill MoE at full size: M=512 bf16 tokens, Zipf-biased
-    routing, 256 experts INT8 g128; 4 sampled tokens through the oracle."""
+    routing, 256 experts INT8 g128; 64 or more tokens through the oracle,
+    covering every tensor-bound expert's token tiles."""
     r = recipes.CFG5
     x, xb = recipes.moe_x(r)
     wr, bias = recipes.moe_router(r)
@@ -545,9 +547,274 @@ def test_moe_prefill_full_size_sampled(dev):
     oidx, ow = oracle.topk(oracle.router_logits(x, wr, bias), r.k)
     np.testing.assert_array_equal(idx.cpu().numpy(), oidx)
     assert np.abs(w.cpu().numpy() - ow).max() <= 2e-6
+    # Tokens: for every expert with 64 or more tokens (the tensor-bound
+    # ones), its first and last token -- the last one sits in the expert's
+    # last, ragged 128-token tile -- and one from the middle of each further
+    # tile; then tokens of the lightest experts; then random ones, 64 or more
+    # in all.
+    toks = set()
+    for e in np.where(np.bincount(oidx.reshape(-1), minlength=r.E) >= 64)[0]:
+        mine = np.where((oidx == e).any(axis=1))[0]
+        toks.update(int(t) for t in mine[[0, -1]])
+        toks.update(int(mine[min(len(mine) - 1, 128 * j + 64)]) for j in range((len(mine) + 127) // 128))
+    counts = np.bincount(oidx.reshape(-1), minlength=r.E)
+    for e in np.where((counts > 0) & (counts <= 2))[0][:8]:
+        toks.add(int(np.where((oidx == e).any(axis=1))[0][0]))
+    rng = np.random.default_rng(5)
+    while len(toks) < 64:
+        toks.add(int(rng.integers(0, r.M)))
+    toks = np.array(sorted(toks))
+    yref, bound = oracle_pool.moe_tokens(r.name, toks, x[toks], oidx[toks], ow[toks], dw=2e-6)
     for ydt in (torch.float32, torch.bfloat16):
         y = q.moe_ffn_forward(xd, idx, w, ex, y_dtype=ydt).float().cpu().numpy()
-        toks = np.array([0, 137, 300, 511])
-        og, ou, od = _oracle_experts(r, oidx[toks].reshape(-1))
-        yref, bound = oracle.moe_ffn(x[toks], oidx[toks], ow[toks], og, ou, od, dw=2e-6)
-        assert_bf16_rows(y[toks], yref, f"prefill y={ydt}")
+        assert_bf16_rows(y[toks], yref, f"prefill y={ydt} ({len(toks)} tokens)")
+
+
+# ------------------------- activations with massive channels (wide slices)
+#
+# A few channels 1e3..1e5 times larger than the rest, and weight rows whose
+# dequantised weight at those channels is exactly zero (a zero weight
+# quantises to q = zp): those rows' outputs get nothing from the large
+# channels, so their tolerance is set by the small activations alone, while
+# the large ones share the kernels' per-lane activation slices with them.
+
+def _massive_x(seed, M, K, sigma, chans, big):
+    x = synth.normal(seed, 1, M * K, sigma).reshape(M, K)
+    for j, c in enumerate(chans):
+        x[:, c] = big * (1.0 if j % 2 == 0 else -1.0) * (1.0 + 0.1 * np.arange(M))
+    return x.astype(np.float32)
+
+
+def _zero_columns(w, chans, every=2):
+    w = w.copy()
+    for c in chans:
+        w[::every, c] = 0.0
+    return w
+
+
+MASSIVE = [(1e-2, 1e3), (1e-2, 1e4), (1e-3, 1e3), (1e-3, 1e4), (1.0, 1e5)]
+
+
+@pytest.mark.parametrize("sigma,big", MASSIVE)
+@pytest.mark.parametrize("M", [1, 2, 3, 8])
+def test_linear_small_m_massive_activations(dev, sigma, big, M):
+    """INT8 g64, K = 4096 (the vocab-head row length and kernel) and INT4
+    g128 K = 2048, M = 1..8, fp32 activations with three massive channels."""
+    for bits, group, K, N in ((8, 64, 4096, 1536), (4, 128, 2048, 1000)):
+        chans = [5, 1000, K - 7]
+        w = _zero_columns(_weights(N, K, outl=True), chans)
+        x = _massive_x(40 + M, M, K, sigma, chans, big)
+        oq = oracle.quantize(w, bits, group)
+        assert all((oracle.dequantize(oq)[::2, c] == 0).all() for c in chans)
+        g = q.qmm_quantize_groupwise(T(w, dev), bits, group)
+        y = q.qmm_linear(T(x, dev), g).cpu().numpy()
+        assert_within(y, oracle.linear_fused(x, oq), oracle.linear_bound(x, oq),
+                      f"massive b{bits} K{K} M{M} sigma={sigma} big={big}")
+
+
+@pytest.mark.parametrize("sigma,big", [(1e-2, 1e3), (1e-3, 1e4)])
+def test_linear_small_m_massive_bf16_activations(dev, sigma, big):
+    K, N, M = 4096, 1000, 2
+    chans = [64, 2047, 3000]
+    w = _zero_columns(_weights(N, K), chans)
+    x, xd = _bf16_x(_massive_x(50, M, K, sigma, chans, big), dev)
+    oq = oracle.quantize(w, 8, 64)
+    g = q.qmm_quantize_groupwise(T(w, dev), 8, 64)
+    y = q.qmm_linear(xd, g).cpu().numpy()
+    assert_within(y, oracle.linear_fused(x, oq), oracle.linear_bound(x, oq), "massive bf16")
+
+
+@pytest.mark.parametrize("sigma,big", [(1e-2, 1e3), (1e-3, 1e4), (1.0, 1e5)])
+def test_moe_decode_massive_activations(dev, sigma, big):
+    """Decode-sized MoE (INT4 g64, the one-token-per-pass expert kernels with
+    32 columns per lane) on tokens with massive channels; the gate and up rows
+    of every other intermediate feature hold a zero weight at those channels."""
+    E, H, I, k, M = 8, 2048, 2048, 3, 6
+    chans = [3, 777, 2040]
+
+    def fill(which, e, out):
+        stream = {"gate": 11, "up": 12, "down": 13}[which] + 10 * e
+        out[...] = synth.normal(21, stream, out.size, 0.05).reshape(out.shape)
+        if which != "down":
+            out[...] = _zero_columns(out, chans)
+
+    ex = q.quantize_experts(E, H, I, 4, 64, fill, device=dev)
+    og, ou, od = [], [], []
+    for e in range(E):
+        for which, lst in (("gate", og), ("up", ou), ("down", od)):
+            rows, cols = (I, H) if which != "down" else (H, I)
+            buf = np.empty((rows, cols), np.float32)
+            fill(which, e, buf)
+            lst.append(oracle.quantize(buf, 4, 64))
+    x = _massive_x(60, M, H, sigma, chans, big)
+    idx = np.array([[m % E, (m + 3) % E, (m + 5) % E] for m in range(M)], np.int32)
+    w = np.tile(np.array([0.5, 0.3, 0.2], np.float32), (M, 1))
+    _moe_check(dev, x, T(x, dev), idx, w, ex, og, ou, od, what=f"massive sigma={sigma} big={big}")
+
+
+# ------------- tensor-core path: weights and tokens outside fp16's easy range
+#
+# The fp16 operands of the tensor-core path are kept in range by power-of-two
+# scalings (per weight row, per token row, per SwiGLU row) and groups whose
+# zero point is outside the fast form's exact range are dequantised exactly.
+# Weights of 1e-3 and 1e-4 (scales far below fp16's normal range),
+# single-signed groups (zero points in the thousands and in the millions) and
+# bf16 tokens at +-1e5 (beyond fp16's largest finite value) must all meet
+# the bf16 bar.
+
+def _domain_experts(dev, E, H, I, kind, seed):
+    def fill(which, e, out):
+        stream = {"gate": 11, "up": 12, "down": 13}[which] + 10 * e
+        if kind in ("tiny3", "tiny4"):
+            sigma = 1e-3 if kind == "tiny3" else 1e-4
+            out[...] = synth.normal(seed, stream, out.size, sigma).reshape(out.shape)
+        elif kind == "offset":
+            # gate: all positive around 1 (zp near -4600); up: all negative
+            # around -0.5 (zp near +2200); down: 100 + small noise (zp in the
+            # millions)
+            centre, sig = {"gate": (1.0, 0.01), "up": (-0.5, 0.01), "down": (100.0, 0.001)}[which]
+            out[...] = centre + synth.normal(seed, stream, out.size, sig).reshape(out.shape)
+        else:
+            out[...] = synth.normal(seed, stream, out.size, 0.05).reshape(out.shape)
+    ex = q.quantize_experts(E, H, I, 8, 128, fill, device=dev)
+    og, ou, od = [], [], []
+    for e in range(E):
+        for which, lst in (("gate", og), ("up", ou), ("down", od)):
+            rows, cols = (I, H) if which != "down" else (H, I)
+            buf = np.empty((rows, cols), np.float32)
+            fill(which, e, buf)
+            lst.append(oracle.quantize(buf, 8, 128))
+    return ex, og, ou, od
+
+
+@pytest.mark.parametrize("kind", ["tiny3", "tiny4", "offset", "big_tokens"])
+def test_moe_tensor_core_numeric_domain(dev, kind):
+    E, k, H, I, M = 6, 2, 1024, 512, 160
+    ex, og, ou, od = _domain_experts(dev, E, H, I, kind, seed=31)
+    if kind == "offset":
+        zg, zd = og[3].zps, od[3].zps
+        assert zg.min() < -3000 and ou[3].zps.max() > 1100 and np.abs(zd).min() > 10 ** 5
+    x = synth.normal(32, 1, M * H).reshape(M, H)
+    if kind == "big_tokens":
+        x[::3, ::97] = 1e5
+        x[1::3, 5::101] = -1e5
+    x, xd = _bf16_x(x, dev)
+    if kind == "big_tokens":
+        assert np.abs(x).max() > 65504
+    idx = np.zeros((M, k), np.int32)
+    idx[:, 0] = 3
+    idx[:, 1] = np.where(np.arange(M) % 17 == 0, 1, np.where(np.arange(M) % 5 == 0, 5, 0))
+    idx[7, 1] = 2  # one single-token expert (small-M kernels beside the tensor cores)
+    w = np.full((M, k), 0.5, np.float32)
+    for ydt in (torch.float32, torch.bfloat16):
+        _moe_check(dev, x, xd, idx, w, ex, og, ou, od, y_dtype=ydt, what=f"tc {kind} y={ydt}")
+
+
+# ----------------------------------------------------- routing load check
+
+@pytest.mark.parametrize("M,E,k,zipf", [(512, 256, 6, True), (8, 256, 6, False), (37, 16, 3, True),
+                                        (1000, 1024, 8, True)])
+def test_route_load_stats(dev, M, E, k, zipf):
+    """Load statistics of the router's own histogram, bit-exact against the
+    oracle's count of its top-k indices; the overload bit is set exactly when
+    the largest count exceeds the threshold."""
+    H = 512
+    x = synth.normal(70 + M, 1, M * H).reshape(M, H)
+    wr = synth.normal(71, 10, E * H, 0.05).reshape(E, H)
+    bias = synth.zipf_bias(0, 20, E, 1.1) * 4 if zipf else None
+    idx, w, cnt = q.moe_route_topk(T(x, dev), T(wr, dev), None if bias is None else T(bias, dev), k)
+    oidx, _ = oracle.topk(oracle.router_logits(x, wr, bias), k)
+    np.testing.assert_array_equal(idx.cpu().numpy(), oidx)
+    ref, _ = oracle.load_stats(oidx, E, 0)
+    for thr in (int(ref[0]) - 1, int(ref[0])):
+        q.qmm_device_status(clear=True)
+        st = q.moe_route_load_stats(cnt, thr).cpu().numpy()
+        np.testing.assert_array_equal(st, ref)
+        over = bool(q.qmm_device_status(clear=True) & q.QMM_DEV_EXPERT_OVERLOAD)
+        assert over == (ref[0] > thr)
+
+
+def test_route_load_stats_ties_and_empty(dev):
+    """Equal largest counts report the lowest expert; a histogram of zeros
+    reports nothing touched."""
+    cnt = torch.tensor([0, 5, 2, 5, 0, 5], dtype=torch.int32, device=dev)
+    np.testing.assert_array_equal(q.moe_route_load_stats(cnt, 100).cpu().numpy(), [5, 1, 4, 17])
+    z = torch.zeros(7, dtype=torch.int32, device=dev)
+    np.testing.assert_array_equal(q.moe_route_load_stats(z, 0).cpu().numpy(), [0, 0, 0, 0])
+    assert q.qmm_device_status(clear=True) == 0
+
+
+# ------------------------------------------------------------ bounded waits
+
+def test_bounded_wait_expires_and_reports(dev):
+    """A wait that nothing completes gives up after its limit: the kernel
+    returns, QMM_DEV_WAIT_TIMEOUT is set, and the device keeps working."""
+    import time
+    q.qmm_device_status(clear=True)
+    t0 = time.time()
+    q.qmm_diag_wait_timeout(1_000_000)  # 1 ms
+    status = q.qmm_device_status(clear=True)  # synchronises: the kernel returned
+    assert status & q.QMM_DEV_WAIT_TIMEOUT
+    assert time.time() - t0 < 30
+    assert q.qmm_device_status(clear=True) == 0
+    # the context is still usable: a linear call afterwards is correct
+    w = _weights(64, 256)
+    x = synth.normal(80, 1, 256).reshape(1, 256)
+    oq = oracle.quantize(w, 8, 64)
+    y = q.qmm_linear(T(x, dev), q.qmm_quantize_groupwise(T(w, dev), 8, 64)).cpu().numpy()
+    assert_within(y, oracle.linear_fused(x, oq), oracle.linear_bound(x, oq), "after timeout")
+
+
+# ------------------------------------- batched linear layer on the tensor cores
+
+@pytest.mark.parametrize("M", [9, 16, 33, 64, 200])
+@pytest.mark.parametrize("group,N,K", [(64, 1000, 4096), (128, 384, 2048)])
+def test_linear_batched_tensor_cores(dev, M, group, N, K):
+    """bf16 rows, INT8 codes: the tensor-core linear path (split K, ordered
+    reduction of the splits, ragged N) against the oracle at the bf16 bar, for
+    fp32 and bf16 outputs; two calls give identical bits."""
+    w = _weights(N, K, outl=True, stream=7)
+    x, xd = _bf16_x(synth.normal(90 + M, 1, M * K).reshape(M, K), dev)
+    oq = oracle.quantize(w, 8, group)
+    g = q.qmm_quantize_groupwise(T(w, dev), 8, group)
+    assert q.qmm_linear_batched_workspace_bytes(M, g) > 256
+    ref = oracle.linear_fused(x, oq)
+    y1 = q.qmm_linear_batched(xd, g)
+    y2 = q.qmm_linear_batched(xd, g)
+    np.testing.assert_array_equal(y1.cpu().numpy().view(np.uint32), y2.cpu().numpy().view(np.uint32))
+    assert_bf16_rows(y1.cpu().numpy(), ref, f"batched M{M} g{group} N{N}")
+    yb = q.qmm_linear_batched(xd, g, y_dtype=torch.bfloat16).float().cpu().numpy()
+    assert_bf16_rows(yb, ref, f"batched bf16 out M{M}")
+
+
+def test_linear_batched_numeric_domain(dev):
+    """Tiny and single-signed weights and bf16 rows beyond fp16's range on the
+    tensor-core linear path (the power-of-two row scalings and the exact
+    dequantisation of far zero points)."""
+    M, N, K = 24, 256, 1024
+    rows = [synth.normal(95, 7, 64 * K, 1e-4).reshape(64, K),
+            1.0 + synth.normal(95, 8, 64 * K, 0.01).reshape(64, K),
+            100.0 + synth.normal(95, 9, 64 * K, 0.001).reshape(64, K),
+            synth.normal(95, 10, 64 * K, 0.05).reshape(64, K)]
+    w = np.concatenate(rows).astype(np.float32)
+    xr = synth.normal(96, 1, M * K).reshape(M, K)
+    xr[::5, ::61] = 1e5
+    x, xd = _bf16_x(xr, dev)
+    oq = oracle.quantize(w, 8, 128)
+    assert oq.zps.min() < -10 ** 5
+    g = q.qmm_quantize_groupwise(T(w, dev), 8, 128)
+    y = q.qmm_linear_batched(xd, g).cpu().numpy()
+    assert_bf16_rows(y, oracle.linear_fused(x, oq), "batched domain")
+
+
+def test_linear_batched_falls_back(dev):
+    """fp32 rows, or fewer than nine rows, take qmm_linear's CUDA-core paths
+    (the fp32 bound) through the same entry point."""
+    N, K = 300, 1024
+    w = _weights(N, K, stream=9)
+    oq = oracle.quantize(w, 8, 64)
+    g = q.qmm_quantize_groupwise(T(w, dev), 8, 64)
+    for M in (4, 12):
+        x = synth.normal(97, 1, M * K).reshape(M, K)
+        y = q.qmm_linear_batched(T(x, dev), g).cpu().numpy()
+        assert_within(y, oracle.linear_fused(x, oq), oracle.linear_bound(x, oq), f"fallback M{M}")

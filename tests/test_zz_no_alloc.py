@@ -75,9 +75,27 @@ def test_noalloc_router_matches_workspace_router_twice(dev):
         i0, w0, c0 = _with_workspace(xd, wr, bias, k)
         i1, w1, c1 = _noalloc_c_abi(xd, wr, bias, k)
         torch.cuda.synchronize()
+        # the same kernels on the same inputs: the outputs are bit-identical,
+        # so whatever the scratch held before does not leak into them
         np.testing.assert_array_equal(i1.cpu().numpy(), i0.cpu().numpy())
-        assert np.abs(w1.cpu().numpy() - w0.cpu().numpy()).max() <= 2e-6
+        np.testing.assert_array_equal(w1.cpu().numpy().view(np.uint32),
+                                      w0.cpu().numpy().view(np.uint32))
         np.testing.assert_array_equal(c1.cpu().numpy(), c0.cpu().numpy())
+
+
+def test_noalloc_router_at_its_scratch_limit(dev):
+    # M * E equal to the built-in scratch size: the last logit of the array is
+    # written and read
+    E, H = 256, 64
+    M = q.QMM_NOALLOC_MAX_LOGITS // E
+    assert M * E == q.QMM_NOALLOC_MAX_LOGITS
+    xd, wr, bias = _case(24, M, E, H, 6, False, True, dev)
+    i0, w0, c0 = _with_workspace(xd, wr, bias, 6)
+    i1, w1, c1 = _noalloc_c_abi(xd, wr, bias, 6)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(i1.cpu().numpy(), i0.cpu().numpy())
+    np.testing.assert_array_equal(w1.cpu().numpy().view(np.uint32), w0.cpu().numpy().view(np.uint32))
+    np.testing.assert_array_equal(c1.cpu().numpy(), c0.cpu().numpy())
 
 
 def test_noalloc_router_refuses_sizes_beyond_its_scratch(dev):
@@ -90,3 +108,8 @@ def test_noalloc_router_refuses_sizes_beyond_its_scratch(dev):
                                         idx.data_ptr(), w.data_ptr(), None, None)
     assert rc == q.QMM_ERR_WORKSPACE
     assert "exceeds" in q.qmm_last_error()
+    # a token count whose product with E would wrap around 64 bits is refused
+    # by the same check, before anything touches the scratch
+    rc = q.lib().moe_route_topk_noalloc(xd.data_ptr(), q.QMM_F32, (1 << 62) + 1, H, wr.data_ptr(),
+                                        None, E, 6, idx.data_ptr(), w.data_ptr(), None, None)
+    assert rc == q.QMM_ERR_WORKSPACE
