@@ -780,7 +780,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-moe", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
-    ap.add_argument("--only", choices=["gemv", "moe_decode", "moe_prefill"], default=None,
+    ap.add_argument("--only", choices=["gemv", "moe_decode", "moe_prefill", "linear_batched"],
+                    default=None,
                     help="run one workload only (profiling)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
     ap.add_argument("--experts", type=int, default=None,
@@ -817,6 +818,10 @@ def main():
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
 
+    if args.only == "linear_batched":
+        if rank == 0:
+            print(json.dumps({"only": args.only, **run_linear_batched(dev, args.steps)}))
+        return
     if args.only in ("moe_decode", "moe_prefill"):
         r = recipes.CFG4 if args.only == "moe_decode" else recipes.CFG5
         if args.experts:

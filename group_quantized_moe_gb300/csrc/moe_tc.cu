@@ -549,8 +549,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float *sp = a.sc[t] + it.e * a.gstride[t] + wrow * a.G;
           const int32_t *zq = a.zp[t] + it.e * a.gstride[t] + wrow * a.G;
           float m = 0.0f;
-          // rows past the matrix (a ragged last tile) read nothing
-          for (int g = 0; g < (wrow < a.rows ? a.G : 0); g += 4) {
+          // the groups of this item's K range (each K split accumulates and
+          // rescales its own partial sums); rows past the matrix (a ragged
+          // last tile) read nothing
+          const int g0 = ((it.ks * kps * kBK) >> a.group_shift) & ~3;
+          const int g1 = wrow < a.rows ? min(a.G, ((((it.ks + 1) * kps * kBK) >> a.group_shift) + 3) & ~3) : g0;
+          for (int g = g0; g < g1; g += 4) {
             const float4 s4 = __ldg(reinterpret_cast<const float4 *>(sp + g));
             const int4 z4 = __ldg(reinterpret_cast<const int4 *>(zq + g));
             const float sv[4] = {s4.x, s4.y, s4.z, s4.w};
@@ -992,17 +996,19 @@ __global__ void __launch_bounds__(256) split_reduce_kernel(const float *__restri
     static_cast<float *>(y)[i] = acc;
 }
 
-// K splits of a linear layer with M rows on the tensor cores: enough work
-// items for two per SM, at least four 64-wide K stages per split, and a
-// divisor of the stage count.
+// K splits of a linear layer with M rows on the tensor cores: the smallest
+// divisor of the number of 64-wide K stages that gives work items for about
+// every SM (each item pays a pipeline fill and an epilogue, so one long item
+// per CTA beats two short ones), with at least four stages per split.
 int linear_tc_splits(int64_t M, int64_t N, int64_t K) {
   const int64_t items = ((M + kBN - 1) / kBN) * ((N + kBM - 1) / kBM);
   const int kst = static_cast<int>(K / kBK);
-  int want = static_cast<int>((2 * sm_count() + items - 1) / items);
-  want = want < 1 ? 1 : want;
+  const int64_t target = (4 * static_cast<int64_t>(sm_count())) / 5;
+  for (int d = 1; d <= kst / 4; ++d)
+    if (kst % d == 0 && items * d >= target) return d;
   int best = 1;
   for (int d = 1; d <= kst / 4; ++d)
-    if (kst % d == 0 && d <= want) best = d;
+    if (kst % d == 0) best = d;
   return best;
 }
 

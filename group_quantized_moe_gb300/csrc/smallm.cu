@@ -44,9 +44,15 @@ cudaError_t launch_smallm_linear(const void *x, bool x_bf16, int64_t M, const QM
   a.x = x;
   a.y = y;
   a.y_bf16 = y_bf16;
-  // One segment of M rows: the class its token count selects (one row: 32
-  // columns per lane, which spreads the per-row work over twice the codes).
-  if (M == 1) return smallm::run_one(smallm::kLinear, x_bf16, a, s);
+  // One segment of M rows.  One or two rows: the two-row digit kernel; but
+  // a small INT4 matrix with one row takes the eight-row fp32 kernel, whose
+  // activations need no conversion: such a launch is bound by its latency
+  // chain (activation load and conversion, one or two tiles per CTA, the
+  // output), not by its arithmetic (GB300: INT4 g128 4096x4096 + 2048x4096,
+  // 12.4 us per pair against 13.1 with the digit kernel; INT8 4096x4096 pairs
+  // are faster on the digit kernel, 14.6 against 15.5 us).
+  if (M == 1 && w.bits == 4 && w.rows * w.cols <= (int64_t(1) << 25))
+    return smallm::run_hi(smallm::kLinear, x_bf16, a, s);
   return M <= 2 ? smallm::run_lo(smallm::kLinear, x_bf16, a, s)
                 : smallm::run_hi(smallm::kLinear, x_bf16, a, s);
 }

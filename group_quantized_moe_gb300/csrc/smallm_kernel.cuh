@@ -1,8 +1,9 @@
 // smallm_kernel.cuh -- the small-M fused dequantise-matmul kernel template
 // (design notes in smallm.cuh), instantiated by smallm_one.cu (one
-// activation row per pass), smallm_lo.cu (two rows per pass; both two CTAs
-// per SM, balanced-digit integer arithmetic) and smallm_hi.cu (eight fp32
-// rows per pass, one CTA per SM; the linear layer with 3..8 rows).
+// activation row per pass: the decode experts), smallm_lo.cu (two rows per
+// pass; both two CTAs per SM, balanced-digit integer arithmetic) and
+// smallm_hi.cu (eight fp32 rows per pass, one CTA per SM; the linear layer
+// with 3..8 rows and small INT4 matrices with one row).
 #pragma once
 
 #include <cstdint>
@@ -565,6 +566,28 @@ __device__ __forceinline__ void tile_compute_digits(uint32_t stage, int rowbytes
                                                     const int32_t (&sl)[TBMAX][kDigits],
                                                     const float (&xsc)[TBMAX], float *red_w,
                                                     int lane) {
+  if constexpr (WIDE) {
+    // All five digits (rare): one row per iteration and a plain warp sum per
+    // row and token, which keeps this path's code small next to the
+    // unrolled common path.
+    const uint32_t sc0 = stage + NR * rowbytes + 4 * gi;
+    const uint32_t zp0 = sc0 + NR * G * 4;
+#pragma unroll 1
+    for (int r = 0; r < NRW; ++r) {
+      const int row = row0 + r;
+      const float s = lds_f32(sc0 + row * G * 4);
+      const int32_t zp = lds_s32(zp0 + row * G * 4);
+      float d[TB];
+      row_dot_digits<true, BITS, XPL, TB, TBMAX>(stage + row * rowbytes + lane_off, zp, xl, low,
+                                                 lane, sl, xsc, d);
+#pragma unroll
+      for (int t = 0; t < TB; ++t) {
+        const float v = warp_sum(s * d[t]);
+        if (lane == 0) red_w[r * TB + t] = v;
+      }
+    }
+    return;
+  }
   // at most 16 row x token values per butterfly (fewer live registers)
   constexpr int NRS = (NRW * TB <= 16) ? NRW : 16 / TB;
   constexpr int V = NRS * TB;
@@ -939,12 +962,6 @@ __global__ void __launch_bounds__(kThreads, Cfg<TBMAX>::kCtas) smallm_kernel(con
     cur_s = s;
     cur_b = b;
   };
-  // The first pass's activations are read before the first weight stage is
-  // waited for, so that their latency overlaps the stage's copy.
-  {
-    const TileIt it0 = it_begin();
-    if (it0.valid) load_act(it0.s, it0.b);
-  }
   int64_t i = 0, pending = 0;
   bool stop = false;
   for (TileIt it = it_begin(); it.valid && !stop; it_next(it), ++i) {
@@ -954,6 +971,9 @@ __global__ void __launch_bounds__(kThreads, Cfg<TBMAX>::kCtas) smallm_kernel(con
     const int p0 = s_off[e];
     const int T = s_off[e + 1] - p0;
     const int st = static_cast<int>(i % STAGES);
+    // A new (segment, pass) reads its activations before the stage is waited
+    // for, so that their latency overlaps the stage's copy.
+    if (s != cur_s || b != cur_b) load_act(s, b);
     // warp-uniform, so that every lane takes part in the warp's shuffles
     const bool ok = __all_sync(0xFFFFFFFFu,
                                wait_ok(smem_addr(&full_bar[st]),
@@ -966,7 +986,6 @@ __global__ void __launch_bounds__(kThreads, Cfg<TBMAX>::kCtas) smallm_kernel(con
     const int TB = Tb <= 1 ? 1 : Tb <= 2 ? 2 : Tb <= 4 ? 4 : 8;
     float *red_w = red + (i & 1) * kCW * RED + warp * RED;
     if (ok) {
-      if (s != cur_s || b != cur_b) load_act(s, b);
       if constexpr (kD) {
         if (TBMAX == 1 || TB == 1) {
           if (wide)
@@ -1071,7 +1090,11 @@ cudaError_t run(const Args &a, cudaStream_t s) {
   const int smem = Cfg<TBMAX>::smem_bytes(a.E, a.idx ? a.MK : 0);
   cudaError_t e = ensure_smem(reinterpret_cast<const void *>(k), smem);
   if (e != cudaSuccess) return e;
-  return launch_pdl(k, dim3(Cfg<TBMAX>::kCtas * sm_count()), dim3(kThreads), smem, s, a);
+  // A linear layer with fewer tiles than CTA slots gets one CTA per tile,
+  // which leaves the other slots to the next launch's early prologue.
+  int grid = Cfg<TBMAX>::kCtas * sm_count();
+  if (MODE == kLinear && a.tiles < grid) grid = a.tiles;
+  return launch_pdl(k, dim3(grid), dim3(kThreads), smem, s, a);
 }
 
 // K = 4096: eight warps of 16 columns per lane.  K = 2048: the digit form
@@ -1083,9 +1106,8 @@ template <int MODE, bool XBF16, int TBMAX>
 cudaError_t run_shape(const Args &a, cudaStream_t s) {
   const bool wide = a.K == 4096;
   if constexpr (TBMAX == 1) {
-    // one row (linear) or token (routed experts) per pass: 32 columns per
-    // lane (K = 4096: four warps per row, two row groups; K = 2048: two
-    // warps, four groups)
+    // routed experts, one token per pass: 32 columns per lane (K = 4096:
+    // four warps per row, two row groups; K = 2048: two warps, four groups)
     if (a.w0.bits == 4)
       return wide ? run<4, 32, 4, MODE, XBF16, TBMAX>(a, s) : run<4, 32, 2, MODE, XBF16, TBMAX>(a, s);
     return wide ? run<8, 32, 4, MODE, XBF16, TBMAX>(a, s) : run<8, 32, 2, MODE, XBF16, TBMAX>(a, s);
@@ -1108,8 +1130,6 @@ cudaError_t run_class(int mode, bool x_bf16, const Args &a, cudaStream_t s) {
     if (mode == kGateUp)
       return x_bf16 ? run_shape<kGateUp, true, 1>(a, s) : run_shape<kGateUp, false, 1>(a, s);
     if (mode == kDown) return run_shape<kDown, false, 1>(a, s);
-    if (mode == kLinear)
-      return x_bf16 ? run_shape<kLinear, true, 1>(a, s) : run_shape<kLinear, false, 1>(a, s);
     return cudaErrorInvalidValue;
   } else {
     if (mode == kLinear)
