@@ -495,6 +495,46 @@ def test_moe_decode_bad_expert_index_flagged(dev):
     assert_within(y, yref, bound, "decode bad index")
 
 
+def test_moe_decode_combine_outputs(dev):
+    """Decode batches (the in-kernel grouping): every output element is
+    written (y starts as NaN), a token with no valid slot gets zeros, a
+    workspace left dirty by an earlier call is reused, bf16 output rounds the
+    fp32 sum, and repeated calls agree bit for bit."""
+    E, H, I = 8, 2048, 2048
+    ex, og, ou, od = _small_experts(dev, E, H, I, 8, 64, seed=21)
+    M, k = 6, 3
+    x = synth.normal(21, 1, M * H).reshape(M, H)
+    idx = np.array([[0, 5, 2], [-1, 9, 100], [3, 3, 5], [7, 6, 1], [4, -2, 4], [1, 0, 2]],
+                   np.int32)
+    w = np.array([[0.5, 0.3, 0.2], [0.4, 0.4, 0.2], [0.6, 0.3, 0.1], [0.2, 0.3, 0.5],
+                  [0.7, 0.2, 0.1], [0.25, 0.25, 0.5]], np.float32)
+    ok = (idx >= 0) & (idx < E)
+    yref, bound = oracle.moe_ffn(x, np.where(ok, idx, 0).astype(np.int32),
+                                 np.where(ok, w, 0).astype(np.float32), og, ou, od)
+    xd, idxd, wd = T(x, dev), T(idx, dev), T(w, dev)
+    nbytes = q.moe_ffn_workspace_bytes(M, k, ex)
+    ws = torch.full((nbytes,), 0x5A, dtype=torch.uint8, device=dev)
+    outs = []
+    for rep in range(3):
+        y = torch.full((M, H), float("nan"), dtype=torch.float32, device=dev)
+        q.qmm_device_status(clear=True)
+        q.moe_ffn_forward(xd, idxd, wd, ex, y=y, workspace=ws)
+        assert q.qmm_device_status(clear=True) & q.QMM_DEV_BAD_EXPERT
+        outs.append(y.cpu().numpy())
+    yv = outs[0].astype(np.float64)
+    assert np.isfinite(yv).all()
+    assert (outs[0][1] == 0).all()
+    assert_within(yv, yref, bound, "decode combine")
+    for o in outs[1:]:
+        np.testing.assert_array_equal(o.view(np.uint32), outs[0].view(np.uint32))
+    yb = torch.full((M, H), float("nan"), dtype=torch.bfloat16, device=dev)
+    q.moe_ffn_forward(xd, idxd, wd, ex, y=yb, workspace=ws)
+    q.qmm_device_status(clear=True)
+    expect = torch.from_numpy(outs[0]).to(torch.bfloat16)
+    np.testing.assert_array_equal(yb.cpu().view(torch.int16).numpy(),
+                                  expect.view(torch.int16).numpy())
+
+
 # ----------------------------------------------- full-size MoE workloads
 
 def _full_moe(dev, r):
