@@ -1,4 +1,5 @@
-"""CPU oracle for the group-wise quantised linear layer and the routed MoE FFN.
+"""CPU oracle for the group-wise quantised linear layer, the routed MoE FFN and
+the decode attention step that uses the same quantised projections.
 
 TEST INFRASTRUCTURE ONLY: the test suite, the smoke check and the benchmark's
 CPU-baseline leg are the only callers.  The arithmetic lives in plain C
@@ -72,6 +73,16 @@ def _load():
             lib.orc_moe_ffn.restype = ctypes.c_int
             lib.orc_load_stats.argtypes = [vp, i64, i32, i32, i64, vp]
             lib.orc_load_stats.restype = ctypes.c_int
+            lib.orc_rope_table.argtypes = [i64, i32, dbl, vp, vp]
+            lib.orc_rope_table.restype = None
+            lib.orc_rope_apply.argtypes = [vp, i32, i32, i64, vp, vp, vp]
+            lib.orc_rope_apply.restype = None
+            lib.orc_attention.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i64,
+                                          i64, vp, vp]
+            lib.orc_attention.restype = None
+            lib.orc_attn_decode.argtypes = [vp, i64, i32, i32, i32, i64, pqw, pqw, pqw, pqw,
+                                            vp, vp, vp, vp, vp, vp, vp]
+            lib.orc_attn_decode.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -216,3 +227,77 @@ def load_stats(idx: np.ndarray, E: int, threshold: int):
     if flag < 0:
         raise MemoryError("orc_load_stats")
     return stats, bool(flag)
+
+
+# ------------------------------------------------------------ decode attention
+
+def _ptr(a):
+    return a.ctypes.data if a is not None else None
+
+
+def rope_table(max_seq: int, head_dim: int, base: float = 10000.0):
+    """cos, sin float32 [max_seq, head_dim/2] of pos * base^(-2i/head_dim)."""
+    hp = head_dim // 2
+    c = np.empty((max_seq, hp), dtype=np.float32)
+    s = np.empty((max_seq, hp), dtype=np.float32)
+    _load().orc_rope_table(max_seq, head_dim, float(base), c.ctypes.data, s.ctypes.data)
+    return c, s
+
+
+def rope_apply(x: np.ndarray, pos: int, cos_t: np.ndarray, sin_t: np.ndarray) -> np.ndarray:
+    """Rotates each row of x [n_vec, head_dim] (pairs 2i, 2i+1) to position pos."""
+    x = _c(x, np.float64)
+    n_vec, hd = x.shape
+    cos_t, sin_t = _c(cos_t, np.float32), _c(sin_t, np.float32)
+    assert 0 <= pos < cos_t.shape[0] and cos_t.shape[1] == hd // 2
+    out = np.empty_like(x)
+    _load().orc_rope_apply(x.ctypes.data, n_vec, hd, pos, cos_t.ctypes.data, sin_t.ctypes.data,
+                           out.ctypes.data)
+    return out
+
+
+def attention(q: np.ndarray, k_cache: np.ndarray, v_cache: np.ndarray, T: int,
+              dq: np.ndarray | None = None, k_last=None, v_last=None, dk_last=None,
+              dv_last=None):
+    """Decode attention: q [n_head, hd]; caches float32 [n_kv, max_seq, hd],
+    rows t < T (row T-1 from k_last / v_last [n_kv, hd] when given).  Returns
+    (out [n_head, hd] double, bound)."""
+    q = _c(q, np.float64)
+    n_head, hd = q.shape
+    k_cache, v_cache = _c(k_cache, np.float32), _c(v_cache, np.float32)
+    n_kv, max_seq, hd2 = k_cache.shape
+    assert hd2 == hd and v_cache.shape == k_cache.shape and 1 <= T <= max_seq
+    assert n_head % n_kv == 0
+    conv = [None if a is None else _c(a, np.float64) for a in (dq, k_last, v_last, dk_last, dv_last)]
+    out = np.empty((n_head, hd), dtype=np.float64)
+    bound = np.empty((n_head, hd), dtype=np.float64)
+    _load().orc_attention(q.ctypes.data, *[_ptr(a) for a in conv[:1]], k_cache.ctypes.data,
+                          v_cache.ctypes.data, *[_ptr(a) for a in conv[1:]], n_head, n_kv, hd,
+                          max_seq, T, out.ctypes.data, bound.ctypes.data)
+    return out, bound
+
+
+def attn_decode(x: np.ndarray, pos: int, n_head: int, n_kv: int, head_dim: int,
+                wq: QWeight, wk: QWeight, wv: QWeight, wo: QWeight, cos_t, sin_t,
+                cache_in: np.ndarray):
+    """One decode token through the attention layer.  cache_in float32
+    [2, n_kv, max_seq, head_dim] (rows < pos are read).  Returns (y [D_out]
+    double, bound, kv_new [2, n_kv, head_dim] double, kv_bound)."""
+    x = _c(x, np.float32).reshape(-1)
+    cache_in = _c(cache_in, np.float32)
+    two, nkv2, max_seq, hd2 = cache_in.shape
+    assert two == 2 and nkv2 == n_kv and hd2 == head_dim and 0 <= pos < max_seq
+    cos_t, sin_t = _c(cos_t, np.float32), _c(sin_t, np.float32)
+    y = np.empty(wo.N, dtype=np.float64)
+    bound = np.empty(wo.N, dtype=np.float64)
+    kv_new = np.empty((2, n_kv, head_dim), dtype=np.float64)
+    kv_bound = np.empty((2, n_kv, head_dim), dtype=np.float64)
+    rc = _load().orc_attn_decode(x.ctypes.data, pos, n_head, n_kv, head_dim, max_seq,
+                                 ctypes.byref(wq._struct()), ctypes.byref(wk._struct()),
+                                 ctypes.byref(wv._struct()), ctypes.byref(wo._struct()),
+                                 cos_t.ctypes.data, sin_t.ctypes.data, cache_in.ctypes.data,
+                                 kv_new.ctypes.data, kv_bound.ctypes.data, y.ctypes.data,
+                                 bound.ctypes.data)
+    if rc != 0:
+        raise ValueError(f"orc_attn_decode failed ({rc})")
+    return y, bound, kv_new, kv_bound

@@ -381,3 +381,192 @@ int orc_moe_ffn(const float *x, int64_t M, int64_t H, int64_t I,
   free(dh);
   return 0;
 }
+
+/* ------------------------------------------------------------------ */
+/* Decode attention with rotary positions [P1 section 3.4]             */
+/* ------------------------------------------------------------------ */
+/*
+ * Readings where the page is silent (listed in the design notes):
+ *  - a "pair of dimensions" is (2i, 2i+1) of a head vector, rotated by the
+ *    angle pos * theta_i with theta_i = base^(-2i/head_dim); base 10000 is
+ *    the caller's choice, not the page's;
+ *  - the table holds cos and sin of those angles rounded to fp32, and the
+ *    rotation is (a, b) -> (a cos - b sin, a sin + b cos);
+ *  - query head h reads key/value head h / (n_head / n_kv) (n_kv = n_head:
+ *    the page's multi-head attention; fewer: grouped heads as in the ds4
+ *    walkthrough's 64 query heads over one key/value head);
+ *  - the KV cache of one layer is [2][n_kv][max_seq][head_dim] fp32 (keys,
+ *    then values), the page's [layers, 2, heads, max_seq, head_dim] for one
+ *    layer; the decode step writes row pos and attends over rows 0..pos.
+ */
+
+void orc_rope_table(int64_t max_seq, int32_t head_dim, double base, float *cos_t, float *sin_t) {
+  const int32_t hp = head_dim / 2;
+  for (int64_t p = 0; p < max_seq; ++p) {
+    for (int32_t i = 0; i < hp; ++i) {
+      const double theta = pow(base, -2.0 * (double)i / (double)head_dim);
+      const double ang = (double)p * theta;
+      cos_t[p * hp + i] = (float)cos(ang);
+      sin_t[p * hp + i] = (float)sin(ang);
+    }
+  }
+}
+
+void orc_rope_apply(const double *x, int32_t n_vec, int32_t head_dim, int64_t pos,
+                    const float *cos_t, const float *sin_t, double *out) {
+  const int32_t hp = head_dim / 2;
+  for (int32_t v = 0; v < n_vec; ++v) {
+    for (int32_t i = 0; i < hp; ++i) {
+      const double c = (double)cos_t[pos * hp + i], s = (double)sin_t[pos * hp + i];
+      const double a = x[v * head_dim + 2 * i], b = x[v * head_dim + 2 * i + 1];
+      out[v * head_dim + 2 * i] = a * c - b * s;
+      out[v * head_dim + 2 * i + 1] = a * s + b * c;
+    }
+  }
+}
+
+/* Bound of the rotated values from bounds da of the inputs: the rotation in
+ * fp32 (|err| <= 1e-5 (|a c| + |b s|) + 1e-6, the fp32 rule of a two-term
+ * dot product) plus |c| da + |s| db. */
+static void rope_bound(const double *x, const double *dx, int32_t n_vec, int32_t head_dim,
+                       int64_t pos, const float *cos_t, const float *sin_t, double *bound) {
+  const int32_t hp = head_dim / 2;
+  for (int32_t v = 0; v < n_vec; ++v) {
+    for (int32_t i = 0; i < hp; ++i) {
+      const double c = fabs((double)cos_t[pos * hp + i]), s = fabs((double)sin_t[pos * hp + i]);
+      const double a = fabs(x[v * head_dim + 2 * i]), b = fabs(x[v * head_dim + 2 * i + 1]);
+      const double da = dx ? dx[v * head_dim + 2 * i] : 0.0;
+      const double db = dx ? dx[v * head_dim + 2 * i + 1] : 0.0;
+      bound[v * head_dim + 2 * i] = 1e-5 * (a * c + b * s) + 1e-6 + c * da + s * db;
+      bound[v * head_dim + 2 * i + 1] = 1e-5 * (a * s + b * c) + 1e-6 + s * da + c * db;
+    }
+  }
+}
+
+void orc_attention(const double *q, const double *dq, const float *k_cache, const float *v_cache,
+                   const double *k_last, const double *v_last, const double *dk_last,
+                   const double *dv_last, int32_t n_head, int32_t n_kv, int32_t head_dim,
+                   int64_t max_seq, int64_t T, double *out, double *bound) {
+  const int32_t grp = n_head / n_kv;
+  const double scale = 1.0 / sqrt((double)head_dim);
+  double *s = (double *)malloc((size_t)T * sizeof(double));
+  double *ds = (double *)malloc((size_t)T * sizeof(double));
+  double *p = (double *)malloc((size_t)T * sizeof(double));
+  if (!s || !ds || !p) { free(s); free(ds); free(p); return; }
+  for (int32_t h = 0; h < n_head; ++h) {
+    const int32_t kvh = h / grp;
+    const double *qh = q + (int64_t)h * head_dim;
+    /* row t of the keys / values of head kvh: the cache, or row T-1 from
+     * k_last / v_last when given (the row this decode step writes) */
+    for (int64_t t = 0; t < T; ++t) {
+      double dot = 0.0, adot = 0.0, prop = 0.0;
+      for (int32_t i = 0; i < head_dim; ++i) {
+        const int64_t ci = ((int64_t)kvh * max_seq + t) * head_dim + i;
+        const int last = (t == T - 1) && k_last;
+        const double kv = last ? k_last[(int64_t)kvh * head_dim + i] : (double)k_cache[ci];
+        dot += qh[i] * kv;
+        adot += fabs(qh[i] * kv);
+        if (dq) prop += fabs(kv) * dq[(int64_t)h * head_dim + i];
+        if (last && dk_last) prop += fabs(qh[i]) * dk_last[(int64_t)kvh * head_dim + i];
+      }
+      s[t] = dot * scale;
+      ds[t] = (1e-5 * adot + prop) * scale + 1e-6;
+    }
+    /* softmax with the maximum subtracted first */
+    double mx = s[0];
+    for (int64_t t = 1; t < T; ++t) mx = s[t] > mx ? s[t] : mx;
+    double z = 0.0;
+    for (int64_t t = 0; t < T; ++t) { p[t] = exp(s[t] - mx); z += p[t]; }
+    double mean_ds = 0.0;
+    for (int64_t t = 0; t < T; ++t) { p[t] /= z; mean_ds += p[t] * ds[t]; }
+    for (int32_t d = 0; d < head_dim; ++d) {
+      double acc = 0.0, b = 0.0, apv = 0.0;
+      for (int64_t t = 0; t < T; ++t) {
+        const int64_t ci = ((int64_t)kvh * max_seq + t) * head_dim + d;
+        const int last = (t == T - 1) && v_last;
+        const double vv = last ? v_last[(int64_t)kvh * head_dim + d] : (double)v_cache[ci];
+        acc += p[t] * vv;
+        apv += p[t] * fabs(vv);
+        /* first order: dp_t <= p_t (ds_t + sum_u p_u ds_u + 1e-6) */
+        b += p[t] * (ds[t] + mean_ds + 1e-6) * fabs(vv);
+        if (last && dv_last) b += p[t] * dv_last[(int64_t)kvh * head_dim + d];
+      }
+      out[(int64_t)h * head_dim + d] = acc;
+      if (bound) bound[(int64_t)h * head_dim + d] = b + 1e-5 * apv + 1e-6;
+    }
+  }
+  free(s);
+  free(ds);
+  free(p);
+}
+
+int orc_attn_decode(const float *x, int64_t pos, int32_t n_head, int32_t n_kv, int32_t head_dim,
+                    int64_t max_seq, const orc_qweight *wq, const orc_qweight *wk,
+                    const orc_qweight *wv, const orc_qweight *wo, const float *cos_t,
+                    const float *sin_t, const float *cache_in, double *kv_new, double *kv_bound,
+                    double *y, double *bound) {
+  const int64_t D = wq->K, nq = (int64_t)n_head * head_dim, nk = (int64_t)n_kv * head_dim;
+  if (wk->K != D || wv->K != D || wq->N != nq || wk->N != nk || wv->N != nk || wo->K != nq)
+    return -1;
+  double *xd = (double *)malloc((size_t)D * sizeof(double));
+  double *q = (double *)malloc((size_t)(4 * nq + 4 * nk) * sizeof(double));
+  if (!xd || !q) { free(xd); free(q); return -2; }
+  double *dq = q + nq, *qr = dq + nq, *dqr = qr + nq;
+  double *k = dqr + nq, *dk = k + nk, *v = dk + nk, *dv = v + nk;
+  double *a = (double *)malloc((size_t)(2 * nq + 2 * nk) * sizeof(double));
+  if (!a) { free(xd); free(q); return -2; }
+  double *da = a + nq, *kr = da + nq, *dkr = kr + nk;
+  for (int64_t c = 0; c < D; ++c) xd[c] = (double)x[c];
+  /* the three projections (fused dequantised linear layers) */
+  for (int64_t n = 0; n < nq; ++n) {
+    double val, av;
+    dot_row(xd, wq, n, &val, &av, NULL);
+    q[n] = val;
+    dq[n] = 1e-5 * av + 1e-6;
+  }
+  for (int64_t n = 0; n < nk; ++n) {
+    double val, av;
+    dot_row(xd, wk, n, &val, &av, NULL);
+    k[n] = val;
+    dk[n] = 1e-5 * av + 1e-6;
+    dot_row(xd, wv, n, &val, &av, NULL);
+    v[n] = val;
+    dv[n] = 1e-5 * av + 1e-6;
+  }
+  /* rotary positions for the query and the new key */
+  orc_rope_apply(q, n_head, head_dim, pos, cos_t, sin_t, qr);
+  rope_bound(q, dq, n_head, head_dim, pos, cos_t, sin_t, dqr);
+  orc_rope_apply(k, n_kv, head_dim, pos, cos_t, sin_t, kr);
+  rope_bound(k, dk, n_kv, head_dim, pos, cos_t, sin_t, dkr);
+  if (kv_new) {
+    memcpy(kv_new, kr, (size_t)nk * sizeof(double));
+    memcpy(kv_new + nk, v, (size_t)nk * sizeof(double));
+  }
+  if (kv_bound) {
+    memcpy(kv_bound, dkr, (size_t)nk * sizeof(double));
+    memcpy(kv_bound + nk, dv, (size_t)nk * sizeof(double));
+  }
+  /* attention over cache rows 0..pos, row pos being this step's key/value */
+  const float *kc = cache_in, *vc = cache_in + (int64_t)n_kv * max_seq * head_dim;
+  orc_attention(qr, dqr, kc, vc, kr, v, dkr, dv, n_head, n_kv, head_dim, max_seq, pos + 1, a, da);
+  /* output projection, with the propagated bound sum_j |Wo[n,j]| da_j */
+  const int64_t G = nq / wo->group;
+  for (int64_t n = 0; n < wo->N; ++n) {
+    double val, av;
+    dot_row(a, wo, n, &val, &av, NULL);
+    y[n] = val;
+    if (bound) {
+      double prop = 0.0;
+      for (int64_t j = 0; j < nq; ++j) {
+        const int64_t gi = n * G + j / wo->group;
+        prop += fabs((double)dequant_one(orc_code_at(wo, n, j), wo->zps[gi], wo->scales[gi])) *
+                da[j];
+      }
+      bound[n] = 1e-5 * av + prop + 1e-6;
+    }
+  }
+  free(xd);
+  free(q);
+  free(a);
+  return 0;
+}

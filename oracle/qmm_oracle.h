@@ -43,6 +43,28 @@ int orc_moe_ffn(const float *x, int64_t M, int64_t H, int64_t I,
                 const orc_qweight *gate, const orc_qweight *up,
                 const orc_qweight *down, double dw, double *y, double *bound);
 
+/* Decode attention [P1 section 3.4] (readings in qmm_oracle.c).  RoPE table
+ * cos/sin [max_seq, head_dim/2] fp32; rope_apply rotates n_vec head vectors
+ * (double) at position pos; attention: q [n_head*hd] double, caches fp32
+ * [n_kv, max_seq, hd], rows t < T (row T-1 from k_last / v_last when they are
+ * not NULL), bounds dq / dk_last / dv_last may be NULL; out, bound
+ * [n_head*hd].  attn_decode: one token through q/k/v projections, RoPE, the
+ * cache (cache_in [2][n_kv][max_seq][hd], rows < pos), attention over
+ * 0..pos and the output projection; kv_new / kv_bound [2][n_kv*hd] (NULL
+ * allowed) get the key/value row written at pos; y, bound [wo->N]. */
+void orc_rope_table(int64_t max_seq, int32_t head_dim, double base, float *cos_t, float *sin_t);
+void orc_rope_apply(const double *x, int32_t n_vec, int32_t head_dim, int64_t pos,
+                    const float *cos_t, const float *sin_t, double *out);
+void orc_attention(const double *q, const double *dq, const float *k_cache, const float *v_cache,
+                   const double *k_last, const double *v_last, const double *dk_last,
+                   const double *dv_last, int32_t n_head, int32_t n_kv, int32_t head_dim,
+                   int64_t max_seq, int64_t T, double *out, double *bound);
+int orc_attn_decode(const float *x, int64_t pos, int32_t n_head, int32_t n_kv, int32_t head_dim,
+                    int64_t max_seq, const orc_qweight *wq, const orc_qweight *wk,
+                    const orc_qweight *wv, const orc_qweight *wo, const float *cos_t,
+                    const float *sin_t, const float *cache_in, double *kv_new, double *kv_bound,
+                    double *y, double *bound);
+
 #ifdef __cplusplus
 }
 #endif
