@@ -37,7 +37,8 @@ EXPORTED = ("qmm_quantize_groupwise", "qmm_linear", "moe_route_workspace_bytes",
             "moe_ffn_workspace_bytes", "moe_ffn_forward", "qmm_last_error", "qmm_launch_count",
             "qmm_device_status", "moe_route_topk_noalloc", "moe_route_load_stats",
             "qmm_diag_wait_timeout", "qmm_linear_batched_workspace_bytes",
-            "qmm_linear_batched")
+            "qmm_linear_batched", "qmm_rope_table", "qmm_attn_decode_workspace_bytes",
+            "qmm_attn_decode")
 QMM_NOALLOC_MAX_LOGITS = 262144
 
 
@@ -60,6 +61,13 @@ class _ExpertWeights(ctypes.Structure):
                 ("codes", ctypes.c_void_p), ("codes_stride", ctypes.c_int64),
                 ("scales", ctypes.c_void_p), ("zps", ctypes.c_void_p),
                 ("groups_stride", ctypes.c_int64)]
+
+
+class _AttnLayer(ctypes.Structure):
+    _fields_ = [("n_head", ctypes.c_int32), ("n_head_kv", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("max_seq", ctypes.c_int64),
+                ("wq", _Weight), ("wk", _Weight), ("wv", _Weight), ("wo", _Weight),
+                ("rope_cos", ctypes.c_void_p), ("rope_sin", ctypes.c_void_p)]
 
 
 class _Experts(ctypes.Structure):
@@ -115,6 +123,13 @@ def lib() -> ctypes.CDLL:
             L.qmm_linear_batched.argtypes = [vp, i32, i64, ctypes.POINTER(_Weight), vp, i32, vp,
                                              sz, vp]
             L.qmm_linear_batched.restype = ctypes.c_int
+            L.qmm_rope_table.argtypes = [i64, i32, ctypes.c_double, vp, vp, vp]
+            L.qmm_rope_table.restype = ctypes.c_int
+            L.qmm_attn_decode_workspace_bytes.argtypes = [ctypes.POINTER(_AttnLayer)]
+            L.qmm_attn_decode_workspace_bytes.restype = sz
+            L.qmm_attn_decode.argtypes = [vp, i32, i64, ctypes.POINTER(_AttnLayer), vp, vp, i32,
+                                          vp, sz, vp]
+            L.qmm_attn_decode.restype = ctypes.c_int
             _lib = L
     return _lib
 
@@ -551,3 +566,77 @@ def quantize_experts(E: int, H: int, I: int, bits: int, group: int, rows_fn, dev
             j += 1
     torch.cuda.synchronize(device)
     return ex
+
+
+# ------------------------------------------------------------ decode attention
+
+def rope_table(max_seq: int, head_dim: int, base: float = 10000.0, device="cuda", stream=None):
+    """cos, sin fp32 [max_seq, head_dim / 2] of pos * base^(-2i / head_dim)
+    (see include/qmm.h)."""
+    hp = head_dim // 2
+    c = torch.empty((max_seq, hp), dtype=torch.float32, device=device)
+    s = torch.empty((max_seq, hp), dtype=torch.float32, device=device)
+    _check(lib().qmm_rope_table(max_seq, head_dim, float(base), _ptr(c), _ptr(s),
+                                _stream(stream)))
+    return c, s
+
+
+@dataclass
+class AttnLayer:
+    """One attention layer for decoding: quantised projections and the RoPE
+    table (device tensors), shapes as in include/qmm.h."""
+    n_head: int
+    n_head_kv: int
+    head_dim: int
+    max_seq: int
+    wq: QWeight
+    wk: QWeight
+    wv: QWeight
+    wo: QWeight
+    rope_cos: torch.Tensor
+    rope_sin: torch.Tensor
+
+    def _c(self) -> _AttnLayer:
+        return _AttnLayer(self.n_head, self.n_head_kv, self.head_dim, self.max_seq,
+                          self.wq._c(), self.wk._c(), self.wv._c(), self.wo._c(),
+                          _ptr(self.rope_cos), _ptr(self.rope_sin))
+
+    def kv_cache(self, device="cuda") -> torch.Tensor:
+        """A zeroed cache [2, n_head_kv, max_seq, head_dim] fp32."""
+        return torch.zeros((2, self.n_head_kv, self.max_seq, self.head_dim),
+                           dtype=torch.float32, device=device)
+
+
+def qmm_attn_decode_workspace_bytes(layer: AttnLayer) -> int:
+    return int(lib().qmm_attn_decode_workspace_bytes(ctypes.byref(layer._c())))
+
+
+def attn_decode(x: torch.Tensor, pos: int, layer: AttnLayer, kv_cache: torch.Tensor,
+                y: torch.Tensor | None = None, y_dtype: torch.dtype = torch.float32,
+                workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """One decode step of the attention layer for the token x [D] at position
+    pos: writes row pos of kv_cache and returns y [D_out] (see include/qmm.h)."""
+    D = layer.wq.K
+    if x.numel() != D:
+        raise ValueError(f"x has {x.numel()} elements, expected D = {D}")
+    _dtype_code(x)
+    for name in ("wq", "wk", "wv", "wo"):
+        _qweight_sizes(getattr(layer, name), name)
+    hp = layer.head_dim // 2
+    _need(layer.rope_cos, layer.max_seq * hp, (torch.float32,), "rope_cos")
+    _need(layer.rope_sin, layer.max_seq * hp, (torch.float32,), "rope_sin")
+    _need(kv_cache, 2 * layer.n_head_kv * layer.max_seq * layer.head_dim, (torch.float32,),
+          "kv_cache")
+    _need(y, layer.wo.N, (torch.float32, torch.bfloat16), "y")
+    ts = [t for w in (layer.wq, layer.wk, layer.wv, layer.wo) for t in _qweight_tensors(w)]
+    _require_cuda(x, kv_cache, y, workspace, layer.rope_cos, layer.rope_sin, *ts)
+    desc = layer._c()
+    if y is None:
+        y = torch.empty((layer.wo.N,), dtype=y_dtype, device=x.device)
+    if workspace is None:  # a caller's workspace is size-checked by the library
+        nbytes = int(lib().qmm_attn_decode_workspace_bytes(ctypes.byref(desc)))
+        workspace = torch.empty((max(nbytes, 1),), dtype=torch.uint8, device=x.device)
+    _check(lib().qmm_attn_decode(_ptr(x), _dtype_code(x), pos, ctypes.byref(desc), _ptr(kv_cache),
+                                 _ptr(y), _dtype_code(y), _ptr(workspace), _nbytes(workspace),
+                                 _stream(stream)))
+    return y

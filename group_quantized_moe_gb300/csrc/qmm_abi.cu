@@ -484,3 +484,114 @@ int moe_ffn_forward(const void *x, int32_t x_dtype, int64_t M, const int32_t *to
 }
 
 }  // extern "C"
+
+// ------------------------------------------------------------ decode attention
+
+namespace {
+
+struct AttnLayout {
+  size_t q, k, v, attn, part, total;
+};
+
+AttnLayout attn_layout(const qmm_attn_layer *L) {
+  AttnLayout a;
+  const size_t nq = static_cast<size_t>(L->n_head) * L->head_dim;
+  const size_t nk = static_cast<size_t>(L->n_head_kv) * L->head_dim;
+  size_t o = 0;
+  a.q = o;    o += round256(4 * nq);
+  a.k = o;    o += round256(4 * nk);
+  a.v = o;    o += round256(4 * nk);
+  a.attn = o; o += round256(4 * nq);
+  a.part = o; o += round256(4 * static_cast<size_t>(L->n_head) * attn_chunks(L->max_seq) *
+                            (L->head_dim + 2));
+  a.total = o;
+  return a;
+}
+
+int check_attn_layer(const qmm_attn_layer *L, const char *who) {
+  if (!L) return fail(QMM_ERR_INVALID_ARG, "%s: layer descriptor is NULL", who);
+  if (L->n_head < 1 || L->n_head_kv < 1 || L->n_head % L->n_head_kv != 0)
+    return fail(QMM_ERR_INVALID_ARG, "%s: n_head must be a positive multiple of n_head_kv", who);
+  if (L->head_dim < 4 || L->head_dim > 512 || L->head_dim % 4 != 0)
+    return fail(QMM_ERR_UNSUPPORTED, "%s: head_dim must be a multiple of 4 in [4, 512]", who);
+  if (L->max_seq < 1 || L->max_seq > (int64_t(1) << 31))
+    return fail(QMM_ERR_INVALID_ARG, "%s: max_seq must be in [1, 2^31]", who);
+  const int64_t nq = int64_t(L->n_head) * L->head_dim, nk = int64_t(L->n_head_kv) * L->head_dim;
+  const int64_t D = L->wq.K;
+  if (L->wq.N != nq || L->wk.N != nk || L->wv.N != nk || L->wk.K != D || L->wv.K != D ||
+      L->wo.K != nq || L->wo.N < 1 || D < 1)
+    return fail(QMM_ERR_SHAPE,
+                "%s: need wq [n_head*head_dim, D], wk / wv [n_head_kv*head_dim, D], "
+                "wo [D_out, n_head*head_dim]", who);
+  if (!L->rope_cos || !L->rope_sin)
+    return fail(QMM_ERR_INVALID_ARG, "%s: null RoPE table", who);
+  return QMM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int qmm_rope_table(int64_t max_seq, int32_t head_dim, double base, float *cos_t, float *sin_t,
+                   qmm_stream_t stream) {
+  g_err[0] = '\0';
+  if (max_seq < 1 || head_dim < 2 || head_dim % 2 != 0 || max_seq > (int64_t(1) << 31) ||
+      head_dim > 65536)
+    return fail(QMM_ERR_INVALID_ARG, "qmm_rope_table: need max_seq >= 1 and an even head_dim");
+  if (!(base > 0.0)) return fail(QMM_ERR_INVALID_ARG, "qmm_rope_table: base must be positive");
+  if (!cos_t || !sin_t) return fail(QMM_ERR_INVALID_ARG, "qmm_rope_table: null pointer");
+  if ((reinterpret_cast<uintptr_t>(cos_t) & 3u) || (reinterpret_cast<uintptr_t>(sin_t) & 3u))
+    return fail(QMM_ERR_ALIGN, "qmm_rope_table: tables must be 4-byte aligned");
+  const cudaError_t e =
+      launch_rope_table(max_seq, head_dim, base, cos_t, sin_t, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "qmm_rope_table");
+  return QMM_OK;
+}
+
+size_t qmm_attn_decode_workspace_bytes(const qmm_attn_layer *L) {
+  if (!L || L->n_head < 1 || L->n_head_kv < 1 || L->head_dim < 4 || L->head_dim > 512 ||
+      L->max_seq < 1 || L->max_seq > (int64_t(1) << 31))
+    return 0;
+  return attn_layout(L).total;
+}
+
+int qmm_attn_decode(const void *x, int32_t x_dtype, int64_t pos, const qmm_attn_layer *L,
+                    float *kv_cache, void *y, int32_t y_dtype, void *workspace,
+                    size_t workspace_bytes, qmm_stream_t stream) {
+  g_err[0] = '\0';
+  int rc = check_attn_layer(L, "qmm_attn_decode");
+  if (rc) return rc;
+  if (x_dtype != QMM_F32 && x_dtype != QMM_BF16)
+    return fail(QMM_ERR_INVALID_ARG, "qmm_attn_decode: x_dtype must be QMM_F32 or QMM_BF16");
+  if (y_dtype != QMM_F32 && y_dtype != QMM_BF16)
+    return fail(QMM_ERR_INVALID_ARG, "qmm_attn_decode: y_dtype must be QMM_F32 or QMM_BF16");
+  if (pos < 0 || pos >= L->max_seq)
+    return fail(QMM_ERR_INVALID_ARG, "qmm_attn_decode: pos must be in [0, max_seq)");
+  if (!x || !kv_cache || !y)
+    return fail(QMM_ERR_INVALID_ARG, "qmm_attn_decode: null pointer");
+  if (!aligned16(kv_cache))
+    return fail(QMM_ERR_ALIGN, "qmm_attn_decode: kv_cache must be 16-byte aligned");
+  const AttnLayout A = attn_layout(L);
+  if (!workspace || workspace_bytes < A.total)
+    return fail(QMM_ERR_WORKSPACE, "qmm_attn_decode: workspace needs %zu bytes", A.total);
+  if (!aligned256(workspace))
+    return fail(QMM_ERR_ALIGN, "qmm_attn_decode: workspace must be 256-byte aligned");
+  uint8_t *base = static_cast<uint8_t *>(workspace);
+  float *q = reinterpret_cast<float *>(base + A.q), *k = reinterpret_cast<float *>(base + A.k);
+  float *v = reinterpret_cast<float *>(base + A.v);
+  float *attn = reinterpret_cast<float *>(base + A.attn);
+  float *part = reinterpret_cast<float *>(base + A.part);
+  // the three projections, each a fused dequantised linear layer
+  rc = qmm_linear(x, x_dtype, 1, &L->wq, q, QMM_F32, stream);
+  if (rc == QMM_OK) rc = qmm_linear(x, x_dtype, 1, &L->wk, k, QMM_F32, stream);
+  if (rc == QMM_OK) rc = qmm_linear(x, x_dtype, 1, &L->wv, v, QMM_F32, stream);
+  if (rc != QMM_OK) return rc;
+  const cudaError_t e = launch_attn_decode_core(
+      q, k, v, L->n_head, L->n_head_kv, L->head_dim, L->max_seq, pos, L->rope_cos, L->rope_sin,
+      kv_cache, part, attn, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "qmm_attn_decode");
+  // output projection
+  return qmm_linear(attn, QMM_F32, 1, &L->wo, y, y_dtype, stream);
+}
+
+}  // extern "C"

@@ -116,6 +116,19 @@ cudaError_t launch_moe_combine(int64_t M, int k, int64_t H, const float *topk_w,
 }  // namespace qmm
 
 namespace qmm {
+// Decode attention (attn.cu): the RoPE table, and the steps between the
+// projections (rotation and cache write, chunked softmax-weighted sums,
+// their merge).  part: [n_head, attn_chunks(pos + 1), head_dim + 2] fp32.
+int attn_chunks(int64_t T);
+cudaError_t launch_rope_table(int64_t max_seq, int head_dim, double base, float *cos_t,
+                              float *sin_t, cudaStream_t s);
+cudaError_t launch_attn_decode_core(float *q, const float *k, const float *v, int n_head,
+                                    int n_kv, int head_dim, int64_t max_seq, int64_t pos,
+                                    const float *cos_t, const float *sin_t, float *cache,
+                                    float *part, float *attn_out, cudaStream_t s);
+}  // namespace qmm
+
+namespace qmm {
 // Rows of `copies` matrices (row = `rowbytes` of codes + G groups) one copy
 // slot of the CUDA-core kernels holds per tile; 0 if a row does not fit.
 int gemv_rows_per_tile(int64_t rowbytes, int64_t G, int copies);

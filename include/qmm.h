@@ -10,7 +10,8 @@
  *       INT4 codes per byte), section 3.3 (the matmul), section 3.4 (softmax
  *       with the maximum subtracted) and section 3.5 (MoE router = linear +
  *       softmax + top-k; tokens grouped by expert; weighted sum of expert
- *       outputs).
+ *       outputs).  Section 3.4 also defines the decode attention step
+ *       (rotary positions from a precomputed table, KV cache, softmax).
  *  [P2] "ds4 code walkthrough", Trace 2 (256 experts, 6 per token, width 4096)
  *       and Trace 3 (opaque C API style), the allocation guard (no allocation
  *       inside the generation loop).
@@ -226,6 +227,62 @@ int moe_ffn_forward(const void *x, int32_t x_dtype, int64_t M,
                     const moe_experts *ex, void *y, int32_t y_dtype,
                     void *workspace, size_t workspace_bytes,
                     qmm_stream_t stream);
+
+/*
+ * Rotary-position table [P1 section 3.4: RoPE rotates pairs of Q/K
+ * dimensions by position-dependent angles, from a cos/sin table
+ * [max_seq_len, head_dim/2] precomputed once]:
+ *   cos_t[p, i] = cos(p * base^(-2i / head_dim)),  sin_t[p, i] = sin(...)
+ * for 0 <= p < max_seq, 0 <= i < head_dim / 2, evaluated in double and
+ * rounded to fp32.  The page gives no base; 10000 is the usual one.
+ * cos_t, sin_t: device, fp32 [max_seq, head_dim / 2].  head_dim even.
+ */
+int qmm_rope_table(int64_t max_seq, int32_t head_dim, double base, float *cos_t, float *sin_t,
+                   qmm_stream_t stream);
+
+/* One attention layer for decoding (device pointers in the weights and
+ * tables).  Query heads n_head, key/value heads n_head_kv (n_head a multiple
+ * of it: query head h reads key/value head h / (n_head / n_head_kv)),
+ * head_dim a multiple of 4 in [4, 512], max_seq cache rows (<= 2^31).
+ * wq [n_head * head_dim, D], wk and wv [n_head_kv * head_dim, D],
+ * wo [D_out, n_head * head_dim]: quantised weights as for qmm_linear.
+ * rope_cos / rope_sin: tables from qmm_rope_table for max_seq and head_dim. */
+typedef struct qmm_attn_layer {
+  int32_t n_head, n_head_kv, head_dim;
+  int64_t max_seq;
+  qmm_weight wq, wk, wv, wo;
+  const float *rope_cos, *rope_sin;
+} qmm_attn_layer;
+
+/* Bytes of device workspace qmm_attn_decode needs (0 for an invalid layer). */
+size_t qmm_attn_decode_workspace_bytes(const qmm_attn_layer *L);
+
+/*
+ * One decode step of an attention layer for one token at position pos
+ * [P1 section 3.4], with the projections as fused dequantised linear layers
+ * (qmm_linear):
+ *   q = x Wq^T, k = x Wk^T, v = x Wv^T (fp32);
+ *   pairs (2i, 2i+1) of every head of q and k rotated by the angles of row pos
+ *   of the table: (a, b) -> (a cos - b sin, a sin + b cos);
+ *   kv_cache row pos <- rotated k (keys) and v (values);
+ *   for each query head: s_t = q . k_t / sqrt(head_dim) over rows 0..pos,
+ *   p = softmax(s) with the maximum subtracted first, o = sum_t p_t v_t;
+ *   y = o Wo^T.
+ * kv_cache: device fp32 [2][n_head_kv][max_seq][head_dim] (keys, then values:
+ * one layer of the page's [layers, 2, heads, max_seq, head_dim] cache),
+ * 16-byte aligned; rows < pos must hold the earlier steps' keys and values,
+ * rows > pos are neither read nor written.  x: [D] fp32 or bf16; y: [D_out]
+ * fp32 or bf16.  workspace: device scratch of qmm_attn_decode_workspace_bytes
+ * bytes, 256-byte aligned; contents on entry do not matter.  The softmax is
+ * split over chunks of 64 rows whose partial results are merged in a fixed
+ * order (results reproducible bit for bit).  Accuracy: fp32 arithmetic; the
+ * tests hold every stage to 1e-5 * sum |terms| + 1e-6 and propagate it to y.
+ * Requires 0 <= pos < max_seq.  Seven kernel launches, asynchronous on
+ * `stream`.
+ */
+int qmm_attn_decode(const void *x, int32_t x_dtype, int64_t pos, const qmm_attn_layer *L,
+                    float *kv_cache, void *y, int32_t y_dtype, void *workspace,
+                    size_t workspace_bytes, qmm_stream_t stream);
 
 /*
  * Allocation-free router (no counterpart on the pages: it is a calling

@@ -277,3 +277,70 @@ int main(void) {
     assert r.returncode == 0, r.stderr
     r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=120)
     assert r.returncode == 0 and r.stdout.startswith("ok"), (r.returncode, r.stdout, r.stderr)
+
+
+# ------------------------------------------------------------ decode attention
+
+def _attn(L, n_head=4, n_kv=2, hd=32, max_seq=16, D=128, **over):
+    # the structure types the loaded library was declared with (an earlier
+    # test reloads the binding module, which makes new classes)
+    AL = L.qmm_attn_decode_workspace_bytes.argtypes[0]._type_
+    W = dict(AL._fields_)["wq"]
+
+    def w(N, K):
+        return W(8, 64, N, K, P, P, P)
+
+    layer = AL(n_head, n_kv, hd, max_seq, w(n_head * hd, D), w(n_kv * hd, D), w(n_kv * hd, D),
+               w(D, n_head * hd), P, P)
+    for k, v in over.items():
+        if k in ("wq", "wk", "wv", "wo"):
+            v = w(*v)
+        setattr(layer, k, v)
+    return layer
+
+
+def test_rope_table_rejects(Lfake):
+    f = Lfake.qmm_rope_table
+    assert f(0, 64, 10000.0, P, P2, None) == q.QMM_ERR_INVALID_ARG
+    assert f(16, 63, 10000.0, P, P2, None) == q.QMM_ERR_INVALID_ARG
+    assert f(16, 64, 0.0, P, P2, None) == q.QMM_ERR_INVALID_ARG
+    assert f(16, 64, -1.0, P, P2, None) == q.QMM_ERR_INVALID_ARG
+    assert f(16, 64, 10000.0, None, P2, None) == q.QMM_ERR_INVALID_ARG
+    assert f(16, 64, 10000.0, P + 2, P2, None) == q.QMM_ERR_ALIGN
+
+
+def test_attn_workspace_bytes(L):
+    f = L.qmm_attn_decode_workspace_bytes
+    assert f(None) == 0
+    assert f(ctypes.byref(_attn(L, head_dim=3))) == 0
+    assert f(ctypes.byref(_attn(L, max_seq=0))) == 0
+    # q, k, v, output rows, and n_head x ceil(max_seq / 64) x (head_dim + 2) partials
+    small = f(ctypes.byref(_attn(L, max_seq=64)))
+    more = f(ctypes.byref(_attn(L, max_seq=65)))
+    assert small > 0 and more - small == ((4 * 2 * 34 * 4 + 255) // 256 * 256
+                                          - (4 * 1 * 34 * 4 + 255) // 256 * 256)
+
+
+def test_attn_decode_rejects(Lfake):
+    ws = Lfake.qmm_attn_decode_workspace_bytes(ctypes.byref(_attn(Lfake)))
+
+    def call(layer=None, pos=3, dt=q.QMM_F32, ydt=q.QMM_F32, x=P, cache=P, y=P, w=P2, wsb=ws):
+        layer = _attn(Lfake) if layer is None else layer
+        return Lfake.qmm_attn_decode(x, dt, pos, ctypes.byref(layer), cache, y, ydt, w, wsb, None)
+
+    assert call(pos=16) == q.QMM_ERR_INVALID_ARG
+    assert call(pos=-1) == q.QMM_ERR_INVALID_ARG
+    assert call(layer=_attn(Lfake, n_head=3)) == q.QMM_ERR_INVALID_ARG
+    assert call(layer=_attn(Lfake, n_kv=0)) == q.QMM_ERR_INVALID_ARG
+    assert call(layer=_attn(Lfake, hd=6)) == q.QMM_ERR_UNSUPPORTED
+    assert call(layer=_attn(Lfake, hd=1024)) == q.QMM_ERR_UNSUPPORTED
+    assert call(layer=_attn(Lfake, wk=(3 * 32, 128))) == q.QMM_ERR_SHAPE
+    assert call(layer=_attn(Lfake, wo=(128, 64))) == q.QMM_ERR_SHAPE
+    assert call(layer=_attn(Lfake, rope_cos=None)) == q.QMM_ERR_INVALID_ARG
+    assert call(dt=2) == q.QMM_ERR_INVALID_ARG
+    assert call(ydt=5) == q.QMM_ERR_INVALID_ARG
+    assert call(x=None) == q.QMM_ERR_INVALID_ARG
+    assert call(cache=P + 4) == q.QMM_ERR_ALIGN
+    assert call(wsb=ws - 1) == q.QMM_ERR_WORKSPACE
+    assert call(w=None) == q.QMM_ERR_WORKSPACE
+    assert call(w=P2 + 16) == q.QMM_ERR_ALIGN
