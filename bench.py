@@ -552,6 +552,92 @@ def run_cfg1(dev, steps: int):
             "weight_bytes": weight_bytes(r.N, r.K, r.bits, r.group)}
 
 
+ATTN = dict(D=4096, n_head=32, n_kv=32, hd=128, max_seq=4096, pos=511, bits=8, group=64)
+
+
+def _attn_setup(dev):
+    """The attention layer of the decode workload: width 4096, 32 heads of
+    128, INT8 g64 projections (seeded N(0, 0.02) weights quantised on the
+    GPU, q/k/v stacked in one matrix), a 4096-row cache whose first 511 rows
+    hold seeded N(0, 1) values, the token at position 511 (a 512-token
+    context)."""
+    import torch
+    import synth
+    import group_quantized_moe_gb300 as q
+    a = ATTN
+    D, nq, nk = a["D"], a["n_head"] * a["hd"], a["n_kv"] * a["hd"]
+    ws = [torch.from_numpy(synth.normal(91, i, N * K, 0.02).reshape(N, K)).to(dev)
+          for i, (N, K) in enumerate(((nq, D), (nk, D), (nk, D), (D, nq)))]
+    # q, k and v quantised as one stacked matrix: one projection launch
+    layer = q.quantize_attn_layer(*ws, a["n_head"], a["n_kv"], a["hd"], a["max_seq"],
+                                  a["bits"], a["group"])
+    del ws
+    cache = torch.from_numpy(synth.normal(92, 0, 2 * a["n_kv"] * a["max_seq"] * a["hd"]).reshape(
+        2, a["n_kv"], a["max_seq"], a["hd"])).to(dev)
+    x = torch.from_numpy(synth.normal(93, 0, D)).to(dev)
+    return layer, cache, x
+
+
+def run_attn_decode(dev, steps: int, peaks):
+    """One decode step of the attention layer (projections, RoPE and cache
+    write, attention over 512 rows, output projection), timed alone after an
+    L2 flush; bytes = the four quantised weights + the 512 cache rows read."""
+    import torch
+    import group_quantized_moe_gb300 as q
+    a = ATTN
+    layer, cache, x = _attn_setup(dev)
+    y = torch.empty((a["D"],), dtype=torch.float32, device=dev)
+    wsp = torch.empty((q.qmm_attn_decode_workspace_bytes(layer),), dtype=torch.uint8, device=dev)
+    flush = torch.empty((256 << 20,), dtype=torch.uint8, device=dev)
+    s = torch.cuda.current_stream()
+    for _ in range(5):
+        q.attn_decode(x, a["pos"], layer, cache, y=y, workspace=wsp, stream=s)
+    torch.cuda.synchronize()
+    n0 = q.qmm_launch_count()
+    q.attn_decode(x, a["pos"], layer, cache, y=y, workspace=wsp, stream=s)
+    launches = q.qmm_launch_count() - n0
+    ts = []
+    for _ in range(max(10, min(steps, 200))):
+        flush.zero_()
+        torch.cuda._sleep(100000)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        q.attn_decode(x, a["pos"], layer, cache, y=y, workspace=wsp, stream=s)
+        e1.record(s)
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1))
+    D, nq, nk = a["D"], a["n_head"] * a["hd"], a["n_kv"] * a["hd"]
+    wbytes = sum(weight_bytes(N, K, a["bits"], a["group"])
+                 for N, K in ((nq, D), (nk, D), (nk, D), (D, nq)))
+    kvbytes = 2 * nk * (a["pos"] + 1) * 4
+    ms = float(np.median(ts))
+    return {"workload": "attention decode: x[4096] -> INT8 g64 Wq/Wk/Wv [4096,4096], RoPE, "
+                        "32 heads x 128 over 512 cache rows, Wo [4096,4096]",
+            "us_per_step": ms * 1e3, "us_per_step_min": float(np.min(ts)) * 1e3,
+            "bytes": wbytes + kvbytes, "weight_bytes": wbytes, "kv_bytes": kvbytes,
+            "gbs": (wbytes + kvbytes) / (ms * 1e-3) / 1e9,
+            "hbm_frac": (wbytes + kvbytes) / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+            "gpu_launches_per_step": launches,
+            "l2": "256 MB written between steps"}
+
+
+def oracle_attn_step():
+    """The oracle's decode step on the same workload (seconds, one thread)."""
+    import oracle
+    import synth
+    a = ATTN
+    D, nq, nk = a["D"], a["n_head"] * a["hd"], a["n_kv"] * a["hd"]
+    ws = [oracle.quantize(synth.normal(91, i, N * K, 0.02).reshape(N, K), a["bits"], a["group"])
+          for i, (N, K) in enumerate(((nq, D), (nk, D), (nk, D), (D, nq)))]
+    c, sn = oracle.rope_table(a["max_seq"], a["hd"], 10000.0)
+    cache = synth.normal(92, 0, 2 * a["n_kv"] * a["max_seq"] * a["hd"]).reshape(
+        2, a["n_kv"], a["max_seq"], a["hd"])
+    x = synth.normal(93, 0, D)
+    t0 = time.perf_counter()
+    oracle.attn_decode(x, a["pos"], a["n_head"], a["n_kv"], a["hd"], *ws, c, sn, cache)
+    return time.perf_counter() - t0
+
+
 # ------------------------------------------------------------ oracle (CPU)
 
 def oracle_gemv_sample(seconds: float):
@@ -780,7 +866,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-moe", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
-    ap.add_argument("--only", choices=["gemv", "moe_decode", "moe_prefill", "linear_batched"],
+    ap.add_argument("--only", choices=["gemv", "moe_decode", "moe_prefill", "linear_batched",
+                                       "attn_decode"],
                     default=None,
                     help="run one workload only (profiling)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
@@ -821,6 +908,10 @@ def main():
     if args.only == "linear_batched":
         if rank == 0:
             print(json.dumps({"only": args.only, **run_linear_batched(dev, args.steps)}))
+        return
+    if args.only == "attn_decode":
+        if rank == 0:
+            print(json.dumps({"only": args.only, **run_attn_decode(dev, args.steps, peaks)}))
         return
     if args.only in ("moe_decode", "moe_prefill"):
         r = recipes.CFG4 if args.only == "moe_decode" else recipes.CFG5
@@ -885,6 +976,10 @@ def main():
             line["linear_batched"] = run_linear_batched(dev, args.steps)
         except Exception as e:  # keep the headline line even if an extra fails
             line["linear_batched"] = {"error": f"{type(e).__name__}: {e}"}
+        try:
+            line["attn_decode"] = run_attn_decode(dev, args.steps, peaks)
+        except Exception as e:  # keep the headline line even if an extra fails
+            line["attn_decode"] = {"error": f"{type(e).__name__}: {e}"}
         release()
     if not args.no_moe and args.only is None:
         extras = {}
@@ -903,6 +998,14 @@ def main():
         line.update(extras)
     if rank == 0 and not args.no_cpu:
         line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
+        if isinstance(line.get("attn_decode"), dict) and "error" not in line["attn_decode"]:
+            try:
+                sec = oracle_attn_step()
+                line["attn_decode"]["cpu_baseline"] = {
+                    "value": sec * 1e6, "unit": "us per step", "cores": 1, "kind": "oracle",
+                    "sample": "one decode step of the same workload (fp64, with error bounds)"}
+            except Exception as e:  # the GPU figures stand without it
+                line["attn_decode"]["cpu_baseline"] = {"error": f"{type(e).__name__}: {e}"}
         workers = max(1, host_cores() - 1)
         for key, r in (("moe_decode", recipes.CFG4), ("moe_prefill", recipes.CFG5)):
             if isinstance(line.get(key), dict) and "error" not in line[key]:

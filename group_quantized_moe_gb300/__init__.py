@@ -205,6 +205,11 @@ class QWeight:
         return _Weight(self.bits, self.group, self.N, self.K, _ptr(self.codes), _ptr(self.scales),
                        _ptr(self.zps))
 
+    def rows(self, r0: int, r1: int) -> "QWeight":
+        """Rows [r0, r1) as a QWeight sharing this one's storage."""
+        return QWeight(self.bits, self.group, r1 - r0, self.K, self.codes[r0:r1],
+                       self.scales[r0:r1], self.zps[r0:r1])
+
 
 def alloc_qweight(N: int, K: int, bits: int, group: int, device="cuda") -> QWeight:
     """Uninitialised output buffers for qmm_quantize_groupwise."""
@@ -605,6 +610,21 @@ class AttnLayer:
         """A zeroed cache [2, n_head_kv, max_seq, head_dim] fp32."""
         return torch.zeros((2, self.n_head_kv, self.max_seq, self.head_dim),
                            dtype=torch.float32, device=device)
+
+
+def quantize_attn_layer(wq: torch.Tensor, wk: torch.Tensor, wv: torch.Tensor, wo: torch.Tensor,
+                        n_head: int, n_head_kv: int, head_dim: int, max_seq: int, bits: int = 8,
+                        group: int = 64, base: float = 10000.0, stream=None) -> AttnLayer:
+    """An AttnLayer from fp32 weights: wq, wk, wv quantised as one stacked
+    matrix (so that the decode step runs the three projections as one
+    launch), wo on its own, and the RoPE table."""
+    nq, nk = wq.shape[0], wk.shape[0]
+    qkv = qmm_quantize_groupwise(torch.cat([wq, wk, wv], dim=0).contiguous(), bits, group,
+                                 stream=stream)
+    c, s = rope_table(max_seq, head_dim, base, device=wq.device, stream=stream)
+    return AttnLayer(n_head, n_head_kv, head_dim, max_seq, qkv.rows(0, nq),
+                     qkv.rows(nq, nq + nk), qkv.rows(nq + nk, nq + 2 * nk),
+                     qmm_quantize_groupwise(wo, bits, group, stream=stream), c, s)
 
 
 def qmm_attn_decode_workspace_bytes(layer: AttnLayer) -> int:

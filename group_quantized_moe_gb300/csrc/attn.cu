@@ -3,13 +3,14 @@
 // 3.4): the kernels between the layer's quantised projections (qmm_linear).
 //
 //   rope_table_kernel  cos / sin of pos * base^(-2i/d), one thread per entry
-//   rope_kv_kernel     rotates the query heads in place and the new key, and
-//                      writes key and value into cache row pos
 //   attn_part_kernel   one CTA per (query head, chunk of 64 cache rows):
-//                      scores q.k / sqrt(d), their maximum, the exponentials
-//                      and their sum, and the exponential-weighted sum of the
-//                      value rows (a split of the softmax over the rows, so
-//                      that long caches spread over the SMs)
+//                      rotates the query (and, in the last chunk, this
+//                      step's key, which it writes to cache row pos with the
+//                      value), then the scores q.k / sqrt(d), their maximum,
+//                      the exponentials and their sum, and the
+//                      exponential-weighted sum of the value rows (a split of
+//                      the softmax over the rows, so that long caches spread
+//                      over the SMs)
 //   attn_merge_kernel  one CTA per query head: the chunks' partial results
 //                      rescaled to the overall maximum and summed in chunk
 //                      order, divided by the overall sum
@@ -27,7 +28,7 @@ namespace qmm {
 namespace {
 
 constexpr int kChunk = 64;      // cache rows per partial CTA
-constexpr int kPartThreads = 128;
+constexpr int kPartThreads = 256;
 
 __global__ void __launch_bounds__(256) rope_table_kernel(int64_t max_seq, int head_dim,
                                                           double base, float *cos_t,
@@ -46,72 +47,131 @@ __global__ void __launch_bounds__(256) rope_table_kernel(int64_t max_seq, int he
   }
 }
 
-// Pairs (2i, 2i + 1) of every head vector rotate by the angle of position
-// pos: (a, b) -> (a c - b s, a s + b c).  Threads [0, n_head hp) take the
-// query pairs (in place), the next n_kv hp the key pairs (to cache row pos),
-// the next n_kv d the value elements.
-__global__ void __launch_bounds__(256) rope_kv_kernel(float *q, const float *k, const float *v,
-                                                      int n_head, int n_kv, int head_dim,
-                                                      int64_t max_seq, int64_t pos,
-                                                      const float *cos_t, const float *sin_t,
-                                                      float *cache) {
-  pdl_enter();
-  const int hp = head_dim / 2;
-  const int nq = n_head * hp, nk = n_kv * hp, nv = n_kv * head_dim;
-  const int u = blockIdx.x * blockDim.x + threadIdx.x;
-  if (u < nq + nk) {
-    const bool isq = u < nq;
-    const int w = isq ? u : u - nq;  // pair index within q or k
-    const int h = w / hp, i = w - h * hp;
-    const float c = cos_t[pos * hp + i], s = sin_t[pos * hp + i];
-    const float *src = isq ? q : k;
-    const float a = src[h * head_dim + 2 * i], b = src[h * head_dim + 2 * i + 1];
-    const float r0 = fmaf(a, c, -b * s), r1 = fmaf(a, s, b * c);
-    float *dst = isq ? q + h * head_dim : cache + (static_cast<int64_t>(h) * max_seq + pos) * head_dim;
-    dst[2 * i] = r0;
-    dst[2 * i + 1] = r1;
-  } else if (u < nq + nk + nv) {
-    const int w = u - nq - nk;
-    const int h = w / head_dim, d = w - h * head_dim;
-    cache[(static_cast<int64_t>(n_kv + h) * max_seq + pos) * head_dim + d] = v[w];
-  }
-}
-
 // Partial softmax-weighted sum over cache rows [c * 64, min(T, c * 64 + 64))
-// of query head blockIdx.x (key/value head blockIdx.x / (n_head / n_kv)):
-// part = {max score, sum of exp(score - max), sum of exp(score - max) v}.
-__global__ void __launch_bounds__(kPartThreads) attn_part_kernel(const float *q,
-                                                                 const float *cache, int n_head,
-                                                                 int n_kv, int head_dim,
-                                                                 int64_t max_seq, int64_t T,
-                                                                 float scale, float *part) {
+// of query head blockIdx.x (key/value head kvh = blockIdx.x / (n_head /
+// n_kv)): part = {max score, sum of exp(score - max), sum of
+// exp(score - max) v}.  The query arrives unrotated and is rotated here
+// (pairs (2i, 2i + 1) by the angles of position pos: (a, b) ->
+// (a c - b s, a s + b c)); the last chunk also takes this step's key (rotated
+// here) and value from the projections for row pos, which the CTA of the
+// group's first query head writes to the cache.
+// 256 threads: warp w scores rows 8w .. 8w + 7 (lane l holds the 16-byte
+// column units l, l + 32, ...; a batch of rows' loads is in flight before
+// the sums); the value rows are summed by (row group, column unit) threads
+// and the row groups combined in order.
+template <int NU>  // 16-byte column units per lane: ceil(head_dim / 128)
+__global__ void __launch_bounds__(kPartThreads) attn_part_kernel(
+    const float *q, const float *knew, const float *vnew, float *cache, int n_head, int n_kv,
+    int head_dim, int64_t max_seq, int64_t pos, const float *cos_t, const float *sin_t,
+    float scale, float *part) {
   __shared__ __align__(16) float qs[512];
+  __shared__ __align__(16) float kn[512];
+  __shared__ __align__(16) float vn[512];
   __shared__ float ps[kChunk];
   __shared__ float red[kPartThreads / 32];
+  __shared__ __align__(16) float4 vred[kPartThreads];
   pdl_enter();
   const int h = blockIdx.x, c = blockIdx.y;
-  const int kvh = h / (n_head / n_kv);
+  const int grp = n_head / n_kv, kvh = h / grp;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t T = pos + 1;
   const int64_t t0 = static_cast<int64_t>(c) * kChunk;
   const int nt = static_cast<int>(min64(kChunk, T - t0));
-  for (int d = threadIdx.x; d < head_dim; d += kPartThreads) qs[d] = q[h * head_dim + d];
+  const bool last = t0 + nt == T;         // this chunk holds row pos ...
+  const int nc = last ? nt - 1 : nt;      // ... which is not read from the cache
+  const int hp = head_dim / 2, d4 = head_dim / 4;
+  const float *cr = cos_t + pos * hp, *sr = sin_t + pos * hp;
+  for (int i = threadIdx.x; i < hp; i += kPartThreads) {
+    const float cc = cr[i], ss = sr[i];
+    const float a = q[h * head_dim + 2 * i], b = q[h * head_dim + 2 * i + 1];
+    qs[2 * i] = fmaf(a, cc, -b * ss);
+    qs[2 * i + 1] = fmaf(a, ss, b * cc);
+    if (last) {
+      const float ka = knew[kvh * head_dim + 2 * i], kb = knew[kvh * head_dim + 2 * i + 1];
+      kn[2 * i] = fmaf(ka, cc, -kb * ss);
+      kn[2 * i + 1] = fmaf(ka, ss, kb * cc);
+      vn[2 * i] = vnew[kvh * head_dim + 2 * i];
+      vn[2 * i + 1] = vnew[kvh * head_dim + 2 * i + 1];
+    }
+  }
   __syncthreads();
-  // scores: warp w takes rows w, w + 4, ...; lane l columns 4l + 128j
+  if (last && h % grp == 0) {  // this step's key and value into cache row pos
+    float *kd = cache + (static_cast<int64_t>(kvh) * max_seq + pos) * head_dim;
+    float *vd = cache + (static_cast<int64_t>(n_kv + kvh) * max_seq + pos) * head_dim;
+    for (int d = threadIdx.x; d < head_dim; d += kPartThreads) {
+      kd[d] = kn[d];
+      vd[d] = vn[d];
+    }
+  }
+  // value rows of this thread (row group g, column unit u: rows g, g + RG,
+  // ...), requested now so that their latency overlaps the scores
+  const float *vb = cache + (static_cast<int64_t>(n_kv + kvh) * max_seq + t0) * head_dim;
+  const int RG = kPartThreads / d4;  // row groups (>= 2: head_dim <= 512)
+  const int g = threadIdx.x / d4, u = threadIdx.x - g * d4;
+  constexpr int VPF = NU == 1 ? 8 : 1;  // value rows held per thread (RG >= 8 when NU == 1)
+  float4 vpre[VPF];
+#pragma unroll
+  for (int i = 0; i < VPF; ++i) {
+    const int r = g + RG * i;
+    vpre[i] = (g < RG && r < nc)
+                  ? __ldg(reinterpret_cast<const float4 *>(vb + static_cast<int64_t>(r) * head_dim) + u)
+                  : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  // scores of the cache rows
+  float4 qv[NU];
+#pragma unroll
+  for (int u = 0; u < NU; ++u) {
+    const int j = lane + 32 * u;
+    qv[u] = j < d4 ? reinterpret_cast<const float4 *>(qs)[j] : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  constexpr int RPW = kChunk / (kPartThreads / 32);  // rows per warp
+  constexpr int RB = NU == 1 ? 8 : NU == 2 ? 4 : 2;  // rows per batch of loads
   const float *kb = cache + (static_cast<int64_t>(kvh) * max_seq + t0) * head_dim;
-  const int d4 = head_dim / 4;
-  for (int r = warp; r < nt; r += kPartThreads / 32) {
-    const float4 *kr = reinterpret_cast<const float4 *>(kb + static_cast<int64_t>(r) * head_dim);
+#pragma unroll 1
+  for (int rb = 0; rb < RPW; rb += RB) {
+    float4 kv[RB][NU];
+#pragma unroll
+    for (int r = 0; r < RB; ++r) {
+      const int row = warp * RPW + rb + r;
+#pragma unroll
+      for (int u = 0; u < NU; ++u) {
+        const int j = lane + 32 * u;
+        kv[r][u] = (row < nc && j < d4)
+                       ? __ldg(reinterpret_cast<const float4 *>(kb + static_cast<int64_t>(row) *
+                                                                         head_dim) + j)
+                       : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < RB; ++r) {
+      float acc = 0.0f;
+#pragma unroll
+      for (int u = 0; u < NU; ++u) {
+        acc = fmaf(qv[u].x, kv[r][u].x, acc);
+        acc = fmaf(qv[u].y, kv[r][u].y, acc);
+        acc = fmaf(qv[u].z, kv[r][u].z, acc);
+        acc = fmaf(qv[u].w, kv[r][u].w, acc);
+      }
+      acc = warp_sum(acc);
+      const int row = warp * RPW + rb + r;
+      if (lane == 0 && row < nc) ps[row] = acc * scale;
+    }
+  }
+  if (last && warp == 0) {  // the score of row pos, from the rotated new key
     float acc = 0.0f;
-    for (int j = lane; j < d4; j += 32) {
-      const float4 kv = kr[j];
-      const float4 qv = *reinterpret_cast<const float4 *>(qs + 4 * j);
-      acc = fmaf(qv.x, kv.x, acc);
-      acc = fmaf(qv.y, kv.y, acc);
-      acc = fmaf(qv.z, kv.z, acc);
-      acc = fmaf(qv.w, kv.w, acc);
+#pragma unroll
+    for (int u = 0; u < NU; ++u) {
+      const int j = lane + 32 * u;
+      if (j < d4) {
+        const float4 kk = reinterpret_cast<const float4 *>(kn)[j];
+        acc = fmaf(qv[u].x, kk.x, acc);
+        acc = fmaf(qv[u].y, kk.y, acc);
+        acc = fmaf(qv[u].z, kk.z, acc);
+        acc = fmaf(qv[u].w, kk.w, acc);
+      }
     }
     acc = warp_sum(acc);
-    if (lane == 0) ps[r] = acc * scale;
+    if (lane == 0) ps[nt - 1] = acc * scale;
   }
   __syncthreads();
   // maximum and exponentials (thread r < nt owns row r)
@@ -122,19 +182,63 @@ __global__ void __launch_bounds__(kPartThreads) attn_part_kernel(const float *q,
   __syncthreads();
   if (threadIdx.x < nt) ps[threadIdx.x] = e;
   // sum of the exponentials: warp sums, then the warps in order
-  const float ws = warp_sum(e);
-  if (lane == 0) red[warp] = ws;
+  const float wsum = warp_sum(e);
+  if (lane == 0) red[warp] = wsum;
   __syncthreads();
   float l = 0.0f;
 #pragma unroll
   for (int w = 0; w < kPartThreads / 32; ++w) l += red[w];
-  // exponential-weighted sum of the value rows, rows in order
-  const float *vb = cache + (static_cast<int64_t>(n_kv + kvh) * max_seq + t0) * head_dim;
+  // value rows: thread (g, u) sums rows g, g + RG, ... of column unit u
+  // (the first VPF of them already in registers); row pos (the new value)
+  // comes last, after the row groups are combined
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (g < RG) {
+#pragma unroll
+    for (int i = 0; i < VPF; ++i) {
+      const int r = g + RG * i;
+      if (r < nc) {
+        const float p = ps[r];
+        acc.x = fmaf(p, vpre[i].x, acc.x);
+        acc.y = fmaf(p, vpre[i].y, acc.y);
+        acc.z = fmaf(p, vpre[i].z, acc.z);
+        acc.w = fmaf(p, vpre[i].w, acc.w);
+      }
+    }
+#pragma unroll 4
+    for (int r = g + RG * VPF; r < nc; r += RG) {
+      const float p = ps[r];
+      const float4 vv = __ldg(reinterpret_cast<const float4 *>(vb + static_cast<int64_t>(r) *
+                                                                        head_dim) + u);
+      acc.x = fmaf(p, vv.x, acc.x);
+      acc.y = fmaf(p, vv.y, acc.y);
+      acc.z = fmaf(p, vv.z, acc.z);
+      acc.w = fmaf(p, vv.w, acc.w);
+    }
+  }
+  vred[threadIdx.x] = acc;
+  __syncthreads();
   float *out = part + (static_cast<int64_t>(h) * gridDim.y + c) * (head_dim + 2);
-  for (int d = threadIdx.x; d < head_dim; d += kPartThreads) {
-    float acc = 0.0f;
-    for (int r = 0; r < nt; ++r) acc = fmaf(ps[r], vb[static_cast<int64_t>(r) * head_dim + d], acc);
-    out[2 + d] = acc;
+  if (threadIdx.x < d4) {
+    float4 t = vred[threadIdx.x];
+    for (int gg = 1; gg < RG; ++gg) {
+      const float4 o = vred[gg * d4 + threadIdx.x];
+      t.x += o.x;
+      t.y += o.y;
+      t.z += o.z;
+      t.w += o.w;
+    }
+    if (last) {
+      const float p = ps[nt - 1];
+      const float4 vv = reinterpret_cast<const float4 *>(vn)[threadIdx.x];
+      t.x = fmaf(p, vv.x, t.x);
+      t.y = fmaf(p, vv.y, t.y);
+      t.z = fmaf(p, vv.z, t.z);
+      t.w = fmaf(p, vv.w, t.w);
+    }
+    out[2 + 4 * threadIdx.x] = t.x;
+    out[3 + 4 * threadIdx.x] = t.y;
+    out[4 + 4 * threadIdx.x] = t.z;
+    out[5 + 4 * threadIdx.x] = t.w;
   }
   if (threadIdx.x == 0) {
     out[0] = m;
@@ -177,20 +281,24 @@ cudaError_t launch_rope_table(int64_t max_seq, int head_dim, double base, float 
                     max_seq, head_dim, base, cos_t, sin_t);
 }
 
-cudaError_t launch_attn_decode_core(float *q, const float *k, const float *v, int n_head,
+cudaError_t launch_attn_decode_core(const float *q, const float *k, const float *v, int n_head,
                                     int n_kv, int head_dim, int64_t max_seq, int64_t pos,
                                     const float *cos_t, const float *sin_t, float *cache,
                                     float *part, float *attn_out, cudaStream_t s) {
-  const int nthreads = (n_head + n_kv) * (head_dim / 2) + n_kv * head_dim;
-  cudaError_t e = launch_pdl(rope_kv_kernel, dim3((nthreads + 255) / 256), dim3(256), 0, s, q, k,
-                             v, n_head, n_kv, head_dim, max_seq, pos, cos_t, sin_t, cache);
-  if (e != cudaSuccess) return e;
-  const int64_t T = pos + 1;
-  const int nchunk = attn_chunks(T);
+  const int nchunk = attn_chunks(pos + 1);
   const float scale = static_cast<float>(1.0 / sqrt(static_cast<double>(head_dim)));
-  e = launch_pdl(attn_part_kernel, dim3(n_head, nchunk), dim3(kPartThreads), 0, s,
-                 static_cast<const float *>(q), static_cast<const float *>(cache), n_head, n_kv,
-                 head_dim, max_seq, T, scale, part);
+  const dim3 grid(n_head, nchunk);
+  const int nu = (head_dim + 127) / 128;
+  cudaError_t e;
+  if (nu == 1)
+    e = launch_pdl(attn_part_kernel<1>, grid, dim3(kPartThreads), 0, s, q, k, v, cache, n_head,
+                   n_kv, head_dim, max_seq, pos, cos_t, sin_t, scale, part);
+  else if (nu == 2)
+    e = launch_pdl(attn_part_kernel<2>, grid, dim3(kPartThreads), 0, s, q, k, v, cache, n_head,
+                   n_kv, head_dim, max_seq, pos, cos_t, sin_t, scale, part);
+  else
+    e = launch_pdl(attn_part_kernel<4>, grid, dim3(kPartThreads), 0, s, q, k, v, cache, n_head,
+                   n_kv, head_dim, max_seq, pos, cos_t, sin_t, scale, part);
   if (e != cudaSuccess) return e;
   return launch_pdl(attn_merge_kernel, dim3(n_head), dim3(kPartThreads), 0, s,
                     static_cast<const float *>(part), nchunk, head_dim, attn_out);

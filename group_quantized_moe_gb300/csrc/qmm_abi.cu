@@ -498,9 +498,12 @@ AttnLayout attn_layout(const qmm_attn_layer *L) {
   const size_t nq = static_cast<size_t>(L->n_head) * L->head_dim;
   const size_t nk = static_cast<size_t>(L->n_head_kv) * L->head_dim;
   size_t o = 0;
-  a.q = o;    o += round256(4 * nq);
-  a.k = o;    o += round256(4 * nk);
-  a.v = o;    o += round256(4 * nk);
+  // q, k, v back to back (one linear layer fills all three when the weights
+  // are stacked)
+  a.q = o;
+  a.k = a.q + 4 * nq;
+  a.v = a.k + 4 * nk;
+  o = round256(a.v + 4 * nk);
   a.attn = o; o += round256(4 * nq);
   a.part = o; o += round256(4 * static_cast<size_t>(L->n_head) * attn_chunks(L->max_seq) *
                             (L->head_dim + 2));
@@ -526,6 +529,20 @@ int check_attn_layer(const qmm_attn_layer *L, const char *who) {
   if (!L->rope_cos || !L->rope_sin)
     return fail(QMM_ERR_INVALID_ARG, "%s: null RoPE table", who);
   return QMM_OK;
+}
+
+// Whether wk and wv follow wq in memory as rows of one [Nq + 2 Nk, D]
+// matrix (codes, scales and zero points each contiguous, one scheme).
+bool qkv_stacked(const qmm_attn_layer *L) {
+  const qmm_weight &a = L->wq, &b = L->wk, &c = L->wv;
+  if (a.bits != b.bits || a.bits != c.bits || a.group != b.group || a.group != c.group ||
+      a.K != b.K || a.K != c.K || a.group <= 0)
+    return false;
+  const int64_t rb = a.K * a.bits / 8, G = a.K / a.group;
+  auto at = [](const void *p, int64_t off) { return static_cast<const uint8_t *>(p) + off; };
+  return b.codes == at(a.codes, a.N * rb) && c.codes == at(b.codes, b.N * rb) &&
+         b.scales == a.scales + a.N * G && c.scales == b.scales + b.N * G &&
+         b.zps == a.zps + a.N * G && c.zps == b.zps + b.N * G;
 }
 
 }  // namespace
@@ -581,10 +598,17 @@ int qmm_attn_decode(const void *x, int32_t x_dtype, int64_t pos, const qmm_attn_
   float *v = reinterpret_cast<float *>(base + A.v);
   float *attn = reinterpret_cast<float *>(base + A.attn);
   float *part = reinterpret_cast<float *>(base + A.part);
-  // the three projections, each a fused dequantised linear layer
-  rc = qmm_linear(x, x_dtype, 1, &L->wq, q, QMM_F32, stream);
-  if (rc == QMM_OK) rc = qmm_linear(x, x_dtype, 1, &L->wk, k, QMM_F32, stream);
-  if (rc == QMM_OK) rc = qmm_linear(x, x_dtype, 1, &L->wv, v, QMM_F32, stream);
+  // the three projections, fused dequantised linear layers: one launch over
+  // the stacked rows when the weights are stored as one matrix, else three
+  if (qkv_stacked(L)) {
+    qmm_weight w = L->wq;
+    w.N = L->wq.N + L->wk.N + L->wv.N;
+    rc = qmm_linear(x, x_dtype, 1, &w, q, QMM_F32, stream);
+  } else {
+    rc = qmm_linear(x, x_dtype, 1, &L->wq, q, QMM_F32, stream);
+    if (rc == QMM_OK) rc = qmm_linear(x, x_dtype, 1, &L->wk, k, QMM_F32, stream);
+    if (rc == QMM_OK) rc = qmm_linear(x, x_dtype, 1, &L->wv, v, QMM_F32, stream);
+  }
   if (rc != QMM_OK) return rc;
   const cudaError_t e = launch_attn_decode_core(
       q, k, v, L->n_head, L->n_head_kv, L->head_dim, L->max_seq, pos, L->rope_cos, L->rope_sin,

@@ -117,12 +117,13 @@ cudaError_t launch_moe_combine(int64_t M, int k, int64_t H, const float *topk_w,
 
 namespace qmm {
 // Decode attention (attn.cu): the RoPE table, and the steps between the
-// projections (rotation and cache write, chunked softmax-weighted sums,
-// their merge).  part: [n_head, attn_chunks(pos + 1), head_dim + 2] fp32.
+// projections (rotation, cache write and chunked softmax-weighted sums in
+// one kernel, their merge in a second).  q, k, v: the projections
+// (unrotated); part: [n_head, attn_chunks(pos + 1), head_dim + 2] fp32.
 int attn_chunks(int64_t T);
 cudaError_t launch_rope_table(int64_t max_seq, int head_dim, double base, float *cos_t,
                               float *sin_t, cudaStream_t s);
-cudaError_t launch_attn_decode_core(float *q, const float *k, const float *v, int n_head,
+cudaError_t launch_attn_decode_core(const float *q, const float *k, const float *v, int n_head,
                                     int n_kv, int head_dim, int64_t max_seq, int64_t pos,
                                     const float *cos_t, const float *sin_t, float *cache,
                                     float *part, float *attn_out, cudaStream_t s);

@@ -277,7 +277,10 @@ size_t qmm_attn_decode_workspace_bytes(const qmm_attn_layer *L);
  * split over chunks of 64 rows whose partial results are merged in a fixed
  * order (results reproducible bit for bit).  Accuracy: fp32 arithmetic; the
  * tests hold every stage to 1e-5 * sum |terms| + 1e-6 and propagate it to y.
- * Requires 0 <= pos < max_seq.  Seven kernel launches, asynchronous on
+ * Requires 0 <= pos < max_seq.  When wk and wv follow wq in memory as rows of
+ * one [(n_head + 2 n_head_kv) head_dim, D] matrix (codes, scales and zero
+ * points each contiguous, same bits and group), the three projections run as
+ * one launch: four kernel launches in all (else six), asynchronous on
  * `stream`.
  */
 int qmm_attn_decode(const void *x, int32_t x_dtype, int64_t pos, const qmm_attn_layer *L,

@@ -49,8 +49,24 @@ def _to_device(ow, dev):
                      T(ow.zps, dev))
 
 
+def _stacked(ows, dev):
+    """The oracle's wq, wk, wv as one device matrix (row-wise quantisation:
+    the same bytes as quantising the stacked matrix) and three row views."""
+    cat = [np.concatenate([getattr(o, f).reshape(o.N, -1) for o in ows])
+           for f in ("codes", "scales", "zps")]
+    if ows[0].bits == 8:
+        cat[0] = cat[0].view(np.int8)
+    N = sum(o.N for o in ows)
+    big = q.QWeight(ows[0].bits, ows[0].group, N, ows[0].K, *(T(a, dev) for a in cat))
+    out, r = [], 0
+    for o in ows:
+        out.append(big.rows(r, r + o.N))
+        r += o.N
+    return out
+
+
 def _build(dev, seed, D, n_head, n_kv, hd, max_seq, bits=8, group=64, D_out=None,
-           base=10000.0, sigma=0.05):
+           base=10000.0, sigma=0.05, stacked=False):
     D_out = D if D_out is None else D_out
     r = synth.normal
     ow = {
@@ -62,8 +78,11 @@ def _build(dev, seed, D, n_head, n_kv, hd, max_seq, bits=8, group=64, D_out=None
     }
     oc, os_ = oracle.rope_table(max_seq, hd, base)
     gc, gs = q.rope_table(max_seq, hd, base, device=dev)
-    layer = q.AttnLayer(n_head, n_kv, hd, max_seq, *(_to_device(ow[k], dev) for k in
-                                                      ("wq", "wk", "wv", "wo")), gc, gs)
+    if stacked:
+        wqkv = _stacked([ow["wq"], ow["wk"], ow["wv"]], dev)
+    else:
+        wqkv = [_to_device(ow[k], dev) for k in ("wq", "wk", "wv")]
+    layer = q.AttnLayer(n_head, n_kv, hd, max_seq, *wqkv, _to_device(ow["wo"], dev), gc, gs)
     return layer, ow, oc, os_
 
 
@@ -106,13 +125,18 @@ def test_rope_table_matches_oracle(dev):
             assert (np.abs(g - o) <= ulp).all(), (max_seq, hd, base, float(np.abs(g - o).max()))
 
 
-@pytest.mark.parametrize("n_head,n_kv,hd,bits,group", [(4, 4, 64, 8, 64), (8, 2, 32, 4, 128),
-                                                       (6, 1, 128, 8, 32), (2, 2, 512, 8, 64)])
-def test_attn_decode_positions(dev, n_head, n_kv, hd, bits, group):
+@pytest.mark.parametrize("n_head,n_kv,hd,bits,group,stacked",
+                         [(4, 4, 64, 8, 64, False), (8, 2, 32, 4, 128, True),
+                          (6, 1, 128, 8, 32, False), (2, 2, 512, 8, 64, True),
+                          (4, 2, 256, 8, 64, True), (16, 16, 4, 8, 64, False)])
+def test_attn_decode_positions(dev, n_head, n_kv, hd, bits, group, stacked):
     """Positions at chunk edges (one row, the last row of a chunk, the first
-    of the next, a ragged last chunk, the last cache row)."""
+    of the next, a ragged last chunk, the last cache row); head sizes from 4
+    to 512; q/k/v weights stored apart (three projection launches) or as one
+    stacked matrix (one launch)."""
     D, max_seq = 256, 300
-    layer, ow, oc, os_ = _build(dev, 5 + n_head, D, n_head, n_kv, hd, max_seq, bits, group)
+    layer, ow, oc, os_ = _build(dev, 5 + n_head, D, n_head, n_kv, hd, max_seq, bits, group,
+                                stacked=stacked)
     cache = _cache(6 + hd, n_kv, max_seq, hd)
     for pos in (0, 1, 63, 64, 65, 130, max_seq - 1):
         x = synth.normal(7 + pos, 1, D)
@@ -158,7 +182,7 @@ def test_attn_decode_full_size(dev):
     """Width 4096, 32 heads of 128 (multi-head), INT8 g64 projections, a
     4096-row cache, the token at position 511 (a 512-token context)."""
     D, n_head, n_kv, hd, max_seq, pos = 4096, 32, 32, 128, 4096, 511
-    layer, ow, oc, os_ = _build(dev, 41, D, n_head, n_kv, hd, max_seq, sigma=0.02)
+    layer, ow, oc, os_ = _build(dev, 41, D, n_head, n_kv, hd, max_seq, sigma=0.02, stacked=True)
     cache = _cache(42, n_kv, max_seq, hd)
     _check_step(dev, layer, ow, oc, os_, synth.normal(43, 1, D), pos, cache, what="full")
 
@@ -187,3 +211,30 @@ def test_attn_decode_rejects_bad_arguments(dev):
     with pytest.raises(q.QmmError):
         q.attn_decode(x, 0, bad, cd)                  # n_head not a multiple of n_kv
     assert (cd == 0).all()                            # nothing was enqueued
+
+
+def test_attn_decode_launches(dev):
+    """Stacked q/k/v weights: one projection launch, then the attention's two
+    kernels and the output projection; apart: three projection launches.
+    quantize_attn_layer builds the stacked form."""
+    D, n_head, n_kv, hd, max_seq = 256, 4, 2, 64, 64
+    for stacked, expect in ((True, 4), (False, 6)):
+        layer, ow, oc, os_ = _build(dev, 71, D, n_head, n_kv, hd, max_seq, stacked=stacked)
+        cd = layer.kv_cache(dev)
+        x = T(synth.normal(72, 1, D), dev)
+        q.attn_decode(x, 3, layer, cd)
+        torch.cuda.synchronize()
+        n0 = q.qmm_launch_count()
+        q.attn_decode(x, 3, layer, cd)
+        assert q.qmm_launch_count() - n0 == expect
+    wq, wk, wv = (torch.from_numpy(synth.normal(73, i, n * D, 0.05).reshape(n, D)).to(dev)
+                  for i, n in enumerate((n_head * hd, n_kv * hd, n_kv * hd)))
+    wo = torch.from_numpy(synth.normal(74, 0, D * n_head * hd, 0.05).reshape(D, n_head * hd))
+    layer = q.quantize_attn_layer(wq, wk, wv, wo.to(dev), n_head, n_kv, hd, max_seq)
+    cd = layer.kv_cache(dev)
+    x = T(synth.normal(75, 1, D), dev)
+    q.attn_decode(x, 0, layer, cd)
+    torch.cuda.synchronize()
+    n0 = q.qmm_launch_count()
+    q.attn_decode(x, 1, layer, cd)
+    assert q.qmm_launch_count() - n0 == 4
