@@ -38,7 +38,7 @@ EXPORTED = ("qmm_quantize_groupwise", "qmm_linear", "moe_route_workspace_bytes",
             "qmm_device_status", "moe_route_topk_noalloc", "moe_route_load_stats",
             "qmm_diag_wait_timeout", "qmm_linear_batched_workspace_bytes",
             "qmm_linear_batched", "qmm_rope_table", "qmm_attn_decode_workspace_bytes",
-            "qmm_attn_decode")
+            "qmm_attn_decode", "moe_decode_workspace_bytes", "moe_decode_forward")
 QMM_NOALLOC_MAX_LOGITS = 262144
 
 
@@ -123,6 +123,11 @@ def lib() -> ctypes.CDLL:
             L.qmm_linear_batched.argtypes = [vp, i32, i64, ctypes.POINTER(_Weight), vp, i32, vp,
                                              sz, vp]
             L.qmm_linear_batched.restype = ctypes.c_int
+            L.moe_decode_workspace_bytes.argtypes = [i64, i32, ctypes.POINTER(_Experts)]
+            L.moe_decode_workspace_bytes.restype = sz
+            L.moe_decode_forward.argtypes = [vp, i32, i64, vp, vp, i32, ctypes.POINTER(_Experts),
+                                             vp, i32, vp, vp, vp, vp, sz, vp]
+            L.moe_decode_forward.restype = ctypes.c_int
             L.qmm_rope_table.argtypes = [i64, i32, ctypes.c_double, vp, vp, vp]
             L.qmm_rope_table.restype = ctypes.c_int
             L.qmm_attn_decode_workspace_bytes.argtypes = [ctypes.POINTER(_AttnLayer)]
@@ -475,6 +480,50 @@ def moe_ffn_forward(x: torch.Tensor, topk_idx: torch.Tensor, topk_w: torch.Tenso
     _check(lib().moe_ffn_forward(_ptr(x), _dtype_code(x), M, _ptr(topk_idx), _ptr(topk_w), k,
                                  ctypes.byref(desc), _ptr(y), _dtype_code(y), _ptr(workspace),
                                  _nbytes(workspace), _stream(stream)))
+    return y
+
+
+def _experts_desc(experts: MoeExperts):
+    """The experts' descriptor, checked once and kept (see moe_ffn_forward)."""
+    ts = _experts_tensors(experts)
+    shape = (experts.E, experts.H, experts.I, experts.bits, experts.group)
+    c = experts.__dict__.get("_desc_for")
+    if (c is not None and c[2] == shape and all(map(operator.is_, c[0], ts))
+            and c[1] == tuple(t.data_ptr() for t in ts)):
+        return c[3]
+    _experts_sizes(experts)
+    _require_cuda(*ts)
+    desc = experts._c()
+    experts.__dict__["_desc_for"] = (ts, tuple(t.data_ptr() for t in ts), shape, desc)
+    return desc
+
+
+def moe_decode_workspace_bytes(M: int, k: int, experts: MoeExperts) -> int:
+    return int(lib().moe_decode_workspace_bytes(M, k, ctypes.byref(_experts_desc(experts))))
+
+
+def moe_decode_forward(x: torch.Tensor, w_router: torch.Tensor, bias: torch.Tensor | None, k: int,
+                       experts: MoeExperts, y: torch.Tensor | None = None,
+                       y_dtype: torch.dtype = torch.float32, topk_idx=None, topk_w=None,
+                       expert_counts=None, workspace: torch.Tensor | None = None, stream=None):
+    """The routed MoE layer of a decode batch (1..8 tokens) in one launch:
+    router, top-k, grouping, experts and combine (see include/qmm.h).
+    Returns y; topk_idx / topk_w / expert_counts are filled when given."""
+    M, H, E = _check_route(x, w_router, bias, k, topk_idx, topk_w, expert_counts)
+    if H != experts.H or E != experts.E:
+        raise ValueError(f"router is [{E}, {H}], experts have E = {experts.E}, H = {experts.H}")
+    _need(y, M * H, (torch.float32, torch.bfloat16), "y")
+    _require_cuda(y, workspace)
+    desc = _experts_desc(experts)
+    if y is None:
+        y = torch.empty((M, H), dtype=y_dtype, device=x.device)
+    if workspace is None:  # a caller's workspace is size-checked by the library
+        nbytes = int(lib().moe_decode_workspace_bytes(M, k, ctypes.byref(desc)))
+        workspace = torch.empty((max(nbytes, 1),), dtype=torch.uint8, device=x.device)
+    _check(lib().moe_decode_forward(_ptr(x), _dtype_code(x), M, _ptr(w_router), _ptr(bias), k,
+                                    ctypes.byref(desc), _ptr(y), _dtype_code(y), _ptr(topk_idx),
+                                    _ptr(topk_w), _ptr(expert_counts), _ptr(workspace),
+                                    _nbytes(workspace), _stream(stream)))
     return y
 
 

@@ -485,6 +485,61 @@ int moe_ffn_forward(const void *x, int32_t x_dtype, int64_t M, const int32_t *to
 
 }  // extern "C"
 
+// ------------------------------------------------------- one-launch decode layer
+
+extern "C" {
+
+size_t moe_decode_workspace_bytes(int64_t M, int32_t k, const moe_experts *ex) {
+  if (!ex || M < 1 || M > 8 || k < 1 || ex->E < 1) return 0;
+  return ws_layout(M, k, ex).total + round256(sizeof(float) * M * ex->E) + 256;
+}
+
+int moe_decode_forward(const void *x, int32_t x_dtype, int64_t M, const float *w_router,
+                       const float *bias, int32_t k, const moe_experts *ex, void *y,
+                       int32_t y_dtype, int32_t *topk_idx, float *topk_w, int32_t *expert_counts,
+                       void *workspace, size_t workspace_bytes, qmm_stream_t stream) {
+  g_err[0] = '\0';
+  int rc = check_experts(ex);
+  if (rc) return rc;
+  if (x_dtype != QMM_F32 && x_dtype != QMM_BF16)
+    return fail(QMM_ERR_INVALID_ARG, "moe_decode_forward: x_dtype must be QMM_F32 or QMM_BF16");
+  if (y_dtype != QMM_F32 && y_dtype != QMM_BF16)
+    return fail(QMM_ERR_INVALID_ARG, "moe_decode_forward: y_dtype must be QMM_F32 or QMM_BF16");
+  if (k < 1 || k > 16 || k > ex->E)
+    return fail(QMM_ERR_INVALID_ARG, "moe_decode_forward: k must be in [1, min(E, 16)]");
+  if (M < 0) return fail(QMM_ERR_SHAPE, "moe_decode_forward: negative M");
+  if (M == 0) return QMM_OK;
+  if (!x || !w_router || !y)
+    return fail(QMM_ERR_INVALID_ARG, "moe_decode_forward: null pointer");
+  if (!aligned16(x) || !aligned16(y) || !aligned16(w_router))
+    return fail(QMM_ERR_ALIGN, "moe_decode_forward: x, w_router and y must be 16-byte aligned");
+  if (!moe_decode_supported(qmat(ex->gate), qmat(ex->down), M, ex->E, k, ex->H, ex->I))
+    return fail(QMM_ERR_UNSUPPORTED,
+                "moe_decode_forward: takes 1..8 tokens, E <= 256, H = 4096, I = 2048 and "
+                "group >= 64 with H / group and I / group multiples of 4");
+  const WsLayout L = ws_layout(M, k, ex);
+  const size_t logits_off = L.total, bar_off = L.total + round256(sizeof(float) * M * ex->E);
+  if (!workspace || workspace_bytes < bar_off + 256)
+    return fail(QMM_ERR_WORKSPACE, "moe_decode_forward: workspace needs %zu bytes",
+                bar_off + 256);
+  if (!aligned256(workspace))
+    return fail(QMM_ERR_ALIGN, "moe_decode_forward: workspace must be 256-byte aligned");
+  uint8_t *base = static_cast<uint8_t *>(workspace);
+  MoeWork ws{};
+  ws.pos = reinterpret_cast<int32_t *>(base + L.pos);
+  ws.h = reinterpret_cast<float *>(base + L.h);
+  ws.out = reinterpret_cast<float *>(base + L.out);
+  const cudaError_t e = launch_moe_decode(
+      x, x_dtype == QMM_BF16, M, w_router, bias, ex->E, k, qmat(ex->gate), qmat(ex->up),
+      qmat(ex->down), ws, reinterpret_cast<float *>(base + logits_off),
+      reinterpret_cast<unsigned *>(base + bar_off), topk_idx, topk_w, expert_counts, y,
+      y_dtype == QMM_BF16, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "moe_decode_forward");
+  return QMM_OK;
+}
+
+}  // extern "C"
+
 // ------------------------------------------------------------ decode attention
 
 namespace {

@@ -116,6 +116,21 @@ cudaError_t launch_moe_combine(int64_t M, int k, int64_t H, const float *topk_w,
 }  // namespace qmm
 
 namespace qmm {
+// The routed MoE layer of a decode batch in one cooperative launch
+// (moe_decode.cu): router, top-k, grouping, gate/up, down and combine.
+// ws: the moe_ffn_forward workspace of (M, k); logits [M, E]; bar: one
+// counter (zeroed by the launcher).  Outputs topk_idx / topk_w / counts
+// may be NULL.
+bool moe_decode_supported(const QMat &gate, const QMat &down, int64_t M, int E, int k, int64_t H,
+                          int64_t I);
+cudaError_t launch_moe_decode(const void *x, bool x_bf16, int64_t M, const float *wr,
+                              const float *bias, int E, int k, const QMat &gate, const QMat &up,
+                              const QMat &down, const MoeWork &ws, float *logits,
+                              unsigned *bar, int32_t *topk_idx, float *topk_w, int32_t *counts,
+                              void *y, bool y_bf16, cudaStream_t s);
+}  // namespace qmm
+
+namespace qmm {
 // Decode attention (attn.cu): the RoPE table, and the steps between the
 // projections (rotation, cache write and chunked softmax-weighted sums in
 // one kernel, their merge in a second).  q, k, v: the projections

@@ -7,7 +7,6 @@
 
 namespace qmm {
 namespace smallm {
-namespace {
 
 Args base_args(const QMat &w, int nm) {
   Args a{};
@@ -25,7 +24,6 @@ Args base_args(const QMat &w, int nm) {
   return a;
 }
 
-}  // namespace
 }  // namespace smallm
 
 bool smallm_supported(int bits, int group, int64_t K) {

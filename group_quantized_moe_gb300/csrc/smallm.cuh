@@ -117,6 +117,10 @@ __host__ __device__ __forceinline__ int tile_cost(int T, int TBMAX) {
   return 2 * ((T + TBMAX - 1) / TBMAX) + T;
 }
 
+// Arguments for nm matrices of w's shape sharing a tile (gate/up: 2), the
+// rest zero (host).
+Args base_args(const QMat &w, int nm);
+
 // Launch with TBMAX 1 (the routed experts), 2 (any mode) or 8 (the linear
 // layer only).
 cudaError_t run_one(int mode, bool x_bf16, const Args &a, cudaStream_t s);

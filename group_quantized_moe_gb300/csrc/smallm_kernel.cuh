@@ -644,8 +644,18 @@ struct TileIt {
 
 // KW warps split the K range of a row (K = 32 KW XPL); the kCW / KW row
 // groups of a CTA take disjoint rows of every stage (KW = 4: two groups).
-template <int BITS, int XPL, int KW, int MODE, bool XBF16, int TBMAX>
-__global__ void __launch_bounds__(kThreads, Cfg<TBMAX>::kCtas) smallm_kernel(const Args a) {
+// The body of smallm_kernel, also run as two phases of the one-launch decode
+// layer (moe_decode.cu).  `a` is read in place (a kernel parameter: a copy
+// would live in local memory); idx replaces a.idx (the decode layer passes
+// its top-k in shared memory).  before_act() is called by every thread once
+// the first weight tiles have been requested and before anything a
+// preceding step writes is read (the down projection and the linear layer;
+// gate/up waits at its start); it returns false to abandon the work (every
+// thread gets the same answer), after which the kernel only drains its
+// copies.
+template <int BITS, int XPL, int KW, int MODE, bool XBF16, int TBMAX, class BeforeAct>
+__device__ __forceinline__ void smallm_body(const Args &a, const int32_t *idx,
+                                            BeforeAct before_act) {
   // Gate/up needs the routing of the immediately preceding kernel (the
   // dispatch) before anything else.  The linear layer and the down
   // projection first request their leading weight tiles (see gemv_kernel)
@@ -689,12 +699,12 @@ __global__ void __launch_bounds__(kThreads, Cfg<TBMAX>::kCtas) smallm_kernel(con
       s_off[1] = static_cast<int32_t>(a.M);
       nseg_s = 1;
     }
-  } else if (a.idx) {
+  } else if (idx) {
     // Decode batch: group the assignments by expert here (a stable counting
     // sort, the dispatch kernel's order: expert, then assignment).
     const int MK = static_cast<int>(a.MK), E = a.E;
     for (int t = threadIdx.x; t < MK; t += blockDim.x) {
-      const int e = a.idx[t];
+      const int e = idx[t];
       const bool valid = e >= 0 && e < E;
       s_idx[t] = valid ? e : -1;
       if (!valid && MODE == kGateUp && blockIdx.x == 0) atomicOr(a.status, kDevBadExpert);
@@ -914,7 +924,9 @@ __global__ void __launch_bounds__(kThreads, Cfg<TBMAX>::kCtas) smallm_kernel(con
     it_next(pit);
     ++issued;
   }
-  if constexpr (MODE != kGateUp) pdl_enter();
+  if constexpr (MODE != kGateUp) {
+    if (!before_act() && threadIdx.x == 0) abort_s = 1;  // read after the next barrier
+  }
 
   const int kslot = (warp % KW) * 32 + lane;  // this lane's slice of K
   const int col0 = kslot * XPL;               // its columns
@@ -947,7 +959,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<TBMAX>::kCtas) smallm_kernel(con
         xr[t] = XBF16 ? static_cast<const void *>(static_cast<const uint16_t *>(a.x) + tt * a.K)
                       : static_cast<const void *>(static_cast<const float *>(a.x) + tt * a.K);
       } else if constexpr (MODE == kGateUp) {
-        const int64_t tok = (a.idx ? s_asg[p0 + tt] : a.ws.assign[p0 + tt]) / a.k;
+        const int64_t tok = (idx ? s_asg[p0 + tt] : a.ws.assign[p0 + tt]) / a.k;
         xr[t] = XBF16 ? static_cast<const void *>(static_cast<const uint16_t *>(a.x) + tok * a.K)
                       : static_cast<const void *>(static_cast<const float *>(a.x) + tok * a.K);
       } else {
@@ -1082,6 +1094,14 @@ __global__ void __launch_bounds__(kThreads, Cfg<TBMAX>::kCtas) smallm_kernel(con
                         a.status);
   }
   __syncthreads();
+}
+
+template <int BITS, int XPL, int KW, int MODE, bool XBF16, int TBMAX>
+__global__ void __launch_bounds__(kThreads, Cfg<TBMAX>::kCtas) smallm_kernel(const Args a) {
+  smallm_body<BITS, XPL, KW, MODE, XBF16, TBMAX>(a, a.idx, []() {
+    pdl_enter();
+    return true;
+  });
 }
 
 template <int BITS, int XPL, int KW, int MODE, bool XBF16, int TBMAX>

@@ -288,6 +288,35 @@ int qmm_attn_decode(const void *x, int32_t x_dtype, int64_t pos, const qmm_attn_
                     size_t workspace_bytes, qmm_stream_t stream);
 
 /*
+ * The routed MoE layer of a decode batch in one launch [P1 section 3.5: the
+ * router, the grouping of tokens by expert and the experts' weighted sum as
+ * one step]: computes exactly what moe_route_topk followed by
+ * moe_ffn_forward compute (the same fixed-order logits, so the same expert
+ * indices, weights and histogram bit for bit; the same expert arithmetic),
+ * as one cooperative kernel whose phases (logits, top-k, grouping, gate/up,
+ * down, combine) are separated by grid-wide barriers instead of launches.
+ * Takes 1..8 tokens, E <= 256, H = 4096, I = 2048 (the decode shape of the
+ * DeepSeek layer this library targets), INT8 or INT4 experts with
+ * group >= 64 and H / group, I / group multiples of 4; anything else
+ * returns QMM_ERR_UNSUPPORTED (use the two calls).  x: [M, H] fp32 or bf16;
+ * w_router [E, H] fp32, bias [E] or NULL; y: [M, H] fp32 or bf16.
+ * topk_idx [M, k] int32, topk_w [M, k] fp32 and expert_counts [E] int32 are
+ * optional outputs (NULL to skip).  workspace: moe_decode_workspace_bytes
+ * bytes, 256-byte aligned, contents on entry do not matter (a counter in it
+ * is cleared by an asynchronous memset before the kernel).  Every barrier
+ * wait is bounded (QMM_DEV_WAIT_TIMEOUT on expiry).  Needs all of its CTAs
+ * resident at once (two per SM): it returns QMM_ERR_CUDA if the device
+ * cannot hold them.
+ */
+size_t moe_decode_workspace_bytes(int64_t M, int32_t k, const moe_experts *ex);
+
+int moe_decode_forward(const void *x, int32_t x_dtype, int64_t M, const float *w_router,
+                       const float *bias, int32_t k, const moe_experts *ex, void *y,
+                       int32_t y_dtype, int32_t *topk_idx, float *topk_w,
+                       int32_t *expert_counts, void *workspace, size_t workspace_bytes,
+                       qmm_stream_t stream);
+
+/*
  * Allocation-free router (no counterpart on the pages: it is a calling
  * convention, not part of the method).  Computes exactly what moe_route_topk
  * computes, with the same arguments minus the workspace, for callers that

@@ -233,6 +233,35 @@ def test_moe_rejects_args(Lfake):
     assert f(P, q.QMM_F32, 8, P, P, 6, ctypes.byref(big), P2, q.QMM_F32, P2, 1 << 40, None) == q.QMM_ERR_UNSUPPORTED
 
 
+def test_decode_one_launch_rejects(Lfake):
+    """moe_decode_forward: argument errors, and shapes it does not take, return
+    before anything is enqueued."""
+    f = Lfake.moe_decode_forward
+    ex = _experts(E=16, H=4096, I=2048, bits=4, group=64)
+    need = Lfake.moe_decode_workspace_bytes(8, 6, ctypes.byref(ex))
+    assert need > 0 and Lfake.moe_decode_workspace_bytes(9, 6, ctypes.byref(ex)) == 0
+
+    def call(x=P, dt=q.QMM_F32, M=8, wr=P, k=6, e=ex, y=P2, ydt=q.QMM_F32, ws=P2 + (1 << 30),
+             wsb=need):
+        return f(x, dt, M, wr, None, k, ctypes.byref(e), y, ydt, None, None, None, ws, wsb, None)
+
+    assert call(M=0) == q.QMM_OK  # a no-op
+    assert call(M=9) == q.QMM_ERR_UNSUPPORTED
+    assert call(k=0) == q.QMM_ERR_INVALID_ARG
+    assert call(k=17) == q.QMM_ERR_INVALID_ARG
+    assert call(dt=4) == q.QMM_ERR_INVALID_ARG
+    assert call(ydt=4) == q.QMM_ERR_INVALID_ARG
+    assert call(x=None) == q.QMM_ERR_INVALID_ARG
+    assert call(wr=None) == q.QMM_ERR_INVALID_ARG
+    assert call(x=P + 4) == q.QMM_ERR_ALIGN
+    assert call(wsb=need - 1) == q.QMM_ERR_WORKSPACE
+    assert call(ws=P2 + 16) == q.QMM_ERR_ALIGN
+    # shapes outside the one-launch form: another width, more than 256 experts
+    assert call(e=_experts(E=16, H=2048, I=2048, bits=4, group=64)) == q.QMM_ERR_UNSUPPORTED
+    big = _experts(E=512, H=4096, I=2048, bits=4, group=64)
+    assert call(e=big, wsb=1 << 40) == q.QMM_ERR_UNSUPPORTED
+
+
 def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
     """No silent fallback: a missing library is an error, not a CPU path."""
     import importlib

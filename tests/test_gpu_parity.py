@@ -573,6 +573,93 @@ def test_moe_decode_full_size(dev):
     assert_within(y, yref, bound, "decode pipeline")
 
 
+# ------------------------------------------- one-launch decode layer (f)2
+
+def _route_and_ffn(dev, x, xd, wr, bias, k, ex, y_dtype=torch.float32):
+    """The two-call path (moe_route_topk, moe_ffn_forward) on the same inputs."""
+    idx, w, cnt = q.moe_route_topk(xd, T(wr, dev), None if bias is None else T(bias, dev), k)
+    y = q.moe_ffn_forward(xd, idx, w, ex, y_dtype=y_dtype)
+    return idx, w, cnt, y
+
+
+@pytest.mark.parametrize("bits,group", [(4, 64), (8, 128)])
+@pytest.mark.parametrize("bf16", [False, True])
+def test_moe_decode_one_launch(dev, bits, group, bf16):
+    """The whole decode layer in one cooperative launch: the top-k indices and
+    the histogram bit-exact against the oracle, weights within 2e-6, outputs
+    within the fp32 bound (routing-weight difference included), and
+    bit-identical to the two-call path (same logits order, same expert
+    kernels, same combine order) for fp32 and bf16 outputs."""
+    E, H, I = 16, 4096, 2048
+    ex, og, ou, od = _small_experts(dev, E, H, I, bits, group, seed=31)
+    wr = synth.normal(32, 10, E * H, 0.05).reshape(E, H)
+    bias = synth.normal(33, 20, E, 0.5)
+    for M, k, b in ((1, 6, None), (3, 1, bias), (8, 6, bias), (5, 16, None)):
+        x = synth.normal(34 + M, 1, M * H).reshape(M, H)
+        if bf16:
+            x, xd = _bf16_x(x, dev)
+        else:
+            xd = T(x, dev)
+        bd = None if b is None else T(b, dev)
+        idx = torch.empty((M, k), dtype=torch.int32, device=dev)
+        w = torch.empty((M, k), dtype=torch.float32, device=dev)
+        cnt = torch.empty((E,), dtype=torch.int32, device=dev)
+        y = q.moe_decode_forward(xd, T(wr, dev), bd, k, ex, topk_idx=idx, topk_w=w,
+                                 expert_counts=cnt)
+        oidx, ow = oracle.topk(oracle.router_logits(x, wr, b), k)
+        np.testing.assert_array_equal(idx.cpu().numpy(), oidx)
+        assert np.abs(w.cpu().numpy() - ow).max() <= 2e-6
+        np.testing.assert_array_equal(cnt.cpu().numpy(), np.bincount(oidx.reshape(-1), minlength=E))
+        yref, bound = oracle.moe_ffn(x, oidx, ow, og, ou, od, dw=2e-6)
+        assert_within(y.cpu().numpy().astype(np.float64), yref, bound, f"one launch M{M} k{k}")
+        i2, w2, c2, y2 = _route_and_ffn(dev, x, xd, wr, b, k, ex)
+        np.testing.assert_array_equal(idx.cpu().numpy(), i2.cpu().numpy())
+        np.testing.assert_array_equal(w.cpu().numpy().view(np.uint32), w2.cpu().numpy().view(np.uint32))
+        np.testing.assert_array_equal(y.cpu().numpy().view(np.uint32), y2.cpu().numpy().view(np.uint32))
+        yb = q.moe_decode_forward(xd, T(wr, dev), bd, k, ex, y_dtype=torch.bfloat16)
+        _, _, _, yb2 = _route_and_ffn(dev, x, xd, wr, b, k, ex, y_dtype=torch.bfloat16)
+        np.testing.assert_array_equal(yb.cpu().view(torch.int16).numpy(),
+                                      yb2.cpu().view(torch.int16).numpy())
+
+
+def test_moe_decode_one_launch_repeatable_with_dirty_workspace(dev):
+    E, H, I, M, k = 8, 4096, 2048, 8, 6
+    ex, og, ou, od = _small_experts(dev, E, H, I, 4, 64, seed=41)
+    wr = T(synth.normal(42, 10, E * H, 0.05).reshape(E, H), dev)
+    x = T(synth.normal(43, 1, M * H).reshape(M, H), dev)
+    ws = torch.full((q.moe_decode_workspace_bytes(M, k, ex),), 0x77, dtype=torch.uint8, device=dev)
+    ys = [q.moe_decode_forward(x, wr, None, k, ex, workspace=ws).cpu().numpy() for _ in range(3)]
+    for yy in ys[1:]:
+        np.testing.assert_array_equal(yy.view(np.uint32), ys[0].view(np.uint32))
+    with pytest.raises(q.QmmError):  # a shape it does not take
+        ex2, *_ = _small_experts(dev, 4, 2048, 2048, 4, 64, seed=44)
+        q.moe_decode_forward(T(synth.normal(45, 1, 2 * 2048).reshape(2, 2048), dev),
+                             T(synth.normal(46, 10, 4 * 2048, 0.05).reshape(4, 2048), dev),
+                             None, 2, ex2)
+
+
+@pytest.mark.slow
+def test_moe_decode_one_launch_full_size(dev):
+    """The full decode layer (M = 8, 256 INT4 g64 experts, top-6) in one
+    launch: indices exact, outputs of every token within the bound of the
+    oracle, and bit-identical to the two-call path."""
+    r = recipes.CFG4
+    x, _ = recipes.moe_x(r)
+    wr, bias = recipes.moe_router(r)
+    ex = _full_moe(dev, r)
+    idx = torch.empty((r.M, r.k), dtype=torch.int32, device=dev)
+    w = torch.empty((r.M, r.k), dtype=torch.float32, device=dev)
+    y = q.moe_decode_forward(T(x, dev), T(wr, dev), None if bias is None else T(bias, dev), r.k,
+                             ex, topk_idx=idx, topk_w=w)
+    oidx, ow = oracle.topk(oracle.router_logits(x, wr, bias), r.k)
+    np.testing.assert_array_equal(idx.cpu().numpy(), oidx)
+    og, ou, od = _oracle_experts(r, oidx.reshape(-1))
+    yref, bound = oracle.moe_ffn(x, oidx, ow, og, ou, od, dw=2e-6)
+    assert_within(y.cpu().numpy().astype(np.float64), yref, bound, "one launch full size")
+    _, _, _, y2 = _route_and_ffn(dev, x, T(x, dev), wr, bias, r.k, ex)
+    np.testing.assert_array_equal(y.cpu().numpy().view(np.uint32), y2.cpu().numpy().view(np.uint32))
+
+
 @pytest.mark.slow
 def test_moe_prefill_full_size_sampled(dev):
     """Batched-prefill MoE at full size: M=512 bf16 tokens, Zipf-biased
