@@ -436,8 +436,10 @@ int moe_ffn_forward(const void *x, int32_t x_dtype, int64_t M, const int32_t *to
   const bool tc = xb && !small_gu && moe_tc_supported(qmat(ex->gate), qmat(ex->down), ex->H, ex->I);
   // On the tensor-core path, experts with one or two tokens skip the
   // dequantise -> fp16 -> MMA pipeline (a 16-row token tile for two tokens at
-  // most) and stream their weights through the small-M integer kernels, both
-  // tokens in one pass.
+  // most) and stream their weights through the small-M integer kernels, one
+  // token per pass (for two tokens the second pass reads the tiles from L2;
+  // on the prefill workload this beat the two-tokens-per-pass kernel by 3.5 %
+  // of the layer, and moving three- or four-token experts here lost 5-6 %).
   const int light_max = (tc && smallm_supported(ex->gate.bits, ex->gate.group, ex->H) &&
                          smallm_supported(ex->down.bits, ex->down.group, ex->I))
                             ? 2
@@ -460,17 +462,16 @@ int moe_ffn_forward(const void *x, int32_t x_dtype, int64_t M, const int32_t *to
       MoeWork wl = ws;
       wl.active = ws.active_light;
       wl.num_active = ws.num_light;
-      e = launch_smallm_gateup(x, xb, k, ex->E, qmat(ex->gate), qmat(ex->up), wl, s, light_max);
+      e = launch_smallm_gateup(x, xb, k, ex->E, qmat(ex->gate), qmat(ex->up), wl, s);
       if (e != cudaSuccess) return cuda_fail(e, "moe_ffn_forward (few-token gate/up)");
-      e = launch_smallm_down(k, ex->E, qmat(ex->down), wl, s, light_max);
+      e = launch_smallm_down(k, ex->E, qmat(ex->down), wl, s);
       if (e != cudaSuccess) return cuda_fail(e, "moe_ffn_forward (few-token down)");
     }
   } else if (self_grouped) {
     const int64_t MK = M * k;
-    e = launch_smallm_gateup(x, xb, k, ex->E, qmat(ex->gate), qmat(ex->up), ws, s, 1, topk_idx,
-                             MK);
+    e = launch_smallm_gateup(x, xb, k, ex->E, qmat(ex->gate), qmat(ex->up), ws, s, topk_idx, MK);
     if (e != cudaSuccess) return cuda_fail(e, "moe_ffn_forward (gate/up)");
-    e = launch_smallm_down(k, ex->E, qmat(ex->down), ws, s, 1, topk_idx, MK);
+    e = launch_smallm_down(k, ex->E, qmat(ex->down), ws, s, topk_idx, MK);
     if (e != cudaSuccess) return cuda_fail(e, "moe_ffn_forward (down)");
   } else {
     e = launch_moe_gateup(x, xb, M, k, ex->E, qmat(ex->gate), qmat(ex->up), ws, s);

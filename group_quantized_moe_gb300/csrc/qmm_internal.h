@@ -162,19 +162,18 @@ namespace qmm {
 bool smallm_supported(int bits, int group, int64_t K);
 cudaError_t launch_smallm_linear(const void *x, bool x_bf16, int64_t M, const QMat &w, void *y,
                                  bool y_bf16, cudaStream_t s);
-// rows_per_pass: 1 (one token per pass, 32 columns per lane: decode batches)
-// or 2 (two tokens per pass, 16 columns per lane: the experts of a prefill
-// batch with at most two tokens).
+// The routed experts on the small-M kernels, one token per pass (32
+// columns per lane): decode batches, and the experts of a prefill batch with
+// one or two tokens (two passes for two: the second reads the expert's tiles
+// from L2, and still beats the two-token kernel on those experts).
 // idx (decode batches, M k <= 128 assignments): the kernels group the
 // assignments by expert themselves from the top-k indices instead of reading
 // the dispatch kernel's lists; gate/up writes ws.pos for the combine.
 cudaError_t launch_smallm_gateup(const void *x, bool x_bf16, int k, int E, const QMat &gate,
                                  const QMat &up, const MoeWork &ws, cudaStream_t s,
-                                 int rows_per_pass = 1, const int32_t *idx = nullptr,
-                                 int64_t MK = 0);
+                                 const int32_t *idx = nullptr, int64_t MK = 0);
 cudaError_t launch_smallm_down(int k, int E, const QMat &down, const MoeWork &ws, cudaStream_t s,
-                               int rows_per_pass = 1, const int32_t *idx = nullptr,
-                               int64_t MK = 0);
+                               const int32_t *idx = nullptr, int64_t MK = 0);
 }  // namespace qmm
 
 namespace qmm {

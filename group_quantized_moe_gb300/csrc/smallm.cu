@@ -57,7 +57,7 @@ cudaError_t launch_smallm_linear(const void *x, bool x_bf16, int64_t M, const QM
 
 cudaError_t launch_smallm_gateup(const void *x, bool x_bf16, int k, int E, const QMat &gate,
                                  const QMat &up, const MoeWork &ws, cudaStream_t s,
-                                 int rows_per_pass, const int32_t *idx, int64_t MK) {
+                                 const int32_t *idx, int64_t MK) {
   smallm::Args a = smallm::base_args(gate, 2);
   a.w1 = up;
   a.E = E;
@@ -67,20 +67,18 @@ cudaError_t launch_smallm_gateup(const void *x, bool x_bf16, int k, int E, const
   a.idx = idx;
   a.MK = MK;
   a.pos_out = idx ? ws.pos : nullptr;
-  return rows_per_pass == 2 ? smallm::run_lo(smallm::kGateUp, x_bf16, a, s)
-                            : smallm::run_one(smallm::kGateUp, x_bf16, a, s);
+  return smallm::run_one(smallm::kGateUp, x_bf16, a, s);
 }
 
 cudaError_t launch_smallm_down(int k, int E, const QMat &down, const MoeWork &ws, cudaStream_t s,
-                               int rows_per_pass, const int32_t *idx, int64_t MK) {
+                               const int32_t *idx, int64_t MK) {
   smallm::Args a = smallm::base_args(down, 1);
   a.E = E;
   a.k = k;
   a.ws = ws;
   a.idx = idx;
   a.MK = MK;
-  return rows_per_pass == 2 ? smallm::run_lo(smallm::kDown, false, a, s)
-                            : smallm::run_one(smallm::kDown, false, a, s);
+  return smallm::run_one(smallm::kDown, false, a, s);
 }
 
 }  // namespace qmm

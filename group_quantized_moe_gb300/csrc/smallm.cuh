@@ -47,14 +47,14 @@ constexpr int kStageBytes = 40960;
 // Three configurations (TBMAX = activation rows per pass).  TBMAX 1 and 2
 // use two CTAs per SM (128 registers) and integer byte dot products of the
 // codes with the activations held as balanced digits (smallm_kernel.cuh).
-// TBMAX 1 runs the routed experts of decode batches: most of them have one token, and with one row per pass a
-// lane can hold 32 columns, which halves the per-row work (scale, zero
-// point, conversions, reduction) per code; an expert with T tokens is
-// applied in T passes, each a sweep over the CTA's tiles of that expert
-// (activations load once per pass, the tiles stream again).  TBMAX 2 (16
-// columns per lane) runs the linear layer with one or two rows and the experts of a
-// prefill batch that have one or two tokens (both tokens in one pass, so the
-// weights stream once).  TBMAX 8 (one CTA per SM, eight fp32 rows per pass)
+// TBMAX 1 runs the routed experts of decode batches and the experts of a
+// prefill batch that have one or two tokens: most of them have one token, and
+// with one row per pass a lane can hold 32 columns, which halves the per-row
+// work (scale, zero point, conversions, reduction) per code; an expert with T
+// tokens is applied in T passes, each a sweep over the CTA's tiles of that
+// expert (activations load once per pass, the tiles stream again, from L2
+// after the first pass).  TBMAX 2 (16 columns per lane) runs the linear layer
+// with one or two rows.  TBMAX 8 (one CTA per SM, eight fp32 rows per pass)
 // runs the linear layer with 3..8 rows, where every tile serves all M rows,
 // and small INT4 matrices with one row (no activation conversion).
 template <int TBMAX>

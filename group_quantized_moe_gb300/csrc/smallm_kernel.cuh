@@ -1142,8 +1142,8 @@ cudaError_t run_shape(const Args &a, cudaStream_t s) {
   }
 }
 
-// TBMAX 1: the routed experts (gate/up, down); TBMAX 2: the linear layer
-// and experts of up to two tokens in one pass; TBMAX 8: the linear layer.
+// TBMAX 1: the routed experts (gate/up, down); TBMAX 2 and 8: the linear
+// layer.
 template <int TBMAX>
 cudaError_t run_class(int mode, bool x_bf16, const Args &a, cudaStream_t s) {
   if constexpr (TBMAX == 1) {
@@ -1154,11 +1154,6 @@ cudaError_t run_class(int mode, bool x_bf16, const Args &a, cudaStream_t s) {
   } else {
     if (mode == kLinear)
       return x_bf16 ? run_shape<kLinear, true, TBMAX>(a, s) : run_shape<kLinear, false, TBMAX>(a, s);
-    if constexpr (TBMAX == 2) {  // experts with up to two tokens in one pass
-      if (mode == kGateUp)
-        return x_bf16 ? run_shape<kGateUp, true, 2>(a, s) : run_shape<kGateUp, false, 2>(a, s);
-      if (mode == kDown) return run_shape<kDown, false, 2>(a, s);
-    }
     return cudaErrorInvalidValue;
   }
 }
