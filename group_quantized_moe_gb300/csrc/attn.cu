@@ -13,7 +13,10 @@
 //                      over the SMs)
 //   attn_merge_kernel  one CTA per query head: the chunks' partial results
 //                      rescaled to the overall maximum and summed in chunk
-//                      order, divided by the overall sum
+//                      order, divided by the overall sum (for up to eight
+//                      chunks -- 512 cache rows -- the chunks of a head run
+//                      as one cluster and merge in distributed shared memory
+//                      instead, with no second launch)
 //
 // GB300: the step is bound by reading the cache (2 n_kv T d fp32 values) and
 // by launch latency; every kernel is launched with programmatic stream
@@ -29,6 +32,34 @@ namespace {
 
 constexpr int kChunk = 64;      // cache rows per partial CTA
 constexpr int kPartThreads = 256;
+constexpr int kMaxCluster = 8;  // chunks merged inside a cluster (portable cluster size)
+
+// Distributed shared memory of the thread-block cluster.
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ float ld_cluster_f32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+  return v;
+}
+// Every thread of every CTA of the cluster; shared-memory writes before it
+// are visible to the cluster after it.
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;"
+               ::: "memory");
+}
+// Requests `bytes` (a multiple of 16) at `src` into L2.
+__device__ __forceinline__ void prefetch_l2_bulk(const void *src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
 
 __global__ void __launch_bounds__(256) rope_table_kernel(int64_t max_seq, int head_dim,
                                                           double base, float *cos_t,
@@ -58,19 +89,25 @@ __global__ void __launch_bounds__(256) rope_table_kernel(int64_t max_seq, int he
 // 256 threads: warp w scores rows 8w .. 8w + 7 (lane l holds the 16-byte
 // column units l, l + 32, ...; a batch of rows' loads is in flight before
 // the sums); the value rows are summed by (row group, column unit) threads
-// and the row groups combined in order.
-template <int NU>  // 16-byte column units per lane: ceil(head_dim / 128)
+// and the row groups combined in order.  The chunk's cache rows (written by
+// earlier steps, complete before this launch may start) are requested into
+// L2 before the wait for the projections.
+// CLUSTER: the chunks of a head form one thread-block cluster (at most 8);
+// each CTA leaves its partial result in shared memory and the cluster's
+// first CTA merges them in chunk order (as attn_merge_kernel does) and
+// writes the head's output, so no merge launch follows.
+template <int NU, bool CLUSTER>  // NU: 16-byte column units per lane, ceil(head_dim / 128)
 __global__ void __launch_bounds__(kPartThreads) attn_part_kernel(
     const float *q, const float *knew, const float *vnew, float *cache, int n_head, int n_kv,
     int head_dim, int64_t max_seq, int64_t pos, const float *cos_t, const float *sin_t,
-    float scale, float *part) {
+    float scale, float *part, float *attn_out) {
   __shared__ __align__(16) float qs[512];
   __shared__ __align__(16) float kn[512];
   __shared__ __align__(16) float vn[512];
   __shared__ float ps[kChunk];
   __shared__ float red[kPartThreads / 32];
   __shared__ __align__(16) float4 vred[kPartThreads];
-  pdl_enter();
+  __shared__ __align__(16) float cpart[CLUSTER ? 512 + 2 : 1];  // this chunk's result
   const int h = blockIdx.x, c = blockIdx.y;
   const int grp = n_head / n_kv, kvh = h / grp;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -79,6 +116,12 @@ __global__ void __launch_bounds__(kPartThreads) attn_part_kernel(
   const int nt = static_cast<int>(min64(kChunk, T - t0));
   const bool last = t0 + nt == T;         // this chunk holds row pos ...
   const int nc = last ? nt - 1 : nt;      // ... which is not read from the cache
+  if (threadIdx.x == 0 && nc > 0) {
+    const uint32_t bytes = static_cast<uint32_t>(nc) * head_dim * 4;
+    prefetch_l2_bulk(cache + (static_cast<int64_t>(kvh) * max_seq + t0) * head_dim, bytes);
+    prefetch_l2_bulk(cache + (static_cast<int64_t>(n_kv + kvh) * max_seq + t0) * head_dim, bytes);
+  }
+  pdl_enter();
   const int hp = head_dim / 2, d4 = head_dim / 4;
   const float *cr = cos_t + pos * hp, *sr = sin_t + pos * hp;
   for (int i = threadIdx.x; i < hp; i += kPartThreads) {
@@ -217,7 +260,7 @@ __global__ void __launch_bounds__(kPartThreads) attn_part_kernel(
   }
   vred[threadIdx.x] = acc;
   __syncthreads();
-  float *out = part + (static_cast<int64_t>(h) * gridDim.y + c) * (head_dim + 2);
+  float *out = CLUSTER ? cpart : part + (static_cast<int64_t>(h) * gridDim.y + c) * (head_dim + 2);
   if (threadIdx.x < d4) {
     float4 t = vred[threadIdx.x];
     for (int gg = 1; gg < RG; ++gg) {
@@ -243,6 +286,32 @@ __global__ void __launch_bounds__(kPartThreads) attn_part_kernel(
   if (threadIdx.x == 0) {
     out[0] = m;
     out[1] = l;
+  }
+  if constexpr (CLUSTER) {
+    // the cluster's first CTA merges the chunks' results in chunk order:
+    // sum_c exp(m_c - M) o_c / sum_c exp(m_c - M) l_c, M = max_c m_c
+    cluster_sync_all();
+    if (cluster_rank() == 0) {
+      const int nch = static_cast<int>(gridDim.y);
+      const uint32_t base = smem_addr(cpart);
+      float M = -3.402823466e38f;
+      for (int r = 0; r < nch; ++r) M = fmaxf(M, ld_cluster_f32(map_to_rank(base, r)));
+      float L = 0.0f;
+      for (int r = 0; r < nch; ++r) {
+        const uint32_t b = map_to_rank(base, r);
+        L = fmaf(expf(ld_cluster_f32(b) - M), ld_cluster_f32(b + 4), L);
+      }
+      const float inv = 1.0f / L;
+      for (int d = threadIdx.x; d < head_dim; d += kPartThreads) {
+        float a = 0.0f;
+        for (int r = 0; r < nch; ++r) {
+          const uint32_t b = map_to_rank(base, r);
+          a = fmaf(expf(ld_cluster_f32(b) - M), ld_cluster_f32(b + 4 * (2 + d)), a);
+        }
+        attn_out[h * head_dim + d] = a * inv;
+      }
+    }
+    cluster_sync_all();  // the other CTAs' shared memory stays until it has been read
   }
 }
 
@@ -289,16 +358,38 @@ cudaError_t launch_attn_decode_core(const float *q, const float *k, const float 
   const float scale = static_cast<float>(1.0 / sqrt(static_cast<double>(head_dim)));
   const dim3 grid(n_head, nchunk);
   const int nu = (head_dim + 127) / 128;
+  if (nchunk <= kMaxCluster) {
+    // one cluster per head: the merge happens in distributed shared memory
+    auto kern = nu == 1 ? attn_part_kernel<1, true>
+                        : (nu == 2 ? attn_part_kernel<2, true> : attn_part_kernel<4, true>);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kPartThreads);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = 1;
+    attr[1].val.clusterDim.y = static_cast<unsigned>(nchunk);
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, q, k, v, cache, n_head, n_kv, head_dim,
+                                             max_seq, pos, cos_t, sin_t, scale, part, attn_out);
+    count_launch();
+    return e;
+  }
   cudaError_t e;
   if (nu == 1)
-    e = launch_pdl(attn_part_kernel<1>, grid, dim3(kPartThreads), 0, s, q, k, v, cache, n_head,
-                   n_kv, head_dim, max_seq, pos, cos_t, sin_t, scale, part);
+    e = launch_pdl(attn_part_kernel<1, false>, grid, dim3(kPartThreads), 0, s, q, k, v, cache,
+                   n_head, n_kv, head_dim, max_seq, pos, cos_t, sin_t, scale, part, attn_out);
   else if (nu == 2)
-    e = launch_pdl(attn_part_kernel<2>, grid, dim3(kPartThreads), 0, s, q, k, v, cache, n_head,
-                   n_kv, head_dim, max_seq, pos, cos_t, sin_t, scale, part);
+    e = launch_pdl(attn_part_kernel<2, false>, grid, dim3(kPartThreads), 0, s, q, k, v, cache,
+                   n_head, n_kv, head_dim, max_seq, pos, cos_t, sin_t, scale, part, attn_out);
   else
-    e = launch_pdl(attn_part_kernel<4>, grid, dim3(kPartThreads), 0, s, q, k, v, cache, n_head,
-                   n_kv, head_dim, max_seq, pos, cos_t, sin_t, scale, part);
+    e = launch_pdl(attn_part_kernel<4, false>, grid, dim3(kPartThreads), 0, s, q, k, v, cache,
+                   n_head, n_kv, head_dim, max_seq, pos, cos_t, sin_t, scale, part, attn_out);
   if (e != cudaSuccess) return e;
   return launch_pdl(attn_merge_kernel, dim3(n_head), dim3(kPartThreads), 0, s,
                     static_cast<const float *>(part), nchunk, head_dim, attn_out);

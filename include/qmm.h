@@ -280,8 +280,8 @@ size_t qmm_attn_decode_workspace_bytes(const qmm_attn_layer *L);
  * Requires 0 <= pos < max_seq.  When wk and wv follow wq in memory as rows of
  * one [(n_head + 2 n_head_kv) head_dim, D] matrix (codes, scales and zero
  * points each contiguous, same bits and group), the three projections run as
- * one launch: four kernel launches in all (else six), asynchronous on
- * `stream`.
+ * one launch: three kernel launches in all (else five), one more when
+ * pos >= 512 (the chunks' merge), asynchronous on `stream`.
  */
 int qmm_attn_decode(const void *x, int32_t x_dtype, int64_t pos, const qmm_attn_layer *L,
                     float *kv_cache, void *y, int32_t y_dtype, void *workspace,

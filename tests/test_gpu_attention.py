@@ -213,12 +213,25 @@ def test_attn_decode_rejects_bad_arguments(dev):
     assert (cd == 0).all()                            # nothing was enqueued
 
 
+def test_attn_decode_long_cache(dev):
+    """Up to 512 rows the chunks of a head merge inside one cluster; from 513
+    rows (nine chunks) a merge kernel does it: both sides of that boundary,
+    and a long cache."""
+    D, n_head, n_kv, hd, max_seq = 256, 4, 2, 64, 1100
+    layer, ow, oc, os_ = _build(dev, 81, D, n_head, n_kv, hd, max_seq, stacked=True)
+    cache = _cache(82, n_kv, max_seq, hd)
+    for pos in (511, 512, 513, 1099):
+        _check_step(dev, layer, ow, oc, os_, synth.normal(83 + pos, 1, D), pos, cache,
+                    what="long cache")
+
+
 def test_attn_decode_launches(dev):
-    """Stacked q/k/v weights: one projection launch, then the attention's two
-    kernels and the output projection; apart: three projection launches.
+    """Stacked q/k/v weights: one projection launch, the attention kernel (its
+    chunks merged inside a cluster up to 512 rows, by a second kernel beyond)
+    and the output projection; apart: three projection launches.
     quantize_attn_layer builds the stacked form."""
     D, n_head, n_kv, hd, max_seq = 256, 4, 2, 64, 64
-    for stacked, expect in ((True, 4), (False, 6)):
+    for stacked, expect in ((True, 3), (False, 5)):
         layer, ow, oc, os_ = _build(dev, 71, D, n_head, n_kv, hd, max_seq, stacked=stacked)
         cd = layer.kv_cache(dev)
         x = T(synth.normal(72, 1, D), dev)
@@ -237,4 +250,4 @@ def test_attn_decode_launches(dev):
     torch.cuda.synchronize()
     n0 = q.qmm_launch_count()
     q.attn_decode(x, 1, layer, cd)
-    assert q.qmm_launch_count() - n0 == 4
+    assert q.qmm_launch_count() - n0 == 3
