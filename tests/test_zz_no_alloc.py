@@ -5,9 +5,10 @@ a framework plugin limited to the buffers it is handed), or whose loops must
 not pay for cudaMalloc and its implicit synchronisation, cannot supply the
 router's logits workspace.  This entry point keeps that scratch in a fixed
 1 MiB array inside the library.  The test calls it through the C ABI and
-checks it against the workspace-taking moe_route_topk on two calls in a row
-(the array keeps the first call's contents when the second one runs), and
-that sizes beyond the built-in scratch are refused with a clear error.
+checks it against the oracle and, bit for bit, against the workspace-taking
+moe_route_topk on two calls in a row (the array keeps the first call's
+contents when the second one runs), and that sizes beyond the built-in
+scratch are refused with a clear error.
 
 The file sorts last so that a run stopping at the first failure has already
 run every other test; it also passes on its own in a fresh process.
@@ -18,6 +19,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import synth
 import group_quantized_moe_gb300 as q
 from group_quantized_moe_gb300 import build_lib
@@ -81,6 +83,13 @@ def test_noalloc_router_matches_workspace_router_twice(dev):
         np.testing.assert_array_equal(w1.cpu().numpy().view(np.uint32),
                                       w0.cpu().numpy().view(np.uint32))
         np.testing.assert_array_equal(c1.cpu().numpy(), c0.cpu().numpy())
+        # and against the oracle: indices exact, weights within 2e-6
+        x = xd.float().cpu().numpy()
+        b = None if bias is None else bias.cpu().numpy()
+        oi, ow = oracle.topk(oracle.router_logits(x, wr.cpu().numpy(), b), k)
+        np.testing.assert_array_equal(i1.cpu().numpy(), oi)
+        assert np.abs(w1.cpu().numpy() - ow).max() <= 2e-6
+        np.testing.assert_array_equal(c1.cpu().numpy(), np.bincount(oi.reshape(-1), minlength=E))
 
 
 def test_noalloc_router_at_its_scratch_limit(dev):
