@@ -15,7 +15,7 @@
 //   gate/up: D_g, D_u in TMEM, epilogue h = silu(D_g) * D_u -> fp16 [tok, I]
 //   down:    D_d in TMEM, epilogue -> fp32 out[tok, H]
 //
-// CTA = 18 warps, one CTA per SM, persistent over work items
+// CTA = 16 warps, one CTA per SM, persistent over work items
 // (token tile of an expert, 128-feature tile):
 //   warp 12 (one lane): TMA producer of weight codes [128 rows x 64 K] into a
 //     ring (64B swizzle for INT8).
@@ -24,22 +24,20 @@
 //     16-row boxes for up to 64 tokens, one 128-row box above.
 //   warps 0-11 = three dequant warpgroups; warpgroup g converts the stages
 //     whose global number is g (mod 3), thread t the whole 64-K row t % 128
-//     of each weight tile,
-//     so three stages are being converted at once (one stage's conversion is
-//     latency bound; stages pipeline).  Codes -> fp16 (q - zp) * s, exact up
-//     to the final fp16 rounding, stored with tcgen05.st straight into tensor
-//     memory, where the MMA reads its A operand (row = TMEM lane, two K values
-//     per 32-bit column); this keeps shared memory for the TMA rings.  After
-//     an item's last stage all three run the epilogue (tcgen05.ld from TMEM,
-//     16-token column blocks in turn).  Each item's scale and zero-point
-//     lines are prefetched into L2 when the item starts.
-//   warps 14-17: one lane each issues tcgen05.mma (kind::f16, fp32
-//     accumulate) and one tcgen05.commit per stage, which frees the stage's
-//     A and B slots.  A single thread issues only about one MMA per 60-100
-//     cycles whatever N is, so items with few tokens split every stage's
-//     MMAs over the four issuers (four accumulators, summed in the
-//     epilogue); items with more tokens are tensor-bound and use two.
-//     Warp 14 also allocates TMEM.
+//     of each weight tile, so three stages are being converted at once (one
+//     stage's conversion is latency bound; stages pipeline).  A stage's codes
+//     are read into registers and its code slot released at once; they are
+//     converted to fp16 (q - zp) * s, exact up to the final fp16 rounding,
+//     and stored with tcgen05.st straight into tensor memory, where the MMA
+//     reads its A operand (row = TMEM lane, two K values per 32-bit column);
+//     this keeps shared memory for the TMA rings.  After an item's last stage
+//     all three run the epilogue (tcgen05.ld from TMEM, 16-token column
+//     blocks in turn).
+//   warp 14 (one lane): issues every tcgen05.mma (kind::f16, fp32
+//     accumulate) in stage order, with one tcgen05.commit per stage that
+//     frees the stage's A and B slots; also allocates TMEM.
+//   warp 15: the row exponents of each item's weight tile (see below), one
+//     item ahead.
 // Every wait is bounded; on a timeout the CTA raises QMM_DEV_WAIT_TIMEOUT,
 // stops issuing work, waits (bounded) for what is in flight, frees its TMEM
 // and returns.
@@ -63,10 +61,9 @@ constexpr int kDequantGroups = 3;  // warpgroups converting stages round-robin
 constexpr int kDequantWarps = 4 * kDequantGroups;  // warps 0-11
 constexpr int kWarpCodes = kDequantWarps;          // TMA producer of weight codes
 constexpr int kWarpRows = kDequantWarps + 1;       // TMA producer of token rows
-constexpr int kWarpMma = kDequantWarps + 2;        // first of the four MMA issuers
-constexpr int kWarpRexp = kDequantWarps + 6;       // row exponents, one item ahead
-constexpr int kThreads = (kDequantWarps + 7) * 32;
-constexpr int kLightN = 64;  // items with at most this many (padded) tokens use 4 issuers
+constexpr int kWarpMma = kDequantWarps + 2;        // the MMA issuer
+constexpr int kWarpRexp = kDequantWarps + 3;       // row exponents, one item ahead
+constexpr int kThreads = (kDequantWarps + 4) * 32;
 constexpr int kACols = kBK / 2;         // TMEM columns of one A tile stage
 constexpr int kBTile = kBN * kBK * 2;   // 16 KB fp16
 constexpr int kCTile = kBM * kBK;       // 8 KB INT8 codes (64B swizzle)
@@ -108,8 +105,8 @@ struct Smem {
   static constexpr int c_off = b_off + kB * kBTile;
   static constexpr int bar_off = c_off + kC * NT * kCTile;
   // barriers: c_full[kC], c_free[kC], a_full[kA], ab_free[kA], b_full[kB],
-  // acc_full, acc_free, rexp_full[2], rexp_free[2]
-  static constexpr int nbar = 2 * kC + 2 * kA + kB + 2 + 4;
+  // acc_full, acc_free, rexp_full[2], rexp_free[2], drain
+  static constexpr int nbar = 2 * kC + 2 * kA + kB + 2 + 4 + 1;
   static constexpr int misc_off = bar_off + nbar * 8;
   static constexpr int rexp_off = misc_off + 16;  // int32 [2 slots][NT][128 rows]
   static constexpr int meta_off = rexp_off + 2 * NT * kBM * 4;  // offsets[E+1], tile_start[E+1]
@@ -215,6 +212,10 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t *r) {
       : "memory");
 }
 
+__device__ __forceinline__ void sts_u32(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
 __device__ __forceinline__ void tmem_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
@@ -245,27 +246,17 @@ __device__ __forceinline__ void tmem_ld16x2(uint32_t a0, uint32_t a1, float (&v0
   }
 }
 
-// The same for four addresses.
-__device__ __forceinline__ void tmem_ld16x4(uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                            float (&v0)[16], float (&v1)[16], float (&v2)[16],
-                                            float (&v3)[16]) {
-  uint32_t r[64];
+// 16 columns at one TMEM address of this thread's lane.
+__device__ __forceinline__ void tmem_ld16x1(uint32_t a0, float (&v0)[16]) {
+  uint32_t r[16];
   asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%64];\n\t"
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%65];\n\t"
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47}, [%66];\n\t"
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [%67];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];\n\t"
       "tcgen05.wait::ld.sync.aligned;"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3)
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(a0)
       : "memory");
 #pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    v0[i] = __uint_as_float(r[i]);
-    v1[i] = __uint_as_float(r[16 + i]);
-    v2[i] = __uint_as_float(r[32 + i]);
-    v3[i] = __uint_as_float(r[48 + i]);
-  }
+  for (int i = 0; i < 16; ++i) v0[i] = __uint_as_float(r[i]);
 }
 
 // Shared-memory operand descriptor: K-major, 128B swizzle, 8-row groups 1024 B
@@ -380,6 +371,35 @@ __device__ __forceinline__ void dequant16_exact(uint4 v, int32_t zp, float s, ui
   o1 = make_uint4(r[4], r[5], r[6], r[7]);
 }
 
+// One matrix's 64 codes of a thread's weight row (four 16-byte chunks in K
+// order) -> 64 fp16 weights stored into 32 TMEM columns of the thread's lane
+// at taddr (asynchronous: tmem_wait_st() waits for the stores).  kChoose:
+// the fast or the exact form per this thread's `fast`; otherwise the fast
+// form.  Every lane of the warp must call it (the stores are warp-collective).
+template <bool kChoose>
+__device__ __forceinline__ void convert_row(const uint4 (&cv)[4], __half2 mz2, __half2 s2,
+                                            int32_t zp, float s, bool fast, uint32_t taddr) {
+  uint32_t packed[32];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    uint4 o0, o1;
+    if (!kChoose || fast)
+      dequant16(cv[j], mz2, s2, o0, o1);
+    else
+      dequant16_exact(cv[j], zp, s, o0, o1);
+    packed[8 * j + 0] = o0.x;
+    packed[8 * j + 1] = o0.y;
+    packed[8 * j + 2] = o0.z;
+    packed[8 * j + 3] = o0.w;
+    packed[8 * j + 4] = o1.x;
+    packed[8 * j + 5] = o1.y;
+    packed[8 * j + 6] = o1.z;
+    packed[8 * j + 7] = o1.w;
+  }
+  tmem_st16(taddr, packed);
+  tmem_st16(taddr + 16, packed + 16);
+}
+
 // 2^s and 2^-s for the power of two s that puts a positive magnitude m into
 // [2^14, 2^15) (s clamped to [-126, 126], so that both are normal fp32; m = 0
 // gives the largest s).  Read from m's exponent bits.
@@ -420,9 +440,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   // row-exponent slots: filled by the exponent warp one item ahead
   auto rexp_full = [&](int i) { return acc_free + 8 + 8 * i; };
   auto rexp_free = [&](int i) { return acc_free + 24 + 8 * i; };
+  // tracks the issuer's MMAs in flight after an abort
+  const uint32_t drain_bar = acc_free + 40;
   int32_t *s_rexp = reinterpret_cast<int32_t *>(gbase + S::rexp_off);
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + S::misc_off);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(gbase + S::misc_off + 4);
+  // written, never read: see the release of a code slot below
+  const uint32_t sink = base + S::misc_off + 8;
   int32_t *s_off = reinterpret_cast<int32_t *>(gbase + S::meta_off);
   int32_t *s_ts = s_off + a.E + 1;
   if (a.lin_M > 0) {
@@ -448,14 +472,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(c_free(i), 4);  // one arrival per warp of the converting warpgroup
     }
     for (int i = 0; i < kA; ++i) mbar_init(a_full(i), 4);
-    for (int i = 0; i < kA; ++i) mbar_init(ab_free(i), 4);  // one commit per MMA issuer
+    // two commits per gate/up stage, one per down stage (see the MMA issuers)
+    for (int i = 0; i < kA; ++i) mbar_init(ab_free(i), 1);  // the issuer's commit
     for (int i = 0; i < kB; ++i) mbar_init(b_full(i), 1);
-    mbar_init(acc_full, 4);
+    mbar_init(acc_full, 1);
     mbar_init(acc_free, kDequantWarps);
     for (int i = 0; i < 2; ++i) {
       mbar_init(rexp_full(i), 32);             // every lane of the exponent warp
       mbar_init(rexp_free(i), kDequantWarps);  // one arrival per dequant warp
     }
+    mbar_init(drain_bar, 1);
     *abort_flag = 0;
     mbar_fence_init();
   }
@@ -484,6 +510,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int c = static_cast<int>(gs % kC);
           const uint32_t cu = static_cast<uint32_t>(gs / kC);
           if (!wait_ok(c_free(c), (cu & 1u) ^ 1u, a.status, abort_flag)) break;
+          // the converting warps' reads of the slot (generic proxy) before
+          // the copy's writes into it (async proxy)
+          fence_proxy_async_smem();
           mbar_arrive_expect_tx(c_full(c), NT * kCTile);
           tma_load_3d(sC + (c * NT + 0) * kCTile, &tm_codes0, kb * kBK, it.f * kBM, it.e, c_full(c),
                       pol);
@@ -572,56 +601,45 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       mbar_arrive(rexp_full(slot));
     }
-  } else if (warp >= kWarpMma) {
-    // ---------------------------------------------------- MMA issuers
-    // A single thread issues only about one MMA per 60-100 cycles whatever
-    // N is, so light items (at most kLightN tokens) spread each stage's MMAs
-    // over four issuers with one accumulator each (64 TMEM columns):
-    //   gate/up: issuer i -> matrix i >> 1, the 16-K steps of parity i & 1
-    //   down:    issuer i -> the 16-K step i of every stage
-    // Heavier items are tensor-bound: issuers 0 and 1 each own a 128-column
-    // accumulator (gate/up: matrix i; down: K steps of parity i), and 2, 3
-    // only take part in the commits.  The epilogue adds the partial sums.
-    const int issuer = warp - kWarpMma;
+  } else if (warp == kWarpMma) {
+    // ---------------------------------------------------- MMA issuer
+    // One thread issues every MMA, stage after stage: gate/up into two
+    // accumulators (columns 0 and 128, npad columns each), down into one
+    // (column 0).  In-order issue keeps the rings' barrier phases in order:
+    // a stage's A and B slots are freed by one commit after its MMAs, and
+    // the slot's next user can never see a phase two uses old.  Back-to-back
+    // MMAs of one thread issue about every 70 cycles, so a gate/up stage
+    // (eight MMAs) issues in about the time HBM takes to deliver its codes.
     if (lane == 0) {
       int64_t gs = 0;
       uint32_t nitem_done = 0;
       for (int64_t item = blockIdx.x; item < nitems && !*abort_flag; item += gridDim.x) {
         const Item it = decode_item(s_off, s_ts, a.E, item, ftiles, a.nsplit);
         const int npad = (it.ntok + 15) & ~15;
-        const bool light = npad <= kLightN;
-        const bool active = light || issuer < 2;
         const uint32_t idesc = idesc_f16(npad);
-        const uint32_t d_tmem = tmem + (light ? 64u : 128u) * static_cast<uint32_t>(issuer);
-        const int mat = NT == 2 ? (light ? issuer >> 1 : issuer) : 0;
         // the previous item's epilogue has drained the accumulators
         if (!wait_ok(acc_free, (nitem_done & 1u) ^ 1u, a.status, abort_flag)) break;
         tc_fence_after();
         bool ok = true;
-        uint32_t acc = 0;  // the first MMA of the item into this accumulator overwrites it
+        uint32_t acc = 0;  // the item's first MMA into an accumulator overwrites it
         for (int kb = 0; kb < kps; ++kb, ++gs) {
           const int sa = static_cast<int>(gs % kA), sb = static_cast<int>(gs % kB);
           const uint32_t ua = static_cast<uint32_t>(gs / kA), ub = static_cast<uint32_t>(gs / kB);
-          // every issuer waits for the stage, so that no commit runs ahead of
-          // the slot's phase
           if (!wait_ok(b_full(sb), ub & 1u, a.status, abort_flag) ||
               !wait_ok(a_full(sa), ua & 1u, a.status, abort_flag)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          if (active) {
+          const uint64_t bd = smem_desc_sw128(sB + sb * kBTile);
+          const uint32_t a0 = tmem + a_col(sa, 0);
+          // the descriptor's start address is in 16-byte units: +2 per 16 K
 #pragma unroll
-            for (int kk = 0; kk < kBK / 16; ++kk) {
-              bool mine;
-              if constexpr (NT == 2) mine = light ? ((kk & 1) == (issuer & 1)) : true;
-              else mine = light ? (kk == issuer) : ((kk & 1) == issuer);
-              if (mine) {
-                tc_mma_ts(d_tmem, tmem + a_col(sa, mat) + kk * 8,
-                          smem_desc_sw128(sB + sb * kBTile + kk * 32), idesc, acc);
-                acc = 1u;
-              }
-            }
+          for (int kk = 0; kk < kBK / 16; ++kk) {
+            tc_mma_ts(tmem, a0 + kk * 8, bd + 2 * kk, idesc, acc);
+            if constexpr (NT == 2)
+              tc_mma_ts(tmem + kBN, a0 + kACols + kk * 8, bd + 2 * kk, idesc, acc);
+            acc = 1u;
           }
           tc_commit(ab_free(sa));
         }
@@ -629,11 +647,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_commit(acc_full);
         ++nitem_done;
       }
-      // After an abort, wait (bounded) for the MMAs already committed.
-      if (*abort_flag)
-        for (int64_t j = (gs > kA ? gs - kA : 0); j < gs; ++j)
-          mbar_wait_bounded(ab_free(static_cast<int>(j % kA)),
-                            static_cast<uint32_t>((j / kA) & 1), a.status);
+      // After an abort, wait (bounded) for the MMAs in flight.
+      if (*abort_flag) {
+        tc_commit(drain_bar);
+        mbar_wait_bounded(drain_bar, 0u, a.status);
+      }
     }
   } else {
     // ------------------------------------------ dequantisation + epilogue
@@ -694,8 +712,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       bool ok = true;
-      for (int kb = kbs; kb < kbe; ++kb, ++gs) {
-        if (static_cast<int>(gs % kDequantGroups) != wg) continue;
+      // This warpgroup's stages of the item, directly (stage kb has global
+      // number gs_item + kb - kbs).
+      const int64_t gs_item = gs;
+      gs += kps;
+      for (int kb = kb0; kb < kbe; kb += kDequantGroups) {
+        const int64_t g = gs_item + (kb - kbs);
         // Fast form (q - zp exact in fp16, times the fp16 scale) while the
         // zero point keeps 1024 + zp and every q - zp (|.| <= 2048) exact in
         // fp16 and the scaled scale is a normal fp16; the exact form otherwise.
@@ -719,50 +741,67 @@ __global__ void __launch_bounds__(kThreads, 1)
             z_nx[t] = __ldg(zpp[t] + gi);
           }
         }
-        const int c = static_cast<int>(gs % kC);
-        const uint32_t cu = static_cast<uint32_t>(gs / kC);
-        const int s = static_cast<int>(gs % kA);
-        const uint32_t su = static_cast<uint32_t>(gs / kA);
-        bool got = wait_ok(c_full(c), cu & 1u, a.status, abort_flag) &&
-                   wait_ok(ab_free(s), (su & 1u) ^ 1u, a.status, abort_flag);
-        if (!__all_sync(0xFFFFFFFFu, got)) {  // warp-uniform exit
-          ok = false;
+        const int c = static_cast<int>(g % kC);
+        const uint32_t cu = static_cast<uint32_t>(g / kC);
+        const int s = static_cast<int>(g % kA);
+        const uint32_t su = static_cast<uint32_t>(g / kA);
+        if (!__all_sync(0xFFFFFFFFu, wait_ok(c_full(c), cu & 1u, a.status, abort_flag))) {
+          ok = false;  // warp-uniform exit
           break;
         }
-        tc_fence_after();
+        // Every code chunk of the stage is read before any is converted, and
+        // the fast / exact choice is made once per matrix and stage: with a
+        // branch per chunk each read waited behind the previous chunk's
+        // conversion.
+        uint4 cv[NT][4];
 #pragma unroll
         for (int t = 0; t < NT; ++t) {
           // codes row `row`: 64 bytes, 16-byte chunk j stored at j ^ ((row >> 1) & 3)
           const uint32_t crow = sC + (c * NT + t) * kCTile + row * kBK;
-          uint32_t packed[32];
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const uint4 v = lds128(crow + ((j ^ ((row >> 1) & 3)) << 4));
-            uint4 o0, o1;
-            if (fast[t])
-              dequant16(v, mz2[t], s2[t], o0, o1);
-            else
-              dequant16_exact(v, zx[t], sx[t], o0, o1);
-            packed[8 * j + 0] = o0.x;
-            packed[8 * j + 1] = o0.y;
-            packed[8 * j + 2] = o0.z;
-            packed[8 * j + 3] = o0.w;
-            packed[8 * j + 4] = o1.x;
-            packed[8 * j + 5] = o1.y;
-            packed[8 * j + 6] = o1.z;
-            packed[8 * j + 7] = o1.w;
-          }
-          // A[row][k] -> TMEM lane row, column k / 2 of the stage slot
-          tmem_st16(tmem + lane_base + a_col(s, t), packed);
-          tmem_st16(tmem + lane_base + a_col(s, t) + 16, packed + 16);
+          for (int j = 0; j < 4; ++j) cv[t][j] = lds128(crow + ((j ^ ((row >> 1) & 3)) << 4));
+        }
+        // The code slot is released as soon as its reads have returned (not
+        // after the conversion), so that its refill from HBM overlaps this
+        // warpgroup's conversion: the slots then spend their time loading.
+        // A store of a value computed from every word read cannot issue
+        // before all the reads have completed; the arrive follows it.
+        {
+          uint32_t dep = 0;
+#pragma unroll
+          for (int t = 0; t < NT; ++t)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) dep ^= cv[t][j].x ^ cv[t][j].y ^ cv[t][j].z ^ cv[t][j].w;
+          sts_u32(sink, dep);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(c_free(c));
+        if (!__all_sync(0xFFFFFFFFu, wait_ok(ab_free(s), (su & 1u) ^ 1u, a.status, abort_flag))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        bool all_fast = true;
+#pragma unroll
+        for (int t = 0; t < NT; ++t) all_fast = all_fast && fast[t];
+        // A[row][k] -> TMEM lane row, column k / 2 of the stage slot.  The
+        // branch is warp-uniform (the TMEM stores are warp-collective); a
+        // warp with any row outside the fast form's range chooses per chunk.
+        if (__all_sync(0xFFFFFFFFu, all_fast)) {
+#pragma unroll
+          for (int t = 0; t < NT; ++t)
+            convert_row<false>(cv[t], mz2[t], s2[t], zx[t], sx[t], true,
+                               tmem + lane_base + a_col(s, t));
+        } else {
+#pragma unroll
+          for (int t = 0; t < NT; ++t)
+            convert_row<true>(cv[t], mz2[t], s2[t], zx[t], sx[t], fast[t],
+                              tmem + lane_base + a_col(s, t));
         }
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(a_full(s));
-          mbar_arrive(c_free(c));
-        }
+        if (lane == 0) mbar_arrive(a_full(s));
       }
       if (!ok) break;
       // ---------------------------------------------------- epilogue
@@ -770,23 +809,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       tc_fence_after();
       const int feat = it.f * kBM + row;
-      // Accumulators (see the MMA issuers): light items four of 64 columns,
-      // heavy items two of 128; partial sums are added in a fixed order.
-      const bool light = ((it.ntok + 15) & ~15) <= kLightN;
+      // Accumulators (see the MMA issuer): gate at column 0 and up at kBN
+      // (gate/up), or the down projection's at column 0.
       for (int c0 = 16 * wg; c0 < it.ntok; c0 += 16 * kDequantGroups) {
         float v0[16], v1[16];
-        if (light) {
-          float p0[16], p1[16];
-          tmem_ld16x4(tmem + lane_base + c0, tmem + lane_base + 64 + c0,
-                      tmem + lane_base + 128 + c0, tmem + lane_base + 192 + c0, v0, p0, v1, p1);
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            v0[j] += p0[j];
-            v1[j] += p1[j];
-          }
-        } else {
+        if constexpr (NT == 2)
           tmem_ld16x2(tmem + lane_base + c0, tmem + lane_base + kBN + c0, v0, v1);
-        }
+        else
+          tmem_ld16x1(tmem + lane_base + c0, v0);
         // accumulators x (token row's 2^c) x (weight row's 2^-r): exact
         // power-of-two rescaling back to the true products
         const float *cs = a.colscale + it.t0 + c0;
@@ -803,12 +833,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                   silu_f(v0[j] * c * rdn[0]) * (v1[j] * c * rdn[1]);
             }
         } else {
-          // partial sums over disjoint K steps
 #pragma unroll
           for (int j = 0; j < 16; ++j)
             if (c0 + j < it.ntok && feat_ok)
               outp[static_cast<int64_t>(it.t0 + c0 + j) * a.out_ld + feat] =
-                  (v0[j] + v1[j]) * __ldg(cs + j) * rdn[0];
+                  v0[j] * __ldg(cs + j) * rdn[0];
         }
       }
       tc_fence_before();
