@@ -15,13 +15,13 @@
 //   gate/up: D_g, D_u in TMEM, epilogue h = silu(D_g) * D_u -> fp16 [tok, I]
 //   down:    D_d in TMEM, epilogue -> fp32 out[tok, H]
 //
-// CTA = 16 warps, one CTA per SM, persistent over work items
+// CTA = 17 warps, one CTA per SM, persistent over work items
 // (token tile of an expert, 128-feature tile):
 //   warp 12 (one lane): TMA producer of weight codes [128 rows x 64 K] into a
 //     ring (64B swizzle for INT8).
 //   warp 13 (one lane): TMA producer of token rows [npad x 64 K] fp16 into
-//     the B stages (128B swizzle, the canonical K-major operand layout):
-//     16-row boxes for up to 64 tokens, one 128-row box above.
+//     the B stages (128B swizzle, the canonical K-major operand layout), one
+//     box of 16, 32, 64 or 128 rows per stage.
 //   warps 0-11 = three dequant warpgroups; warpgroup g converts the stages
 //     whose global number is g (mod 3), thread t the whole 64-K row t % 128
 //     of each weight tile, so three stages are being converted at once (one
@@ -33,10 +33,12 @@
 //     this keeps shared memory for the TMA rings.  After an item's last stage
 //     all three run the epilogue (tcgen05.ld from TMEM, 16-token column
 //     blocks in turn).
-//   warp 14 (one lane): issues every tcgen05.mma (kind::f16, fp32
-//     accumulate) in stage order, with one tcgen05.commit per stage that
-//     frees the stage's A and B slots; also allocates TMEM.
-//   warp 15: the row exponents of each item's weight tile (see below), one
+//   warps 14 and 15 (one lane each): issue the tcgen05.mma (kind::f16, fp32
+//     accumulate) of one weight matrix each (gate, up; down uses the first),
+//     every stage in order, with one tcgen05.commit per stage; a stage's A
+//     and B slots are free once both commits have arrived.  Warp 14 also
+//     allocates TMEM.
+//   warp 16: the row exponents of each item's weight tile (see below), one
 //     item ahead.
 // Every wait is bounded; on a timeout the CTA raises QMM_DEV_WAIT_TIMEOUT,
 // stops issuing work, waits (bounded) for what is in flight, frees its TMEM
@@ -61,9 +63,9 @@ constexpr int kDequantGroups = 3;  // warpgroups converting stages round-robin
 constexpr int kDequantWarps = 4 * kDequantGroups;  // warps 0-11
 constexpr int kWarpCodes = kDequantWarps;          // TMA producer of weight codes
 constexpr int kWarpRows = kDequantWarps + 1;       // TMA producer of token rows
-constexpr int kWarpMma = kDequantWarps + 2;        // the MMA issuer
-constexpr int kWarpRexp = kDequantWarps + 3;       // row exponents, one item ahead
-constexpr int kThreads = (kDequantWarps + 4) * 32;
+constexpr int kWarpMma = kDequantWarps + 2;        // MMA issuers (one per matrix)
+constexpr int kWarpRexp = kDequantWarps + 4;       // row exponents, one item ahead
+constexpr int kThreads = (kDequantWarps + 5) * 32;
 constexpr int kACols = kBK / 2;         // TMEM columns of one A tile stage
 constexpr int kBTile = kBN * kBK * 2;   // 16 KB fp16
 constexpr int kCTile = kBM * kBK;       // 8 KB INT8 codes (64B swizzle)
@@ -105,8 +107,8 @@ struct Smem {
   static constexpr int c_off = b_off + kB * kBTile;
   static constexpr int bar_off = c_off + kC * NT * kCTile;
   // barriers: c_full[kC], c_free[kC], a_full[kA], ab_free[kA], b_full[kB],
-  // acc_full, acc_free, rexp_full[2], rexp_free[2], drain
-  static constexpr int nbar = 2 * kC + 2 * kA + kB + 2 + 4 + 1;
+  // acc_full, acc_free, rexp_full[2], rexp_free[2], drain[2]
+  static constexpr int nbar = 2 * kC + 2 * kA + kB + 2 + 4 + 2;
   static constexpr int misc_off = bar_off + nbar * 8;
   static constexpr int rexp_off = misc_off + 16;  // int32 [2 slots][NT][128 rows]
   static constexpr int meta_off = rexp_off + 2 * NT * kBM * 4;  // offsets[E+1], tile_start[E+1]
@@ -415,7 +417,9 @@ template <int NT>
 __global__ void __launch_bounds__(kThreads, 1)
     moe_tc_kernel(const __grid_constant__ CUtensorMap tm_codes0,
                   const __grid_constant__ CUtensorMap tm_codes1,
-                  const __grid_constant__ CUtensorMap tm_x,
+                  const __grid_constant__ CUtensorMap tm_x16,
+                  const __grid_constant__ CUtensorMap tm_x32,
+                  const __grid_constant__ CUtensorMap tm_x64,
                   const __grid_constant__ CUtensorMap tm_x128, TcArgs a) {
   pdl_enter();
   using S = Smem<NT>;
@@ -431,8 +435,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto c_full = [&](int i) { return bar0 + 8 * i; };
   auto c_free = [&](int i) { return bar0 + 8 * (kC + i); };
   auto a_full = [&](int i) { return bar0 + 8 * (2 * kC + i); };
-  // A and B slot s are freed by one MMA commit: commits are costly for the
-  // single issuing thread.
+  // A and B slot s are freed together by the stage's MMA commits
   auto ab_free = [&](int slot) { return bar0 + 8 * (2 * kC + kA + slot); };
   auto b_full = [&](int i) { return bar0 + 8 * (2 * kC + 2 * kA + i); };
   const uint32_t acc_full = bar0 + 8 * (2 * kC + 2 * kA + kB);
@@ -440,8 +443,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   // row-exponent slots: filled by the exponent warp one item ahead
   auto rexp_full = [&](int i) { return acc_free + 8 + 8 * i; };
   auto rexp_free = [&](int i) { return acc_free + 24 + 8 * i; };
-  // tracks the issuer's MMAs in flight after an abort
-  const uint32_t drain_bar = acc_free + 40;
+  // per MMA issuer: tracks its MMAs in flight after an abort
+  auto drain_bar = [&](int i) { return acc_free + 40 + 8 * i; };
   int32_t *s_rexp = reinterpret_cast<int32_t *>(gbase + S::rexp_off);
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + S::misc_off);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(gbase + S::misc_off + 4);
@@ -473,15 +476,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < kA; ++i) mbar_init(a_full(i), 4);
     // two commits per gate/up stage, one per down stage (see the MMA issuers)
-    for (int i = 0; i < kA; ++i) mbar_init(ab_free(i), 1);  // the issuer's commit
+    for (int i = 0; i < kA; ++i) mbar_init(ab_free(i), NT);  // one commit per issuer
     for (int i = 0; i < kB; ++i) mbar_init(b_full(i), 1);
-    mbar_init(acc_full, 1);
+    mbar_init(acc_full, NT);
     mbar_init(acc_free, kDequantWarps);
     for (int i = 0; i < 2; ++i) {
       mbar_init(rexp_full(i), 32);             // every lane of the exponent warp
       mbar_init(rexp_free(i), kDequantWarps);  // one arrival per dequant warp
     }
-    mbar_init(drain_bar, 1);
+    mbar_init(drain_bar(0), 1);
+    mbar_init(drain_bar(1), 1);
     *abort_flag = 0;
     mbar_fence_init();
   }
@@ -535,20 +539,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int64_t item = blockIdx.x; item < nitems && !*abort_flag; item += gridDim.x) {
         const Item it = decode_item(s_off, s_ts, a.E, item, ftiles, a.nsplit);
         const int npad = (it.ntok + 15) & ~15;
+        const int box_rows = npad <= 16 ? 16 : npad <= 32 ? 32 : npad <= 64 ? 64 : kBN;
+        const CUtensorMap *box = npad <= 16   ? &tm_x16
+                                 : npad <= 32 ? &tm_x32
+                                 : npad <= 64 ? &tm_x64
+                                              : &tm_x128;
         for (int kb = it.ks * kps; kb < (it.ks + 1) * kps; ++kb, ++gs) {
           const int s = static_cast<int>(gs % kB);
           const uint32_t su = static_cast<uint32_t>(gs / kB);
           if (!wait_ok(ab_free(s), (su & 1u) ^ 1u, a.status, abort_flag)) break;
-          if (npad > 64) {
-            // one 128-row box (rows past the item's tokens are never used)
-            mbar_arrive_expect_tx(b_full(s), kBN * kBK * 2);
-            tma_load_2d(sB + s * kBTile, &tm_x128, kb * kBK, it.t0, b_full(s), pol);
-          } else {
-            mbar_arrive_expect_tx(b_full(s), npad * kBK * 2);
-            for (int r = 0; r < npad; r += 16)
-              tma_load_2d(sB + s * kBTile + r * kBK * 2, &tm_x, kb * kBK, it.t0 + r, b_full(s),
-                          pol);
-          }
+          // one box of 16, 32, 64 or 128 rows (a thread issues one TMA copy
+          // per few hundred cycles); rows past the item's tokens are never
+          // used, rows past the buffer are filled with zeros
+          mbar_arrive_expect_tx(b_full(s), box_rows * kBK * 2);
+          tma_load_2d(sB + s * kBTile, box, kb * kBK, it.t0, b_full(s), pol);
         }
       }
       if (*abort_flag)
@@ -601,18 +605,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       mbar_arrive(rexp_full(slot));
     }
-  } else if (warp == kWarpMma) {
-    // ---------------------------------------------------- MMA issuer
-    // One thread issues every MMA, stage after stage: gate/up into two
-    // accumulators (columns 0 and 128, npad columns each), down into one
-    // (column 0).  In-order issue keeps the rings' barrier phases in order:
-    // a stage's A and B slots are freed by one commit after its MMAs, and
-    // the slot's next user can never see a phase two uses old.  Back-to-back
-    // MMAs of one thread issue about every 70 cycles, so a gate/up stage
-    // (eight MMAs) issues in about the time HBM takes to deliver its codes.
-    if (lane == 0) {
+  } else if (warp == kWarpMma || warp == kWarpMma + 1) {
+    // ---------------------------------------------------- MMA issuers
+    // Issuer t (one per weight matrix: gate and up, or down alone) issues
+    // that matrix's MMAs of every stage, in stage order, into its own
+    // accumulator (gate at column 0, up at kBN, down at 0; npad columns),
+    // and commits once per stage: a stage's A and B slots are free when
+    // every issuer's commit has arrived.  One thread issues back-to-back
+    // MMAs about every 70 cycles and spends about as long again per stage on
+    // its barrier waits, so the gate/up stage's eight MMAs go to two
+    // threads (the down stage's four to one: splitting them by K step was
+    // slower).  Each issuer walks every stage in order, so it sees every
+    // phase of the rings' barriers in order.
+    const int t = warp - kWarpMma;
+    if (lane == 0 && t < NT) {
       int64_t gs = 0;
       uint32_t nitem_done = 0;
+      const uint32_t d = tmem + kBN * static_cast<uint32_t>(t);
       for (int64_t item = blockIdx.x; item < nitems && !*abort_flag; item += gridDim.x) {
         const Item it = decode_item(s_off, s_ts, a.E, item, ftiles, a.nsplit);
         const int npad = (it.ntok + 15) & ~15;
@@ -621,7 +630,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!wait_ok(acc_free, (nitem_done & 1u) ^ 1u, a.status, abort_flag)) break;
         tc_fence_after();
         bool ok = true;
-        uint32_t acc = 0;  // the item's first MMA into an accumulator overwrites it
+        uint32_t acc = 0;  // the item's first MMA into the accumulator overwrites it
         for (int kb = 0; kb < kps; ++kb, ++gs) {
           const int sa = static_cast<int>(gs % kA), sb = static_cast<int>(gs % kB);
           const uint32_t ua = static_cast<uint32_t>(gs / kA), ub = static_cast<uint32_t>(gs / kB);
@@ -632,13 +641,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc_fence_after();
           const uint64_t bd = smem_desc_sw128(sB + sb * kBTile);
-          const uint32_t a0 = tmem + a_col(sa, 0);
+          const uint32_t a0 = tmem + a_col(sa, t);
           // the descriptor's start address is in 16-byte units: +2 per 16 K
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk) {
-            tc_mma_ts(tmem, a0 + kk * 8, bd + 2 * kk, idesc, acc);
-            if constexpr (NT == 2)
-              tc_mma_ts(tmem + kBN, a0 + kACols + kk * 8, bd + 2 * kk, idesc, acc);
+            tc_mma_ts(d, a0 + kk * 8, bd + 2 * kk, idesc, acc);
             acc = 1u;
           }
           tc_commit(ab_free(sa));
@@ -647,10 +654,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_commit(acc_full);
         ++nitem_done;
       }
-      // After an abort, wait (bounded) for the MMAs in flight.
+      // After an abort, wait (bounded) for this issuer's MMAs in flight.
       if (*abort_flag) {
-        tc_commit(drain_bar);
-        mbar_wait_bounded(drain_bar, 0u, a.status);
+        tc_commit(drain_bar(t));
+        mbar_wait_bounded(drain_bar(t), 0u, a.status);
       }
     }
   } else {
@@ -663,13 +670,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int64_t item = blockIdx.x; item < nitems && !*abort_flag; item += gridDim.x) {
       const Item it = decode_item(s_off, s_ts, a.E, item, ftiles, a.nsplit);
       const int64_t wrow = static_cast<int64_t>(it.f) * kBM + row;
-      const float *scp[NT];
-      const int32_t *zpp[NT];
-#pragma unroll
-      for (int t = 0; t < NT; ++t) {
-        scp[t] = a.sc[t] + it.e * a.gstride[t] + wrow * a.G;
-        zpp[t] = a.zp[t] + it.e * a.gstride[t] + wrow * a.G;
-      }
+      // element offset of this row's groups in matrix t's scale and
+      // zero-point arrays (the matrices of one launch have the same shape)
+      const int64_t goff = it.e * a.gstride[0] + wrow * a.G;
       // Row scale 2^r of each matrix (from the exponent warp) and its inverse,
       // which the epilogue applies.
       float rup[NT], rdn[NT];
@@ -707,8 +710,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int gi = (kb0 * kBK) >> a.group_shift;
 #pragma unroll
         for (int t = 0; t < NT; ++t) {
-          s_nx[t] = __ldg(scp[t] + gi);
-          z_nx[t] = __ldg(zpp[t] + gi);
+          s_nx[t] = __ldg(a.sc[t] + goff + gi);
+          z_nx[t] = __ldg(a.zp[t] + goff + gi);
         }
       }
       bool ok = true;
@@ -737,8 +740,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int gi = ((kb + kDequantGroups) * kBK) >> a.group_shift;
 #pragma unroll
           for (int t = 0; t < NT; ++t) {
-            s_nx[t] = __ldg(scp[t] + gi);
-            z_nx[t] = __ldg(zpp[t] + gi);
+            s_nx[t] = __ldg(a.sc[t] + goff + gi);
+            z_nx[t] = __ldg(a.zp[t] + goff + gi);
           }
         }
         const int c = static_cast<int>(g % kC);
@@ -809,7 +812,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       tc_fence_after();
       const int feat = it.f * kBM + row;
-      // Accumulators (see the MMA issuer): gate at column 0 and up at kBN
+      // Accumulators (see the MMA issuers): gate at column 0 and up at kBN
       // (gate/up), or the down projection's at column 0.
       for (int c0 = 16 * wg; c0 < it.ntok; c0 += 16 * kDequantGroups) {
         float v0[16], v1[16];
@@ -987,6 +990,18 @@ bool make_codes_map(CUtensorMap *m, const QMat &w, int E) {
 }
 
 // fp16 token rows [MK, K] as a 2-D map, box [64, box_rows], 128-byte swizzle.
+// Maps of one fp16 row buffer with boxes of 16, 32, 64 and 128 rows.
+struct RowMaps {
+  CUtensorMap m[4];
+};
+
+bool make_rows_map(CUtensorMap *m, const __half *p, int64_t MK, int64_t K, int box_rows);
+
+bool make_row_maps(RowMaps *r, const __half *p, int64_t MK, int64_t K) {
+  return make_rows_map(&r->m[0], p, MK, K, 16) && make_rows_map(&r->m[1], p, MK, K, 32) &&
+         make_rows_map(&r->m[2], p, MK, K, 64) && make_rows_map(&r->m[3], p, MK, K, kBN);
+}
+
 bool make_rows_map(CUtensorMap *m, const __half *p, int64_t MK, int64_t K, int box_rows) {
   auto fn = encode_fn();
   if (!fn) return false;
@@ -1000,13 +1015,14 @@ bool make_rows_map(CUtensorMap *m, const __half *p, int64_t MK, int64_t K, int b
 }
 
 template <int NT>
-cudaError_t run_tc(const CUtensorMap &c0, const CUtensorMap &c1, const CUtensorMap &x,
-                   const CUtensorMap &x128, const TcArgs &a, cudaStream_t s) {
+cudaError_t run_tc(const CUtensorMap &c0, const CUtensorMap &c1, const RowMaps &x,
+                   const TcArgs &a, cudaStream_t s) {
   auto k = moe_tc_kernel<NT>;
   const int bytes = Smem<NT>::bytes_for(a.E);
   cudaError_t e = ensure_smem(reinterpret_cast<const void *>(k), bytes);
   if (e != cudaSuccess) return e;
-  return launch_pdl(k, dim3(sm_count()), dim3(kThreads), bytes, s, c0, c1, x, x128, a);
+  return launch_pdl(k, dim3(sm_count()), dim3(kThreads), bytes, s, c0, c1, x.m[0], x.m[1],
+                    x.m[2], x.m[3], a);
 }
 
 // y = the sum of the nsplit partial results of the split K range, added in
@@ -1071,11 +1087,11 @@ cudaError_t launch_linear_tc(const void *x, int64_t M, const QMat &w, void *y, b
                              static_cast<const int32_t *>(nullptr),
                              static_cast<const int32_t *>(nullptr), M, xg, xs);
   if (e != cudaSuccess) return e;
-  CUtensorMap mw, mx, mx128;
+  CUtensorMap mw;
+  RowMaps mx;
   QMat w1 = w;
   w1.codes_stride = N * K;  // one matrix: any positive stride of whole 16-byte units
-  if (!make_codes_map(&mw, w1, 1) || !make_rows_map(&mx, xg, M, K, 16) ||
-      !make_rows_map(&mx128, xg, M, K, kBN))
+  if (!make_codes_map(&mw, w1, 1) || !make_row_maps(&mx, xg, M, K))
     return cudaErrorInvalidValue;
   // 2) the GEMM: partial sums of each K split (fp32 y directly when there is
   // one split)
@@ -1101,7 +1117,7 @@ cudaError_t launch_linear_tc(const void *x, int64_t M, const QMat &w, void *y, b
   a.lin_M = static_cast<int>(M);
   a.nsplit = S;
   a.out_split = M * N;
-  e = run_tc<1>(mw, mw, mx, mx128, a, s);
+  e = run_tc<1>(mw, mw, mx, a, s);
   if (e != cudaSuccess || direct) return e;
   // 3) the splits added in order
   const int64_t n = M * N;
@@ -1113,9 +1129,12 @@ cudaError_t launch_linear_tc(const void *x, int64_t M, const QMat &w, void *y, b
                     static_cast<const float *>(part), S, n, y);
 }
 
-bool moe_tc_supported(const QMat &gate, const QMat &down, int64_t H, int64_t I) {
-  return gate.bits == 8 && down.bits == 8 && gate.group >= 64 && H % kBM == 0 && I % kBM == 0 &&
-         H % kBK == 0 && I % kBK == 0 && encode_fn() != nullptr;
+bool moe_tc_supported(const QMat &gate, const QMat &up, const QMat &down, int64_t H, int64_t I) {
+  // gate and up share one scale / zero-point offset per dequantising thread
+  const bool same_layout = up.groups_stride == gate.groups_stride && up.group == gate.group &&
+                           up.rows == gate.rows && up.cols == gate.cols;
+  return gate.bits == 8 && up.bits == 8 && down.bits == 8 && gate.group >= 64 && same_layout &&
+         H % kBM == 0 && I % kBM == 0 && H % kBK == 0 && I % kBK == 0 && encode_fn() != nullptr;
 }
 
 cudaError_t launch_moe_tc(const void *x, int64_t M, int k, int E, const QMat &gate, const QMat &up,
@@ -1130,11 +1149,11 @@ cudaError_t launch_moe_tc(const void *x, int64_t M, int k, int E, const QMat &ga
                                static_cast<const int32_t *>(ws.assign), MK, ws.xg, ws.xs);
     if (e != cudaSuccess) return e;
   }
-  CUtensorMap mg, mu, md, mx, mx128, mh, mh128;
+  CUtensorMap mg, mu, md;
+  RowMaps mx, mh;
   if (!make_codes_map(&mg, gate, E) || !make_codes_map(&mu, up, E) ||
-      !make_codes_map(&md, down, E) || !make_rows_map(&mx, ws.xg, MK, H, 16) ||
-      !make_rows_map(&mx128, ws.xg, MK, H, kBN) || !make_rows_map(&mh, ws.hh, MK, I, 16) ||
-      !make_rows_map(&mh128, ws.hh, MK, I, kBN))
+      !make_codes_map(&md, down, E) || !make_row_maps(&mx, ws.xg, MK, H) ||
+      !make_row_maps(&mh, ws.hh, MK, I))
     return cudaErrorInvalidValue;
   // 2) gate + up with SwiGLU -> fp32 h
   TcArgs a{};
@@ -1160,7 +1179,7 @@ cudaError_t launch_moe_tc(const void *x, int64_t M, int k, int E, const QMat &ga
   a.lin_M = 0;
   a.nsplit = 1;
   a.out_split = 0;
-  cudaError_t e = run_tc<2>(mg, mu, mx, mx128, a, s);
+  cudaError_t e = run_tc<2>(mg, mu, mx, a, s);
   if (e != cudaSuccess) return e;
   // 3) h -> scaled fp16 rows
   e = launch_pdl(h_convert_kernel, dim3(static_cast<unsigned>(MK)), dim3(256), 0, s,
@@ -1183,7 +1202,7 @@ cudaError_t launch_moe_tc(const void *x, int64_t M, int k, int E, const QMat &ga
   d.colscale = ws.hs;
   d.out = ws.out;
   d.out_ld = H;
-  return run_tc<1>(md, md, mh, mh128, d, s);
+  return run_tc<1>(md, md, mh, d, s);
 }
 
 }  // namespace qmm

@@ -433,7 +433,8 @@ int moe_ffn_forward(const void *x, int32_t x_dtype, int64_t M, const int32_t *to
   // caller repeats an expert within a token) use the small-M kernels.
   const bool small_gu = M <= 8 && smallm_supported(ex->gate.bits, ex->gate.group, ex->H);
   const bool small_dn = M <= 8 && smallm_supported(ex->down.bits, ex->down.group, ex->I);
-  const bool tc = xb && !small_gu && moe_tc_supported(qmat(ex->gate), qmat(ex->down), ex->H, ex->I);
+  const bool tc = xb && !small_gu && moe_tc_supported(qmat(ex->gate), qmat(ex->up), qmat(ex->down),
+                                                             ex->H, ex->I);
   // On the tensor-core path, experts with one or two tokens skip the
   // dequantise -> fp16 -> MMA pipeline (a 16-row token tile for two tokens at
   // most) and stream their weights through the small-M integer kernels, one

@@ -98,7 +98,7 @@ cudaError_t launch_moe_down(int64_t M, int k, int E, const QMat &down, const Moe
                             cudaStream_t s);
 
 // Tensor-core (tcgen05) path of the routed experts for bf16 activations.
-bool moe_tc_supported(const QMat &gate, const QMat &down, int64_t H, int64_t I);
+bool moe_tc_supported(const QMat &gate, const QMat &up, const QMat &down, int64_t H, int64_t I);
 cudaError_t launch_moe_tc(const void *x, int64_t M, int k, int E, const QMat &gate, const QMat &up,
                           const QMat &down, const MoeWork &ws, cudaStream_t s);
 
