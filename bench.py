@@ -252,7 +252,6 @@ def run_gemv(dev, steps: int, warmup: int, world: int):
         step(evs[i])
     torch.cuda.synchronize()
     t_vocab = np.mean([e[0].elapsed_time(e[1]) for e in evs])
-    t_trunk = ms - t_vocab
 
     # end to end through the C ABI with host buffers (pinned), copies inside
     xh = torch.from_numpy(recipes.linear_x(recipes.CFG2_TRUNK)).pin_memory()
@@ -274,7 +273,7 @@ def run_gemv(dev, steps: int, warmup: int, world: int):
 
     b_trunk = weight_bytes(wt.N, wt.K, 8, 64)
     b_vocab = weight_bytes(wv.N, wv.K, 8, 64)
-    return {"ms": ms, "ms_e2e": ms_e2e, "bytes": b_trunk + b_vocab, "t_trunk_ms": float(t_trunk),
+    return {"ms": ms, "ms_e2e": ms_e2e, "bytes": b_trunk + b_vocab,
             "t_vocab_ms": float(t_vocab), "b_trunk": b_trunk, "b_vocab": b_vocab,
             "launches": int(launches), "clocks": clk.summary(t0, t1),
             "h2d": xh.numel() * 4, "d2h": yh.numel() * 4}
@@ -972,8 +971,11 @@ def main():
                          "frac": ach / peaks["hbm_gbs"], "traffic": traffic,
                          "peak_source": peaks["source"],
                          "frac_vs_8tbs": ach / 8000.0},
-            "kernels_ms": {"vocab_129280": g["t_vocab_ms"],
-                           "rest_of_step": g["t_trunk_ms"]},
+            "kernels_ms": {"vocab_129280": g["t_vocab_ms"], "step": ms,
+                           "note": "vocab head timed alone by events around each launch "
+                                   "(second pass); in the step it starts under the trunk "
+                                   "projection (programmatic dependent launch), so the two "
+                                   "are not subtracted"},
             "gpu_launches": g["launches"],
             "clocks": g["clocks"],
             "e2e": {"value": world * g["bytes"] / (ms_e2e * 1e-3) / 1e9, "unit": "GB/s",
