@@ -111,7 +111,8 @@ struct Smem {
   static constexpr int nbar = 2 * kC + 2 * kA + kB + 2 + 4 + 2;
   static constexpr int misc_off = bar_off + nbar * 8;
   static constexpr int rexp_off = misc_off + 16;  // int32 [2 slots][NT][128 rows]
-  static constexpr int meta_off = rexp_off + 2 * NT * kBM * 4;  // offsets[E+1], tile_start[E+1]
+  static constexpr int cs_off = rexp_off + 2 * NT * kBM * 4;  // fp32 [2 slots][128 tokens]
+  static constexpr int meta_off = cs_off + 2 * kBN * 4;  // offsets[E+1], tile_start[E+1]
   static constexpr int bytes_for(int E) { return meta_off + 8 * (E + 1) + 1024; }
 };
 
@@ -446,6 +447,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // per MMA issuer: tracks its MMAs in flight after an abort
   auto drain_bar = [&](int i) { return acc_free + 40 + 8 * i; };
   int32_t *s_rexp = reinterpret_cast<int32_t *>(gbase + S::rexp_off);
+  float *s_cs = reinterpret_cast<float *>(gbase + S::cs_off);
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + S::misc_off);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(gbase + S::misc_off + 4);
   // written, never read: see the release of a code slot below
@@ -603,6 +605,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           s_rexp[(slot * NT + t) * kBM + rr] = max(-126, min(126, 14 - e));
         }
       }
+      // the item's token column scales, which the epilogue applies
+      for (int i = lane; i < it.ntok; i += 32) s_cs[slot * kBN + i] = __ldg(a.colscale + it.t0 + i);
       mbar_arrive(rexp_full(slot));
     }
   } else if (warp == kWarpMma || warp == kWarpMma + 1) {
@@ -667,6 +671,34 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     int64_t gs = 0;
     uint32_t nitem_done = 0;
+    // Scale / zero point of this warpgroup's next stage, loaded one of its
+    // stages ahead; those of an item's first stage are loaded before the
+    // previous item's epilogue (a row past the matrix, in a ragged last
+    // tile, dequantises to zero and reads no scales).
+    float s_nx[NT];
+    int32_t z_nx[NT];
+    auto load_first = [&](int64_t nx_item, int64_t nx_gs) {
+#pragma unroll
+      for (int t = 0; t < NT; ++t) {
+        s_nx[t] = 0.0f;
+        z_nx[t] = 0;
+      }
+      if (nx_item >= nitems) return;
+      const Item nx = decode_item(s_off, s_ts, a.E, nx_item, ftiles, a.nsplit);
+      const int64_t nx_row = static_cast<int64_t>(nx.f) * kBM + row;
+      const int nx_kbs = nx.ks * kps;
+      const int nx_kb0 = nx_kbs + static_cast<int>((wg - nx_gs % kDequantGroups + kDequantGroups) %
+                                                   kDequantGroups);
+      if (nx_kb0 < nx_kbs + kps && nx_row < a.rows) {
+        const int64_t off = nx.e * a.gstride[0] + nx_row * a.G + ((nx_kb0 * kBK) >> a.group_shift);
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+          s_nx[t] = __ldg(a.sc[t] + off);
+          z_nx[t] = __ldg(a.zp[t] + off);
+        }
+      }
+    };
+    load_first(blockIdx.x, 0);
     for (int64_t item = blockIdx.x; item < nitems && !*abort_flag; item += gridDim.x) {
       const Item it = decode_item(s_off, s_ts, a.E, item, ftiles, a.nsplit);
       const int64_t wrow = static_cast<int64_t>(it.f) * kBM + row;
@@ -674,46 +706,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       // zero-point arrays (the matrices of one launch have the same shape)
       const int64_t goff = it.e * a.gstride[0] + wrow * a.G;
       // Row scale 2^r of each matrix (from the exponent warp) and its inverse,
-      // which the epilogue applies.
+      // which the epilogue applies; the slot (with the item's token column
+      // scales) is released after the epilogue.
+      const int rslot = static_cast<int>(nitem_done & 1u);
       float rup[NT], rdn[NT];
       {
-        const int slot = static_cast<int>(nitem_done & 1u);
         const uint32_t use = nitem_done >> 1;
-        if (!__all_sync(0xFFFFFFFFu, wait_ok(rexp_full(slot), use & 1u, a.status, abort_flag)))
+        if (!__all_sync(0xFFFFFFFFu, wait_ok(rexp_full(rslot), use & 1u, a.status, abort_flag)))
           break;
 #pragma unroll
         for (int t = 0; t < NT; ++t) {
-          const int sh = s_rexp[(slot * NT + t) * kBM + row];
+          const int sh = s_rexp[(rslot * NT + t) * kBM + row];
           rup[t] = __int_as_float((127 + sh) << 23);
           rdn[t] = __int_as_float((127 - sh) << 23);
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(rexp_free(slot));
       }
       // the item's stages [kbs, kbe); this warpgroup's first one (stages are
-      // dealt by their global number gs); a row past the matrix (a ragged
-      // last tile) dequantises to zero and reads no scales
+      // dealt by their global number gs)
       const int kbs = it.ks * kps, kbe = kbs + kps;
       const bool row_ok = wrow < a.rows;
       const int kb0 =
           kbs + static_cast<int>((wg - gs % kDequantGroups + kDequantGroups) % kDequantGroups);
-      // scale / zero point of this warpgroup's next stage, loaded one of its
-      // stages ahead
-      float s_nx[NT];
-      int32_t z_nx[NT];
-#pragma unroll
-      for (int t = 0; t < NT; ++t) {
-        s_nx[t] = 0.0f;
-        z_nx[t] = 0;
-      }
-      if (kb0 < kbe && row_ok) {
-        const int gi = (kb0 * kBK) >> a.group_shift;
-#pragma unroll
-        for (int t = 0; t < NT; ++t) {
-          s_nx[t] = __ldg(a.sc[t] + goff + gi);
-          z_nx[t] = __ldg(a.zp[t] + goff + gi);
-        }
-      }
       bool ok = true;
       // This warpgroup's stages of the item, directly (stage kb has global
       // number gs_item + kb - kbs).
@@ -807,6 +820,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_arrive(a_full(s));
       }
       if (!ok) break;
+      load_first(item + gridDim.x, gs);  // gs: the next item's first stage
       // ---------------------------------------------------- epilogue
       if (!__all_sync(0xFFFFFFFFu, wait_ok(acc_full, nitem_done & 1u, a.status, abort_flag)))
         break;
@@ -822,7 +836,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld16x1(tmem + lane_base + c0, v0);
         // accumulators x (token row's 2^c) x (weight row's 2^-r): exact
         // power-of-two rescaling back to the true products
-        const float *cs = a.colscale + it.t0 + c0;
+        const float *cs = s_cs + rslot * kBN + c0;
         float *const outp = a.out + it.ks * a.out_split;
         const bool feat_ok = feat < a.rows;
         if constexpr (NT == 2) {
@@ -831,7 +845,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int j = 0; j < 16; ++j)
             if (c0 + j < it.ntok && feat_ok) {
-              const float c = __ldg(cs + j);
+              const float c = cs[j];
               outp[static_cast<int64_t>(it.t0 + c0 + j) * a.out_ld + feat] =
                   silu_f(v0[j] * c * rdn[0]) * (v1[j] * c * rdn[1]);
             }
@@ -840,12 +854,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int j = 0; j < 16; ++j)
             if (c0 + j < it.ntok && feat_ok)
               outp[static_cast<int64_t>(it.t0 + c0 + j) * a.out_ld + feat] =
-                  v0[j] * __ldg(cs + j) * rdn[0];
+                  v0[j] * cs[j] * rdn[0];
         }
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(acc_free);
+      if (lane == 0) {
+        mbar_arrive(acc_free);
+        mbar_arrive(rexp_free(rslot));
+      }
       ++nitem_done;
     }
   }
