@@ -251,31 +251,43 @@ __global__ void __launch_bounds__(tiled::kThreads, TE <= 8 ? 2 : 1)
     mbar_fence_init();
   }
   __syncthreads();
-  // Thread 0 requests chunk c into stage c % kNST: the router rows (no
+  // Warp 0 requests chunk c into stage c % kNST: the router rows (no
   // kernel of this library writes them, so the first chunks go out before
-  // the wait for the preceding kernel) and the token rows.
-  auto issue_w = [&](int c) {
+  // the wait for the preceding kernel) and the token rows, one row per lane
+  // (a thread issues a bulk copy only every few hundred cycles, and a chunk
+  // is up to TE + kTM copies).  Lane 0 registers the stage's bytes first.
+  static_assert(TE + kTM <= 32, "one copy per lane of warp 0");
+  auto expect = [&](int c) {
+    if (lane == 0)
+      mbar_arrive_expect_tx(bar(c % kNST), static_cast<uint32_t>(mv * kCH * XB + ev * kCH * 4));
+    __syncwarp();
+  };
+  auto issue_w = [&](int c) {  // lanes [0, ev)
     const int s = c % kNST;
     const uint32_t ws = base + s * SB + kTM * kCH * XB;
-    mbar_arrive_expect_tx(bar(s), static_cast<uint32_t>(mv * kCH * XB + ev * kCH * 4));
-    for (int e = 0; e < ev; ++e)
-      bulk_g2s(ws + e * kCH * 4, wr + int64_t(e0 + e) * H + int64_t(c) * kCH, kCH * 4, bar(s));
+    if (lane < ev)
+      bulk_g2s(ws + lane * kCH * 4, wr + int64_t(e0 + lane) * H + int64_t(c) * kCH, kCH * 4,
+               bar(s));
   };
-  auto issue_x = [&](int c) {
+  auto issue_x = [&](int c) {  // lanes [TE, TE + mv)
     const int s = c % kNST;
     const uint32_t xs = base + s * SB;
-    for (int m = 0; m < mv; ++m)
+    const int m = lane - TE;
+    if (m >= 0 && m < mv)
       bulk_g2s(xs + m * kCH * XB,
                static_cast<const uint8_t *>(x) + ((m0 + m) * H + int64_t(c) * kCH) * XB,
                kCH * XB, bar(s));
   };
   const int npre = min(kNST, nch);
-  if (tid == 0)
-    for (int c = 0; c < npre; ++c) issue_w(c);
+  if (tid < 32)
+    for (int c = 0; c < npre; ++c) {
+      expect(c);
+      issue_w(c);
+    }
   pdl_enter();
   if (counts && blockIdx.x == 0 && blockIdx.y == 0)
     for (int e = tid; e < E; e += blockDim.x) counts[e] = 0;
-  if (tid == 0)
+  if (tid < 32)
     for (int c = 0; c < npre; ++c) issue_x(c);
 
   float acc[8][TE];
@@ -319,8 +331,11 @@ __global__ void __launch_bounds__(tiled::kThreads, TE <= 8 ? 2 : 1)
       aborted = true;
       break;
     }
-    if (tid == 0 && issued < nch) {
+    if (tid < 32 && issued < nch) {
+      // every thread's reads of the stage (generic proxy) before the copies'
+      // writes (async proxy)
       fence_proxy_async_smem();
+      expect(issued);
       issue_w(issued);
       issue_x(issued);
       ++issued;
