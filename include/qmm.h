@@ -210,8 +210,9 @@ size_t moe_ffn_workspace_bytes(int64_t M, int32_t k, const moe_experts *ex);
  *    every output is within 1e-5 * sum |x w^| + 1e-6 per linear stage of the
  *    exact result (propagated through SwiGLU and the weighted sum).
  *  - bf16 activations with M > 8 and INT8 experts (batched prefill, H and I
- *    multiples of 128, group >= 64): experts with three or more tokens run on
- *    the tensor cores with fp16 operands and fp32 accumulation.  Each token
+ *    multiples of 128, group >= 64, gate and up with the same groups_stride):
+ *    experts with three or more tokens run on the tensor cores with fp16
+ *    operands and fp32 accumulation.  Each token
  *    row, each SwiGLU row and each weight row is scaled by its own power of
  *    two so that its largest magnitude lies in [2^14, 2^15) (no overflow,
  *    fp16's full 11-bit precision for every value within 2^28 of its row's
@@ -221,6 +222,8 @@ size_t moe_ffn_workspace_bytes(int64_t M, int32_t k, const moe_experts *ex);
  *    token row a relative L2 error within 1e-2 of the exact result (the
  *    operands' fp16 rounding, about 2^-11 relative per value).  Experts
  *    with one or two tokens in such a batch run on the CUDA-core kernels.
+ *  - bf16 activations with M > 8 whose experts do not qualify: the CUDA-core
+ *    kernels, with the fp32 bound of the first case.
  */
 int moe_ffn_forward(const void *x, int32_t x_dtype, int64_t M,
                     const int32_t *topk_idx, const float *topk_w, int32_t k,

@@ -8,6 +8,8 @@ layer); bf16 outputs within a 1e-2 relative L2 error per row with the same
 arg-max.  Full-size workloads are checked on sampled rows / tokens that the
 oracle computes one by one.
 """
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -380,6 +382,32 @@ def test_moe_tensor_core_tiles(dev, group, H, I):
     w_ok = np.where(bad < E, w[:7], 0).astype(np.float32)
     yref, _ = oracle.moe_ffn(x[:7], np.where(bad < E, bad, 0).astype(np.int32), w_ok, og, ou, od)
     assert_bf16_rows(y, yref, "tc bad index")
+
+
+def test_moe_gate_up_layouts_differ(dev):
+    """Gate and up whose scale and zero-point arrays have different strides
+    between experts (up's live in padded buffers): the tensor-core path, whose
+    dequantising threads share one scale offset between the two matrices, is
+    not taken, and the CUDA-core kernels give the strict fp32 bound for bf16
+    tokens.  The same experts in one layout take the tensor-core path."""
+    E, H, I, group, k = 6, 512, 256, 64, 2
+    ex, og, ou, od = _small_experts(dev, E, H, I, 8, group, seed=11)
+    G = H // group
+    pad = 128
+    us = torch.zeros((E, I + pad, G), dtype=torch.float32, device=dev)
+    uz = torch.zeros((E, I + pad, G), dtype=torch.int32, device=dev)
+    us[:, :I] = ex.up_scales.view(E, I, G)
+    uz[:, :I] = ex.up_zps.view(E, I, G)
+    ex2 = dataclasses.replace(ex, up_scales=us[:, :I], up_zps=uz[:, :I])
+    assert ex2.up_scales.stride(0) != ex2.gate_scales.stride(0)
+    M = 40
+    x, xd = _bf16_x(synth.normal(11, 1, M * H).reshape(M, H), dev)
+    idx = np.stack([np.full(M, 2), np.where(np.arange(M) % 3 == 0, 4, 0)], axis=1).astype(np.int32)
+    w = np.full((M, k), 0.5, np.float32)
+    y = q.moe_ffn_forward(xd, T(idx, dev), T(w, dev), ex2).cpu().numpy().astype(np.float64)
+    yref, bound = oracle.moe_ffn(x, idx, w, og, ou, od)
+    assert_within(y, yref, bound, "gate and up in different layouts")
+    _moe_check(dev, x, xd, idx, w, ex, og, ou, od, what="gate and up in one layout")
 
 
 def test_moe_bad_expert_index_flagged(dev):
