@@ -8,7 +8,7 @@ layer); bf16 outputs within a 1e-2 relative L2 error per row with the same
 arg-max.  Full-size workloads are checked on sampled rows / tokens that the
 oracle computes one by one.
 """
-import dataclasses
+import ctypes
 
 import numpy as np
 import pytest
@@ -386,10 +386,11 @@ def test_moe_tensor_core_tiles(dev, group, H, I):
 
 def test_moe_gate_up_layouts_differ(dev):
     """Gate and up whose scale and zero-point arrays have different strides
-    between experts (up's live in padded buffers): the tensor-core path, whose
-    dequantising threads share one scale offset between the two matrices, is
-    not taken, and the CUDA-core kernels give the strict fp32 bound for bf16
-    tokens.  The same experts in one layout take the tensor-core path."""
+    between experts (up's inside padded buffers, described to the library
+    through its C descriptor): the tensor-core path, whose dequantising
+    threads share one scale offset between the two matrices, is not taken,
+    and the CUDA-core kernels give the strict fp32 bound for bf16 tokens.
+    The same experts in one layout take the tensor-core path."""
     E, H, I, group, k = 6, 512, 256, 64, 2
     ex, og, ou, od = _small_experts(dev, E, H, I, 8, group, seed=11)
     G = H // group
@@ -398,15 +399,28 @@ def test_moe_gate_up_layouts_differ(dev):
     uz = torch.zeros((E, I + pad, G), dtype=torch.int32, device=dev)
     us[:, :I] = ex.up_scales.view(E, I, G)
     uz[:, :I] = ex.up_zps.view(E, I, G)
-    ex2 = dataclasses.replace(ex, up_scales=us[:, :I], up_zps=uz[:, :I])
-    assert ex2.up_scales.stride(0) != ex2.gate_scales.stride(0)
+    desc = ex._c()
+    desc.up.scales = us.data_ptr()
+    desc.up.zps = uz.data_ptr()
+    desc.up.groups_stride = (I + pad) * G
+    assert desc.up.groups_stride != desc.gate.groups_stride
     M = 40
     x, xd = _bf16_x(synth.normal(11, 1, M * H).reshape(M, H), dev)
     idx = np.stack([np.full(M, 2), np.where(np.arange(M) % 3 == 0, 4, 0)], axis=1).astype(np.int32)
     w = np.full((M, k), 0.5, np.float32)
-    y = q.moe_ffn_forward(xd, T(idx, dev), T(w, dev), ex2).cpu().numpy().astype(np.float64)
+    idx_d, w_d = T(idx, dev), T(w, dev)
+    y = torch.empty((M, H), dtype=torch.float32, device=dev)
+    L = q.lib()
+    ws = torch.empty((int(L.moe_ffn_workspace_bytes(M, k, ctypes.byref(desc))),),
+                     dtype=torch.uint8, device=dev)
+    rc = L.moe_ffn_forward(xd.data_ptr(), q.QMM_BF16, M, idx_d.data_ptr(), w_d.data_ptr(), k,
+                           ctypes.byref(desc), y.data_ptr(), q.QMM_F32, ws.data_ptr(),
+                           ws.numel(), None)
+    assert rc == 0, q.lib().qmm_last_error()
+    torch.cuda.synchronize()
     yref, bound = oracle.moe_ffn(x, idx, w, og, ou, od)
-    assert_within(y, yref, bound, "gate and up in different layouts")
+    assert_within(y.cpu().numpy().astype(np.float64), yref, bound,
+                  "gate and up in different layouts")
     _moe_check(dev, x, xd, idx, w, ex, og, ou, od, what="gate and up in one layout")
 
 
