@@ -74,19 +74,19 @@ template <int NT>
 struct Ring;  // NT = weight tiles sharing one token tile (2: gate+up, 1: down)
 // Three independent rings: codes (TMA -> dequant), A (dequant -> MMA) and
 // B (TMA -> MMA), each with its own depth.
-// TMEM: accumulators in columns [0, 256) (gate, up for NT=2; the two k-step
-// parities for NT=1), then the A stages: NT=2 uses 256 + 4*2*32 = 512
+// TMEM: accumulators in columns [0, 256) (gate at 0 and up at 128 for NT=2,
+// one at 0 for NT=1), then the A stages: NT=2 uses 256 + 4*2*32 = 512
 // columns, NT=1 uses 256 + 4*32 = 384 (allocation 512).
-// The A and B rings have the same depth, so that one commit frees the A
-// and B slots of a stage together.  The code ring's depth is a multiple of
+// The A and B rings have the same depth, so that the MMA issuers' commits
+// free the A and B slots of a stage together.  The code ring's depth is a multiple of
 // the three dequant warpgroups: stage gs goes to code slot gs mod kC and to
 // warpgroup gs mod 3, so every use of a slot belongs to the same warpgroup,
 // in order.  Its wait on the slot's barrier can then never see a phase two
 // uses old (which the parity test would take as complete: with a depth that
 // is not a multiple of 3, a warpgroup that runs ahead could read a slot whose
 // copy is still landing and arrive on the wrong phase of its free barrier).
-// Three warpgroups hold three slots while they convert, so the ring also
-// needs more than three slots to keep loads in flight.
+// A warpgroup releases its slot as soon as it has read the codes, so nearly
+// the whole ring is loading at any time (deeper rings measured slower).
 template <>
 struct Ring<2> {
   static constexpr int kA = 4, kB = 4, kC = 6;
