@@ -54,10 +54,13 @@ class Barrier:
         return parity != (self.done & 1)
 
 
-def run(items, kps, kA, kC, issuers, seed):
+def run(items, kps, kA, kC, issuers, seed, n_issuers=2):
     """One CTA's items (kps stages each) through the rings.  issuers:
-    "per_matrix" (the kernel: two issuers, each issuing its matrix of every
-    stage in order) or "alternate" (issuer i owns the stages g = i mod 2)."""
+    "per_matrix" (the kernel: n_issuers issuers, each issuing its matrix of
+    every stage in order; two for gate/up, one for down) or "alternate"
+    (two issuers, issuer i owning the stages g = i mod 2)."""
+    if issuers == "alternate":
+        n_issuers = 2
     rng = random.Random(seed)
     kB = kA
     S = items * kps
@@ -65,9 +68,9 @@ def run(items, kps, kA, kC, issuers, seed):
     c_full = [Barrier(1) for _ in range(kC)]
     c_free = [Barrier(4) for _ in range(kC)]       # one arrival per warp
     a_full = [Barrier(4) for _ in range(kA)]
-    ab_free = [Barrier(2) for _ in range(kA)]      # one commit per issuer
+    ab_free = [Barrier(n_issuers) for _ in range(kA)]  # one commit per issuer
     b_full = [Barrier(1) for _ in range(kB)]
-    acc_full, acc_free = Barrier(2), Barrier(4 * G)
+    acc_full, acc_free = Barrier(n_issuers), Barrier(4 * G)
     # slot contents: the stage written last, and the last stage read
     code_slot = [None] * kC
     code_read = [set() for _ in range(kC)]
@@ -138,7 +141,7 @@ def run(items, kps, kA, kC, issuers, seed):
             pipe.append(("commit", acc_full))
 
     agents = [code_producer(), rows_producer()] + [warpgroup(w) for w in range(G)]
-    agents += [issuer(i) for i in range(2)]
+    agents += [issuer(i) for i in range(n_issuers)]
     # Each run gives every agent its own speed and the copies and the tensor
     # pipe their own rates, so that skewed schedules (one warpgroup or one
     # issuer far behind the others) are explored as well as even ones.
@@ -165,7 +168,7 @@ def run(items, kps, kA, kC, issuers, seed):
             if op[0] == "mma":
                 _, g, i = op
                 issued.setdefault(g, set()).add(i)
-                need = {0, 1} if issuers == "per_matrix" else {g % 2}
+                need = set(range(n_issuers)) if issuers == "per_matrix" else {g % 2}
                 if issued[g] >= need:
                     mma_done.add(g)
             else:
@@ -182,13 +185,13 @@ def run(items, kps, kA, kC, issuers, seed):
             del live[id(v[0])]
 
 
-@pytest.mark.parametrize("kA,kC", [(4, 6), (4, 9)])
-def test_kernel_protocol_holds(kA, kC):
-    """The kernel's rings (gate/up: code ring 6, down: 9; A and B rings 4)
-    with per-matrix issuers: no wait ever passes on a stale phase and no slot
-    is overwritten early, over many random interleavings."""
+@pytest.mark.parametrize("kA,kC,n_issuers", [(4, 6, 2), (4, 9, 1)])
+def test_kernel_protocol_holds(kA, kC, n_issuers):
+    """The kernel's rings (gate/up: code ring 6 and two issuers, down: 9 and
+    one; A and B rings 4): no wait ever passes on a stale phase and no slot is
+    overwritten early, over many random interleavings."""
     for seed in range(400):
-        run(items=2, kps=32, kA=kA, kC=kC, issuers="per_matrix", seed=seed)
+        run(items=2, kps=32, kA=kA, kC=kC, issuers="per_matrix", seed=seed, n_issuers=n_issuers)
 
 
 def test_alternate_stage_issuers_are_caught():
