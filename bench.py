@@ -493,13 +493,37 @@ def run_tc_subset(dev, r, ex, x, idx, counts, steps: int, flush):
         torch.cuda.synchronize()
         times.append(e0.elapsed_time(e1))
     ms = float(np.mean(times))
+    # The two GEMM launches alone: the library records events around them
+    # (a second pass: the events keep the launches from overlapping).
+    gu, dn = [], []
+    q.qmm_tc_timing(True)
+    try:
+        for _ in range(steps):
+            flush.zero_()
+            torch.cuda._sleep(400000)
+            call()
+            g_ms, d_ms = q.qmm_tc_timing_ms()
+            gu.append(g_ms)
+            dn.append(d_ms)
+    finally:
+        q.qmm_tc_timing(False)
+    g_ms, d_ms = float(np.mean(gu)), float(np.mean(dn))
     flops = 2.0 * 3 * r.H * r.I * m_sub
+    f_gu, f_dn = 2.0 * 2 * r.H * r.I * m_sub, 2.0 * r.H * r.I * m_sub
     peaks = load_peaks()
+    pk = peaks["bf16_tflops"]
     return {"experts": int(hot.sum()), "assignments": int(m_sub), "ms": ms,
             "flops": flops, "tflops": flops / (ms * 1e-3) / 1e12,
-            "tc_frac": flops / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"],
-            "peak_tflops": peaks["bf16_tflops"], "peak": "bf16 burst (the call runs < 1 ms)",
-            "timed": "whole moe_ffn_forward call on the experts with >= 64 tokens"}
+            "tc_frac": flops / (ms * 1e-3) / 1e12 / pk,
+            "peak_tflops": pk, "peak": "bf16 burst (the call runs < 1 ms)",
+            "timed": "whole moe_ffn_forward call on the experts with >= 64 tokens",
+            "gemm_kernels": {
+                "gateup_ms": g_ms, "down_ms": d_ms,
+                "tflops": flops / ((g_ms + d_ms) * 1e-3) / 1e12,
+                "tc_frac": flops / ((g_ms + d_ms) * 1e-3) / 1e12 / pk,
+                "gateup_tc_frac": f_gu / (g_ms * 1e-3) / 1e12 / pk,
+                "down_tc_frac": f_dn / (d_ms * 1e-3) / 1e12 / pk,
+                "timed": "library events around each moe_tc_kernel launch (qmm_tc_timing)"}}
 
 
 def run_linear_batched(dev, steps: int):

@@ -38,7 +38,8 @@ EXPORTED = ("qmm_quantize_groupwise", "qmm_linear", "moe_route_workspace_bytes",
             "qmm_device_status", "moe_route_topk_noalloc", "moe_route_load_stats",
             "qmm_diag_wait_timeout", "qmm_linear_batched_workspace_bytes",
             "qmm_linear_batched", "qmm_rope_table", "qmm_attn_decode_workspace_bytes",
-            "qmm_attn_decode", "moe_decode_workspace_bytes", "moe_decode_forward")
+            "qmm_attn_decode", "moe_decode_workspace_bytes", "moe_decode_forward",
+            "qmm_tc_timing", "qmm_tc_timing_ms")
 QMM_NOALLOC_MAX_LOGITS = 262144
 
 
@@ -109,6 +110,11 @@ def lib() -> ctypes.CDLL:
             L.qmm_last_error.restype = ctypes.c_char_p
             L.qmm_launch_count.argtypes = []
             L.qmm_launch_count.restype = u64
+            L.qmm_tc_timing.argtypes = [i32]
+            L.qmm_tc_timing.restype = ctypes.c_int
+            L.qmm_tc_timing_ms.argtypes = [ctypes.POINTER(ctypes.c_float),
+                                           ctypes.POINTER(ctypes.c_float)]
+            L.qmm_tc_timing_ms.restype = ctypes.c_int
             L.qmm_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32), i32]
             L.qmm_device_status.restype = ctypes.c_int
             L.moe_route_topk_noalloc.argtypes = [vp, i32, i64, i64, vp, vp, i32, i32, vp, vp, vp,
@@ -577,6 +583,20 @@ def qmm_last_error() -> str:
 
 def qmm_launch_count() -> int:
     return int(lib().qmm_launch_count())
+
+
+def qmm_tc_timing(enable: bool) -> None:
+    """Switch the timing of the tensor-core prefill GEMM launches on or off
+    (see include/qmm.h)."""
+    _check(lib().qmm_tc_timing(1 if enable else 0))
+
+
+def qmm_tc_timing_ms() -> tuple[float, float]:
+    """(gate/up ms, down ms) of the last tensor-core moe_ffn_forward since
+    timing was switched on; waits for that call's events."""
+    g, d = ctypes.c_float(), ctypes.c_float()
+    _check(lib().qmm_tc_timing_ms(ctypes.byref(g), ctypes.byref(d)))
+    return float(g.value), float(d.value)
 
 
 def qmm_device_status(clear: bool = False) -> int:

@@ -1146,6 +1146,59 @@ cudaError_t launch_linear_tc(const void *x, int64_t M, const QMat &w, void *y, b
                     static_cast<const float *>(part), S, n, y);
 }
 
+// Timing of the two GEMM launches (off unless enabled): events of the
+// device that was current when timing was switched on, recorded around the
+// gate/up and the down launch of every tensor-core moe_ffn_forward.
+namespace {
+struct TcTiming {
+  std::mutex mu;
+  bool on = false;
+  bool recorded = false;
+  int dev = -1;
+  cudaEvent_t ev[4] = {};
+};
+TcTiming &tc_timing() {
+  static TcTiming t;
+  return t;
+}
+// Records event i on s when timing is on for the current device.
+cudaError_t tc_mark(int i, cudaStream_t s) {
+  TcTiming &t = tc_timing();
+  std::lock_guard<std::mutex> lock(t.mu);
+  if (!t.on) return cudaSuccess;
+  int d = -1;
+  cudaError_t e = cudaGetDevice(&d);
+  if (e != cudaSuccess || d != t.dev) return e;
+  e = cudaEventRecord(t.ev[i], s);
+  if (e == cudaSuccess && i == 3) t.recorded = true;
+  return e;
+}
+}  // namespace
+
+cudaError_t tc_timing_enable(bool on) {
+  TcTiming &t = tc_timing();
+  std::lock_guard<std::mutex> lock(t.mu);
+  if (on && t.ev[0] == nullptr) {
+    cudaError_t e = cudaGetDevice(&t.dev);
+    for (int i = 0; i < 4 && e == cudaSuccess; ++i) e = cudaEventCreate(&t.ev[i]);
+    if (e != cudaSuccess) return e;
+  }
+  t.on = on;
+  t.recorded = false;
+  return cudaSuccess;
+}
+
+cudaError_t tc_timing_read(float *gateup_ms, float *down_ms, bool *have) {
+  TcTiming &t = tc_timing();
+  std::lock_guard<std::mutex> lock(t.mu);
+  *have = t.recorded;
+  if (!t.recorded) return cudaSuccess;
+  cudaError_t e = cudaEventSynchronize(t.ev[3]);
+  if (e == cudaSuccess) e = cudaEventElapsedTime(gateup_ms, t.ev[0], t.ev[1]);
+  if (e == cudaSuccess) e = cudaEventElapsedTime(down_ms, t.ev[2], t.ev[3]);
+  return e;
+}
+
 bool moe_tc_supported(const QMat &gate, const QMat &up, const QMat &down, int64_t H, int64_t I) {
   // gate and up share one scale / zero-point offset per dequantising thread
   const bool same_layout = up.groups_stride == gate.groups_stride && up.group == gate.group &&
@@ -1196,7 +1249,9 @@ cudaError_t launch_moe_tc(const void *x, int64_t M, int k, int E, const QMat &ga
   a.lin_M = 0;
   a.nsplit = 1;
   a.out_split = 0;
-  cudaError_t e = run_tc<2>(mg, mu, mx, a, s);
+  cudaError_t e = tc_mark(0, s);
+  if (e == cudaSuccess) e = run_tc<2>(mg, mu, mx, a, s);
+  if (e == cudaSuccess) e = tc_mark(1, s);
   if (e != cudaSuccess) return e;
   // 3) h -> scaled fp16 rows
   e = launch_pdl(h_convert_kernel, dim3(static_cast<unsigned>(MK)), dim3(256), 0, s,
@@ -1219,7 +1274,10 @@ cudaError_t launch_moe_tc(const void *x, int64_t M, int k, int E, const QMat &ga
   d.colscale = ws.hs;
   d.out = ws.out;
   d.out_ld = H;
-  return run_tc<1>(md, md, mh, d, s);
+  e = tc_mark(2, s);
+  if (e == cudaSuccess) e = run_tc<1>(md, md, mh, d, s);
+  if (e == cudaSuccess) e = tc_mark(3, s);
+  return e;
 }
 
 }  // namespace qmm

@@ -122,6 +122,23 @@ const char *qmm_last_error(void) { return g_err; }
 
 uint64_t qmm_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
+int qmm_tc_timing(int32_t enable) {
+  cudaError_t e = tc_timing_enable(enable != 0);
+  if (e != cudaSuccess) return cuda_fail(e, "qmm_tc_timing");
+  return QMM_OK;
+}
+
+int qmm_tc_timing_ms(float *gateup_ms, float *down_ms) {
+  if (!gateup_ms || !down_ms) return fail(QMM_ERR_INVALID_ARG, "qmm_tc_timing_ms: NULL output");
+  bool have = false;
+  cudaError_t e = tc_timing_read(gateup_ms, down_ms, &have);
+  if (e != cudaSuccess) return cuda_fail(e, "qmm_tc_timing_ms");
+  if (!have)
+    return fail(QMM_ERR_INVALID_ARG,
+                "qmm_tc_timing_ms: no tensor-core launch recorded since timing was enabled");
+  return QMM_OK;
+}
+
 int qmm_device_status(uint32_t *status, int32_t clear) {
   if (!status) return fail(QMM_ERR_INVALID_ARG, "qmm_device_status: status is NULL");
   cudaError_t e = cudaDeviceSynchronize();

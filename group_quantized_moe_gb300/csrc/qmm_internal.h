@@ -106,6 +106,9 @@ cudaError_t launch_moe_tc(const void *x, int64_t M, int k, int E, const QMat &ga
 // workspace bytes for M rows, and the launch (gather, GEMM with K splits,
 // ordered reduction of the splits).
 bool linear_tc_supported(const QMat &w);
+// Timing of the tensor-core MoE GEMM launches (qmm_tc_timing).
+cudaError_t tc_timing_enable(bool on);
+cudaError_t tc_timing_read(float *gateup_ms, float *down_ms, bool *have);
 size_t linear_tc_workspace_bytes(int64_t M, const QMat &w);
 cudaError_t launch_linear_tc(const void *x, int64_t M, const QMat &w, void *y, bool y_bf16,
                              void *workspace, cudaStream_t s);

@@ -381,6 +381,20 @@ const char *qmm_last_error(void);
 /* Number of kernels this library has launched in this process. */
 uint64_t qmm_launch_count(void);
 
+/*
+ * Timing of the tensor-core prefill GEMMs (a profiling aid; no counterpart on
+ * the pages).  After qmm_tc_timing(1), every moe_ffn_forward on the current
+ * device that takes the tensor-core path records CUDA events owned by the
+ * library around its gate/up GEMM launch and around its down GEMM launch (the
+ * launches then no longer overlap the tails of the kernels before them);
+ * qmm_tc_timing(0) stops it.  qmm_tc_timing_ms waits for the events of the
+ * last such call and returns the two launches' durations in milliseconds;
+ * QMM_ERR_INVALID_ARG if no call was recorded since timing was enabled.
+ * Not for concurrent use from several threads' streams (one set of events).
+ */
+int qmm_tc_timing(int32_t enable);
+int qmm_tc_timing_ms(float *gateup_ms, float *down_ms);
+
 /* Reads (and, if clear != 0, resets) the device status word of the current
  * device.  Synchronises the device.  Returns QMM_OK or QMM_ERR_CUDA. */
 int qmm_device_status(uint32_t *status, int32_t clear);

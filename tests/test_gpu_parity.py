@@ -384,6 +384,28 @@ def test_moe_tensor_core_tiles(dev, group, H, I):
     assert_bf16_rows(y, yref, "tc bad index")
 
 
+def test_tc_timing_events(dev):
+    """qmm_tc_timing: the tensor-core path records its two GEMM launches;
+    the result is unchanged and the durations are positive."""
+    E, H, I, k = 6, 512, 256, 2
+    ex, og, ou, od = _small_experts(dev, E, H, I, 8, 64, seed=13)
+    M = 96
+    x, xd = _bf16_x(synth.normal(13, 1, M * H).reshape(M, H), dev)
+    idx = np.stack([np.full(M, 3), np.where(np.arange(M) % 4 == 0, 1, 5)], axis=1).astype(np.int32)
+    w = np.full((M, k), 0.5, np.float32)
+    y0 = _moe_check(dev, x, xd, idx, w, ex, og, ou, od, what="tc, timing off")
+    q.qmm_tc_timing(True)
+    try:
+        with pytest.raises(q.QmmError):
+            q.qmm_tc_timing_ms()  # nothing recorded yet
+        y1 = _moe_check(dev, x, xd, idx, w, ex, og, ou, od, what="tc, timing on")
+        g_ms, d_ms = q.qmm_tc_timing_ms()
+    finally:
+        q.qmm_tc_timing(False)
+    np.testing.assert_array_equal(y1, y0)
+    assert 0.0 < g_ms < 1000.0 and 0.0 < d_ms < 1000.0, (g_ms, d_ms)
+
+
 def test_moe_gate_up_layouts_differ(dev):
     """Gate and up whose scale and zero-point arrays have different strides
     between experts (up's inside padded buffers, described to the library
